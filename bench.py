@@ -1,0 +1,519 @@
+"""Benchmark of the SAM-drafting + lossless-verification hot path on GB300.
+
+One step = one pass of the per-step hot path over a batch: the device suffix
+automata are extended with the tokens the previous verification emitted and
+queried for K drafts (sam_step, one launch), then the drafts are verified
+against that step's target logits (spec_verify, one launch).  The emitted
+tokens feed the next step, as in a decode loop.
+
+Default workload (rs_bf16_b64): B=64 sequences per GPU, V=151936, Zipf(1.1)
+histories of 4096 tokens (copy prob 0.3, spans 8-64), K=3 SAM drafts,
+rejection sampling at T=1.0 on bf16 logits N(0, sd 2) + 4 on the stream's
+true continuation.  Logits come from a rotating pool of 16 step tensors
+(1.24 GB, far above the 129 MB L2), so no step finds its rows in L2.
+
+The timed region replays a CUDA graph of exactly --steps steps, bracketed by a
+barrier and a device synchronisation, timed with CUDA events on the capture
+stream; max over ranks.  Under torchrun every rank runs its own batch (weak
+scaling, no collective on the data path).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                  [--workload rs_bf16_b64|sweep_b1024]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "verified sequence-steps/s and spec_verify HBM GB/s vs 8 TB/s; SAM ns/seq-step"
+POOL = 16
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.th = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 7:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.th.join(timeout=5)
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(self.rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _sum_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# inputs of the default workload
+# --------------------------------------------------------------------------
+
+def rs_inputs(rank: int, B: int = 64, V: int = workloads.V_LARGE, n: int = 4096, K: int = 3):
+    """Histories and the continuation used to boost each pool entry's logits."""
+    rng = np.random.default_rng(1002 + 7919 * rank)
+    z = workloads.ZipfTokens(V, 1.1)
+    streams = [workloads.make_stream(rng, n + POOL * (K + 1), V, 0.3, 8, 64, z) for _ in range(B)]
+    hist = np.stack([s[:n] for s in streams]).astype(np.int32)
+    cont = np.stack([s[n:] for s in streams]).astype(np.int32)  # [B, POOL*(K+1)]
+    return hist, cont
+
+
+def rs_logits_pool(device, B, K, V, cont, seed):
+    """POOL bf16 tensors [B, K+1, V]: N(0, sd 2) plus 4 on the continuation."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    pool = []
+    idx_b = torch.arange(B, device=device)
+    for p in range(POOL):
+        x = torch.empty((B, K + 1, V), dtype=torch.float32, device=device).normal_(0.0, 2.0, generator=g)
+        truth = torch.as_tensor(cont[:, p * (K + 1):(p + 1) * (K + 1)], device=device).long()
+        for j in range(K + 1):
+            x[idx_b, j, truth[:, j]] += 4.0
+        pool.append(x.to(torch.bfloat16).contiguous())
+        del x
+    return pool
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def run_gpu(args):
+    import torch
+
+    import sam_drafting_verification_gb300 as ss
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    if args.workload == "sweep_b1024":
+        return run_sweep(args, ws, rank, dev)
+
+    B, V, K, T, n = 64, workloads.V_LARGE, 3, 1.0, 4096
+    hist, cont = rs_inputs(rank, B, V, n, K)
+    steps, warm = args.steps, args.warmup
+    cap = n + (K + 1) * (steps + warm + 8) + 64
+    batch = ss.SamBatch(B, cap, V, device=dev)
+    hist_d = torch.as_tensor(hist, device=dev)
+    nfull = torch.full((B,), n, dtype=torch.int32, device=dev)
+
+    # S1: prefill build (one launch), timed on its own
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    batch.extend(hist_d, nfull)
+    e1.record()
+    torch.cuda.synchronize()
+    prefill_ms = e0.elapsed_time(e1)
+    assert (batch.status() == 0).all()
+    snap = batch.export()
+
+    pool = rs_logits_pool(dev, B, K, V, cont, 4242 + rank)
+    emit = torch.zeros((B, K + 1), dtype=torch.int32, device=dev)
+    emit_len = torch.zeros(B, dtype=torch.int32, device=dev)
+    draft = torch.empty((B, K), dtype=torch.int32, device=dev)
+    dlen = torch.empty(B, dtype=torch.int32, device=dev)
+    mlen = torch.empty(B, dtype=torch.int32, device=dev)
+    mend = torch.empty(B, dtype=torch.int32, device=dev)
+    out = {"accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+           "out_token": torch.empty(B, dtype=torch.int32, device=dev),
+           "emit": emit, "emit_len": emit_len,
+           "status": torch.empty(B, dtype=torch.int32, device=dev)}
+    acc_log = torch.zeros((max(min(steps, 2000), 1), B), dtype=torch.int32, device=dev)
+    wsv = ss.verify_workspace(B, K, V, dev)
+
+    def step(s, log_row=None, only_verify=False):
+        if not only_verify:
+            batch.step(emit, emit_len, K, out=(draft, dlen, mlen, mend))
+        ss.spec_verify(pool[s % POOL], draft, dlen, temperature=T, seed=1002, step=s, out=out,
+                       emit=True, status=True, workspace=wsv)
+        if log_row is not None:
+            log_row.copy_(out["accept_len"])
+
+    # warm-up (eager), then restore the automata to the post-prefill snapshot
+    for s in range(warm):
+        step(s)
+    torch.cuda.synchronize()
+    batch.import_(snap)
+    emit_len.zero_()
+
+    # capture exactly `steps` steps (2 kernels each) in one graph
+    cs = torch.cuda.Stream(device=dev)
+    g = torch.cuda.CUDAGraph()
+    cs.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(g, stream=cs):
+            for s in range(steps):
+                step(warm + s)
+    torch.cuda.synchronize()
+    batch.import_(snap)
+    emit_len.zero_()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    _barrier(ws)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    g.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    _barrier(ws)
+    total_ms = t0.elapsed_time(t1)
+    clk = clocks.stop()
+    st = out["status"].cpu().numpy()
+    assert (st == 0).all() and (batch.status() == 0).all(), "verification or automaton error"
+
+    # acceptance of the first timed steps (eager re-run of the same steps, outside timing)
+    n_acc = min(steps, 2000)
+    batch.import_(snap)
+    emit_len.zero_()
+    for s in range(n_acc):
+        step(warm + s, log_row=acc_log[s])
+    torch.cuda.synchronize()
+    L = acc_log[:n_acc].cpu().numpy().astype(np.int64)
+
+    # attribution: the verify launches alone, replayed as a graph on the same inputs
+    n_att = min(steps, 2000)
+    gv = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(gv, stream=cs):
+            for s in range(n_att):
+                step(warm + s, only_verify=True)
+    torch.cuda.synchronize()
+    v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    v0.record()
+    gv.replay()
+    v1.record()
+    torch.cuda.synchronize()
+    verify_ms = v0.elapsed_time(v1) / n_att
+    Lv = out["accept_len"].cpu().numpy().astype(np.int64)  # last verify's lengths (same drafts each launch)
+
+    ms_step = _max_over_ranks(total_ms / steps, ws, dev)
+    seqs = _sum_over_ranks(float(B), ws, dev)
+    value = seqs / (ms_step / 1e3)
+    sam_ms = max(ms_step - verify_ms, 0.0)
+
+    # verify roofline: algorithmic bytes = rows the accept chains need
+    row_bytes = V * 2
+    verify_bytes = float((Lv + 1).sum()) * row_bytes
+    hbm, peak_kind = _peaks()
+    achieved = verify_bytes / (verify_ms / 1e3) / 1e9
+    roof = {"kernel": "verify_kernel<bf16, one-hot, T>0>", "bound": "hbm",
+            "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "traffic": None,
+            "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
+            "algorithmic_bytes_per_launch": verify_bytes,
+            "kernel_ms": round(verify_ms, 5)}
+
+    cpu = cpu_baseline_rs(hist, cont) if rank == 0 else None
+    e2e = e2e_rs(batch, snap, pool, emit, emit_len, draft, dlen, mlen, mend, out, wsv, B, K, V, T,
+                 steps=min(steps, 200), dev=dev)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "seq-steps/s", "n_gpus": ws,
+        "steps": steps, "warmup": warm, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 (bf16 logits)", "data": "synthetic",
+        "config": {"workload": "rs_bf16_b64", "B_per_gpu": B, "V": V, "K": K, "temperature": T,
+                   "history": n, "logits": "bf16 N(0, sd 2) + 4 on the true continuation",
+                   "drafts": "device SAM (K=3)", "parallelism": f"dp{ws} (independent batches)",
+                   "l2": f"inputs larger than L2: rotating pool of {POOL} logits tensors "
+                         f"({POOL * B * (K + 1) * V * 2 / 1e9:.2f} GB)",
+                   "timing": "CUDA graph of exactly `steps` steps, events on the capture stream"},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * steps,
+        "clocks": clk,
+        "breakdown": {
+            "sam_step_ns_per_seq_step": round(sam_ms * 1e6 / B, 1),
+            "verify_us_per_step": round(verify_ms * 1e3, 2),
+            "verify_algorithmic_GBps": round(achieved, 1),
+            "prefill_tokens_per_s": round(B * n / (prefill_ms / 1e3), 1),
+            "mean_accept_len": round(float(L.mean()), 4),
+            "mean_emitted_per_step": round(float(L.mean()) + 1, 4),
+        },
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def e2e_rs(batch, snap, pool, emit, emit_len, draft, dlen, mlen, mend, out, wsv, B, K, V, T, steps, dev):
+    """Same metric through the public API with host buffers: every step copies
+    its logits from pinned host memory and reads the emitted tokens back."""
+    import torch
+
+    import sam_drafting_verification_gb300 as ss
+    host_pool = [p.cpu().pin_memory() for p in pool[:4]]
+    dev_buf = torch.empty_like(pool[0])
+    host_emit = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    host_len = torch.empty(B, dtype=torch.int32).pin_memory()
+    batch.import_(snap)
+    emit_len.zero_()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(steps):
+        dev_buf.copy_(host_pool[s % len(host_pool)], non_blocking=True)
+        batch.step(emit, emit_len, K, out=(draft, dlen, mlen, mend))
+        ss.spec_verify(dev_buf, draft, dlen, temperature=T, seed=1002, step=s, out=out, emit=True,
+                       status=True, workspace=wsv)
+        host_emit.copy_(emit, non_blocking=True)
+        host_len.copy_(emit_len, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": round(B / (ms / 1e3), 1), "unit": "seq-steps/s",
+            "h2d_bytes_per_step": int(dev_buf.numel() * dev_buf.element_size()),
+            "d2h_bytes_per_step": int(host_emit.numel() * 4 + host_len.numel() * 4),
+            "ms_per_step": round(ms, 4), "steps": steps}
+
+
+class OracleLoop:
+    """The oracle as it stands, on a sample of the same workload: each sampled
+    sequence's automaton is built over its history (untimed); a step extends it
+    with the previously emitted tokens, drafts K and verifies the draft in fp64
+    against that step's logits (host-generated, same distribution, bf16-rounded)."""
+
+    def __init__(self, hist, cont, nseq, npool=4, seed=77):
+        import torch
+
+        import oracle
+        self.oracle = oracle
+        V, K = workloads.V_LARGE, 3
+        self.K, self.T, self.nseq, self.npool = K, 1.0, nseq, npool
+        rng = np.random.default_rng(seed)
+        self.rows = []
+        for p in range(npool):
+            x = workloads.gaussian_logits(rng, (nseq, K + 1, V), 2.0)
+            workloads.boost_truth(x, cont[:nseq, p * (K + 1):(p + 1) * (K + 1)], 4.0)
+            self.rows.append(workloads.to_bf16(x).float().numpy())
+        self.sams = [oracle.Sam(V) for _ in range(nseq)]
+        for b in range(nseq):
+            self.sams[b].extend(hist[b])
+        self.emit = [[] for _ in range(nseq)]
+
+    def seq_step(self, b, s):
+        K = self.K
+        self.sams[b].extend(self.emit[b])
+        d, dl, _, _ = self.sams[b].draft(K)
+        d = np.maximum(d, 0)[None]
+        rows = self.rows[s % self.npool][b:b + 1]
+        r = self.oracle.verify(rows, d, np.array([dl], np.int32), temperature=self.T, seed=1002,
+                               step=s, seq_index=np.array([b]))
+        L = int(r["accept_len"][0])
+        self.emit[b] = list(d[0, :L]) + [int(r["out_token"][0])]
+
+
+def cpu_baseline_rs(hist, cont, nseq=64, nsteps=40):
+    loop = OracleLoop(hist, cont, nseq)
+    t0 = time.perf_counter()
+    for s in range(nsteps):
+        for b in range(nseq):
+            loop.seq_step(b, s)
+    el = time.perf_counter() - t0
+    return {"value": round(nseq * nsteps / el, 2), "unit": "seq-steps/s", "cores": 1, "kind": "oracle",
+            "sample": f"{nseq} sequences x {nsteps} decode steps of the same workload "
+                      f"(extend + draft + fp64 verify, single thread), {el:.2f} s"}
+
+
+# --------------------------------------------------------------------------
+# verification sweep at B=1024
+# --------------------------------------------------------------------------
+
+def run_sweep(args, ws, rank, dev):
+    import torch
+
+    import sam_drafting_verification_gb300 as ss
+    B, V = 1024, workloads.V_LARGE
+    hbm, peak_kind = _peaks()
+    points = []
+    reps = max(args.steps, 1)
+    for K in (1, 3, 5, 8):
+        for dtype in (torch.float32, torch.bfloat16):
+            logits, draft = workloads.sweep_device(7000 + K + 100 * rank, B, K, V, dtype, dev)
+            full_draft = torch.argmax(logits[:, :K].float(), dim=-1).to(torch.int32).contiguous()
+            for T, name, dr in ((0.0, "greedy", draft), (1.0, "T=1", draft), (0.0, "greedy-full-read", full_draft)):
+                wsv = ss.verify_workspace(B, K, V, dev)
+                res = ss.spec_verify(logits, dr, None, temperature=T, seed=5, step=0, workspace=wsv)
+                for _ in range(args.warmup):
+                    ss.spec_verify(logits, dr, None, temperature=T, seed=5, step=0, out=res, workspace=wsv)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for r in range(reps):
+                    ss.spec_verify(logits, dr, None, temperature=T, seed=5, step=r, out=res, workspace=wsv)
+                e1.record()
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / reps
+                Lh = res["accept_len"].cpu().numpy().astype(np.int64)
+                alg = float((Lh + 1).sum()) * V * logits.element_size()
+                points.append({"K": K, "dtype": str(dtype).split(".")[-1], "mode": name,
+                               "us": round(ms * 1e3, 2), "seq_steps_per_s": round(B / (ms / 1e3), 1),
+                               "mean_accept": round(float(Lh.mean()), 4),
+                               "alg_GBps": round(alg / (ms / 1e3) / 1e9, 1),
+                               "frac": round(alg / (ms / 1e3) / 1e9 / hbm, 4)})
+            del logits, draft, full_draft
+            torch.cuda.empty_cache()
+    head = max(points, key=lambda p: p["frac"])
+    line = {"metric": METRIC, "value": head["seq_steps_per_s"], "unit": "seq-steps/s", "n_gpus": ws,
+            "steps": reps, "warmup": args.warmup, "ms_per_step": head["us"] / 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": "sweep_b1024", "B": B, "V": V},
+            "roofline": {"bound": "hbm", "achieved": head["alg_GBps"], "peak": hbm, "unit": "GB/s",
+                         "frac": head["frac"], "traffic": None, "peak_source": peak_kind},
+            "points": points}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# reference arm: the oracle
+# --------------------------------------------------------------------------
+
+def run_reference(args):
+    """The oracle arm: one step = one sequence's decode step (extend + draft +
+    fp64 verification) of the same workload, single-threaded on the host."""
+    ws, rank, local = _dist()
+    if rank != 0:
+        return
+    hist, cont = rs_inputs(0)
+    nseq = 8
+    loop = OracleLoop(hist, cont, nseq)
+    for s in range(max(args.warmup, 0)):
+        loop.seq_step(s % nseq, s // nseq)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        loop.seq_step(s % nseq, 1000 + s // nseq)
+    el = time.perf_counter() - t0
+    v = args.steps / el if el > 0 else 0.0
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": "seq-steps/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 / v, 3) if v else None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "rs_bf16_b64", "B_per_gpu": 64, "V": workloads.V_LARGE, "K": 3,
+                       "temperature": 1.0, "history": 4096},
+            "cpu_baseline": {"value": round(v, 2), "unit": "seq-steps/s", "cores": 1, "kind": "oracle",
+                             "sample": f"each step: one sequence's decode step, {nseq} sequences in turn"},
+            "e2e": {"value": round(v, 2), "unit": "seq-steps/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="rs_bf16_b64", choices=["rs_bf16_b64", "sweep_b1024"])
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "gb300":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,240 @@
+"""GB300-native SAM drafting and lossless speculative verification.
+
+Python face of libsamspec.so (C ABI in include/samspec.h).  The same names as
+the C entry points, over torch CUDA tensors:
+
+  SamBatch(B, capacity_tokens, vocab)   -- sam_batch_create / _destroy
+    .extend(tokens, n_new)              -- sam_extend
+    .draft(K)                           -- sam_draft
+    .step(tokens, n_new, K)             -- sam_step (extend + draft, one launch)
+    .status(), .reset(mask), .dump(b), .export(), .import_(blob)
+  spec_verify(target, draft, ...)       -- spec_verify
+  spec_uniforms(B, K, seed, step)       -- spec_uniforms
+
+Device memory (workspaces, inputs, outputs) comes from torch; each call is
+enqueued on torch's current CUDA stream.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _binding as _b
+from ._binding import (BF16, F32, ST_BADDRAFT, ST_BADROW, ST_CAPACITY, ST_HASHFULL,  # noqa: F401
+                       ST_LOOPCAP, ST_OK, ST_TIMEOUT, ST_TOKEN, SamspecError)
+
+__all__ = ["SamBatch", "spec_verify", "spec_uniforms", "SamspecError", "library_path"]
+
+
+def library_path() -> str:
+    return _b.LIB_PATH
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device=None):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _req(t, dtype, name, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+class SamBatch:
+    """B device-resident dynamic suffix automata (one per sequence)."""
+
+    def __init__(self, B: int, capacity_tokens: int, vocab: int, device=None):
+        self.lib = _b.lib()
+        self.B, self.C, self.V = int(B), int(capacity_tokens), int(vocab)
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        nbytes = self.lib.sam_batch_workspace_bytes(self.B, self.C)
+        if nbytes == 0:
+            raise SamspecError(f"sizes outside the limits: B={B}, capacity={capacity_tokens}")
+        self.ws_bytes = int(nbytes)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        h = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            _b.check(self.lib.sam_batch_create(self.B, self.C, self.V, _ptr(self.workspace),
+                                               self.ws_bytes, _stream(self.device), ctypes.byref(h)),
+                     "sam_batch_create")
+        self._h = h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            self.lib.sam_batch_destroy(h)
+            self._h = None
+
+    def reset(self, mask=None):
+        if mask is not None:
+            _req(mask, torch.int32, "mask", (self.B,))
+        _b.check(self.lib.sam_reset(self._h, _ptr(mask), _stream(self.device)), "sam_reset")
+
+    def extend(self, tokens, n_new):
+        _req(tokens, torch.int32, "tokens")
+        if tokens.dim() != 2 or tokens.shape[0] != self.B:
+            raise ValueError("tokens must be [B, max_new]")
+        _req(n_new, torch.int32, "n_new", (self.B,))
+        _b.check(self.lib.sam_extend(self._h, _ptr(tokens), _ptr(n_new), int(tokens.shape[1]),
+                                     _stream(self.device)), "sam_extend")
+
+    def _outs(self, K, out):
+        if out is None:
+            z = lambda *s: torch.empty(s, dtype=torch.int32, device=self.device)  # noqa: E731
+            out = (z(self.B, K), z(self.B), z(self.B), z(self.B))
+        d, dl, ml, me = out
+        _req(d, torch.int32, "draft", (self.B, K))
+        for t, n in ((dl, "draft_len"), (ml, "match_len"), (me, "min_endpos")):
+            if t is not None:
+                _req(t, torch.int32, n, (self.B,))
+        return out
+
+    def draft(self, K: int, out=None):
+        d, dl, ml, me = self._outs(K, out)
+        _b.check(self.lib.sam_draft(self._h, int(K), _ptr(d), _ptr(dl), _ptr(ml), _ptr(me),
+                                    _stream(self.device)), "sam_draft")
+        return d, dl, ml, me
+
+    def step(self, tokens, n_new, K: int, out=None):
+        _req(tokens, torch.int32, "tokens")
+        if tokens.dim() != 2 or tokens.shape[0] != self.B:
+            raise ValueError("tokens must be [B, max_new]")
+        _req(n_new, torch.int32, "n_new", (self.B,))
+        d, dl, ml, me = self._outs(K, out)
+        _b.check(self.lib.sam_step(self._h, _ptr(tokens), _ptr(n_new), int(tokens.shape[1]), int(K),
+                                   _ptr(d), _ptr(dl), _ptr(ml), _ptr(me), _stream(self.device)),
+                 "sam_step")
+        return d, dl, ml, me
+
+    def status(self):
+        import numpy as np
+        out = np.empty(self.B, np.int32)
+        _b.check(self.lib.sam_get_status(self._h, out.ctypes.data_as(ctypes.c_void_p),
+                                         _stream(self.device)), "sam_get_status")
+        return out
+
+    def export(self):
+        blob = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        _b.check(self.lib.sam_export(self._h, _ptr(blob), self.ws_bytes, _stream(self.device)),
+                 "sam_export")
+        return blob
+
+    def import_(self, blob):
+        _req(blob, torch.uint8, "blob")
+        _b.check(self.lib.sam_import(self._h, _ptr(blob), blob.numel(), _stream(self.device)),
+                 "sam_import")
+
+    def dump(self, b: int):
+        """Sequence b's automaton as numpy arrays (synchronises)."""
+        import numpy as np
+        sc = np.zeros(8, np.int32)
+        _b.check(self.lib.sam_dump_sequence(self._h, int(b), sc.ctypes.data_as(ctypes.c_void_p),
+                                            None, None, None, 0, None, 0, _stream(self.device)),
+                 "sam_dump_sequence")
+        ns, ne = int(sc[2]), int(sc[3])
+        ln = np.empty(max(ns, 1), np.int32)
+        lk = np.empty(max(ns, 1), np.int32)
+        me = np.empty(max(ns, 1), np.int32)
+        ed = np.empty((max(ne, 1), 3), np.int32)
+        vp = lambda a: a.ctypes.data_as(ctypes.c_void_p)  # noqa: E731
+        _b.check(self.lib.sam_dump_sequence(self._h, int(b), vp(sc), vp(ln), vp(lk), vp(me), ns,
+                                            vp(ed), ne, _stream(self.device)), "sam_dump_sequence")
+        return dict(n_tokens=int(sc[0]), last=int(sc[1]), n_states=ns, n_edges=ne,
+                    status=int(sc[4]), len=ln[:ns], link=lk[:ns], min_endpos=me[:ns],
+                    edges=ed[:ne])
+
+
+_ws_cache = {}
+
+
+def verify_workspace(B: int, K: int, V: int, device=None):
+    """A zero-initialised verification workspace, cached per (device, stream)."""
+    lib = _b.lib()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    need = int(lib.spec_verify_workspace_bytes(B, K, V))
+    key = (dev.index, torch.cuda.current_stream(dev).cuda_stream)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        _b.check(lib.spec_verify_workspace_init(_ptr(ws), ws.numel(), _stream(dev)),
+                 "spec_verify_workspace_init")
+        _ws_cache[key] = ws
+    return ws
+
+
+def spec_verify(target, draft, draft_len=None, temperature: float = 0.0, seed: int = 0,
+                step: int = 0, draft_logits=None, out=None, emit: bool = False,
+                status: bool = True, debug: bool = False, workspace=None):
+    """Verify K drafts per sequence against target logits [B, K+1, V].
+
+    Returns a dict of CUDA tensors: accept_len, out_token (+ emit, emit_len,
+    status, and the debug rows row_m, row_z, p_d, q_d, row_arg, res_mass)."""
+    lib = _b.lib()
+    if target.dim() != 3:
+        raise ValueError("target must be [B, K+1, V]")
+    B, K1, V = (int(x) for x in target.shape)
+    K = K1 - 1
+    dt = {torch.float32: F32, torch.bfloat16: BF16}.get(target.dtype)
+    if dt is None:
+        raise TypeError("target must be float32 or bfloat16")
+    _req(target, target.dtype, "target")
+    _req(draft, torch.int32, "draft", (B, K))
+    if draft_len is not None:
+        _req(draft_len, torch.int32, "draft_len", (B,))
+    ddt = F32
+    if draft_logits is not None:
+        ddt = {torch.float32: F32, torch.bfloat16: BF16}.get(draft_logits.dtype)
+        if ddt is None:
+            raise TypeError("draft_logits must be float32 or bfloat16")
+        _req(draft_logits, draft_logits.dtype, "draft_logits", (B, K, V))
+    dev = target.device
+    res = out if out is not None else {}
+
+    def need(key, shape, dtype=torch.int32, fill=None):
+        if key not in res:  # allocate only what the caller did not pass
+            res[key] = (torch.empty(shape, dtype=dtype, device=dev) if fill is None
+                        else torch.full(shape, fill, dtype=dtype, device=dev))
+
+    need("accept_len", (B,))
+    need("out_token", (B,))
+    if emit:
+        need("emit", (B, K1))
+        need("emit_len", (B,))
+    if status:
+        need("status", (B,))
+    dbg = None
+    if debug:
+        for k in ("row_m", "row_z", "p_d", "q_d"):
+            need(k, (B, K1), torch.float32, float("nan"))
+        need("row_arg", (B, K1), torch.int32, -1)
+        need("res_mass", (B,), torch.float32, float("nan"))
+        dbg = _b.VerifyDebug(*[res[k].data_ptr() for k in ("row_m", "row_z", "p_d", "q_d", "row_arg", "res_mass")])
+    ws = workspace if workspace is not None else verify_workspace(B, K, V, dev)
+    rc = lib.spec_verify(_ptr(target), dt, _ptr(draft_logits), ddt, _ptr(draft), _ptr(draft_len),
+                         B, K, V, float(temperature), int(seed) & (2**64 - 1), int(step) & (2**64 - 1),
+                         _ptr(res["accept_len"]), _ptr(res["out_token"]), _ptr(res.get("emit")),
+                         _ptr(res.get("emit_len")), _ptr(res.get("status")),
+                         ctypes.byref(dbg) if dbg is not None else None,
+                         _ptr(ws), ws.numel(), _stream(dev))
+    _b.check(rc, "spec_verify")
+    return res
+
+
+def spec_uniforms(B: int, K: int, seed: int, step: int, device=None):
+    """[B, K+1, 2] float32: (u_j, u'_j) exactly as spec_verify draws them."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    u = torch.empty((B, K + 1, 2), dtype=torch.float32, device=dev)
+    _b.check(_b.lib().spec_uniforms(int(B), int(K), int(seed) & (2**64 - 1), int(step) & (2**64 - 1),
+                                    _ptr(u), _stream(dev)), "spec_uniforms")
+    return u
