@@ -249,10 +249,12 @@ def run_gpu(args):
     _barrier(ws)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed")
     t0.record()
     g.replay()
     t1.record()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     _barrier(ws)
     total_ms = t0.elapsed_time(t1)
     clk = clocks.stop()
