@@ -430,11 +430,19 @@ def run_sweep(args, ws, rank, dev):
     hbm, peak_kind = _peaks()
     points = []
     reps = max(args.steps, 1)
+    only = None
+    if args.point:  # "K,dtype,mode", e.g. "3,bf16,T=1": one sweep point (profiling)
+        k_s, d_s, m_s = args.point.split(",")
+        only = (int(k_s), {"f32": torch.float32, "bf16": torch.bfloat16}[d_s], m_s)
     for K in (1, 3, 5, 8):
         for dtype in (torch.float32, torch.bfloat16):
+            if only and (only[0] != K or only[1] != dtype):
+                continue
             logits, draft = workloads.sweep_device(7000 + K + 100 * rank, B, K, V, dtype, dev)
             full_draft = torch.argmax(logits[:, :K].float(), dim=-1).to(torch.int32).contiguous()
             for T, name, dr in ((0.0, "greedy", draft), (1.0, "T=1", draft), (0.0, "greedy-full-read", full_draft)):
+                if only and only[2] != name:
+                    continue
                 wsv = ss.verify_workspace(B, K, V, dev)
                 res = ss.spec_verify(logits, dr, None, temperature=T, seed=5, step=0, workspace=wsv)
                 for _ in range(args.warmup):
@@ -508,6 +516,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="rs_bf16_b64", choices=["rs_bf16_b64", "sweep_b1024"])
+    ap.add_argument("--point", default="", help="sweep_b1024 only: one point 'K,f32|bf16,greedy|T=1|greedy-full-read'")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":
         args.warmup = 3

@@ -15,27 +15,26 @@
 //     the bonus sample is drawn from the target distribution itself.
 //
 // GB300 design.  A row of V = 151936 logits is 304-608 KB, so verification is
-// a streaming reduction bound by HBM.  Each CTA owns whole sequences (claimed
-// from a global counter) and walks their accept chains itself, so rows after
-// the first rejection are never read and no inter-CTA merge is needed:
-//   warp 16 (producer) claims sequences and issues 1-D bulk copies
-//       (cp.async.bulk, the TMA engine) of 32 KB vocab tiles into a ring of
-//       shared-memory stages, completion counted on mbarriers;
-//   warps 0-15 (consumers) each reduce a 1/16 slice of every tile from shared
-//       memory (16-byte vector reads) to a per-warp record -- max and sum of
-//       2^((l - max) log2(e)/T) with warp shuffles, or (max, argmax) -- and
-//       release the stage;
-//   warp 17 (control) merges the NC tile records of a finished row in fp64,
-//       draws the Philox coins, takes the accept/reject decision and posts the
-//       sequence's next job (next row, residual pass, or the one-tile CDF
-//       search), and writes the outputs.
-// Two sequence slots per CTA keep the producer streaming one sequence while
-// the other waits for its decision.  The resample needs only one tile: the
-// per-tile masses of the rejected row come from its statistics pass, so the
-// control warp finds the tile holding u' * sum(r) and a single tile is fetched
-// again (usually from L2) for the final scan.  Every wait is bounded by a
-// global-timer deadline; a CTA that runs out of time marks its sequences
-// SAMSPEC_ST_TIMEOUT, lets its copies in flight land and exits.
+// a streaming reduction bound by HBM.  Each CTA owns whole sequences and walks
+// their accept chains itself, so rows after the first rejection are never read
+// and no inter-CTA merge is needed:
+//   warp 16 (producer) issues 1-D bulk copies (cp.async.bulk, the TMA engine)
+//       of 32 KB vocab tiles of the rows its sequence slots ask for into a
+//       ring of shared-memory stages, completion counted on mbarriers;
+//   warps 0-15 (consumers) each reduce a 1/16 slice ("warp slice") of every
+//       tile from shared memory (16-byte vector reads) to a record -- the
+//       slice's max and sum of 2^((l - max) log2(e)/T), or its (max, first
+//       argmax) -- and release the stage;
+//   warp 17 (control) claims sequences from a global counter into four slots,
+//       merges the warp-slice records of a finished row in fp64, draws the
+//       Philox coins, decides accept/reject and posts the next row; after the
+//       final row it resamples: the slice records give the mass of every warp
+//       slice, so it finds the slice holding u' * sum(r) and scans just that
+//       2-8 KB slice, read again from L2, in ascending token order.
+// Four slots keep the producer streaming while the control warp decides.
+// Every wait is bounded by a global-timer deadline; a CTA that runs out of
+// time marks its sequences SAMSPEC_ST_TIMEOUT, lets its copies in flight land
+// and exits.
 
 #include <cstdint>
 #include <cstring>
@@ -55,11 +54,12 @@ constexpr int kCtrlWarp = kCW + 1;   // control warp
 constexpr int kThreads = (kCW + 2) * 32;
 constexpr int kStageBytes = 32768;
 constexpr int kMaxStages = 6;
-constexpr int kSlots = 2;
+constexpr int kMinStages = 3;
+constexpr int kSlots = 4;
 constexpr int kMaxChunks = 64;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 
-enum Kind : int32_t { kStats = 0, kResid = 1, kSearch = 2, kExit = 3, kInvalid = 4 };
+enum Kind : int32_t { kStats = 0, kResid = 1, kExit = 3 };
 enum State : int32_t { kEmpty = 0, kReady = 1, kIssued = 2, kDone = 3 };
 
 struct VParams {
@@ -88,23 +88,41 @@ struct Tag {
 
 struct Slot {
   int32_t state;  // State, accessed with volatile loads/stores
-  int32_t kind;   // kind of the current job
+  int32_t kind;   // kind of the current job (kStats: row j; kResid: row L)
   int32_t b, j, nb, L;
-  int32_t c0, c1;          // tiles [c0, c1) of the current job
-  int32_t cnt;             // warp records received for the current job
-  int32_t search_stage;    // stage holding the search tile (kept until scanned)
-  int32_t excl;            // token whose mass is removed (one-hot rejection), or -1
-  int32_t smode;           // 0: r in units of exp(x - m) (one-hot); 1: r = max(0, p - q)
+  int32_t cnt;    // warp records received for the current job
+  int32_t smode;  // residual pass: 1 -> max(0, p - q) in units of p;
+                  //                0 -> p in units of exp(x - m)
   float lmax, gmax, invZ, invZg;
-  double t_local;          // search target inside the chosen tile
-  double zrow;             // Z of the final row
-  double sum_r;            // residual mass, in the units of smode
+};
+
+struct Smem {
+  Slot slot[kSlots];
+  Tag tag[kMaxStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  int32_t stage_parity[kMaxStages];  // parity of the last issue per stage
+  int32_t ctrl_done;
+  int32_t abort;
+  int32_t prod_idle;  // the producer has issued every posted job
 };
 
 __device__ __forceinline__ uint64_t gtimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// NaN-propagating maxima
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 // ---- element access ---------------------------------------------------------
@@ -119,7 +137,7 @@ struct Vec {
     if (ES == 4) return __uint_as_float(w[k]);
     return (k & 1) ? bf16_hi(w[k >> 1]) : bf16_lo(w[k >> 1]);
   }
-  __device__ __forceinline__ void load_smem(const unsigned char* p) {
+  __device__ __forceinline__ void load16(const unsigned char* p) {
     if (kWords == 4) {
       const uint4 v = *reinterpret_cast<const uint4*>(p);
       w[0] = v.x; w[1] = v.y; w[2 % kWords] = v.z; w[3 % kWords] = v.w;
@@ -128,11 +146,14 @@ struct Vec {
       w[0] = v.x; w[1 % kWords] = v.y;
     }
   }
-  // element-wise global loads for rows without 16-byte alignment; elements at
-  // or beyond `valid` are not read (set to 0)
-  __device__ __forceinline__ void load_global(const unsigned char* p, int valid) {
+  __device__ __forceinline__ void zero() {
 #pragma unroll
     for (int q = 0; q < kWords; ++q) w[q] = 0;
+  }
+  // element-wise global loads for rows without 16-byte alignment; elements at
+  // or beyond `valid` are not read (set to 0)
+  __device__ __forceinline__ void load_elems(const unsigned char* p, int valid) {
+    zero();
 #pragma unroll
     for (int k = 0; k < VEC; ++k) {
       if (k < valid) {
@@ -144,6 +165,19 @@ struct Vec {
         }
       }
     }
+  }
+  // NaN-propagating maximum of the vector's elements
+  __device__ __forceinline__ float vmax() const {
+    if (ES == 4) {
+      float m = __uint_as_float(w[0]);
+#pragma unroll
+      for (int k = 1; k < VEC; ++k) m = fmax_nan(m, __uint_as_float(w[k]));
+      return m;
+    }
+    uint32_t a = w[0];
+#pragma unroll
+    for (int q = 1; q < kWords; ++q) a = bf16x2_max_nan(a, w[q]);
+    return fmax_nan(bf16_lo(a), bf16_hi(a));
   }
 };
 
@@ -168,75 +202,119 @@ struct Slice {
   Vec<(C::SD ? C::SD : 4), C::VEC> d[(DT >= 0) ? C::VPL : 1];
 };
 
-// Loads warp slice `w` of a tile for lane `lane` from the stage (bulk-copy
-// mode) or from global memory (direct mode).
-// The draft part is read only when the tile carries one (tg.has_draft).
+// Loads warp slice `w` of a staged tile (bulk-copy mode) or of the tile's
+// global rows (direct mode).  The draft part is read only when the tile
+// carries one.
 template <int TT, int DT>
-__device__ __forceinline__ void load_slice(Slice<TT, DT>& s, const VParams& P,
-                                           const unsigned char* stage, const Tag& tg, int w,
-                                           int lane) {
+__device__ __forceinline__ void load_slice_tile(Slice<TT, DT>& s, const VParams& P,
+                                                const unsigned char* stage, const Tag& tg, int w,
+                                                int lane) {
   using C = Cfg<TT, DT>;
 #pragma unroll
   for (int i = 0; i < C::VPL; ++i) {
     const int e = w * C::SL + (i * 32 + lane) * C::VEC;  // element index in the tile
     if (!P.direct) {
-      s.t[i].load_smem(stage + (size_t)e * C::ST);
-      if (DT >= 0 && tg.has_draft) s.d[i].load_smem(stage + C::DOFF + (size_t)e * C::SD);
+      s.t[i].load16(stage + (size_t)e * C::ST);
+      if (DT >= 0 && tg.has_draft) s.d[i].load16(stage + C::DOFF + (size_t)e * C::SD);
     } else {
       const int valid = tg.nel - e;
-      const size_t row_t = ((size_t)tg.b * (P.K + 1) + tg.j) * (size_t)P.V + tg.elem0 + e;
-      s.t[i].load_global(P.target + row_t * C::ST, valid);
+      const size_t rt = ((size_t)tg.b * (P.K + 1) + tg.j) * (size_t)P.V + tg.elem0 + e;
+      s.t[i].load_elems(P.target + rt * C::ST, valid);
       if (DT >= 0 && tg.has_draft) {
-        const size_t row_d = ((size_t)tg.b * P.K + tg.j) * (size_t)P.V + tg.elem0 + e;
-        s.d[i].load_global(P.draftl + row_d * C::SD, valid);
+        const size_t rd = ((size_t)tg.b * P.K + tg.j) * (size_t)P.V + tg.elem0 + e;
+        s.d[i].load_elems(P.draftl + rd * C::SD, valid);
       }
     }
   }
 }
 
+// Loads warp slice `w` of tile `c` of row L of sequence b straight from global
+// memory (the control warp's resample scan).  Returns the slice's element count.
+template <int TT, int DT>
+__device__ __forceinline__ int load_slice_global(Slice<TT, DT>& s, const VParams& P, int b, int L,
+                                                 int c, int w, bool with_draft, int lane) {
+  using C = Cfg<TT, DT>;
+  const int s0 = c * C::E_TILE + w * C::SL;
+  const size_t rt = ((size_t)b * (P.K + 1) + L) * (size_t)P.V;
+  const size_t rd = ((size_t)b * P.K + L) * (size_t)P.V;
+#pragma unroll
+  for (int i = 0; i < C::VPL; ++i) {
+    const int e = s0 + (i * 32 + lane) * C::VEC;  // vocab index
+    const int valid = P.V - e;
+    if (!P.direct) {
+      // aligned rows hold whole vectors: a vector is either in range or not
+      if (valid > 0) {
+        s.t[i].load16(P.target + (rt + e) * C::ST);
+        if (DT >= 0 && with_draft) s.d[i].load16(P.draftl + (rd + e) * C::SD);
+      } else {
+        s.t[i].zero();
+        if (DT >= 0) s.d[i].zero();
+      }
+    } else {
+      s.t[i].load_elems(P.target + (rt + e) * C::ST, valid);
+      if (DT >= 0) {
+        if (with_draft) s.d[i].load_elems(P.draftl + (rd + e) * C::SD, valid);
+        else s.d[i].zero();
+      }
+    }
+  }
+  const int n = P.V - s0;
+  return n < 0 ? 0 : (n > C::SL ? C::SL : n);
+}
+
 // ---- per-warp reductions over a slice ----------------------------------------
+// NaN-propagating lane maximum of one array over the valid elements
+template <int TT, int DT, bool FULL, bool DRAFT_ARRAY>
+__device__ __forceinline__ float lane_max(const Slice<TT, DT>& s, int w, int lane, int nel) {
+  using C = Cfg<TT, DT>;
+  float m = -__int_as_float(0x7f800000);
+#pragma unroll
+  for (int i = 0; i < C::VPL; ++i) {
+    if (FULL) {
+      m = fmax_nan(m, DRAFT_ARRAY ? s.d[i].vmax() : s.t[i].vmax());
+    } else {
+      const int e = w * C::SL + (i * 32 + lane) * C::VEC;
+#pragma unroll
+      for (int k = 0; k < C::VEC; ++k)
+        if (e + k < nel) m = fmax_nan(m, DRAFT_ARRAY ? s.d[i].at(k) : s.t[i].at(k));
+    }
+  }
+  return m;
+}
+
+// greedy record: {max, first index of the max, NaN seen}
 template <int TT, int DT, bool FULL>
 __device__ __forceinline__ float4 reduce_greedy(const Slice<TT, DT>& s, int w, int lane, int nel,
                                                 int elem0) {
   using C = Cfg<TT, DT>;
-  float best = -__int_as_float(0x7f800000);
-  int32_t bi = 0x7fffffff;
-  bool nan = false;
+  const float ml = lane_max<TT, DT, FULL, false>(s, w, lane, nel);
+  if (__any_sync(kFullMask, ml != ml)) return make_float4(0.f, __int_as_float(0x7fffffff), 1.f, 0.f);
+  const float M = warp_max(ml);
+  int32_t idx = 0x7fffffff;
+  if (ml == M) {  // only the lanes holding the maximum look for its first position
 #pragma unroll
-  for (int i = 0; i < C::VPL; ++i) {
-    const int e = w * C::SL + (i * 32 + lane) * C::VEC;
+    for (int i = 0; i < C::VPL; ++i) {
+      const int e = w * C::SL + (i * 32 + lane) * C::VEC;
 #pragma unroll
-    for (int k = 0; k < C::VEC; ++k) {
-      if (FULL || e + k < nel) {
-        const float x = s.t[i].at(k);
-        nan |= (x != x);
-        if (x > best) {
-          best = x;
-          bi = elem0 + e + k;
-        }
-      }
+      for (int k = 0; k < C::VEC; ++k)
+        if ((FULL || e + k < nel) && s.t[i].at(k) == M && idx == 0x7fffffff) idx = elem0 + e + k;
     }
   }
-  warp_argmax(best, bi);
-  const bool any_nan = __any_sync(kFullMask, nan);
-  return make_float4(best, __int_as_float(bi), any_nan ? 1.f : 0.f, 0.f);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(kFullMask, idx, o));
+  return make_float4(M, __int_as_float(idx), 0.f, 0.f);
 }
 
-// max and sum_x 2^((x - max) * cT) of one array of the slice
+// {max, sum_x 2^((x - max) * cT)} of one array; NaN in the slice -> {NaN, NaN}
 template <int TT, int DT, bool FULL, bool DRAFT_ARRAY>
 __device__ __forceinline__ float2 reduce_softmax(const Slice<TT, DT>& s, int w, int lane, int nel,
                                                  float cT) {
   using C = Cfg<TT, DT>;
   const float NEG_INF = -__int_as_float(0x7f800000);
-  float m = NEG_INF;
-#pragma unroll
-  for (int i = 0; i < C::VPL; ++i) {
-    const int e = w * C::SL + (i * 32 + lane) * C::VEC;
-#pragma unroll
-    for (int k = 0; k < C::VEC; ++k)
-      if (FULL || e + k < nel) m = fmaxf(m, DRAFT_ARRAY ? s.d[i].at(k) : s.t[i].at(k));
-  }
-  m = warp_max(m);
+  const float ml = lane_max<TT, DT, FULL, DRAFT_ARRAY>(s, w, lane, nel);
+  if (__any_sync(kFullMask, ml != ml))
+    return make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
+  const float m = warp_max(ml);
   float z = 0.f;
   if (m != NEG_INF) {
     float part[C::VPL];
@@ -249,7 +327,6 @@ __device__ __forceinline__ float2 reduce_softmax(const Slice<TT, DT>& s, int w, 
         const float x = DRAFT_ARRAY ? s.d[i].at(k) : s.t[i].at(k);
         v[k] = (FULL || e + k < nel) ? ex2_approx((x - m) * cT) : 0.f;
       }
-      // pairwise sum of the vector
 #pragma unroll
       for (int h = C::VEC / 2; h >= 1; h >>= 1)
 #pragma unroll
@@ -265,21 +342,7 @@ __device__ __forceinline__ float2 reduce_softmax(const Slice<TT, DT>& s, int w, 
   return make_float2(m, z);
 }
 
-// residual weight of one element (accurate exp2f: used where a CDF is read)
-template <int TT, int DT>
-__device__ __forceinline__ float resid_elem(const Slice<TT, DT>& s, int i, int k, int vocab,
-                                            const Slot& S, float cT) {
-  const float x = s.t[i].at(k);
-  const float pe = exp2f((x - S.lmax) * cT);
-  if (S.smode == 0) return vocab == S.excl ? 0.f : pe;
-  float g = 0.f;
-  if (DT >= 0) g = s.d[i].at(k);
-  const float qe = exp2f((g - S.gmax) * cT);
-  return fmaxf(0.f, pe * S.invZ - qe * S.invZg);
-}
-
-// residual weight with the fast exponential (statistics pass of the draft model's
-// residual mass)
+// residual-pass record: sum of r over the slice (fast exponential)
 template <int TT, int DT, bool FULL>
 __device__ __forceinline__ float reduce_resid(const Slice<TT, DT>& s, int w, int lane, int nel,
                                               const Slot& S, float cT) {
@@ -293,10 +356,14 @@ __device__ __forceinline__ float reduce_resid(const Slice<TT, DT>& s, int w, int
     for (int k = 0; k < C::VEC; ++k) {
       if (FULL || e + k < nel) {
         const float pe = ex2_approx((s.t[i].at(k) - S.lmax) * cT);
-        float g = 0.f;
-        if (DT >= 0) g = s.d[i].at(k);
-        const float qe = ex2_approx((g - S.gmax) * cT);
-        part += fmaxf(0.f, pe * S.invZ - qe * S.invZg);
+        if (S.smode == 0) {
+          part += pe;
+        } else {
+          float g = 0.f;
+          if (DT >= 0) g = s.d[i].at(k);
+          const float qe = ex2_approx((g - S.gmax) * cT);
+          part += fmaxf(0.f, pe * S.invZ - qe * S.invZg);
+        }
       }
     }
     acc += part;
@@ -304,19 +371,17 @@ __device__ __forceinline__ float reduce_resid(const Slice<TT, DT>& s, int w, int
   return warp_sum(acc);
 }
 
-template <int TT, int DT, bool FULL>
-__device__ __forceinline__ float reduce_search(const Slice<TT, DT>& s, int w, int lane, int nel,
-                                               int elem0, const Slot& S, float cT) {
-  using C = Cfg<TT, DT>;
-  float acc = 0.f;
-#pragma unroll
-  for (int i = 0; i < C::VPL; ++i) {
-    const int e = w * C::SL + (i * 32 + lane) * C::VEC;
-#pragma unroll
-    for (int k = 0; k < C::VEC; ++k)
-      if (FULL || e + k < nel) acc += resid_elem<TT, DT>(s, i, k, elem0 + e + k, S, cT);
-  }
-  return warp_sum(acc);
+// residual weight of one element with the accurate exponential (resample scan)
+template <int TT, int DT>
+__device__ __forceinline__ float resid_elem(const Slice<TT, DT>& s, int i, int k, int vocab,
+                                            int smode, int excl, float lmax, float gmax,
+                                            float invZ, float invZg, float cT) {
+  const float pe = exp2f((s.t[i].at(k) - lmax) * cT);
+  if (smode == 0) return vocab == excl ? 0.f : pe;
+  float g = 0.f;
+  if (DT >= 0) g = s.d[i].at(k);
+  const float qe = exp2f((g - gmax) * cT);
+  return fmaxf(0.f, pe * invZ - qe * invZg);
 }
 
 // ---- outputs ---------------------------------------------------------------
@@ -339,325 +404,120 @@ __device__ __forceinline__ float load_logit(const unsigned char* base, int es, s
   return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(base) + idx) << 16);
 }
 
-struct Smem {
-  Slot slot[kSlots];
-  Tag tag[kMaxStages];
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
-  int32_t prod_done;
-  int32_t abort;
-  int32_t stage_parity[kMaxStages];  // parity of the last issue per stage
-  double cmass[kSlots][kMaxChunks];  // tile masses of the last statistics row
-  float4 rec[kSlots][kMaxChunks][kCW];
-};
+// First lane in [0, n) whose inclusive running sum of v exceeds t, or -1;
+// *before receives the running sum ahead of that lane.
+__device__ __forceinline__ int warp_find(double v, double t, int n, int lane, double* before) {
+  const double x = lane < n ? v : 0.0;
+  const double incl = warp_incl_scan_d(x, lane);
+  const unsigned hit = __ballot_sync(kFullMask, lane < n && incl > t);
+  if (!hit) return -1;
+  const int src = __ffs(hit) - 1;
+  *before = __shfl_sync(kFullMask, incl, src) - __shfl_sync(kFullMask, x, src);
+  return src;
+}
 
-// ---- control warp: merge a finished job and decide --------------------------
+// ---- control warp ------------------------------------------------------------
 template <int TT, int DT, bool GREEDY>
-__device__ void control_handle(const VParams& P, Smem& sm, unsigned char* stages, int si,
-                               int lane) {
+struct Control {
   using C = Cfg<TT, DT>;
-  Slot& S = sm.slot[si];
-  const int b = S.b;
-  const double NEG_INF = -__longlong_as_double(0x7ff0000000000000ll);
+  const VParams& P;
+  Smem& sm;
+  const float4* rec;  // [kSlots][NC][kCW]
+  int lane;
+  bool more;
 
-  auto finish = [&](int L, int out, int st) {
+  __device__ Control(const VParams& p, Smem& s, const float4* r, int l)
+      : P(p), sm(s), rec(r), lane(l), more(true) {}
+
+  __device__ const float4& R(int si, int c, int w) const {
+    return rec[((size_t)si * P.NC + c) * kCW + w];
+  }
+
+  __device__ void finish(int b, int L, int out, int st) {
     if (lane == 0) write_result(P, b, L, out, st);
     __syncwarp();
-    __threadfence_block();
-    if (lane == 0) vstore(&S.state, kEmpty);
-    __syncwarp();
-  };
-  auto post = [&](int kind, int j, int c0, int c1) {
+  }
+
+  __device__ void post(int si, int kind, int j) {
+    Slot& S = sm.slot[si];
     if (lane == 0) {
       S.kind = kind;
       S.j = j;
-      S.c0 = c0;
-      S.c1 = c1;
       S.cnt = 0;
       __threadfence_block();
       vstore(&S.state, kReady);
     }
     __syncwarp();
-  };
-
-  if (S.kind == kInvalid) {
-    finish(-1, -1, SAMSPEC_ST_BADDRAFT);
-    return;
-  }
-  const int j = S.j;
-  const int NC = P.NC;
-
-  if (S.kind == kStats && GREEDY) {
-    float best = -__int_as_float(0x7f800000);
-    int32_t bi = 0x7fffffff;
-    bool nan = false;
-    for (int c = lane; c < NC; c += 32)
-      for (int w = 0; w < kCW; ++w) {
-        const float4 r = sm.rec[si][c][w];
-        const int32_t ri = __float_as_int(r.y);
-        nan |= r.z != 0.f;
-        if (r.x > best || (r.x == best && ri < bi)) {
-          best = r.x;
-          bi = ri;
-        }
-      }
-    warp_argmax(best, bi);
-    nan = __any_sync(kFullMask, nan);
-    const size_t ro = (size_t)b * (P.K + 1) + j;
-    if (lane == 0) {
-      if (P.dbg.row_m) P.dbg.row_m[ro] = best;
-      if (P.dbg.row_arg) P.dbg.row_arg[ro] = (nan || bi == 0x7fffffff) ? -1 : bi;
-    }
-    if (nan || bi == 0x7fffffff) {
-      finish(-1, -1, SAMSPEC_ST_BADROW);
-      return;
-    }
-    if (j < S.nb && P.draft[(size_t)b * P.K + j] == bi) {
-      post(kStats, j + 1, 0, NC);
-      return;
-    }
-    finish(j, bi, 0);
-    return;
   }
 
-  if (S.kind == kStats) {
-    // --- temperature softmax statistics of row j ([P3] SGLang 的实现) ---
-    float lm = -__int_as_float(0x7f800000), gm = lm;
-    for (int c = lane; c < NC; c += 32)
-      for (int w = 0; w < kCW; ++w) {
-        lm = fmaxf(lm, sm.rec[si][c][w].x);
-        if (DT >= 0) gm = fmaxf(gm, sm.rec[si][c][w].z);
-      }
-    lm = warp_max(lm);
-    if (DT >= 0) gm = warp_max(gm);
-    double zt = 0.0, zg = 0.0;
-    double cm_lane[2] = {0.0, 0.0};
-    for (int c = lane, q = 0; c < NC; c += 32, ++q) {
-      double mass = 0.0, gmass = 0.0;
-      for (int w = 0; w < kCW; ++w) {
-        const float4 r = sm.rec[si][c][w];
-        if (r.y != 0.f) mass += (double)r.y * (double)exp2f((r.x - lm) * P.cT);
-        if (r.y != r.y) mass += (double)r.y;  // keep NaN visible
-        if (DT >= 0) {
-          if (r.w != 0.f) gmass += (double)r.w * (double)exp2f((r.z - gm) * P.cT);
-          if (r.w != r.w) gmass += (double)r.w;
-        }
-      }
-      sm.cmass[si][c] = mass;
-      if (q < 2) cm_lane[q] = mass;
-      zt += mass;
-      zg += gmass;
-    }
-    zt = warp_sum_d(zt);
-    if (DT >= 0) zg = warp_sum_d(zg);
-    const size_t ro = (size_t)b * (P.K + 1) + j;
-    const bool bad_t = !(lm > NEG_INF) || isinf(lm) || !isfinite(zt) || !(zt > 0.0);
-    const bool bad_g = DT >= 0 && j < S.nb && (!(gm > NEG_INF) || isinf(gm) || !isfinite(zg) || !(zg > 0.0));
-    if (lane == 0) {
-      if (P.dbg.row_m) P.dbg.row_m[ro] = lm / P.T;
-      if (P.dbg.row_z) P.dbg.row_z[ro] = (float)zt;
-    }
-    if (bad_t || bad_g) {
-      finish(-1, -1, SAMSPEC_ST_BADROW);
-      return;
-    }
-    double pd = 0.0, ed = 0.0, qd = 1.0;
-    int32_t d = -1;
-    if (j < S.nb) {
-      d = P.draft[(size_t)b * P.K + j];
-      const float ld = load_logit(P.target, C::ST, ((size_t)b * (P.K + 1) + j) * P.V + d);
-      ed = exp(((double)ld - (double)lm) / P.Td);
-      pd = ed / zt;
-      if (DT >= 0) {
-        const float gd = load_logit(P.draftl, C::SD, ((size_t)b * P.K + j) * P.V + d);
-        qd = exp(((double)gd - (double)gm) / P.Td) / zg;
-      }
-      float ua, ur;
-      verify_coins(P.seed, P.step, (uint32_t)b, (uint32_t)j, &ua, &ur);
-      if (lane == 0) {
-        if (P.dbg.p_d) P.dbg.p_d[ro] = (float)pd;
-        if (P.dbg.q_d) P.dbg.q_d[ro] = (float)qd;
-      }
-      // accept iff u * q(d) <= p(d)  ([P1] §1.1 eps <= alpha(x); [P2] §2.2)
-      if ((double)ua * qd <= pd) {
-        post(kStats, j + 1, 0, NC);
-        return;
-      }
-    }
-    // j is the final row: rejected (j < nb) or the bonus row (j == nb)
-    float ua, ur;
-    verify_coins(P.seed, P.step, (uint32_t)b, (uint32_t)j, &ua, &ur);
-    if (lane == 0) {
-      S.L = j;
-      S.lmax = lm;
-      S.gmax = gm;
-      S.invZ = (float)(1.0 / zt);
-      S.invZg = DT >= 0 ? (float)(1.0 / zg) : 0.f;
-      S.zrow = zt;
-    }
+  __device__ void release(int si) {
+    if (lane == 0) vstore(&sm.slot[si].state, kEmpty);
     __syncwarp();
-    if (DT >= 0 && j < S.nb) {
-      // residual max(0, p - q) needs both rows' full statistics: one more pass
-      if (lane == 0) S.smode = 1;
-      post(kResid, j, 0, NC);
+  }
+
+  // Claims sequences until one with valid drafts lands in slot si (or none
+  // are left: the slot becomes empty).
+  __device__ void refill(int si) {
+    Slot& S = sm.slot[si];
+    while (more) {
+      uint32_t b = 0;
+      if (lane == 0) b = atomicAdd(&P.ws[0], 1u);
+      b = __shfl_sync(kFullMask, b, 0);
+      if (b >= (uint32_t)P.B) {
+        more = false;
+        break;
+      }
+      const int nb = P.draft_len ? P.draft_len[b] : P.K;
+      bool bad = nb < 0 || nb > P.K;
+      if (!bad && lane < nb) {
+        const int32_t d = P.draft[(size_t)b * P.K + lane];
+        bad = d < 0 || d >= P.V;
+      }
+      if (__any_sync(kFullMask, bad)) {
+        finish((int)b, -1, -1, SAMSPEC_ST_BADDRAFT);
+        continue;
+      }
+      if (lane == 0) {
+        S.b = (int32_t)b;
+        S.nb = nb;
+        S.L = 0;
+      }
+      post(si, kStats, 0);
       return;
     }
-    // one-hot rejection: r = p with the rejected token removed; bonus: r = p.
-    // Units: exp(x - m) (the row's Z is their total).
-    int excl = -1;
-    double sum_r = zt;
-    if (j < S.nb) {
-      excl = d;
-      const int cd = d / C::E_TILE;
-      sum_r = zt - ed;
-      if (sum_r > 0.0) {
-        if ((cd & 31) == lane) {
-          const double nm = cm_lane[cd >> 5] - ed;
-          cm_lane[cd >> 5] = nm > 0.0 ? nm : 0.0;
-        }
-      } else {
-        excl = -1;  // residual of zero mass: fall back to p
-        sum_r = zt;
-      }
-    }
-    const double t = (double)ur * sum_r;
-    // first tile whose running mass exceeds t
-    double base = 0.0;
-    int cstar = -1;
-    double tloc = 0.0;
-    for (int q = 0; q * 32 < NC && q < 2; ++q) {
-      const double mine = cm_lane[q];
-      const double incl = warp_incl_scan_d(mine, lane) + base;
-      const unsigned hit = __ballot_sync(kFullMask, (q * 32 + lane) < NC && incl > t);
-      if (hit) {
-        const int src = __ffs(hit) - 1;
-        cstar = q * 32 + src;
-        tloc = t - (__shfl_sync(kFullMask, incl, src) - __shfl_sync(kFullMask, mine, src));
-        break;
-      }
-      base = __shfl_sync(kFullMask, incl, 31);
-    }
-    if (cstar < 0) {  // rounding left the total at or below t: last tile with mass
-      int lastc = -1;
-      for (int q = 0; q * 32 < NC && q < 2; ++q) {
-        const unsigned pos = __ballot_sync(kFullMask, (q * 32 + lane) < NC && cm_lane[q] > 0.0);
-        if (pos) lastc = q * 32 + 31 - __clz(pos);
-      }
-      cstar = lastc < 0 ? 0 : lastc;
-      const double mc = __shfl_sync(kFullMask, cm_lane[cstar >> 5], cstar & 31);
-      tloc = mc;  // past the end: the scan falls back to the last positive entry
-    }
-    if (lane == 0) {
-      S.excl = excl;
-      S.smode = 0;
-      S.t_local = tloc;
-      S.sum_r = sum_r;
-      if (P.dbg.res_mass) P.dbg.res_mass[b] = (float)(sum_r / zt);
-    }
-    post(kSearch, j, cstar, cstar + 1);
-    return;
+    if (lane == 0) vstore(&S.state, kEmpty);
+    __syncwarp();
   }
 
-  if (S.kind == kResid) {
-    // residual mass per tile (units of p) from the second pass over row L
-    double cm_lane[2] = {0.0, 0.0};
-    double tot = 0.0;
-    for (int c = lane, q = 0; c < NC; c += 32, ++q) {
-      double m = 0.0;
-      for (int w = 0; w < kCW; ++w) m += (double)sm.rec[si][c][w].x;
-      if (q < 2) cm_lane[q] = m;
-      tot += m;
-    }
-    tot = warp_sum_d(tot);
-    float ua, ur;
-    verify_coins(P.seed, P.step, (uint32_t)b, (uint32_t)S.L, &ua, &ur);
-    int smode = 1;
-    double sum_r = tot;
-    if (!(tot > 0.0) || !isfinite(tot)) {
-      // zero residual: sample p itself from the statistics pass's tile masses
-      smode = 0;
-      sum_r = S.zrow;
-      for (int c = lane, q = 0; c < NC && q < 2; c += 32, ++q) cm_lane[q] = sm.cmass[si][c];
-    }
-    const double t = (double)ur * sum_r;
-    double base = 0.0;
-    int cstar = -1;
-    double tloc = 0.0;
-    for (int q = 0; q * 32 < NC && q < 2; ++q) {
-      const double mine = cm_lane[q];
-      const double incl = warp_incl_scan_d(mine, lane) + base;
-      const unsigned hit = __ballot_sync(kFullMask, (q * 32 + lane) < NC && incl > t);
-      if (hit) {
-        const int src = __ffs(hit) - 1;
-        cstar = q * 32 + src;
-        tloc = t - (__shfl_sync(kFullMask, incl, src) - __shfl_sync(kFullMask, mine, src));
-        break;
-      }
-      base = __shfl_sync(kFullMask, incl, 31);
-    }
-    if (cstar < 0) {
-      int lastc = -1;
-      for (int q = 0; q * 32 < NC && q < 2; ++q) {
-        const unsigned pos = __ballot_sync(kFullMask, (q * 32 + lane) < NC && cm_lane[q] > 0.0);
-        if (pos) lastc = q * 32 + 31 - __clz(pos);
-      }
-      cstar = lastc < 0 ? 0 : lastc;
-      tloc = __shfl_sync(kFullMask, cm_lane[cstar >> 5], cstar & 31);
-    }
-    if (lane == 0) {
-      S.smode = smode;
-      S.excl = -1;
-      S.t_local = tloc;
-      S.sum_r = sum_r;
-      if (P.dbg.res_mass) P.dbg.res_mass[b] = (float)(smode ? sum_r : 1.0);
-    }
-    post(kSearch, S.L, cstar, cstar + 1);
-    return;
-  }
-
-  if (S.kind == kSearch) {
-    // --- CDF scan inside the chosen tile, ascending token id ---
-    const int stg = S.search_stage;
-    const Tag tg = sm.tag[stg];
-    const unsigned char* stage = stages + (size_t)stg * kStageBytes;
-    const double t = S.t_local;
-    const float rw = lane < kCW ? sm.rec[si][0][lane].x : 0.f;
-    const double incl = warp_incl_scan_d((double)rw, lane);
-    unsigned hit = __ballot_sync(kFullMask, lane < kCW && incl > t);
-    int ws;
-    double tw;
-    if (hit) {
-      ws = __ffs(hit) - 1;
-      tw = t - (__shfl_sync(kFullMask, incl, ws) - __shfl_sync(kFullMask, (double)rw, ws));
-    } else {
-      const unsigned pos = __ballot_sync(kFullMask, lane < kCW && rw > 0.f);
-      ws = pos ? 31 - __clz(pos) : 0;
-      tw = 1e300;  // past the end of the slice: take its last positive entry
-    }
+  // Resample scan of warp slice (c, w) of row L: the first token whose running
+  // residual exceeds t (ascending token id), with the accurate exponential.
+  __device__ int slice_scan(int b, int L, int c, int w, double t, int smode, int excl, float lmax,
+                            float gmax, float invZ, float invZg) {
     Slice<TT, DT> sl;
-    load_slice<TT, DT>(sl, P, stage, tg, ws, lane);
-    // per-vector sums in index order: vector i of lane l covers slice elements
-    // (i * 32 + l) * VEC .. + VEC - 1
-    int token = -1;
-    double tt = tw;
-    int last_pos = -1;
+    const bool with_draft = DT >= 0 && smode == 1;
+    const int n = load_slice_global<TT, DT>(sl, P, b, L, c, w, with_draft, lane);
+    const int s0 = c * C::E_TILE + w * C::SL;
+    int token = -1, last_pos = -1;
+    double tt = t;
 #pragma unroll
     for (int i = 0; i < C::VPL; ++i) {
-      const int e = ws * C::SL + (i * 32 + lane) * C::VEC;
+      const int e = (i * 32 + lane) * C::VEC;  // index inside the slice
       float r[C::VEC];
       double s_l = 0.0;
 #pragma unroll
       for (int k = 0; k < C::VEC; ++k) {
-        r[k] = (e + k < tg.nel) ? resid_elem<TT, DT>(sl, i, k, tg.elem0 + e + k, S, P.cT) : 0.f;
+        r[k] = (e + k < n) ? resid_elem<TT, DT>(sl, i, k, s0 + e + k, smode, excl, lmax, gmax,
+                                                invZ, invZg, P.cT)
+                           : 0.f;
         s_l += (double)r[k];
-        if (r[k] > 0.f) last_pos = tg.elem0 + e + k;
+        if (r[k] > 0.f) last_pos = s0 + e + k;
       }
       const double li = warp_incl_scan_d(s_l, lane);
       const double row_total = __shfl_sync(kFullMask, li, 31);
       if (token < 0 && row_total > tt) {
         const unsigned h2 = __ballot_sync(kFullMask, li > tt);
         const int ls = __ffs(h2) - 1;
-        double tl = tt - (__shfl_sync(kFullMask, li, ls) - __shfl_sync(kFullMask, s_l, ls));
+        const double tl = tt - (__shfl_sync(kFullMask, li, ls) - __shfl_sync(kFullMask, s_l, ls));
         int found = -1;
         if (lane == ls) {
           double acc = 0.0;
@@ -671,32 +531,255 @@ __device__ void control_handle(const VParams& P, Smem& sm, unsigned char* stages
             }
           }
           if (found < 0) found = lastk;
-          if (found >= 0) found = tg.elem0 + e + found;
+          if (found >= 0) found = s0 + e + found;
         }
         found = __shfl_sync(kFullMask, found, ls);
         if (found >= 0) token = found;
       }
       if (token < 0) tt -= row_total;
     }
-    if (token < 0) {  // fell off the end: last positive entry of the slice / tile
-      int lp = last_pos;
+    if (token < 0) {  // rounding put t past the slice: its last positive entry
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(kFullMask, lp, o));
-      token = lp >= 0 ? lp : tg.elem0 + ws * C::SL;
+      for (int o = 16; o > 0; o >>= 1)
+        last_pos = max(last_pos, __shfl_xor_sync(kFullMask, last_pos, o));
+      token = last_pos >= 0 ? last_pos : s0;
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive_cnt(&sm.empty[stg], kCW);  // release the held stage
-    finish(S.L, token, 0);
-    return;
+    return token;
   }
-}
+
+  // Picks the warp slice holding t from per-tile masses (cm, two per lane:
+  // tiles lane and lane + 32) and the per-slice masses of the chosen tile,
+  // then scans it.
+  template <typename SliceMass>
+  __device__ int resample(int b, int L, double t, const double* cm, SliceMass slice_mass,
+                          int smode, int excl, float lmax, float gmax, float invZ, float invZg) {
+    const int NC = P.NC;
+    int cstar = -1;
+    double base = 0.0, before = 0.0;
+    for (int q = 0; q < 2 && q * 32 < NC; ++q) {
+      const int f = warp_find(cm[q], t - base, NC - q * 32, lane, &before);
+      if (f >= 0) {
+        cstar = q * 32 + f;
+        before += base;
+        break;
+      }
+      base += warp_sum_d((q * 32 + lane) < NC ? cm[q] : 0.0);
+    }
+    double tc;
+    if (cstar < 0) {  // rounding left the total at or below t: last tile with mass
+      int lastc = 0;
+      for (int q = 0; q < 2 && q * 32 < NC; ++q) {
+        const unsigned pos = __ballot_sync(kFullMask, (q * 32 + lane) < NC && cm[q] > 0.0);
+        if (pos) lastc = q * 32 + 31 - __clz(pos);
+      }
+      cstar = lastc;
+      tc = 1e300;
+    } else {
+      tc = t - before;
+    }
+    const double sm_w = lane < kCW ? slice_mass(cstar, lane) : 0.0;
+    double bw = 0.0;
+    int wstar = warp_find(sm_w, tc, kCW, lane, &bw);
+    double tw;
+    if (wstar < 0) {
+      const unsigned pos = __ballot_sync(kFullMask, lane < kCW && sm_w > 0.0);
+      wstar = pos ? 31 - __clz(pos) : 0;
+      tw = 1e300;
+    } else {
+      tw = tc - bw;
+    }
+    return slice_scan(b, L, cstar, wstar, tw, smode, excl, lmax, gmax, invZ, invZg);
+  }
+
+  __device__ void handle(int si) {
+    Slot& S = sm.slot[si];
+    const int b = S.b, j = S.j, nb = S.nb;
+    const int NC = P.NC;
+    const size_t ro = (size_t)b * (P.K + 1) + j;
+
+    if (GREEDY) {
+      float best = -__int_as_float(0x7f800000);
+      int32_t bi = 0x7fffffff;
+      bool nan = false;
+      for (int c = lane; c < NC; c += 32)
+        for (int w = 0; w < kCW; ++w) {
+          const float4 r = R(si, c, w);
+          const int32_t ri = __float_as_int(r.y);
+          nan |= r.z != 0.f;
+          if (r.x > best || (r.x == best && ri < bi)) {
+            best = r.x;
+            bi = ri;
+          }
+        }
+      warp_argmax(best, bi);
+      nan = __any_sync(kFullMask, nan);
+      const bool bad = nan || bi == 0x7fffffff || best == -__int_as_float(0x7f800000);
+      if (lane == 0) {
+        if (P.dbg.row_m) P.dbg.row_m[ro] = best;
+        if (P.dbg.row_arg) P.dbg.row_arg[ro] = bad ? -1 : bi;
+      }
+      if (bad) {
+        finish(b, -1, -1, SAMSPEC_ST_BADROW);
+        release(si);
+        return;
+      }
+      if (j < nb && P.draft[(size_t)b * P.K + j] == bi) {
+        post(si, kStats, j + 1);
+        return;
+      }
+      finish(b, j, bi, 0);
+      release(si);
+      return;
+    }
+
+    if (S.kind == kStats) {
+      // --- temperature-softmax statistics of row j ---
+      float lm = -__int_as_float(0x7f800000), gm = lm;
+      for (int c = lane; c < NC; c += 32)
+        for (int w = 0; w < kCW; ++w) {
+          const float4 r = R(si, c, w);
+          lm = fmaxf(lm, r.x);
+          if (DT >= 0) gm = fmaxf(gm, r.z);
+        }
+      lm = warp_max(lm);
+      if (DT >= 0) gm = warp_max(gm);
+      const float cT = P.cT;
+      // slice mass in units of exp(x - lm); a NaN slice keeps its NaN
+      auto mass_of = [&](const float4& r) -> double {
+        return r.y == 0.f ? 0.0 : (double)r.y * (double)exp2f((r.x - lm) * cT);
+      };
+      double cm[2] = {0.0, 0.0};
+      double zt = 0.0, zg = 0.0;
+      for (int c = lane, q = 0; c < NC; c += 32, ++q) {
+        double m = 0.0, g = 0.0;
+        for (int w = 0; w < kCW; ++w) {
+          const float4 r = R(si, c, w);
+          m += mass_of(r);
+          if (DT >= 0 && r.w != 0.f) g += (double)r.w * (double)exp2f((r.z - gm) * cT);
+        }
+        if (q < 2) cm[q] = m;
+        zt += m;
+        zg += g;
+      }
+      zt = warp_sum_d(zt);
+      if (DT >= 0) zg = warp_sum_d(zg);
+      const float NEG_INF = -__int_as_float(0x7f800000);
+      const bool bad_t = !(lm > NEG_INF) || isinf(lm) || !isfinite(zt) || !(zt > 0.0);
+      const bool bad_g = DT >= 0 && j < nb &&
+                         (!(gm > NEG_INF) || isinf(gm) || !isfinite(zg) || !(zg > 0.0));
+      if (lane == 0) {
+        if (P.dbg.row_m) P.dbg.row_m[ro] = lm / P.T;
+        if (P.dbg.row_z) P.dbg.row_z[ro] = (float)zt;
+      }
+      if (bad_t || bad_g) {
+        finish(b, -1, -1, SAMSPEC_ST_BADROW);
+        release(si);
+        return;
+      }
+      float ua, ur;
+      verify_coins(P.seed, P.step, (uint32_t)b, (uint32_t)j, &ua, &ur);
+      int32_t d = -1;
+      double ed = 0.0;
+      if (j < nb) {
+        d = P.draft[(size_t)b * P.K + j];
+        const float ld = load_logit(P.target, C::ST, ro * P.V + d);
+        ed = exp(((double)ld - (double)lm) / P.Td);
+        const double pd = ed / zt;
+        double qd = 1.0;
+        if (DT >= 0) {
+          const float gd = load_logit(P.draftl, C::SD, ((size_t)b * P.K + j) * P.V + d);
+          qd = exp(((double)gd - (double)gm) / P.Td) / zg;
+        }
+        if (lane == 0) {
+          if (P.dbg.p_d) P.dbg.p_d[ro] = (float)pd;
+          if (P.dbg.q_d) P.dbg.q_d[ro] = (float)qd;
+        }
+        // accept iff u * q(d) <= p(d)  (eps <= alpha(x) with alpha = min(1, p/q))
+        if ((double)ua * qd <= pd) {
+          post(si, kStats, j + 1);
+          return;
+        }
+      }
+      // j is the final row L: rejected (j < nb) or the bonus row (j == nb)
+      if (DT >= 0 && j < nb) {
+        // residual max(0, p - q) needs both rows' full statistics: one more pass
+        if (lane == 0) {
+          S.L = j;
+          S.lmax = lm;
+          S.gmax = gm;
+          S.invZ = (float)(1.0 / zt);
+          S.invZg = (float)(1.0 / zg);
+          S.smode = 1;
+        }
+        post(si, kResid, j);
+        return;
+      }
+      // one-hot rejection: r = p without the rejected token; bonus: r = p.
+      // Units: exp(x - m); the row's Z is their total.
+      int excl = -1;
+      double sum_r = zt;
+      int cd = -1, wd = -1;
+      if (j < nb && zt - ed > 0.0) {
+        excl = d;
+        sum_r = zt - ed;
+        cd = d / C::E_TILE;
+        wd = (d - cd * C::E_TILE) / C::SL;
+        if ((cd & 31) == lane && (cd >> 5) < 2) {
+          const double nm = cm[cd >> 5] - ed;
+          cm[cd >> 5] = nm > 0.0 ? nm : 0.0;
+        }
+      }
+      if (lane == 0 && P.dbg.res_mass) P.dbg.res_mass[b] = (float)(sum_r / zt);
+      const double t = (double)ur * sum_r;
+      auto slice_mass = [&](int c, int w) -> double {
+        double m = mass_of(R(si, c, w));
+        if (c == cd && w == wd) m = m - ed > 0.0 ? m - ed : 0.0;
+        return m;
+      };
+      const int out = resample(b, j, t, cm, slice_mass, 0, excl, lm, gm, 0.f, 0.f);
+      finish(b, j, out, 0);
+      release(si);
+      return;
+    }
+
+    // kResid: per-slice residual masses of row L from the second pass
+    const int L = S.L;
+    double cm[2] = {0.0, 0.0};
+    double tot = 0.0;
+    for (int c = lane, q = 0; c < NC; c += 32, ++q) {
+      double m = 0.0;
+      for (int w = 0; w < kCW; ++w) m += (double)R(si, c, w).x;
+      if (q < 2) cm[q] = m;
+      tot += m;
+    }
+    tot = warp_sum_d(tot);
+    if (S.smode == 1 && (!(tot > 0.0) || !isfinite(tot))) {
+      // zero residual (impossible in exact arithmetic): sample p instead
+      if (lane == 0) S.smode = 0;
+      post(si, kResid, L);
+      return;
+    }
+    float ua, ur;
+    verify_coins(P.seed, P.step, (uint32_t)b, (uint32_t)L, &ua, &ur);
+    if (lane == 0 && P.dbg.res_mass) P.dbg.res_mass[b] = (float)(S.smode ? tot : 1.0);
+    const double t = (double)ur * tot;
+    auto slice_mass = [&](int c, int w) -> double { return (double)R(si, c, w).x; };
+    const int out =
+        resample(b, L, t, cm, slice_mass, S.smode, -1, S.lmax, S.gmax, S.invZ, S.invZg);
+    finish(b, L, out, 0);
+    release(si);
+  }
+};
 
 template <int TT, int DT, bool GREEDY>
 __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
   using C = Cfg<TT, DT>;
   extern __shared__ __align__(1024) unsigned char dsm[];
   Smem& sm = *reinterpret_cast<Smem*>(dsm);
-  unsigned char* stages = dsm + ((sizeof(Smem) + 1023) & ~(size_t)1023);
+  const size_t rec_off = (sizeof(Smem) + 15) & ~(size_t)15;
+  float4* rec = reinterpret_cast<float4*>(dsm + rec_off);
+  const size_t rec_bytes = (size_t)kSlots * P.NC * kCW * sizeof(float4);
+  unsigned char* stages = dsm + ((rec_off + rec_bytes + 1023) & ~(size_t)1023);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int NS = P.NS;
@@ -711,8 +794,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       sm.slot[s].state = kEmpty;
       sm.slot[s].cnt = 0;
     }
-    sm.prod_done = 0;
+    sm.ctrl_done = 0;
     sm.abort = 0;
+    sm.prod_idle = 0;
     mbar_fence_init();
   }
   __syncthreads();
@@ -739,44 +823,37 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       Slot& S = sm.slot[tg.slot];
       const unsigned char* stage = stages + (size_t)cs * kStageBytes;
       Slice<TT, DT> sl;
-      load_slice<TT, DT>(sl, P, stage, tg, warp, lane);
-      if (tg.kind != kSearch) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[cs]);
-      }
+      load_slice_tile<TT, DT>(sl, P, stage, tg, warp, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[cs]);
       const bool full = tg.nel == C::E_TILE;
-      float4 rec = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
       if (tg.kind == kStats) {
         if (GREEDY) {
-          rec = full ? reduce_greedy<TT, DT, true>(sl, warp, lane, tg.nel, tg.elem0)
-                     : reduce_greedy<TT, DT, false>(sl, warp, lane, tg.nel, tg.elem0);
+          r = full ? reduce_greedy<TT, DT, true>(sl, warp, lane, tg.nel, tg.elem0)
+                   : reduce_greedy<TT, DT, false>(sl, warp, lane, tg.nel, tg.elem0);
         } else {
           const float2 a = full ? reduce_softmax<TT, DT, true, false>(sl, warp, lane, tg.nel, P.cT)
                                 : reduce_softmax<TT, DT, false, false>(sl, warp, lane, tg.nel, P.cT);
-          rec.x = a.x;
-          rec.y = a.y;
+          r.x = a.x;
+          r.y = a.y;
           if (DT >= 0 && tg.has_draft) {
             const float2 g = full ? reduce_softmax<TT, DT, true, true>(sl, warp, lane, tg.nel, P.cT)
                                   : reduce_softmax<TT, DT, false, true>(sl, warp, lane, tg.nel, P.cT);
-            rec.z = g.x;
-            rec.w = g.y;
+            r.z = g.x;
+            r.w = g.y;
           }
         }
-      } else if (tg.kind == kResid) {
-        rec.x = full ? reduce_resid<TT, DT, true>(sl, warp, lane, tg.nel, S, P.cT)
-                     : reduce_resid<TT, DT, false>(sl, warp, lane, tg.nel, S, P.cT);
-      } else {  // kSearch
-        rec.x = full ? reduce_search<TT, DT, true>(sl, warp, lane, tg.nel, tg.elem0, S, P.cT)
-                     : reduce_search<TT, DT, false>(sl, warp, lane, tg.nel, tg.elem0, S, P.cT);
+      } else {  // kResid
+        r.x = full ? reduce_resid<TT, DT, true>(sl, warp, lane, tg.nel, S, P.cT)
+                   : reduce_resid<TT, DT, false>(sl, warp, lane, tg.nel, S, P.cT);
       }
       if (lane == 0) {
-        sm.rec[tg.slot][tg.chunk - S.c0][warp] = rec;
+        rec[((size_t)tg.slot * P.NC + tg.chunk) * kCW + warp] = r;
         __threadfence_block();
-        const int total = (S.c1 - S.c0) * kCW;
         const int old = atomicAdd(&S.cnt, 1);
-        if (old == total - 1) {
+        if (old == P.NC * kCW - 1) {
           S.cnt = 0;
-          if (tg.kind == kSearch) S.search_stage = cs;
           __threadfence_block();
           vstore(&S.state, kDone);
         }
@@ -792,66 +869,37 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
     if (lane == 0) {
       int ps = 0;
       uint32_t pph = 0;
-      bool more = true;
+      int rr = 0;
       uint64_t t_idle = gtimer();
       for (;;) {
         if (vload(&sm.abort)) break;
         int si = -1;
-        for (int s = 0; s < kSlots && si < 0; ++s)
+        for (int k = 0; k < kSlots && si < 0; ++k) {
+          const int s = (rr + k) % kSlots;
           if (vload(&sm.slot[s].state) == kReady) si = s;
-        if (si < 0 && more) {
-          for (int s = 0; s < kSlots && si < 0; ++s) {
-            if (vload(&sm.slot[s].state) != kEmpty) continue;
-            const uint32_t b = atomicAdd(&P.ws[0], 1u);
-            if (b >= (uint32_t)P.B) {
-              more = false;
-              break;
-            }
-            Slot& S = sm.slot[s];
-            int nb = P.draft_len ? P.draft_len[b] : P.K;
-            bool bad = nb < 0 || nb > P.K;
-            for (int jj = 0; !bad && jj < nb; ++jj) {
-              const int32_t d = P.draft[(size_t)b * P.K + jj];
-              bad = d < 0 || d >= P.V;
-            }
-            S.b = (int32_t)b;
-            S.nb = bad ? 0 : nb;
-            S.j = 0;
-            S.L = 0;
-            S.cnt = 0;
-            if (bad) {
-              S.kind = kInvalid;
-              __threadfence_block();
-              vstore(&S.state, kDone);
-              continue;  // look for another empty slot
-            }
-            S.kind = kStats;
-            S.c0 = 0;
-            S.c1 = P.NC;
-            si = s;
-          }
         }
         if (si < 0) {
-          bool all_empty = true;
-          for (int s = 0; s < kSlots; ++s) all_empty &= vload(&sm.slot[s].state) == kEmpty;
-          if (!more && all_empty) break;
+          vstore(&sm.prod_idle, 1);
+          if (vload(&sm.ctrl_done)) break;
           if (gtimer() - t_idle > kWaitNs) {
             vstore(&sm.abort, 1);
             break;
           }
-          __nanosleep(64);
+          __nanosleep(32);
           continue;
         }
+        rr = si + 1;
+        vstore(&sm.prod_idle, 0);
         __threadfence_block();
         Slot& S = sm.slot[si];
         vstore(&S.state, kIssued);
         const int kind = S.kind, b = S.b, j = S.j;
-        // the draft model's row is needed for rows with a draft (j < n_b):
-        // statistics, the residual pass, and a residual search
+        // the draft model's row is read for rows with a draft (j < n_b): its
+        // statistics, and the residual pass
         const bool with_draft =
-            DT >= 0 && j < S.nb && (kind != kSearch || S.smode == 1);
+            DT >= 0 && ((kind == kStats && j < S.nb) || (kind == kResid && S.smode == 1));
         bool ok = true;
-        for (int c = S.c0; c < S.c1 && ok; ++c) {
+        for (int c = 0; c < P.NC && ok; ++c) {
           const uint64_t t0 = gtimer();
           while (!mbar_try_wait(&sm.empty[ps], pph ^ 1)) {
             if (vload(&sm.abort) || gtimer() - t0 > kWaitNs) {
@@ -877,10 +925,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
           } else {
             const size_t rt = ((size_t)b * (P.K + 1) + j) * (size_t)P.V + elem0;
             const uint32_t bt = (uint32_t)nel * C::ST;
-            uint32_t bytes = bt;
             const uint32_t bd = with_draft ? (uint32_t)nel * C::SD : 0u;
-            bytes += bd;
-            mbar_arrive_expect_tx(&sm.full[ps], bytes);
+            mbar_arrive_expect_tx(&sm.full[ps], bt + bd);
             bulk_g2s(dst, P.target + rt * C::ST, bt, &sm.full[ps]);
             if (with_draft) {
               const size_t rd = ((size_t)b * P.K + j) * (size_t)P.V + elem0;
@@ -926,26 +972,37 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
           while (!mbar_try_wait(&sm.full[s], (uint32_t)sm.stage_parity[s]))
             if (gtimer() - t0 > kWaitNs) break;
         }
-        // sequences nobody will finish: report them
-        for (uint32_t b = atomicAdd(&P.ws[0], 1u); b < (uint32_t)P.B; b = atomicAdd(&P.ws[0], 1u))
-          write_result(P, (int)b, -1, -1, SAMSPEC_ST_TIMEOUT);
       }
-      __threadfence_block();
-      vstore(&sm.prod_done, 1);
     }
   } else if (warp == kCtrlWarp) {
     // -------------------------------- control -------------------------------
+    // One sequence per CTA to begin with; another is claimed only once the
+    // producer has issued everything posted (its ring still holds up to NS
+    // tiles, which covers the claim), so small batches spread over all CTAs
+    // and large ones keep every producer busy.
+    Control<TT, DT, GREEDY> ctl(P, sm, rec, lane);
+    ctl.refill(0);
     uint64_t t_idle = gtimer();
     for (;;) {
-      int si = -1;
-      if (lane == 0) {
-        for (int s = 0; s < kSlots && si < 0; ++s)
-          if (vload(&sm.slot[s].state) == kDone) si = s;
-      }
+      int si = -1, free_slot = -1, ready = 0;
+      if (lane == 0)
+        for (int s = 0; s < kSlots; ++s) {
+          const int st = vload(&sm.slot[s].state);
+          if (st == kDone && si < 0) si = s;
+          if (st == kEmpty && free_slot < 0) free_slot = s;
+          ready += st == kReady;
+        }
       si = __shfl_sync(kFullMask, si, 0);
+      free_slot = __shfl_sync(kFullMask, free_slot, 0);
+      ready = __shfl_sync(kFullMask, ready, 0);
       if (si >= 0) {
         __threadfence_block();
-        control_handle<TT, DT, GREEDY>(P, sm, stages, si, lane);
+        ctl.handle(si);
+        t_idle = gtimer();
+        continue;
+      }
+      if (ctl.more && ready == 0 && free_slot >= 0 && vload(&sm.prod_idle)) {
+        ctl.refill(free_slot);
         t_idle = gtimer();
         continue;
       }
@@ -953,27 +1010,32 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       if (lane == 0) {
         if (vload(&sm.abort)) {
           stop = 1;
-        } else if (vload(&sm.prod_done)) {
+        } else {
           bool all_empty = true;
           for (int s = 0; s < kSlots; ++s) all_empty &= vload(&sm.slot[s].state) == kEmpty;
-          stop = all_empty;
-        } else if (gtimer() - t_idle > kWaitNs) {
-          vstore(&sm.abort, 1);
-          stop = 1;
+          if (all_empty && !ctl.more) {
+            vstore(&sm.ctrl_done, 1);
+            stop = 1;
+          } else if (gtimer() - t_idle > kWaitNs) {
+            vstore(&sm.abort, 1);
+            stop = 1;
+          }
         }
       }
       stop = __shfl_sync(kFullMask, stop, 0);
       if (stop) break;
-      __nanosleep(64);
+      __nanosleep(32);
+    }
+    if (vload(&sm.abort) && lane == 0) {
+      // sequences held by this CTA's slots, and any nobody will claim now
+      for (int s = 0; s < kSlots; ++s)
+        if (sm.slot[s].state != kEmpty) write_result(P, sm.slot[s].b, -1, -1, SAMSPEC_ST_TIMEOUT);
+      for (uint32_t b = atomicAdd(&P.ws[0], 1u); b < (uint32_t)P.B; b = atomicAdd(&P.ws[0], 1u))
+        write_result(P, (int)b, -1, -1, SAMSPEC_ST_TIMEOUT);
     }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    if (sm.abort) {
-      // sequences still held by this CTA's slots
-      for (int s = 0; s < kSlots; ++s)
-        if (sm.slot[s].state != kEmpty) write_result(P, sm.slot[s].b, -1, -1, SAMSPEC_ST_TIMEOUT);
-    }
     __threadfence();
     if (atomicAdd(&P.ws[1], 1u) == gridDim.x - 1) {
       // last CTA out: reset the counters for the next launch on this workspace
@@ -998,7 +1060,9 @@ int launch(const VParams& P0, cudaStream_t stream) {
   VParams P = P0;
   P.NC = (P.V + C::E_TILE - 1) / C::E_TILE;
   if (P.NC > kMaxChunks) return SAMSPEC_ESIZE;
-  const size_t head = (sizeof(Smem) + 1023) & ~(size_t)1023;
+  const size_t rec_off = (sizeof(Smem) + 15) & ~(size_t)15;
+  const size_t head =
+      (rec_off + (size_t)kSlots * P.NC * kCW * sizeof(float4) + 1023) & ~(size_t)1023;
   // Device properties and the kernel's shared-memory opt-in are set up once per
   // device, so that later launches make no runtime calls besides the launch
   // itself (safe inside stream capture).
@@ -1008,24 +1072,25 @@ int launch(const VParams& P0, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return SAMSPEC_ECUDA;
   if (sms[dev] == 0) {
-    if (cudaDeviceGetAttribute(&max_smem[dev], cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+    if (cudaDeviceGetAttribute(&max_smem[dev], cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
         cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return SAMSPEC_ECUDA;
   }
-  int ns = (int)((max_smem[dev] - (int)head) / kStageBytes);
-  if (ns > kMaxStages) ns = kMaxStages;
-  if (ns < 2) return SAMSPEC_ESIZE;
-  P.NS = ns;
-  const size_t smem = head + (size_t)ns * kStageBytes;
-  auto kern = verify_kernel<TT, DT, GREEDY>;
   if (!attr_done[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+    if (cudaFuncSetAttribute(verify_kernel<TT, DT, GREEDY>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem[dev]) !=
         cudaSuccess)
       return SAMSPEC_ECUDA;
     attr_done[dev] = true;
   }
+  int ns = (int)(((size_t)max_smem[dev] - head) / kStageBytes);
+  if (ns > kMaxStages) ns = kMaxStages;
+  if (ns < kMinStages) return SAMSPEC_ESIZE;
+  P.NS = ns;
+  const size_t smem = head + (size_t)ns * kStageBytes;
   const int grid = P.B < sms[dev] ? P.B : sms[dev];
-  kern<<<grid, kThreads, smem, stream>>>(P);
+  verify_kernel<TT, DT, GREEDY><<<grid, kThreads, smem, stream>>>(P);
   return cudaGetLastError() == cudaSuccess ? SAMSPEC_OK : SAMSPEC_ECUDA;
 }
 
@@ -1053,7 +1118,8 @@ size_t spec_verify_workspace_bytes(int32_t B, int32_t K, int32_t V) {
 
 int spec_verify_workspace_init(void* d_workspace, size_t ws_bytes, samspec_stream_t stream) {
   if (!d_workspace || ws_bytes < 256) return SAMSPEC_EINVAL;
-  return cudaMemsetAsync(d_workspace, 0, 256, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+  return cudaMemsetAsync(d_workspace, 0, 256, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
              ? SAMSPEC_OK
              : SAMSPEC_ECUDA;
 }
@@ -1104,15 +1170,16 @@ int spec_verify(const void* d_target, int32_t target_dtype, const void* d_draft_
   P.ws = static_cast<uint32_t*>(d_workspace);
   P.direct = ((size_t)V * st) % 16 != 0 || (sd && ((size_t)V * sd) % 16 != 0);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return greedy ? dispatch<true>(P, target_dtype, ddt, s) : dispatch<false>(P, target_dtype, ddt, s);
+  return greedy ? dispatch<true>(P, target_dtype, ddt, s)
+                : dispatch<false>(P, target_dtype, ddt, s);
 }
 
 int spec_uniforms(int32_t B, int32_t K, uint64_t seed, uint64_t step, float* d_u,
                   samspec_stream_t stream) {
   if (!d_u || B < 1 || K < 0 || K > 32) return SAMSPEC_EINVAL;
   const int64_t n = (int64_t)B * (K + 1);
-  uniforms_kernel<<<(unsigned)((n + 255) / 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      B, K, seed, step, d_u);
+  uniforms_kernel<<<(unsigned)((n + 255) / 256), 256, 0,
+                    reinterpret_cast<cudaStream_t>(stream)>>>(B, K, seed, step, d_u);
   return cudaGetLastError() == cudaSuccess ? SAMSPEC_OK : SAMSPEC_ECUDA;
 }
 
