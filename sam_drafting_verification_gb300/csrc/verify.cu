@@ -25,13 +25,14 @@
 //       tile from shared memory (16-byte vector reads) to a record -- the
 //       slice's max and sum of 2^((l - max) log2(e)/T), or its (max, first
 //       argmax) -- and release the stage;
-//   warp 17 (control) claims sequences from a global counter into four slots,
+//   warps 17-19 (control, one per sequence slot) claim sequences from a
+//       global counter,
 //       merges the warp-slice records of a finished row in fp64, draws the
 //       Philox coins, decides accept/reject and posts the next row; after the
 //       final row it resamples: the slice records give the mass of every warp
 //       slice, so it finds the slice holding u' * sum(r) and scans just that
 //       2-8 KB slice, read again from L2, in ascending token order.
-// Four slots keep the producer streaming while the control warp decides.
+// Several slots keep the producer streaming while a control warp decides.
 // Every wait is bounded by a global-timer deadline; a CTA that runs out of
 // time marks its sequences SAMSPEC_ST_TIMEOUT, lets its copies in flight land
 // and exits.
@@ -50,17 +51,17 @@ namespace {
 
 constexpr int kCW = 16;              // consumer warps
 constexpr int kProdWarp = kCW;       // producer warp
-constexpr int kCtrlWarp = kCW + 1;   // control warp
-constexpr int kThreads = (kCW + 2) * 32;
+constexpr int kCtrlWarp = kCW + 1;   // first control warp (one per slot)
+constexpr int kSlots = 3;
+constexpr int kThreads = (kCW + 1 + kSlots) * 32;
 constexpr int kStageBytes = 32768;
 constexpr int kMaxStages = 6;
 constexpr int kMinStages = 3;
-constexpr int kSlots = 4;
 constexpr int kMaxChunks = 64;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 
 enum Kind : int32_t { kStats = 0, kResid = 1, kExit = 3 };
-enum State : int32_t { kEmpty = 0, kReady = 1, kIssued = 2, kDone = 3 };
+enum State : int32_t { kEmpty = 0, kReady = 1, kIssued = 2 };
 
 struct VParams {
   const unsigned char* target;
@@ -68,8 +69,9 @@ struct VParams {
   const int32_t* draft;
   const int32_t* draft_len;
   int32_t B, K, V;
-  float T, cT;  // cT = log2(e) / T
-  double Td;
+  float T, cT;  // cT = log2(e) / T, rounded to fp32
+  float cTl;    // cT + cTl = log2(e) / T to about 2^-48 relative
+  double Td, cTd;
   uint64_t seed, step;
   int32_t* accept_len;
   int32_t* out_token;
@@ -84,16 +86,26 @@ struct VParams {
 
 struct Tag {
   int32_t slot, kind, chunk, nel, elem0, has_draft, b, j;
+  int32_t dtok;  // the row's draft token (statistics pass of a drafted row), else -1
+  int32_t pad[3];
 };
 
 struct Slot {
   int32_t state;  // State, accessed with volatile loads/stores
   int32_t kind;   // kind of the current job (kStats: row j; kResid: row L)
   int32_t b, j, nb, L;
-  int32_t cnt;    // warp records received for the current job
   int32_t smode;  // residual pass: 1 -> max(0, p - q) in units of p;
                   //                0 -> p in units of exp(x - m)
   float lmax, gmax, invZ, invZg;
+  int32_t dtok;   // draft token of the current row (-1 for the bonus row)
+  float xd, gd;   // target / draft logit at dtok, captured by the consumers
+  int32_t age;    // claim order inside the CTA: the producer serves the oldest first
+};
+
+// One warp-slice record: softmax statistics of the target (a) and draft (b)
+// rows; greedy {max, 0, NaN seen, 0} in a; residual pass {rh, rl, 0, 0} in a.
+struct Rec {
+  float4 a, b;
 };
 
 struct Smem {
@@ -102,9 +114,16 @@ struct Smem {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   int32_t stage_parity[kMaxStages];  // parity of the last issue per stage
-  int32_t ctrl_done;
   int32_t abort;
-  int32_t prod_idle;  // the producer has issued every posted job
+  int32_t prod_idle;    // the producer has issued every posted job
+  int32_t jobs_issued;  // jobs whose tiles the producer has all issued
+  int32_t ctrl_exited;  // control warps that have finished
+  int32_t claims;       // sequences claimed by this CTA
+  int32_t pool_left;    // sequences not yet claimed, as of this CTA's last claim
+  int32_t claim_lock;   // one control warp claims at a time
+  int32_t tile_cnt[kSlots][kMaxChunks];  // consumer warps done with each tile of a job
+  float4 pre[kSlots][kMaxChunks][2];     // control: mass before each tile {hi, lo, ref, 0}
+  float cmass[kSlots][kMaxChunks];  // control warp: tile masses per slot
 };
 
 __device__ __forceinline__ uint64_t gtimer() {
@@ -123,6 +142,51 @@ __device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
+}
+
+// packed fp32 pairs (Blackwell f32x2 arithmetic)
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// ---- compensated (double-float) sums -------------------------------------------
+// A value is hi + lo with |lo| <= ulp(hi) / 2; additions carry the rounding
+// error of every step (Knuth's TwoSum), so a sum of fp32 terms keeps about 44
+// significant bits.
+struct DF {
+  float hi, lo;
+};
+__device__ __forceinline__ DF df_add(DF x, DF y) {
+  const float s = x.hi + y.hi;
+  const float bb = s - x.hi;
+  const float e = (x.hi - (s - bb)) + (y.hi - bb);
+  const float lo = e + (x.lo + y.lo);
+  const float hi = s + lo;
+  return {hi, lo - (hi - s)};
+}
+__device__ __forceinline__ DF df_warp_sum(float v) {
+  DF a = {v, 0.f};
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const DF o2 = {__shfl_xor_sync(kFullMask, a.hi, o), __shfl_xor_sync(kFullMask, a.lo, o)};
+    a = df_add(a, o2);
+  }
+  return a;
 }
 
 // ---- element access ---------------------------------------------------------
@@ -165,6 +229,11 @@ struct Vec {
         }
       }
     }
+  }
+  // elements (2p, 2p + 1) as a packed fp32 pair
+  __device__ __forceinline__ uint64_t pair(int p) const {
+    if (ES == 4) return pk2(__uint_as_float(w[2 * p]), __uint_as_float(w[2 * p + 1]));
+    return pk2(bf16_lo(w[p]), bf16_hi(w[p]));
   }
   // NaN-propagating maximum of the vector's elements
   __device__ __forceinline__ float vmax() const {
@@ -229,17 +298,20 @@ __device__ __forceinline__ void load_slice_tile(Slice<TT, DT>& s, const VParams&
 }
 
 // Loads warp slice `w` of tile `c` of row L of sequence b straight from global
-// memory (the control warp's resample scan).  Returns the slice's element count.
+// memory for the control warp, lane-major: lane l holds the slice's elements
+// [l * EPL, (l + 1) * EPL) (EPL = SL / 32), vector i covering elements
+// l * EPL + i * VEC + k.  Returns the slice's element count.
 template <int TT, int DT>
-__device__ __forceinline__ int load_slice_global(Slice<TT, DT>& s, const VParams& P, int b, int L,
-                                                 int c, int w, bool with_draft, int lane) {
+__device__ __forceinline__ int load_slice_lanes(Slice<TT, DT>& s, const VParams& P, int b, int L,
+                                                int c, int w, bool with_draft, int lane) {
   using C = Cfg<TT, DT>;
+  constexpr int EPL = C::SL / 32;
   const int s0 = c * C::E_TILE + w * C::SL;
   const size_t rt = ((size_t)b * (P.K + 1) + L) * (size_t)P.V;
   const size_t rd = ((size_t)b * P.K + L) * (size_t)P.V;
 #pragma unroll
   for (int i = 0; i < C::VPL; ++i) {
-    const int e = s0 + (i * 32 + lane) * C::VEC;  // vocab index
+    const int e = s0 + lane * EPL + i * C::VEC;  // vocab index
     const int valid = P.V - e;
     if (!P.direct) {
       // aligned rows hold whole vectors: a vector is either in range or not
@@ -282,41 +354,63 @@ __device__ __forceinline__ float lane_max(const Slice<TT, DT>& s, int w, int lan
   return m;
 }
 
-// greedy record: {max, first index of the max, NaN seen}
+// greedy record: {slice max, 0, NaN seen}.  The first position of the row's
+// maximum is found afterwards, in the one warp slice that holds it.
 template <int TT, int DT, bool FULL>
-__device__ __forceinline__ float4 reduce_greedy(const Slice<TT, DT>& s, int w, int lane, int nel,
-                                                int elem0) {
-  using C = Cfg<TT, DT>;
+__device__ __forceinline__ float4 reduce_greedy(const Slice<TT, DT>& s, int w, int lane, int nel) {
   const float ml = lane_max<TT, DT, FULL, false>(s, w, lane, nel);
-  if (__any_sync(kFullMask, ml != ml)) return make_float4(0.f, __int_as_float(0x7fffffff), 1.f, 0.f);
-  const float M = warp_max(ml);
-  int32_t idx = 0x7fffffff;
-  if (ml == M) {  // only the lanes holding the maximum look for its first position
-#pragma unroll
-    for (int i = 0; i < C::VPL; ++i) {
-      const int e = w * C::SL + (i * 32 + lane) * C::VEC;
-#pragma unroll
-      for (int k = 0; k < C::VEC; ++k)
-        if ((FULL || e + k < nel) && s.t[i].at(k) == M && idx == 0x7fffffff) idx = elem0 + e + k;
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(kFullMask, idx, o));
-  return make_float4(M, __int_as_float(idx), 0.f, 0.f);
+  if (__any_sync(kFullMask, ml != ml)) return make_float4(0.f, 0.f, 1.f, 0.f);
+  return make_float4(warp_max(ml), 0.f, 0.f, 0.f);
 }
 
-// {max, sum_x 2^((x - max) * cT)} of one array; NaN in the slice -> {NaN, NaN}
+// Softmax record of one array of the slice: {m, R, z, 0} with m the slice
+// max, R = ceil(fl(m * cT)) an integer exponent reference and z the fp32 sum
+// of 2^fl(x * cT - R) over the slice (every term in (0, ~1]).
+// Records of one row combine by exact power-of-two scaling 2^(R - max R), so no
+// per-record exponential enters the row's masses.  The element with tile index
+// `excl` (the row's draft token, added back exactly by the control warp) is
+// left out.  An all -inf slice gives {-inf, -inf, 0, 0}; NaN gives NaNs.
 template <int TT, int DT, bool FULL, bool DRAFT_ARRAY>
-__device__ __forceinline__ float2 reduce_softmax(const Slice<TT, DT>& s, int w, int lane, int nel,
-                                                 float cT) {
+__device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, int lane, int nel,
+                                                 float cT, int excl) {
   using C = Cfg<TT, DT>;
   const float NEG_INF = -__int_as_float(0x7f800000);
+  const float QNAN = __int_as_float(0x7fc00000);
   const float ml = lane_max<TT, DT, FULL, DRAFT_ARRAY>(s, w, lane, nel);
-  if (__any_sync(kFullMask, ml != ml))
-    return make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
+  if (__any_sync(kFullMask, ml != ml)) return make_float4(QNAN, QNAN, QNAN, QNAN);
   const float m = warp_max(ml);
-  float z = 0.f;
-  if (m != NEG_INF) {
+  if (m == NEG_INF) return make_float4(NEG_INF, NEG_INF, 0.f, 0.f);
+  const float R = ceilf(m * cT);
+  float z;
+  const bool has_excl = excl >= w * C::SL && excl < (w + 1) * C::SL;
+  if (FULL && !has_excl) {
+    // pairs of elements through packed FFMA / FADD, one MUFU ex2 each
+    const uint64_t c2 = pk2(cT, cT), nr2 = pk2(-R, -R);
+    uint64_t part[C::VPL];
+#pragma unroll
+    for (int i = 0; i < C::VPL; ++i) {
+      uint64_t v[C::VEC / 2];
+#pragma unroll
+      for (int p = 0; p < C::VEC / 2; ++p) {
+        const uint64_t y = fma2(DRAFT_ARRAY ? s.d[i].pair(p) : s.t[i].pair(p), c2, nr2);
+        float y0, y1;
+        upk2(y, y0, y1);
+        v[p] = pk2(ex2_approx(y0), ex2_approx(y1));
+      }
+#pragma unroll
+      for (int h = C::VEC / 4; h >= 1; h >>= 1)
+#pragma unroll
+        for (int p = 0; p < h; ++p) v[p] = add2(v[p], v[p + h]);
+      part[i] = v[0];
+    }
+#pragma unroll
+    for (int h = C::VPL / 2; h >= 1; h >>= 1)
+#pragma unroll
+      for (int i = 0; i < h; ++i) part[i] = add2(part[i], part[i + h]);
+    float lo, hi;
+    upk2(part[0], lo, hi);
+    z = lo + hi;
+  } else {
     float part[C::VPL];
 #pragma unroll
     for (int i = 0; i < C::VPL; ++i) {
@@ -325,7 +419,7 @@ __device__ __forceinline__ float2 reduce_softmax(const Slice<TT, DT>& s, int w, 
 #pragma unroll
       for (int k = 0; k < C::VEC; ++k) {
         const float x = DRAFT_ARRAY ? s.d[i].at(k) : s.t[i].at(k);
-        v[k] = (FULL || e + k < nel) ? ex2_approx((x - m) * cT) : 0.f;
+        v[k] = (e + k < nel && e + k != excl) ? ex2_approx(fmaf(x, cT, -R)) : 0.f;
       }
 #pragma unroll
       for (int h = C::VEC / 2; h >= 1; h >>= 1)
@@ -337,15 +431,32 @@ __device__ __forceinline__ float2 reduce_softmax(const Slice<TT, DT>& s, int w, 
     for (int h = C::VPL / 2; h >= 1; h >>= 1)
 #pragma unroll
       for (int i = 0; i < h; ++i) part[i] += part[i + h];
-    z = warp_sum(part[0]);
+    z = part[0];
   }
-  return make_float2(m, z);
+  // the slice's terms are summed in fp32 (its mass only has to locate a tile
+  // and a slice; the control warp combines slices with compensated sums)
+  return make_float4(m, R, warp_sum(z), 0.f);
 }
 
-// residual-pass record: sum of r over the slice (fast exponential)
+// Residual weight of one element, the same expression in the residual pass and
+// in the resample scan (so a slice's mass and its scan agree):
+//   smode 0: 2^fl(x * cT - RL), units 2^RL;
+//   smode 1: max(0, 2^fl(x * cT - RL) * invZ - 2^fl(g * cT - RG) * invZg), units of p.
+template <int TT, int DT>
+__device__ __forceinline__ float resid_elem(const Slice<TT, DT>& s, int i, int k, int smode,
+                                            float RL, float RG, float invZ, float invZg, float cT) {
+  const float pe = ex2_approx(fmaf(s.t[i].at(k), cT, -RL));
+  if (smode == 0) return pe;
+  float g = 0.f;
+  if (DT >= 0) g = s.d[i].at(k);
+  const float qe = ex2_approx(fmaf(g, cT, -RG));
+  return fmaxf(0.f, pe * invZ - qe * invZg);
+}
+
+// residual-pass record: sum of r over the slice {r, 0, 0, 0}
 template <int TT, int DT, bool FULL>
-__device__ __forceinline__ float reduce_resid(const Slice<TT, DT>& s, int w, int lane, int nel,
-                                              const Slot& S, float cT) {
+__device__ __forceinline__ float4 reduce_resid(const Slice<TT, DT>& s, int w, int lane, int nel,
+                                               const Slot& S, float cT) {
   using C = Cfg<TT, DT>;
   float acc = 0.f;
 #pragma unroll
@@ -353,35 +464,12 @@ __device__ __forceinline__ float reduce_resid(const Slice<TT, DT>& s, int w, int
     const int e = w * C::SL + (i * 32 + lane) * C::VEC;
     float part = 0.f;
 #pragma unroll
-    for (int k = 0; k < C::VEC; ++k) {
-      if (FULL || e + k < nel) {
-        const float pe = ex2_approx((s.t[i].at(k) - S.lmax) * cT);
-        if (S.smode == 0) {
-          part += pe;
-        } else {
-          float g = 0.f;
-          if (DT >= 0) g = s.d[i].at(k);
-          const float qe = ex2_approx((g - S.gmax) * cT);
-          part += fmaxf(0.f, pe * S.invZ - qe * S.invZg);
-        }
-      }
-    }
+    for (int k = 0; k < C::VEC; ++k)
+      if (FULL || e + k < nel)
+        part += resid_elem<TT, DT>(s, i, k, S.smode, S.lmax, S.gmax, S.invZ, S.invZg, cT);
     acc += part;
   }
-  return warp_sum(acc);
-}
-
-// residual weight of one element with the accurate exponential (resample scan)
-template <int TT, int DT>
-__device__ __forceinline__ float resid_elem(const Slice<TT, DT>& s, int i, int k, int vocab,
-                                            int smode, int excl, float lmax, float gmax,
-                                            float invZ, float invZg, float cT) {
-  const float pe = exp2f((s.t[i].at(k) - lmax) * cT);
-  if (smode == 0) return vocab == excl ? 0.f : pe;
-  float g = 0.f;
-  if (DT >= 0) g = s.d[i].at(k);
-  const float qe = exp2f((g - gmax) * cT);
-  return fmaxf(0.f, pe * invZ - qe * invZg);
+  return make_float4(warp_sum(acc), 0.f, 0.f, 0.f);
 }
 
 // ---- outputs ---------------------------------------------------------------
@@ -399,11 +487,6 @@ __device__ void write_result(const VParams& P, int b, int L, int out, int st) {
   }
 }
 
-__device__ __forceinline__ float load_logit(const unsigned char* base, int es, size_t idx) {
-  if (es == 4) return __ldg(reinterpret_cast<const float*>(base) + idx);
-  return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(base) + idx) << 16);
-}
-
 // First lane in [0, n) whose inclusive running sum of v exceeds t, or -1;
 // *before receives the running sum ahead of that lane.
 __device__ __forceinline__ int warp_find(double v, double t, int n, int lane, double* before) {
@@ -417,62 +500,98 @@ __device__ __forceinline__ int warp_find(double v, double t, int n, int lane, do
 }
 
 // ---- control warp ------------------------------------------------------------
+// Records of a slot are indexed r = c * kCW + w (tile c, warp slice w); the
+// merges below give lane l the records r = q * 32 + l, so one pass of the
+// warp covers two tiles (lanes 0-15: tile 2q, lanes 16-31: tile 2q + 1).
+
+// 2^(x * log2(e)/T - R) for one token (R an integer-valued reference),
+// accurate to a few fp32 ulp: log2(e)/T is carried as cT + cTl, x * cT and
+// its rounding error exactly (FMA), the difference to R by TwoSum, and the
+// integer part of the exponent split off before exp2f.
+__device__ __forceinline__ float exp_ref(float x, float R, float cT, float cTl) {
+  const float yh = x * cT;
+  const float e1 = fmaf(x, cT, -yh) + x * cTl;
+  const float s = yh - R;
+  const float bb = s - yh;
+  const float e2 = (yh - (s - bb)) + (-R - bb);
+  const float si = rintf(s);
+  return ldexpf(exp2f((s - si) + (e1 + e2)), (int)fmaxf(si, -300.f));
+}
+
 template <int TT, int DT, bool GREEDY>
 struct Control {
   using C = Cfg<TT, DT>;
+  static constexpr int EPL = C::SL / 32;  // slice elements per lane (lane-major loads)
   const VParams& P;
   Smem& sm;
-  const float4* rec;  // [kSlots][NC][kCW]
-  int lane;
+  const Rec* rec;     // [kSlots][NC][kCW]
+  int lane, si;
   bool more;
+  int32_t tok;        // lane t holds draft token t of the slot's sequence
+  float ua, ur;       // coins of the row in flight (drawn while it streams)
 
-  __device__ Control(const VParams& p, Smem& s, const float4* r, int l)
-      : P(p), sm(s), rec(r), lane(l), more(true) {}
-
-  __device__ const float4& R(int si, int c, int w) const {
-    return rec[((size_t)si * P.NC + c) * kCW + w];
+  __device__ Control(const VParams& p, Smem& s, const Rec* r, int l, int slot)
+      : P(p), sm(s), rec(r), lane(l), si(slot), more(true), tok(-1), ua(0.f), ur(0.f) {
+    reset_row();
   }
 
+  __device__ const Rec& R(int c, int w) const { return rec[((size_t)si * P.NC + c) * kCW + w]; }
+
+  // Outputs of sequence b, written by the warp's lanes in parallel (lane t
+  // holds draft token t).
   __device__ void finish(int b, int L, int out, int st) {
-    if (lane == 0) write_result(P, b, L, out, st);
-    __syncwarp();
-  }
-
-  __device__ void post(int si, int kind, int j) {
-    Slot& S = sm.slot[si];
+    if (P.emit) {
+      int32_t* e = P.emit + (size_t)b * (P.K + 1);
+      if (lane <= P.K) e[lane] = st ? -1 : (lane < L ? tok : (lane == L ? out : -1));
+      if (P.K == 32 && lane == 0) e[32] = st ? -1 : (L == 32 ? out : -1);
+    }
     if (lane == 0) {
-      S.kind = kind;
-      S.j = j;
-      S.cnt = 0;
-      __threadfence_block();
-      vstore(&S.state, kReady);
+      P.accept_len[b] = st ? -1 : L;
+      P.out_token[b] = st ? -1 : out;
+      if (P.status) P.status[b] = st;
+      if (P.emit_len) P.emit_len[b] = st ? 0 : L + 1;
     }
     __syncwarp();
   }
 
-  __device__ void release(int si) {
+  __device__ void release() {
     if (lane == 0) vstore(&sm.slot[si].state, kEmpty);
     __syncwarp();
   }
 
-  // Claims sequences until one with valid drafts lands in slot si (or none
-  // are left: the slot becomes empty).
-  __device__ void refill(int si) {
+  // Posts row j for the producer, then draws the row's coins while it streams.
+  __device__ void post(int kind, int j) {
+    Slot& S = sm.slot[si];
+    const int32_t dt = __shfl_sync(kFullMask, tok, j & 31);
+    if (lane == 0) {
+      S.kind = kind;
+      S.j = j;
+      S.dtok = (kind == kStats && j < S.nb) ? dt : -1;
+      __threadfence_block();
+      vstore(&S.state, kReady);
+    }
+    __syncwarp();
+    if (!GREEDY) verify_coins(P.seed, P.step, (uint32_t)S.b, (uint32_t)j, &ua, &ur);
+  }
+
+  // Claims sequences until one with valid drafts lands in the slot (or none
+  // are left: the slot stays empty).
+  __device__ void refill() {
     Slot& S = sm.slot[si];
     while (more) {
       uint32_t b = 0;
-      if (lane == 0) b = atomicAdd(&P.ws[0], 1u);
+      if (lane == 0) {
+        b = atomicAdd(&P.ws[0], 1u);
+        vstore(&sm.pool_left, b >= (uint32_t)P.B ? 0 : P.B - 1 - (int)b);
+      }
       b = __shfl_sync(kFullMask, b, 0);
       if (b >= (uint32_t)P.B) {
         more = false;
         break;
       }
       const int nb = P.draft_len ? P.draft_len[b] : P.K;
-      bool bad = nb < 0 || nb > P.K;
-      if (!bad && lane < nb) {
-        const int32_t d = P.draft[(size_t)b * P.K + lane];
-        bad = d < 0 || d >= P.V;
-      }
+      tok = (lane < P.K) ? P.draft[(size_t)b * P.K + lane] : -1;
+      bool bad = nb < 0 || nb > P.K || (lane < nb && (tok < 0 || tok >= P.V));
       if (__any_sync(kFullMask, bad)) {
         finish((int)b, -1, -1, SAMSPEC_ST_BADDRAFT);
         continue;
@@ -481,62 +600,152 @@ struct Control {
         S.b = (int32_t)b;
         S.nb = nb;
         S.L = 0;
+        S.age = atomicAdd(&sm.claims, 1);
       }
-      post(si, kStats, 0);
+      __syncwarp();
+      post(kStats, 0);
       return;
     }
-    if (lane == 0) vstore(&S.state, kEmpty);
+  }
+
+  // ---- running row state, updated tile by tile while the row streams -------
+  // Softmax arrays (f = 0 target, 1 draft): max logit, exponent reference
+  // (max slice reference so far) and the compensated mass of the tiles merged
+  // so far in units of 2^ref; the mass before each tile goes to sm.pre.
+  struct Run {
+    float mx, ref;
+    DF sum;
+    bool nan;
+  };
+  Run run[2];
+  // greedy: row max, and the first slice holding it (tile * kCW + slice)
+  float gmax_;
+  int gfirst_;
+  bool gnan_;
+
+  __device__ void reset_row() {
+    const float NEG_INF = -__int_as_float(0x7f800000);
+#pragma unroll
+    for (int f = 0; f < 2; ++f) run[f] = Run{NEG_INF, NEG_INF, DF{0.f, 0.f}, false};
+    gmax_ = NEG_INF;
+    gfirst_ = -1;
+    gnan_ = false;
+  }
+
+  // Adds tile c's slices of array f (records in lanes 0..15) to run[f].
+  __device__ void merge_softmax(int c, int f) {
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    float4 r = make_float4(NEG_INF, NEG_INF, 0.f, 0.f);
+    if (lane < kCW) r = f ? R(c, lane).b : R(c, lane).a;
+    const bool nan = __any_sync(kFullMask, r.x != r.x || r.z != r.z);
+    const float mc = warp_max(r.x);
+    const float Rc = warp_max(r.y);
+    float v = 0.f;
+    if (Rc != NEG_INF && r.z != 0.f) v = ldexpf(r.z, (int)(r.y - Rc));
+    const DF t = df_warp_sum(v);  // the tile's mass over its 16 slices, units 2^Rc
+    Run& R_ = run[f];
+    if (lane == 0) sm.pre[si][c][f] = make_float4(R_.sum.hi, R_.sum.lo, R_.ref, 0.f);
+    R_.nan |= nan;
+    R_.mx = fmaxf(R_.mx, mc);
+    if (Rc != NEG_INF && (t.hi != 0.f || t.lo != 0.f)) {
+      if (Rc > R_.ref) {  // a larger reference: rescale what was summed so far
+        if (R_.ref != NEG_INF) {
+          const int sc = (int)(R_.ref - Rc);
+          R_.sum = DF{ldexpf(R_.sum.hi, sc), ldexpf(R_.sum.lo, sc)};
+        }
+        R_.ref = Rc;
+      }
+      const int sc = (int)(Rc - R_.ref);
+      R_.sum = df_add(R_.sum, DF{ldexpf(t.hi, sc), ldexpf(t.lo, sc)});
+    }
+  }
+
+  __device__ void merge_tile(int c) {
+    Slot& S = sm.slot[si];
+    if (c == 0) reset_row();
+    if (GREEDY) {
+      const float m = lane < kCW ? R(c, lane).a.x : -__int_as_float(0x7f800000);
+      gnan_ |= __any_sync(kFullMask, lane < kCW && R(c, lane).a.z != 0.f);
+      const float M = warp_max(m);
+      if (M > gmax_) {  // tiles arrive in token order: keep the first maximum
+        const unsigned h = __ballot_sync(kFullMask, lane < kCW && m == M);
+        gmax_ = M;
+        gfirst_ = c * kCW + __ffs(h) - 1;
+      }
+    } else if (S.kind == kStats) {
+      merge_softmax(c, 0);
+      if (DT >= 0 && S.j < S.nb) merge_softmax(c, 1);
+    } else {  // residual pass: plain running sum in units of p
+      const DF t = df_warp_sum(lane < kCW ? R(c, lane).a.x : 0.f);
+      if (lane == 0) sm.pre[si][c][0] = make_float4(run[0].sum.hi, run[0].sum.lo, 0.f, 0.f);
+      run[0].sum = df_add(run[0].sum, t);
+      run[0].ref = 0.f;
+    }
     __syncwarp();
   }
 
-  // Resample scan of warp slice (c, w) of row L: the first token whose running
-  // residual exceeds t (ascending token id), with the accurate exponential.
-  __device__ int slice_scan(int b, int L, int c, int w, double t, int smode, int excl, float lmax,
-                            float gmax, float invZ, float invZg) {
+  // First position of value M in warp slice (c, w) of row j (greedy argmax).
+  __device__ int first_index_of(int b, int j, int c, int w, float M) {
     Slice<TT, DT> sl;
-    const bool with_draft = DT >= 0 && smode == 1;
-    const int n = load_slice_global<TT, DT>(sl, P, b, L, c, w, with_draft, lane);
+    const int n = load_slice_lanes<TT, DT>(sl, P, b, j, c, w, false, lane);
     const int s0 = c * C::E_TILE + w * C::SL;
-    int token = -1, last_pos = -1;
-    double tt = t;
+    int idx = 0x7fffffff;
 #pragma unroll
     for (int i = 0; i < C::VPL; ++i) {
-      const int e = (i * 32 + lane) * C::VEC;  // index inside the slice
-      float r[C::VEC];
-      double s_l = 0.0;
+      const int e = lane * EPL + i * C::VEC;
+#pragma unroll
+      for (int k = 0; k < C::VEC; ++k)
+        if (e + k < n && sl.t[i].at(k) == M && idx == 0x7fffffff) idx = s0 + e + k;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(kFullMask, idx, o));
+    return idx;
+  }
+
+  // Resample scan of warp slice (c, w) of row L: the first token whose running
+  // residual exceeds t (in the slice's own units: the expression its record
+  // summed, resid_elem, with token `excl` left out), ascending token order.
+  // Each lane sums its own contiguous elements; one warp scan finds the lane;
+  // that lane walks its elements.
+  __device__ int slice_scan(int b, int L, int c, int w, double t, int smode, int excl, float RL,
+                            float RG, float invZ, float invZg) {
+    Slice<TT, DT> sl;
+    const bool with_draft = DT >= 0 && smode == 1;
+    const int n = load_slice_lanes<TT, DT>(sl, P, b, L, c, w, with_draft, lane);
+    const int s0 = c * C::E_TILE + w * C::SL;
+    auto r_at = [&](int i, int k) -> float {
+      const int e = lane * EPL + i * C::VEC + k;
+      if (e >= n || s0 + e == excl) return 0.f;
+      return resid_elem<TT, DT>(sl, i, k, smode, RL, RG, invZ, invZg, P.cT);
+    };
+    float tot = 0.f;
+    int last_pos = -1;
+#pragma unroll
+    for (int i = 0; i < C::VPL; ++i)
 #pragma unroll
       for (int k = 0; k < C::VEC; ++k) {
-        r[k] = (e + k < n) ? resid_elem<TT, DT>(sl, i, k, s0 + e + k, smode, excl, lmax, gmax,
-                                                invZ, invZg, P.cT)
-                           : 0.f;
-        s_l += (double)r[k];
-        if (r[k] > 0.f) last_pos = s0 + e + k;
+        const float r = r_at(i, k);
+        tot += r;
+        if (r > 0.f) last_pos = s0 + lane * EPL + i * C::VEC + k;
       }
-      const double li = warp_incl_scan_d(s_l, lane);
-      const double row_total = __shfl_sync(kFullMask, li, 31);
-      if (token < 0 && row_total > tt) {
-        const unsigned h2 = __ballot_sync(kFullMask, li > tt);
-        const int ls = __ffs(h2) - 1;
-        const double tl = tt - (__shfl_sync(kFullMask, li, ls) - __shfl_sync(kFullMask, s_l, ls));
-        int found = -1;
-        if (lane == ls) {
-          double acc = 0.0;
-          int lastk = -1;
+    double before = 0.0;
+    const int ls = warp_find((double)tot, t, 32, lane, &before);
+    int token = -1;
+    if (ls >= 0) {
+      if (lane == ls) {
+        // the same values, recomputed in the same order
+        const float tl = (float)(t - before);
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < C::VPL; ++i)
+#pragma unroll
           for (int k = 0; k < C::VEC; ++k) {
-            acc += (double)r[k];
-            if (r[k] > 0.f) lastk = k;
-            if (acc > tl) {
-              found = k;
-              break;
-            }
+            acc += r_at(i, k);
+            if (token < 0 && acc > tl) token = s0 + lane * EPL + i * C::VEC + k;
           }
-          if (found < 0) found = lastk;
-          if (found >= 0) found = s0 + e + found;
-        }
-        found = __shfl_sync(kFullMask, found, ls);
-        if (found >= 0) token = found;
+        if (token < 0) token = last_pos;  // rounding: the lane's last positive entry
       }
-      if (token < 0) tt -= row_total;
+      token = __shfl_sync(kFullMask, token, ls);
     }
     if (token < 0) {  // rounding put t past the slice: its last positive entry
 #pragma unroll
@@ -547,156 +756,122 @@ struct Control {
     return token;
   }
 
-  // Picks the warp slice holding t from per-tile masses (cm, two per lane:
-  // tiles lane and lane + 32) and the per-slice masses of the chosen tile,
-  // then scans it.
-  template <typename SliceMass>
-  __device__ int resample(int b, int L, double t, const double* cm, SliceMass slice_mass,
-                          int smode, int excl, float lmax, float gmax, float invZ, float invZg) {
+  // The tile holding t: the last tile whose prefix mass (sm.pre, rescaled to
+  // units of 2^ref_units) is <= t; then the warp slice from the tile's slice
+  // masses (slice_mass(c, w) -> double); then scan(c, w, t_w) inside it.
+  template <typename SliceMass, typename Scan>
+  __device__ int resample(double t, float ref_units, SliceMass slice_mass, Scan scan) {
     const int NC = P.NC;
-    int cstar = -1;
-    double base = 0.0, before = 0.0;
-    for (int q = 0; q < 2 && q * 32 < NC; ++q) {
-      const int f = warp_find(cm[q], t - base, NC - q * 32, lane, &before);
-      if (f >= 0) {
-        cstar = q * 32 + f;
-        before += base;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    int cstar = 0;
+    double before = 0.0;
+#pragma unroll
+    for (int q = 1; q >= 0; --q) {
+      const int c = q * 32 + lane;
+      double bc = 0.0;
+      bool ok = false;
+      if (c < NC) {
+        const float4 pr = sm.pre[si][c][0];
+        if (pr.z != NEG_INF && (pr.x != 0.f || pr.y != 0.f))
+          bc = ldexp((double)pr.x + (double)pr.y, (int)(pr.z - ref_units));
+        ok = bc <= t;
+      }
+      const unsigned h = __ballot_sync(kFullMask, ok);
+      if (h) {
+        const int src = 31 - __clz(h);
+        cstar = q * 32 + src;
+        before = __shfl_sync(kFullMask, bc, src);
         break;
       }
-      base += warp_sum_d((q * 32 + lane) < NC ? cm[q] : 0.0);
     }
-    double tc;
-    if (cstar < 0) {  // rounding left the total at or below t: last tile with mass
-      int lastc = 0;
-      for (int q = 0; q < 2 && q * 32 < NC; ++q) {
-        const unsigned pos = __ballot_sync(kFullMask, (q * 32 + lane) < NC && cm[q] > 0.0);
-        if (pos) lastc = q * 32 + 31 - __clz(pos);
-      }
-      cstar = lastc;
-      tc = 1e300;
-    } else {
-      tc = t - before;
-    }
+    const double tc = t - before;
     const double sm_w = lane < kCW ? slice_mass(cstar, lane) : 0.0;
     double bw = 0.0;
     int wstar = warp_find(sm_w, tc, kCW, lane, &bw);
     double tw;
-    if (wstar < 0) {
+    if (wstar < 0) {  // rounding put t past the tile: its last slice with mass
       const unsigned pos = __ballot_sync(kFullMask, lane < kCW && sm_w > 0.0);
       wstar = pos ? 31 - __clz(pos) : 0;
       tw = 1e300;
     } else {
       tw = tc - bw;
     }
-    return slice_scan(b, L, cstar, wstar, tw, smode, excl, lmax, gmax, invZ, invZg);
+    return scan(cstar, wstar, tw);
   }
 
-  __device__ void handle(int si) {
+  __device__ void handle() {
     Slot& S = sm.slot[si];
     const int b = S.b, j = S.j, nb = S.nb;
-    const int NC = P.NC;
     const size_t ro = (size_t)b * (P.K + 1) + j;
+    const float NEG_INF = -__int_as_float(0x7f800000);
 
     if (GREEDY) {
-      float best = -__int_as_float(0x7f800000);
-      int32_t bi = 0x7fffffff;
-      bool nan = false;
-      for (int c = lane; c < NC; c += 32)
-        for (int w = 0; w < kCW; ++w) {
-          const float4 r = R(si, c, w);
-          const int32_t ri = __float_as_int(r.y);
-          nan |= r.z != 0.f;
-          if (r.x > best || (r.x == best && ri < bi)) {
-            best = r.x;
-            bi = ri;
-          }
-        }
-      warp_argmax(best, bi);
-      nan = __any_sync(kFullMask, nan);
-      const bool bad = nan || bi == 0x7fffffff || best == -__int_as_float(0x7f800000);
+      const float M = gmax_;
+      int idx = 0x7fffffff;
+      if (!gnan_ && M != NEG_INF && gfirst_ >= 0)
+        idx = first_index_of(b, j, gfirst_ / kCW, gfirst_ % kCW, M);
+      const bool bad = gnan_ || idx == 0x7fffffff;
       if (lane == 0) {
-        if (P.dbg.row_m) P.dbg.row_m[ro] = best;
-        if (P.dbg.row_arg) P.dbg.row_arg[ro] = bad ? -1 : bi;
+        if (P.dbg.row_m) P.dbg.row_m[ro] = M;
+        if (P.dbg.row_arg) P.dbg.row_arg[ro] = bad ? -1 : idx;
       }
       if (bad) {
         finish(b, -1, -1, SAMSPEC_ST_BADROW);
-        release(si);
+        release();
         return;
       }
-      if (j < nb && P.draft[(size_t)b * P.K + j] == bi) {
-        post(si, kStats, j + 1);
+      const int32_t dj = __shfl_sync(kFullMask, tok, j & 31);
+      if (j < nb && dj == idx) {
+        post(kStats, j + 1);
         return;
       }
-      finish(b, j, bi, 0);
-      release(si);
+      finish(b, j, idx, 0);
+      release();
       return;
     }
 
     if (S.kind == kStats) {
-      // --- temperature-softmax statistics of row j ---
-      float lm = -__int_as_float(0x7f800000), gm = lm;
-      for (int c = lane; c < NC; c += 32)
-        for (int w = 0; w < kCW; ++w) {
-          const float4 r = R(si, c, w);
-          lm = fmaxf(lm, r.x);
-          if (DT >= 0) gm = fmaxf(gm, r.z);
-        }
-      lm = warp_max(lm);
-      if (DT >= 0) gm = warp_max(gm);
-      const float cT = P.cT;
-      // slice mass in units of exp(x - lm); a NaN slice keeps its NaN
-      auto mass_of = [&](const float4& r) -> double {
-        return r.y == 0.f ? 0.0 : (double)r.y * (double)exp2f((r.x - lm) * cT);
-      };
-      double cm[2] = {0.0, 0.0};
-      double zt = 0.0, zg = 0.0;
-      for (int c = lane, q = 0; c < NC; c += 32, ++q) {
-        double m = 0.0, g = 0.0;
-        for (int w = 0; w < kCW; ++w) {
-          const float4 r = R(si, c, w);
-          m += mass_of(r);
-          if (DT >= 0 && r.w != 0.f) g += (double)r.w * (double)exp2f((r.z - gm) * cT);
-        }
-        if (q < 2) cm[q] = m;
-        zt += m;
-        zg += g;
+      // --- temperature-softmax statistics of row j from the running state:
+      // row max lm, reference LM, every tile's mass scaled exactly to 2^LM ---
+      const int32_t d = j < nb ? S.dtok : -1;
+      const float lm = run[0].nan ? __int_as_float(0x7fc00000) : run[0].mx;
+      const float LM = run[0].ref;
+      const double zx = (double)run[0].sum.hi + (double)run[0].sum.lo;
+      float gm = NEG_INF, GM = NEG_INF;
+      double zg = 0.0, egd = 0.0;
+      if (DT >= 0 && j < nb) {
+        gm = run[1].nan ? __int_as_float(0x7fc00000) : run[1].mx;
+        GM = run[1].ref;
+        zg = (double)run[1].sum.hi + (double)run[1].sum.lo;
+        egd = (double)exp_ref(S.gd, GM, P.cT, P.cTl);  // draft model's d, units 2^GM
       }
-      zt = warp_sum_d(zt);
-      if (DT >= 0) zg = warp_sum_d(zg);
-      const float NEG_INF = -__int_as_float(0x7f800000);
+      // one-hot: the sums leave d out (zx), so that a rejection's residual is
+      // exact; with draft logits they hold every token
+      const double ed = d >= 0 ? (double)exp_ref(S.xd, LM, P.cT, P.cTl) : 0.0;
+      const double zt = DT < 0 ? zx + ed : zx;
       const bool bad_t = !(lm > NEG_INF) || isinf(lm) || !isfinite(zt) || !(zt > 0.0);
       const bool bad_g = DT >= 0 && j < nb &&
                          (!(gm > NEG_INF) || isinf(gm) || !isfinite(zg) || !(zg > 0.0));
       if (lane == 0) {
         if (P.dbg.row_m) P.dbg.row_m[ro] = lm / P.T;
-        if (P.dbg.row_z) P.dbg.row_z[ro] = (float)zt;
+        // Z relative to the row max: sum exp(x/T - m) = zt * 2^(LM - lm log2(e)/T)
+        if (P.dbg.row_z) P.dbg.row_z[ro] = (float)(zt * exp2((double)LM - (double)lm * P.cTd));
       }
       if (bad_t || bad_g) {
         finish(b, -1, -1, SAMSPEC_ST_BADROW);
-        release(si);
+        release();
         return;
       }
-      float ua, ur;
-      verify_coins(P.seed, P.step, (uint32_t)b, (uint32_t)j, &ua, &ur);
-      int32_t d = -1;
-      double ed = 0.0;
       if (j < nb) {
-        d = P.draft[(size_t)b * P.K + j];
-        const float ld = load_logit(P.target, C::ST, ro * P.V + d);
-        ed = exp(((double)ld - (double)lm) / P.Td);
         const double pd = ed / zt;
-        double qd = 1.0;
-        if (DT >= 0) {
-          const float gd = load_logit(P.draftl, C::SD, ((size_t)b * P.K + j) * P.V + d);
-          qd = exp(((double)gd - (double)gm) / P.Td) / zg;
-        }
+        const double qd = DT >= 0 ? egd / zg : 1.0;
         if (lane == 0) {
           if (P.dbg.p_d) P.dbg.p_d[ro] = (float)pd;
           if (P.dbg.q_d) P.dbg.q_d[ro] = (float)qd;
         }
         // accept iff u * q(d) <= p(d)  (eps <= alpha(x) with alpha = min(1, p/q))
         if ((double)ua * qd <= pd) {
-          post(si, kStats, j + 1);
+          post(kStats, j + 1);
           return;
         }
       }
@@ -705,69 +880,62 @@ struct Control {
         // residual max(0, p - q) needs both rows' full statistics: one more pass
         if (lane == 0) {
           S.L = j;
-          S.lmax = lm;
-          S.gmax = gm;
+          S.lmax = LM;
+          S.gmax = GM;
           S.invZ = (float)(1.0 / zt);
           S.invZg = (float)(1.0 / zg);
           S.smode = 1;
         }
-        post(si, kResid, j);
+        __syncwarp();
+        post(kResid, j);
         return;
       }
-      // one-hot rejection: r = p without the rejected token; bonus: r = p.
-      // Units: exp(x - m); the row's Z is their total.
-      int excl = -1;
-      double sum_r = zt;
-      int cd = -1, wd = -1;
-      if (j < nb && zt - ed > 0.0) {
-        excl = d;
-        sum_r = zt - ed;
-        cd = d / C::E_TILE;
-        wd = (d - cd * C::E_TILE) / C::SL;
-        if ((cd & 31) == lane && (cd >> 5) < 2) {
-          const double nm = cm[cd >> 5] - ed;
-          cm[cd >> 5] = nm > 0.0 ? nm : 0.0;
-        }
+      // one-hot rejection: r = p without the rejected token, which the slice
+      // sums already leave out; bonus row (no draft): r = p.  Units 2^LM.
+      if (j < nb && !(zx > 0.0)) {
+        // every other token has zero mass: p is concentrated on d itself
+        if (lane == 0 && P.dbg.res_mass) P.dbg.res_mass[b] = 1.f;
+        finish(b, j, d, 0);
+        release();
+        return;
       }
-      if (lane == 0 && P.dbg.res_mass) P.dbg.res_mass[b] = (float)(sum_r / zt);
-      const double t = (double)ur * sum_r;
+      if (lane == 0 && P.dbg.res_mass) P.dbg.res_mass[b] = (float)(zx / zt);
+      const double tt = (double)ur * zx;
       auto slice_mass = [&](int c, int w) -> double {
-        double m = mass_of(R(si, c, w));
-        if (c == cd && w == wd) m = m - ed > 0.0 ? m - ed : 0.0;
-        return m;
+        const float4 r = R(c, w).a;
+        if (r.y == NEG_INF || r.z == 0.f) return 0.0;
+        return ldexp((double)r.z, (int)(r.y - LM));
       };
-      const int out = resample(b, j, t, cm, slice_mass, 0, excl, lm, gm, 0.f, 0.f);
+      auto scan = [&](int c, int w, double tw) -> int {
+        // the slice's own units: 2^R_w
+        const float Rw = R(c, w).a.y;
+        return slice_scan(b, j, c, w, ldexp(tw, (int)(LM - Rw)), 0, d, Rw, 0.f, 0.f, 0.f);
+      };
+      const int out = resample(tt, LM, slice_mass, scan);
       finish(b, j, out, 0);
-      release(si);
+      release();
       return;
     }
 
-    // kResid: per-slice residual masses of row L from the second pass
+    // kResid: the running residual mass of row L and its tile prefixes
     const int L = S.L;
-    double cm[2] = {0.0, 0.0};
-    double tot = 0.0;
-    for (int c = lane, q = 0; c < NC; c += 32, ++q) {
-      double m = 0.0;
-      for (int w = 0; w < kCW; ++w) m += (double)R(si, c, w).x;
-      if (q < 2) cm[q] = m;
-      tot += m;
-    }
-    tot = warp_sum_d(tot);
+    const double tot = (double)run[0].sum.hi + (double)run[0].sum.lo;
     if (S.smode == 1 && (!(tot > 0.0) || !isfinite(tot))) {
       // zero residual (impossible in exact arithmetic): sample p instead
       if (lane == 0) S.smode = 0;
-      post(si, kResid, L);
+      __syncwarp();
+      post(kResid, L);
       return;
     }
-    float ua, ur;
-    verify_coins(P.seed, P.step, (uint32_t)b, (uint32_t)L, &ua, &ur);
     if (lane == 0 && P.dbg.res_mass) P.dbg.res_mass[b] = (float)(S.smode ? tot : 1.0);
-    const double t = (double)ur * tot;
-    auto slice_mass = [&](int c, int w) -> double { return (double)R(si, c, w).x; };
-    const int out =
-        resample(b, L, t, cm, slice_mass, S.smode, -1, S.lmax, S.gmax, S.invZ, S.invZg);
+    const double tt = (double)ur * tot;
+    auto slice_mass = [&](int c, int w) -> double { return (double)R(c, w).a.x; };
+    auto scan = [&](int c, int w, double tw) -> int {
+      return slice_scan(b, L, c, w, tw, S.smode, -1, S.lmax, S.gmax, S.invZ, S.invZg);
+    };
+    const int out = resample(tt, 0.f, slice_mass, scan);
     finish(b, L, out, 0);
-    release(si);
+    release();
   }
 };
 
@@ -777,8 +945,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
   extern __shared__ __align__(1024) unsigned char dsm[];
   Smem& sm = *reinterpret_cast<Smem*>(dsm);
   const size_t rec_off = (sizeof(Smem) + 15) & ~(size_t)15;
-  float4* rec = reinterpret_cast<float4*>(dsm + rec_off);
-  const size_t rec_bytes = (size_t)kSlots * P.NC * kCW * sizeof(float4);
+  Rec* rec = reinterpret_cast<Rec*>(dsm + rec_off);
+  const size_t rec_bytes = (size_t)kSlots * P.NC * kCW * sizeof(Rec);
   unsigned char* stages = dsm + ((rec_off + rec_bytes + 1023) & ~(size_t)1023);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -792,11 +960,16 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
     }
     for (int s = 0; s < kSlots; ++s) {
       sm.slot[s].state = kEmpty;
-      sm.slot[s].cnt = 0;
     }
-    sm.ctrl_done = 0;
     sm.abort = 0;
     sm.prod_idle = 0;
+    sm.jobs_issued = 0;
+    sm.ctrl_exited = 0;
+    sm.claims = 0;
+    sm.pool_left = P.B;
+    sm.claim_lock = 0;
+    for (int s = 0; s < kSlots; ++s)
+      for (int c = 0; c < kMaxChunks; ++c) sm.tile_cnt[s][c] = 0;
     mbar_fence_init();
   }
   __syncthreads();
@@ -827,36 +1000,54 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[cs]);
       const bool full = tg.nel == C::E_TILE;
-      float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+      Rec r;
+      r.a = make_float4(0.f, 0.f, 0.f, 0.f);
+      r.b = r.a;
       if (tg.kind == kStats) {
         if (GREEDY) {
-          r = full ? reduce_greedy<TT, DT, true>(sl, warp, lane, tg.nel, tg.elem0)
-                   : reduce_greedy<TT, DT, false>(sl, warp, lane, tg.nel, tg.elem0);
+          r.a = full ? reduce_greedy<TT, DT, true>(sl, warp, lane, tg.nel)
+                     : reduce_greedy<TT, DT, false>(sl, warp, lane, tg.nel);
         } else {
-          const float2 a = full ? reduce_softmax<TT, DT, true, false>(sl, warp, lane, tg.nel, P.cT)
-                                : reduce_softmax<TT, DT, false, false>(sl, warp, lane, tg.nel, P.cT);
-          r.x = a.x;
-          r.y = a.y;
+          // one-hot drafts: the row's draft token is left out of the sums
+          // (tile index, or -1), so the residual of a rejection is exact
+          const int ex = (DT < 0 && tg.dtok >= 0) ? tg.dtok - tg.elem0 : -1;
+          r.a = full ? reduce_softmax<TT, DT, true, false>(sl, warp, lane, tg.nel, P.cT, ex)
+                     : reduce_softmax<TT, DT, false, false>(sl, warp, lane, tg.nel, P.cT, ex);
           if (DT >= 0 && tg.has_draft) {
-            const float2 g = full ? reduce_softmax<TT, DT, true, true>(sl, warp, lane, tg.nel, P.cT)
-                                  : reduce_softmax<TT, DT, false, true>(sl, warp, lane, tg.nel, P.cT);
-            r.z = g.x;
-            r.w = g.y;
+            r.b = full ? reduce_softmax<TT, DT, true, true>(sl, warp, lane, tg.nel, P.cT, ex)
+                       : reduce_softmax<TT, DT, false, true>(sl, warp, lane, tg.nel, P.cT, ex);
           }
         }
       } else {  // kResid
-        r.x = full ? reduce_resid<TT, DT, true>(sl, warp, lane, tg.nel, S, P.cT)
+        r.a = full ? reduce_resid<TT, DT, true>(sl, warp, lane, tg.nel, S, P.cT)
                    : reduce_resid<TT, DT, false>(sl, warp, lane, tg.nel, S, P.cT);
       }
+      if (tg.dtok >= 0) {
+        // the lane holding the draft token keeps its logits for the decision
+        const int o = tg.dtok - tg.elem0 - warp * C::SL;
+        if (o >= 0 && o < C::SL && o + warp * C::SL < tg.nel) {
+          const int v = o / C::VEC, kk = o % C::VEC;
+          if ((v & 31) == lane) {
+            const int ii = v >> 5;
+            float x = 0.f, g = 0.f;
+#pragma unroll
+            for (int i = 0; i < C::VPL; ++i)
+#pragma unroll
+              for (int k = 0; k < C::VEC; ++k)
+                if (i == ii && k == kk) {
+                  x = sl.t[i].at(k);
+                  if (DT >= 0 && tg.has_draft) g = sl.d[i].at(k);
+                }
+            S.xd = x;
+            S.gd = g;
+          }
+        }
+      }
+      __syncwarp();
       if (lane == 0) {
         rec[((size_t)tg.slot * P.NC + tg.chunk) * kCW + warp] = r;
-        __threadfence_block();
-        const int old = atomicAdd(&S.cnt, 1);
-        if (old == P.NC * kCW - 1) {
-          S.cnt = 0;
-          __threadfence_block();
-          vstore(&S.state, kDone);
-        }
+        __threadfence_block();  // the record (and captured logits) before the count
+        atomicAdd(&sm.tile_cnt[tg.slot][tg.chunk], 1);
       }
       __syncwarp();
       if (++cs == NS) {
@@ -869,26 +1060,29 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
     if (lane == 0) {
       int ps = 0;
       uint32_t pph = 0;
-      int rr = 0;
       uint64_t t_idle = gtimer();
       for (;;) {
         if (vload(&sm.abort)) break;
-        int si = -1;
-        for (int k = 0; k < kSlots && si < 0; ++k) {
-          const int s = (rr + k) % kSlots;
-          if (vload(&sm.slot[s].state) == kReady) si = s;
+        int si = -1, best_age = 0x7fffffff;
+        for (int s = 0; s < kSlots; ++s) {
+          if (vload(&sm.slot[s].state) == kReady) {
+            const int a = vload(&sm.slot[s].age);
+            if (a < best_age) {
+              best_age = a;
+              si = s;
+            }
+          }
         }
         if (si < 0) {
           vstore(&sm.prod_idle, 1);
-          if (vload(&sm.ctrl_done)) break;
+          if (vload(&sm.ctrl_exited) == kSlots) break;
           if (gtimer() - t_idle > kWaitNs) {
             vstore(&sm.abort, 1);
             break;
           }
-          __nanosleep(32);
+          __nanosleep(128);
           continue;
         }
-        rr = si + 1;
         vstore(&sm.prod_idle, 0);
         __threadfence_block();
         Slot& S = sm.slot[si];
@@ -919,6 +1113,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
           tg.has_draft = with_draft ? 1 : 0;
           tg.b = b;
           tg.j = j;
+          tg.dtok = kind == kStats ? S.dtok : -1;
           unsigned char* dst = stages + (size_t)ps * kStageBytes;
           if (P.direct) {
             mbar_arrive(&sm.full[ps]);
@@ -943,6 +1138,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
           vstore(&sm.abort, 1);
           break;
         }
+        vstore(&sm.jobs_issued, vload(&sm.jobs_issued) + 1);
         t_idle = gtimer();
       }
       if (!vload(&sm.abort)) {
@@ -974,64 +1170,110 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         }
       }
     }
-  } else if (warp == kCtrlWarp) {
-    // -------------------------------- control -------------------------------
-    // One sequence per CTA to begin with; another is claimed only once the
-    // producer has issued everything posted (its ring still holds up to NS
-    // tiles, which covers the claim), so small batches spread over all CTAs
-    // and large ones keep every producer busy.
-    Control<TT, DT, GREEDY> ctl(P, sm, rec, lane);
-    ctl.refill(0);
+  } else if (warp >= kCtrlWarp && warp < kCtrlWarp + kSlots) {
+    // ----------------------------- control warps ----------------------------
+    // One warp per sequence slot.  Slot 0 claims at once; the others wait
+    // until the producer has issued this CTA's first row (every CTA of the
+    // grid has started by then), so that small batches spread over all CTAs
+    // while large ones keep four sequences in flight per CTA.
+    const int si = warp - kCtrlWarp;
+    Slot& S = sm.slot[si];
+    Control<TT, DT, GREEDY> ctl(P, sm, rec, lane, si);
+    int last_jobs = -1;
     uint64_t t_idle = gtimer();
     for (;;) {
-      int si = -1, free_slot = -1, ready = 0;
-      if (lane == 0)
-        for (int s = 0; s < kSlots; ++s) {
-          const int st = vload(&sm.slot[s].state);
-          if (st == kDone && si < 0) si = s;
-          if (st == kEmpty && free_slot < 0) free_slot = s;
-          ready += st == kReady;
+      if (vload(&sm.abort)) break;
+      const int st = __shfl_sync(kFullMask, vload(&S.state), 0);
+      if (st == kEmpty) {
+        // claim when this is the CTA's first sequence, or when no row is queued
+        // and the producer has issued everything (its ring covers the claim)
+        int go = 0;
+        if (lane == 0) {
+          const bool first = si == 0 && vload(&sm.claims) == 0;
+          bool want = first;
+          if (!want && vload(&sm.jobs_issued) > 0) {
+            // steady state: keep sequences in flight so that one streams while
+            // another's decision is taken; once fewer sequences are
+            // left than CTAs, claim only when the producer has run dry, so the
+            // last sequences spread over the CTAs instead of queueing in few
+            int busy = 0, ready = 0;
+            for (int s2 = 0; s2 < kSlots; ++s2) {
+              const int st2 = vload(&sm.slot[s2].state);
+              busy += st2 != kEmpty;
+              ready += st2 == kReady;
+            }
+            const bool dry = vload(&sm.prod_idle) && ready == 0;
+            // decisions after sampling take longer (resample): keep more in flight
+            const int target = GREEDY ? 2 : 3;
+            want = dry || (busy < target && vload(&sm.pool_left) >= (int)gridDim.x);
+          }
+          if (!want && vload(&sm.ctrl_exited) > 0) want = true;  // nothing else to wait for
+          go = want && atomicCAS(&sm.claim_lock, 0, 1) == 0;
         }
-      si = __shfl_sync(kFullMask, si, 0);
-      free_slot = __shfl_sync(kFullMask, free_slot, 0);
-      ready = __shfl_sync(kFullMask, ready, 0);
-      if (si >= 0) {
-        __threadfence_block();
-        ctl.handle(si);
-        t_idle = gtimer();
-        continue;
-      }
-      if (ctl.more && ready == 0 && free_slot >= 0 && vload(&sm.prod_idle)) {
-        ctl.refill(free_slot);
-        t_idle = gtimer();
-        continue;
-      }
-      int stop = 0;
-      if (lane == 0) {
-        if (vload(&sm.abort)) {
-          stop = 1;
-        } else {
-          bool all_empty = true;
-          for (int s = 0; s < kSlots; ++s) all_empty &= vload(&sm.slot[s].state) == kEmpty;
-          if (all_empty && !ctl.more) {
-            vstore(&sm.ctrl_done, 1);
-            stop = 1;
+        go = __shfl_sync(kFullMask, go, 0);
+        if (go) {
+          ctl.refill();
+          __syncwarp();
+          if (lane == 0) atomicExch(&sm.claim_lock, 0);
+          if (!ctl.more && __shfl_sync(kFullMask, vload(&S.state), 0) == kEmpty) break;
+          t_idle = gtimer();
+          continue;
+        }
+        // an idle slot waits as long as the CTA makes progress
+        int timeout = 0;
+        if (lane == 0) {
+          const int ji = vload(&sm.jobs_issued);
+          if (ji != last_jobs) {
+            last_jobs = ji;
+            t_idle = gtimer();
           } else if (gtimer() - t_idle > kWaitNs) {
             vstore(&sm.abort, 1);
-            stop = 1;
+            timeout = 1;
           }
         }
+        if (__shfl_sync(kFullMask, timeout, 0)) break;
+        __nanosleep(256);
+        continue;
       }
-      stop = __shfl_sync(kFullMask, stop, 0);
-      if (stop) break;
-      __nanosleep(32);
+      // a job is posted: merge its tiles as their records complete (while the
+      // rest of the row streams), then decide
+      bool ok = true;
+      uint64_t t0 = gtimer();
+      for (int c = 0; c < P.NC;) {
+        const int cnt = __shfl_sync(kFullMask, vload(&sm.tile_cnt[si][c]), 0);
+        if (cnt == kCW) {
+          __threadfence_block();
+          ctl.merge_tile(c);
+          if (lane == 0) sm.tile_cnt[si][c] = 0;
+          ++c;
+          t0 = gtimer();
+          continue;
+        }
+        int stop = 0;
+        if (lane == 0) stop = vload(&sm.abort) || gtimer() - t0 > kWaitNs;
+        if (__shfl_sync(kFullMask, stop, 0)) {
+          ok = false;
+          break;
+        }
+        __nanosleep(64);
+      }
+      if (!ok) {
+        if (lane == 0) vstore(&sm.abort, 1);
+        break;
+      }
+      ctl.handle();
+      t_idle = gtimer();
     }
-    if (vload(&sm.abort) && lane == 0) {
-      // sequences held by this CTA's slots, and any nobody will claim now
-      for (int s = 0; s < kSlots; ++s)
-        if (sm.slot[s].state != kEmpty) write_result(P, sm.slot[s].b, -1, -1, SAMSPEC_ST_TIMEOUT);
-      for (uint32_t b = atomicAdd(&P.ws[0], 1u); b < (uint32_t)P.B; b = atomicAdd(&P.ws[0], 1u))
-        write_result(P, (int)b, -1, -1, SAMSPEC_ST_TIMEOUT);
+    if (lane == 0) {
+      if (vload(&sm.abort)) {
+        // this slot's sequence, and (slot 0) any nobody will claim now
+        if (S.state != kEmpty) write_result(P, S.b, -1, -1, SAMSPEC_ST_TIMEOUT);
+        if (si == 0)
+          for (uint32_t b = atomicAdd(&P.ws[0], 1u); b < (uint32_t)P.B; b = atomicAdd(&P.ws[0], 1u))
+            write_result(P, (int)b, -1, -1, SAMSPEC_ST_TIMEOUT);
+      }
+      __threadfence_block();
+      atomicAdd(&sm.ctrl_exited, 1);
     }
   }
   __syncthreads();
@@ -1062,7 +1304,7 @@ int launch(const VParams& P0, cudaStream_t stream) {
   if (P.NC > kMaxChunks) return SAMSPEC_ESIZE;
   const size_t rec_off = (sizeof(Smem) + 15) & ~(size_t)15;
   const size_t head =
-      (rec_off + (size_t)kSlots * P.NC * kCW * sizeof(float4) + 1023) & ~(size_t)1023;
+      (rec_off + (size_t)kSlots * P.NC * kCW * sizeof(Rec) + 1023) & ~(size_t)1023;
   // Device properties and the kernel's shared-memory opt-in are set up once per
   // device, so that later launches make no runtime calls besides the launch
   // itself (safe inside stream capture).
@@ -1158,7 +1400,9 @@ int spec_verify(const void* d_target, int32_t target_dtype, const void* d_draft_
   P.V = V;
   P.T = temperature;
   P.Td = (double)temperature;
-  P.cT = greedy ? 0.f : (float)(1.4426950408889634 / (double)temperature);
+  P.cTd = greedy ? 0.0 : 1.4426950408889634 / (double)temperature;
+  P.cT = (float)P.cTd;
+  P.cTl = (float)(P.cTd - (double)P.cT);
   P.seed = seed;
   P.step = step;
   P.accept_len = d_accept_len;
