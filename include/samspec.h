@@ -216,6 +216,32 @@ int spec_verify(const void* d_target, int32_t target_dtype, const void* d_draft_
                 int32_t* d_emit_len, int32_t* d_status, const spec_verify_debug* dbg,
                 void* d_workspace, size_t ws_bytes, samspec_stream_t stream);
 
+/* spec_verify for callers that cannot allocate device memory: code running
+ * where cudaMalloc is off limits (a host framework that owns every device
+ * allocation through its own pool, a plugin loaded into such a runtime, or a
+ * caller in a context where allocating would synchronise the device).  The
+ * paper has no counterpart; it is a convenience of this library.
+ *
+ * Same arguments, outputs and limits as spec_verify, without the workspace:
+ * its scratch (the kernel's work counters) is a fixed 256-byte array inside
+ * the library, present on every device that loads it until the process
+ * exits.  Sizes whose workspace would not fit it return SAMSPEC_ESIZE.  The
+ * call allocates nothing: it clears the array with cudaMemsetAsync on
+ * `stream` and launches the same kernel as spec_verify.
+ *   - The first call on a device looks the array's device address up (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls on a device share the one array: two calls whose kernels
+ *     overlap on the GPU (different streams, no ordering between them) race
+ *     on it and give wrong results.  Serialise them, or use spec_verify with
+ *     a workspace each. */
+int spec_verify_noalloc(const void* d_target, int32_t target_dtype, const void* d_draft_logits,
+                        int32_t draft_dtype, const int32_t* d_draft, const int32_t* d_draft_len,
+                        int32_t B, int32_t K, int32_t V, float temperature, uint64_t seed,
+                        uint64_t step, int32_t* d_accept_len, int32_t* d_out_token,
+                        int32_t* d_emit, int32_t* d_emit_len, int32_t* d_status,
+                        const spec_verify_debug* dbg, samspec_stream_t stream);
+
 /* Philox4x32-10 uniforms exactly as spec_verify draws them, for inspection:
  * d_u[2 * (b * (K+1) + j) + {0,1}] = (u_j, u'_j) of sequence b, for
  * 0 <= b < B and 0 <= j <= K ([B, K+1, 2] fp32, device).  Asynchronous. */

@@ -39,6 +39,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -1351,6 +1352,35 @@ int dispatch(const VParams& P, int tdt, int ddt, cudaStream_t stream) {
 
 using namespace samspec;
 
+// Scratch of spec_verify_noalloc: the kernel's three work counters (claimed
+// sequences, finished CTAs, error flag), in a fixed array that every device
+// loading this library holds until the process exits.
+constexpr size_t kNoAllocScratchBytes = 256;
+static __device__ __align__(256) uint32_t noalloc_scratch[kNoAllocScratchBytes / 4];
+
+namespace {
+
+// Device address of noalloc_scratch on the current device.  On the host the
+// array's name only stands in for the symbol, so the address is looked up
+// once per device (with that device current) and cached.
+int noalloc_scratch_address(void** out) {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDev] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return SAMSPEC_ECUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, noalloc_scratch) != cudaSuccess || !p) return SAMSPEC_ECUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return SAMSPEC_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 size_t spec_verify_workspace_bytes(int32_t B, int32_t K, int32_t V) {
@@ -1425,6 +1455,27 @@ int spec_uniforms(int32_t B, int32_t K, uint64_t seed, uint64_t step, float* d_u
   uniforms_kernel<<<(unsigned)((n + 255) / 256), 256, 0,
                     reinterpret_cast<cudaStream_t>(stream)>>>(B, K, seed, step, d_u);
   return cudaGetLastError() == cudaSuccess ? SAMSPEC_OK : SAMSPEC_ECUDA;
+}
+
+int spec_verify_noalloc(const void* d_target, int32_t target_dtype, const void* d_draft_logits,
+                        int32_t draft_dtype, const int32_t* d_draft, const int32_t* d_draft_len,
+                        int32_t B, int32_t K, int32_t V, float temperature, uint64_t seed,
+                        uint64_t step, int32_t* d_accept_len, int32_t* d_out_token,
+                        int32_t* d_emit, int32_t* d_emit_len, int32_t* d_status,
+                        const spec_verify_debug* dbg, samspec_stream_t stream) {
+  const size_t need = spec_verify_workspace_bytes(B, K, V);
+  if (need > kNoAllocScratchBytes) return SAMSPEC_ESIZE;
+  void* ws = nullptr;
+  const int rc = noalloc_scratch_address(&ws);
+  if (rc != SAMSPEC_OK) return rc;
+  // the counters must start at zero; the array keeps whatever the last call
+  // on this device left there
+  if (need > 0 &&
+      cudaMemsetAsync(ws, 0, need, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SAMSPEC_ECUDA;
+  return spec_verify(d_target, target_dtype, d_draft_logits, draft_dtype, d_draft, d_draft_len, B,
+                     K, V, temperature, seed, step, d_accept_len, d_out_token, d_emit, d_emit_len,
+                     d_status, dbg, ws, kNoAllocScratchBytes, stream);
 }
 
 }  // extern "C"
