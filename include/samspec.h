@@ -87,7 +87,7 @@ const char* samspec_strerror(int code);
  * creation order, a split's new state before its clone, so the arrays are
  * identical to those of a plain sequential construction.
  *
- * Capacities per sequence for capacity_tokens = C: C tokens, 2C states,
+ * Capacities per sequence for capacity_tokens = C: C tokens, 2C + 1 states,
  * 3C + 4 transitions, and a power-of-two hash of at least 1.5 x (3C + 4)
  * slots.  Limits: 1 <= B <= 2^20, 1 <= C <= 2^22 - 1, 1 <= vocab <= 2^18.
  * ========================================================================= */
@@ -195,8 +195,11 @@ int sam_dump_sequence(sam_batch* batch, int32_t b, int32_t* h_scalars, int32_t* 
  * Workspace: d_workspace of spec_verify_workspace_bytes(B, K, V) bytes,
  * 256-byte aligned, zeroed once with spec_verify_workspace_init before first
  * use and not shared by two calls in flight.  Logits pointers must be 16-byte
- * aligned.  Limits: 1 <= B <= 2^24, 1 <= K <= 32, 1 <= V <= 2^24.
- * Asynchronous; one kernel launch. */
+ * aligned.  Limits: 1 <= B <= 2^24, 1 <= K <= 32, and V at most 64 tiles of
+ * the kernel's 32 KB staging buffer: 524288 (fp32 target, greedy or one-hot
+ * drafts), 1048576 (bf16 target, greedy or one-hot), 524288 (bf16 target and
+ * bf16 draft logits), 262144 (any other pair with draft logits); larger V
+ * returns SAMSPEC_ESIZE.  Asynchronous; one kernel launch. */
 typedef struct spec_verify_debug {
   float* row_m;
   float* row_z;

@@ -10,7 +10,7 @@
 //
 // GB300 layout: per sequence, struct-of-arrays regions in one caller-owned
 // workspace --
-//   states  int4 {len, link, min_endpos, edge_head}   [2C]
+//   states  int4 {len, link, min_endpos, edge_head}   [2C+1]
 //   edges   int2 {token, next}  (per-state out-transition lists) [3C+4]
 //   hash    u64 open-addressed (state, token) -> state, linear probing,
 //           probed 32 slots at a time by the whole warp (one 256-byte window)

@@ -39,6 +39,29 @@ def test_host_only_calls():
     assert lib.samspec_strerror(-1) == b"invalid argument"
 
 
+def test_spec_verify_rejects_bad_arguments_on_the_host():
+    """Argument checks return before any device work, so they run without a
+    GPU: the pointers below are aligned placeholders that are never touched."""
+    import sam_drafting_verification_gb300._binding as bd
+    lib = bd.lib()
+    p = ctypes.c_void_p(4096)
+
+    def call(dtype=bd.F32, K=1, V=1000, T=1.0, ws_bytes=256, target=p):
+        return lib.spec_verify(target, dtype, None, bd.F32, p, None, 1, K, V, T, 0, 0, p, p,
+                               None, None, None, None, p, ws_bytes, None)
+
+    assert call(target=None) == bd.EINVAL
+    assert call(K=0) == bd.ESIZE and call(K=33) == bd.ESIZE
+    assert call(T=-1.0) == bd.EINVAL and call(T=float("nan")) == bd.EINVAL
+    assert call(dtype=7) == bd.EDTYPE
+    assert call(ws_bytes=16) == bd.ESIZE
+    assert call(target=ctypes.c_void_p(4100)) == bd.EALIGN
+    # V above 64 staging tiles: 8192 fp32 / 16384 bf16 logits per tile
+    assert call(dtype=bd.F32, V=64 * 8192 + 1) == bd.ESIZE
+    assert call(dtype=bd.BF16, V=64 * 16384 + 1) == bd.ESIZE
+    assert call(dtype=bd.F32, V=64 * 8192 + 1, T=0.0) == bd.ESIZE
+
+
 def test_binding_refuses_missing_library(tmp_path):
     import sam_drafting_verification_gb300._binding as bd
     with pytest.raises(bd.SamspecError):
