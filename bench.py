@@ -18,7 +18,7 @@ stream; max over ranks.  Under torchrun every rank runs its own batch (weak
 scaling, no collective on the data path).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                  [--workload rs_bf16_b64|sweep_b1024]
+                  [--workload rs_bf16_b64|sweep_b1024|long_rollout_b256]
 """
 from __future__ import annotations
 
@@ -40,6 +40,29 @@ import workloads  # noqa: E402
 
 METRIC = "verified sequence-steps/s and spec_verify HBM GB/s vs 8 TB/s; SAM ns/seq-step"
 POOL = 16
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
+# verify kernel, from the ncu captures summarised under profiles/, keyed by
+# workload, with the SHA-256 of verify.cu they were taken on: a changed kernel
+# reports null until it is captured again.
+VERIFY_TRAFFIC = {
+    "rs_bf16_b64": {"bytes": 19544192.0, "profile": "profiles/verify_kernel_rs_bf16_b64.md",
+                    "verify_cu_sha256": "9b8d7ccf5a3f87e5dc2be592ed0901ce44a9b9b9fd7635586796b575bf2b0393"},
+    "long_rollout_b256": {"bytes": 79012000.0, "profile": "profiles/launches_long_rollout_b256.md",
+                          "verify_cu_sha256": "9b8d7ccf5a3f87e5dc2be592ed0901ce44a9b9b9fd7635586796b575bf2b0393"},
+}
+
+
+def _verify_traffic(workload):
+    import hashlib
+    t = VERIFY_TRAFFIC.get(workload)
+    if t is None:
+        return None
+    src = os.path.join(ROOT, "sam_drafting_verification_gb300", "csrc", "verify.cu")
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != t["verify_cu_sha256"]:
+            return None
+    return t["bytes"]
 
 
 def _peaks():
@@ -181,6 +204,8 @@ def run_gpu(args):
     torch.cuda.set_device(dev)
     if args.workload == "sweep_b1024":
         return run_sweep(args, ws, rank, dev)
+    if args.workload == "long_rollout_b256":
+        return run_rollout(args, ws, rank, dev)
 
     B, V, K, T, n = 64, workloads.V_LARGE, 3, 1.0, 4096
     hist, cont = rs_inputs(rank, B, V, n, K)
@@ -298,7 +323,7 @@ def run_gpu(args):
     achieved = verify_bytes / (verify_ms / 1e3) / 1e9
     roof = {"kernel": "verify_kernel<bf16, one-hot, T>0>", "bound": "hbm",
             "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-            "frac": round(achieved / hbm, 4), "traffic": None,
+            "frac": round(achieved / hbm, 4), "traffic": _verify_traffic("rs_bf16_b64"),
             "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
             "algorithmic_bytes_per_launch": verify_bytes,
             "kernel_ms": round(verify_ms, 5)}
@@ -419,6 +444,177 @@ def cpu_baseline_rs(hist, cont, nseq=64, nsteps=40):
 
 
 # --------------------------------------------------------------------------
+# long-tail rollout: B=256 long histories, 512 decode steps
+# --------------------------------------------------------------------------
+
+def run_rollout(args, ws, rank, dev):
+    """B=256 histories log-uniform in [16k, 32k] tokens (Zipf(1.1), copy prob
+    0.5, spans 16-256), V=151936: one prefill build, then 512 steps of
+    (extend by the stream's next U{1..4} tokens + draft K=3, greedy verify of
+    the drafts on bf16 logits [256, 4, V] ~ N(0, sd 2)).  The SAM step is also
+    timed alone (ns per sequence-step) next to the oracle's extend + draft on
+    a sample of the same sequences."""
+    import torch
+
+    import sam_drafting_verification_gb300 as ss
+    w = workloads.long_rollout(seed=1004 + 7919 * rank)
+    B, V, K, steps = w["B"], w["V"], w["K"], w["steps"]
+    lens, n_new, streams = w["lens"], w["n_new"], w["streams"]
+    cap = int(max(len(x) for x in streams))
+    maxlen = int(lens.max())
+    pre = np.zeros((B, maxlen), np.int32)
+    toks = np.zeros((steps, B, 4), np.int32)
+    for b in range(B):
+        pre[b, :lens[b]] = streams[b][:lens[b]]
+        pos = int(lens[b])
+        for s in range(steps):
+            k = int(n_new[s, b])
+            toks[s, b, :k] = streams[b][pos:pos + k]
+            pos += k
+    batch = ss.SamBatch(B, cap, V, device=dev)
+    pre_d = torch.as_tensor(pre, device=dev)
+    lens_d = torch.as_tensor(lens, device=dev)
+    toks_d = torch.as_tensor(toks, device=dev)
+    nn_d = torch.as_tensor(n_new, device=dev)
+
+    # S1: prefill (one launch), timed after one untimed build
+    batch.extend(pre_d, lens_d)
+    torch.cuda.synchronize()
+    batch.reset()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    batch.extend(pre_d, lens_d)
+    e1.record()
+    torch.cuda.synchronize()
+    prefill_ms = e0.elapsed_time(e1)
+    assert (batch.status() == 0).all()
+    snap = batch.export()
+
+    npool = 4  # 4 x 311 MB of bf16 logits: each step's rows are not in L2
+    g = torch.Generator(device=dev)
+    g.manual_seed(4004 + rank)
+    pool = []
+    for _ in range(npool):
+        x = torch.empty((B, K + 1, V), dtype=torch.bfloat16, device=dev)
+        for b0 in range(0, B, 64):
+            x[b0:b0 + 64] = torch.empty((min(64, B - b0), K + 1, V), device=dev).normal_(0.0, 2.0, generator=g)
+        pool.append(x)
+    draft = torch.empty((B, K), dtype=torch.int32, device=dev)
+    dlen = torch.empty(B, dtype=torch.int32, device=dev)
+    mlen = torch.empty(B, dtype=torch.int32, device=dev)
+    mend = torch.empty(B, dtype=torch.int32, device=dev)
+    out = {"accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+           "out_token": torch.empty(B, dtype=torch.int32, device=dev),
+           "status": torch.empty(B, dtype=torch.int32, device=dev)}
+    wsv = ss.verify_workspace(B, K, V, dev)
+
+    def step(s, sam=True, verify=True):
+        if sam:
+            batch.step(toks_d[s], nn_d[s], K, out=(draft, dlen, mlen, mend))
+        if verify:
+            ss.spec_verify(pool[s % npool], draft, dlen, temperature=0.0, out=out, status=True,
+                           workspace=wsv)
+
+    def graph(**kw):
+        cs = torch.cuda.Stream(device=dev)
+        gr = torch.cuda.CUDAGraph()
+        cs.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(gr, stream=cs):
+                for s in range(steps):
+                    step(s, **kw)
+        torch.cuda.synchronize()
+        return gr
+
+    def timed(gr):
+        batch.import_(snap)
+        torch.cuda.synchronize()
+        _barrier(ws)
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        gr.replay()
+        b_.record()
+        torch.cuda.synchronize()
+        _barrier(ws)
+        return a.elapsed_time(b_)
+
+    for s in range(max(args.warmup, 3)):  # eager warm-up
+        step(s)
+    torch.cuda.synchronize()
+    batch.import_(snap)
+    g_full = graph()
+    g_sam = graph(verify=False)
+    timed(g_full)  # graph warm-up
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    full_ms = timed(g_full)
+    clk = clocks.stop()
+    assert (out["status"].cpu() == 0).all() and (batch.status() == 0).all()
+    sam_ms = timed(g_sam)
+    # drafts of the last step: the automata followed the streams exactly
+    st_ms = _max_over_ranks(full_ms / steps, ws, dev)
+    sam_ns = _max_over_ranks(sam_ms / steps / B * 1e6, ws, dev)
+    seqs = _sum_over_ranks(float(B), ws, dev)
+    verify_ms = max(full_ms - sam_ms, 1e-9) / steps
+    Lh = out["accept_len"].cpu().numpy().astype(np.int64)
+    hbm, peak_kind = _peaks()
+    vbytes = float((Lh + 1).sum()) * V * 2
+    achieved = vbytes / (verify_ms / 1e3) / 1e9
+
+    cpu = None
+    if rank == 0:
+        cpu = oracle_sam_rollout(streams, lens, toks, n_new, K, nseq=B)
+    line = {
+        "metric": METRIC, "value": round(seqs / (st_ms / 1e3), 1), "unit": "seq-steps/s",
+        "n_gpus": ws, "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": round(st_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32 (SAM), f32 (bf16 logits)",
+        "data": "synthetic",
+        "config": {"workload": "long_rollout_b256", "B_per_gpu": B, "V": V, "K": K, "steps": steps,
+                   "history": "log-uniform [16384, 32768]", "prefill_tokens": int(lens.sum()),
+                   "verify": "greedy, bf16 N(0, sd 2)",
+                   "l2": f"inputs larger than L2: {npool} logits tensors of {B * (K + 1) * V * 2 / 1e6:.0f} MB",
+                   "timing": "CUDA graph of the 512 steps, events on the capture stream"},
+        "roofline": {"kernel": "verify_kernel<bf16, greedy>", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "traffic": _verify_traffic("long_rollout_b256"),
+                     "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
+                     "algorithmic_bytes_per_launch": vbytes,
+                     "note": "verify time = (full step - SAM-only step) / steps"},
+        "cpu_baseline": cpu,
+        "gpu_launches": 2 * steps,
+        "clocks": clk,
+        "breakdown": {
+            "sam_step_ns_per_seq_step": round(sam_ns, 1),
+            "sam_vs_oracle": (round(cpu["value"] / sam_ns, 1) if cpu else None),
+            "verify_us_per_step": round(verify_ms * 1e3, 2),
+            "prefill_tokens_per_s": round(float(lens.sum()) / (prefill_ms / 1e3), 1),
+            "prefill_ms": round(prefill_ms, 3),
+        },
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def oracle_sam_rollout(streams, lens, toks, n_new, K, nseq):
+    """The oracle's extend + draft (one C call per step for the sample), on
+    the first nseq sequences of the rollout; the builds are untimed."""
+    import oracle
+    V = workloads.V_LARGE
+    sams = [oracle.Sam(V) for _ in range(nseq)]
+    for b in range(nseq):
+        sams[b].extend(streams[b][:lens[b]])
+    steps = toks.shape[0]
+    t0 = time.perf_counter()
+    for s in range(steps):
+        oracle.step_batch(sams, toks[s, :nseq], n_new[s, :nseq], K)
+    el = time.perf_counter() - t0
+    return {"value": round(el / (steps * nseq) * 1e9, 1), "unit": "ns/seq-step (SAM extend + draft)",
+            "cores": 1, "kind": "oracle",
+            "sample": f"{nseq} of the 256 sequences x {steps} steps, single thread, {el:.2f} s"}
+
+
+# --------------------------------------------------------------------------
 # verification sweep at B=1024
 # --------------------------------------------------------------------------
 
@@ -515,7 +711,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="rs_bf16_b64", choices=["rs_bf16_b64", "sweep_b1024"])
+    ap.add_argument("--workload", default="rs_bf16_b64", choices=["rs_bf16_b64", "sweep_b1024", "long_rollout_b256"])
     ap.add_argument("--point", default="", help="sweep_b1024 only: one point 'K,f32|bf16,greedy|T=1|greedy-full-read'")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":
