@@ -88,8 +88,9 @@ const char* samspec_strerror(int code);
  * identical to those of a plain sequential construction.
  *
  * Capacities per sequence for capacity_tokens = C: C tokens, 2C + 1 states,
- * 3C + 4 transitions, and a power-of-two hash of at least 1.5 x (3C + 4)
- * slots.  Limits: 1 <= B <= 2^20, 1 <= C <= 2^22 - 1, 1 <= vocab <= 2^18.
+ * 3C + 4 transitions (each state's out-tokens kept in a contiguous array of
+ * a pool of 4 x (3C + 4) ints), and a power-of-two hash of at least
+ * 1.5 x (3C + 4) slots.  Limits: 1 <= B <= 2^20, 1 <= C <= 2^22 - 1, 1 <= vocab <= 2^18.
  * ========================================================================= */
 typedef struct sam_batch sam_batch;
 

@@ -10,21 +10,33 @@
 //
 // GB300 layout: per sequence, struct-of-arrays regions in one caller-owned
 // workspace --
-//   states  int4 {len, link, min_endpos, edge_head}   [2C+1]
-//   edges   int2 {token, next}  (per-state out-transition lists) [3C+4]
-//   hash    u64 open-addressed (state, token) -> state, linear probing,
-//           probed 32 slots at a time by the whole warp (one 256-byte window)
+//   states  int4 {len, min_endpos, tok_off, n_out | log2(tok_cap) << 24} [2C+1]
+//   links   int32 suffix link per state                                  [2C+1]
+//   tokens  int32 pool of per-state out-token arrays: a state's tokens sit
+//           contiguously at tok_off, capacity a power of two >= 4, moved to
+//           an array of twice the size when full; 4 x (3C+4) ints bound all
+//           allocations
+//   hash    u64 open-addressed (state, token) -> state, linear probing
 //   history int32 tokens [C]
-//   scalars int32[8] {n, last, n_states, n_edges, status, link(last),
-//           len(last), 0}
+//   chain   int32 [128]: the suffix chain last, link(last), ..., root
+//   scalars int32[16] {n, last, n_states, n_transitions, status, link(last),
+//           len(last), token-pool top, chain length (0: not kept), 0...}
 // A hash slot packs (state + 1) in bits 63..41, the token in 40..23 and the
 // target state in 22..0; 0 marks an empty slot.  Slots are never deleted, so a
 // key, if present, lies before the first empty slot of its probe sequence.
 //
-// The construction is the textbook sequential one, executed by one warp:
-// every lane runs the same scalar control flow, and the lanes cooperate only in
-// the 32-slot hash probes.  States are numbered in creation order with the new
-// state before its clone, so the arrays equal a plain sequential build's.
+// The construction is the textbook sequential one, executed by one warp, with
+// the lanes working on independent pieces of one step.  The link walk of a
+// token visits the suffix chain of `last`; the warp keeps that chain in
+// registers (up to 128 states), so all its (state, token) keys are probed at
+// once instead of one link hop at a time: the new transitions, the out-token
+// appends, the split's redirections and the next chain (the new state, then
+// the distinct targets of the chain states that had the token, then the root)
+// all follow from that one round of probes.  A split copies the clone's
+// transitions 32 at a time.  Longer chains fall back to chasing links in
+// batches of 2, 4, ... 32 states.  States are numbered in
+// creation order with the new state before its clone, so the arrays equal a
+// plain sequential build's.
 
 #include <algorithm>
 #include <cstdint>
@@ -43,40 +55,61 @@ struct sam_batch {
   int64_t H;
   size_t ws_bytes;
   char* ws;
-  size_t off_states, off_edges, off_hash, off_hist, off_scal;
+  int64_t P;  // token-pool ints per sequence
+  size_t off_states, off_links, off_chain, off_pool, off_hash, off_hist, off_scal;
 };
 
 namespace samspec {
 namespace {
 
-constexpr int kScal = 8;
-enum { SC_N = 0, SC_LAST, SC_NS, SC_NE, SC_STATUS, SC_LINKLAST, SC_LENLAST };
+constexpr int kScal = 16;
+enum { SC_N = 0, SC_LAST, SC_NS, SC_NE, SC_STATUS, SC_LINKLAST, SC_LENLAST, SC_POOL, SC_CHAIN };
+
+// The suffix chain of `last` (last, link(last), ..., root) is kept explicitly
+// while it has at most kChainMax states: 4 registers per lane inside a launch,
+// kChainMax ints per sequence between launches.  SC_CHAIN holds its length,
+// 0 while the chain is longer (the walk then chases links).
+constexpr int kChR = 4;
+constexpr int kChainMax = 32 * kChR;
+
+// A state record: {len, min_endpos, tok_off, n_out | log2(tok_cap) << 24};
+// tok_off = -1 while the state has no out-token array.  Links live in their
+// own array (the walks chase them; 16 per 64-byte line).
+__device__ __forceinline__ int32_t rec_nout(int4 r) { return r.w & 0xFFFFFF; }
+__device__ __forceinline__ int32_t rec_cap(int4 r) { return r.z < 0 ? 0 : (1 << (r.w >> 24)); }
+__device__ __forceinline__ int32_t log2_pow2(int32_t x) { return 31 - __clz(x); }
 
 struct SeqView {
-  int4* st;
-  int2* ed;
+  int4* st;        // state records
+  int32_t* lk;     // suffix links
+  int32_t* chn;    // suffix chain of `last` between launches
+  int32_t* pool;   // out-token arrays
   unsigned long long* hs;
   int32_t* hist;
   int32_t* sc;
   int32_t S, E, C, V;
+  int64_t P;
   uint32_t hmask;
-  uint32_t nwin;  // number of 32-slot windows in the table
 };
 
 struct BatchView {
   int4* st;
-  int2* ed;
+  int32_t* lk;
+  int32_t* chn;
+  int32_t* pool;
   unsigned long long* hs;
   int32_t* hist;
   int32_t* sc;
   int32_t B, S, E, C, V;
-  int64_t H;
+  int64_t H, P;
 };
 
 __device__ __forceinline__ SeqView seq_view(const BatchView& v, int b) {
   SeqView s;
   s.st = v.st + (size_t)b * v.S;
-  s.ed = v.ed + (size_t)b * v.E;
+  s.lk = v.lk + (size_t)b * v.S;
+  s.chn = v.chn + (size_t)b * kChainMax;
+  s.pool = v.pool + (size_t)b * v.P;
   s.hs = v.hs + (size_t)b * v.H;
   s.hist = v.hist + (size_t)b * v.C;
   s.sc = v.sc + (size_t)b * kScal;
@@ -84,8 +117,8 @@ __device__ __forceinline__ SeqView seq_view(const BatchView& v, int b) {
   s.E = v.E;
   s.C = v.C;
   s.V = v.V;
+  s.P = v.P;
   s.hmask = (uint32_t)(v.H - 1);
-  s.nwin = (uint32_t)(v.H / 32);
   return s;
 }
 
@@ -101,151 +134,324 @@ __device__ __forceinline__ uint32_t slot_hash(int32_t s, int32_t t) {
 __device__ __forceinline__ uint64_t key_bits(int32_t s, int32_t t) {
   return ((uint64_t)(uint32_t)(s + 1) << 18) | (uint32_t)t;
 }
+__device__ __forceinline__ unsigned long long slot_value(int32_t s, int32_t t, int32_t to) {
+  return (key_bits(s, t) << 23) | (uint32_t)to;
+}
 
-// Warp-cooperative probe of (s, t).  Returns 1 (found: *pos, *val), 0 (absent:
-// *pos = first empty slot of the probe sequence) or -1 (table full).
-__device__ __forceinline__ int probe(const SeqView& v, int32_t s, int32_t t, uint32_t* pos,
-                                     int32_t* val, int lane) {
-  const uint64_t kb = key_bits(s, t);
-  const uint32_t h = slot_hash(s, t);
-  for (uint32_t w = 0; w < v.nwin; ++w) {
-    const uint32_t p = (h + w * 32u + (uint32_t)lane) & v.hmask;
-    const unsigned long long x = v.hs[p];
-    const unsigned m = __ballot_sync(kFullMask, (x >> 23) == kb);
-    if (m) {
-      const int src = __ffs(m) - 1;
-      *pos = __shfl_sync(kFullMask, p, src);
-      *val = (int32_t)(__shfl_sync(kFullMask, x, src) & 0x7FFFFFull);
-      return 1;
+// Per-lane probe of key bits kb from slot p on: linear probing, reading the
+// aligned 4-slot group (one 32-byte sector) that holds the next slot.
+// Returns 1 (found: *val, *pos), 0 (absent: *pos = first empty slot of the
+// probe sequence) or -1 (no empty slot in the table).
+__device__ __forceinline__ int lane_probe_from(const SeqView& v, uint64_t kb, uint32_t p,
+                                               uint32_t* pos, int32_t* val) {
+  const uint32_t ngroups = (v.hmask >> 2) + 2;
+  for (uint32_t g = 0; g < ngroups; ++g) {
+    const uint32_t base = p & ~3u;
+    const ulonglong2* gp = reinterpret_cast<const ulonglong2*>(v.hs + base);
+    const ulonglong2 lo = gp[0], hi = gp[1];
+    const unsigned long long x[4] = {lo.x, lo.y, hi.x, hi.y};
+    const int k0 = (int)(p & 3u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (k < k0) continue;
+      if ((x[k] >> 23) == kb) {
+        *pos = base + k;
+        *val = (int32_t)(x[k] & 0x7FFFFFull);
+        return 1;
+      }
+      if (x[k] == 0ull) {
+        *pos = base + k;
+        return 0;
+      }
     }
-    const unsigned e = __ballot_sync(kFullMask, x == 0ull);
-    if (e) {
-      *pos = __shfl_sync(kFullMask, p, __ffs(e) - 1);
-      return 0;
-    }
+    p = (base + 4) & v.hmask;
   }
   return -1;
 }
+__device__ __forceinline__ int lane_probe(const SeqView& v, int32_t s, int32_t t, uint32_t* pos,
+                                          int32_t* val) {
+  return lane_probe_from(v, key_bits(s, t), slot_hash(s, t) & v.hmask, pos, val);
+}
 
-__device__ __forceinline__ void hash_write(const SeqView& v, uint32_t pos, int32_t s, int32_t t,
-                                           int32_t to, int lane) {
-  if (lane == 0) v.hs[pos] = (key_bits(s, t) << 23) | (uint32_t)to;
-  __syncwarp();
+// The same probe in two halves, so that several keys' first groups are in
+// flight together: probe_issue loads the home group, probe_finish scans it
+// and walks on only if it did not settle the key.
+struct GroupLoad {
+  ulonglong2 lo, hi;
+  uint32_t p;
+};
+__device__ __forceinline__ GroupLoad probe_issue(const SeqView& v, int32_t s, int32_t t, bool on) {
+  GroupLoad g;
+  g.p = slot_hash(s, t) & v.hmask;
+  g.lo = make_ulonglong2(0ull, 0ull);
+  g.hi = g.lo;
+  if (on) {
+    const ulonglong2* gp = reinterpret_cast<const ulonglong2*>(v.hs + (g.p & ~3u));
+    g.lo = gp[0];
+    g.hi = gp[1];
+  }
+  return g;
+}
+__device__ __forceinline__ int probe_finish(const SeqView& v, int32_t s, int32_t t,
+                                            const GroupLoad& g, uint32_t* pos, int32_t* val) {
+  const uint64_t kb = key_bits(s, t);
+  const uint32_t base = g.p & ~3u;
+  const unsigned long long x[4] = {g.lo.x, g.lo.y, g.hi.x, g.hi.y};
+  const int k0 = (int)(g.p & 3u);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (k < k0) continue;
+    if ((x[k] >> 23) == kb) {
+      *pos = base + k;
+      *val = (int32_t)(x[k] & 0x7FFFFFull);
+      return 1;
+    }
+    if (x[k] == 0ull) {
+      *pos = base + k;
+      return 0;
+    }
+  }
+  return lane_probe_from(v, kb, (base + 4) & v.hmask, pos, val);
+}
+
+// Writes slot value `val` for the lanes with `want` set: each lane's key is
+// absent and distinct from the other lanes' keys, and *pos is the first empty
+// slot of its probe sequence as read before any of these writes.  Lanes that
+// share a slot leave it to the lowest of them and walk on to the next empty
+// slot.  Returns false if the table has no room.
+__device__ __forceinline__ bool lane_place(const SeqView& v, uint32_t pos, unsigned long long val,
+                                           bool want, int lane, bool known_empty = true) {
+  uint32_t p = pos;  // known_empty: no write since the probe that saw p empty
+  for (uint32_t i = 0; i <= v.hmask + 1; ++i) {
+    if (!__any_sync(kFullMask, want)) return true;
+    const uint32_t q = p & v.hmask;
+    bool empty = want;
+    if (want && !known_empty) empty = v.hs[q] == 0ull;
+    const uint32_t key = empty ? q : (0x80000000u | (uint32_t)lane);
+    const unsigned grp = __match_any_sync(kFullMask, key);
+    const bool win = empty && lane == __ffs(grp) - 1;
+    __syncwarp();
+    if (win) v.hs[q] = val;
+    __syncwarp();
+    if (win) want = false;
+    known_empty = false;
+    ++p;  // occupied, or taken by a lower lane: the next slot
+  }
+  return !__any_sync(kFullMask, want);
 }
 
 struct Scal {
-  int32_t n, last, ns, ne, status, link_last, len_last;
+  int32_t n, last, ns, ne, status, link_last, len_last, pool;
 };
 
-// Adds token t to state s's out-transition list (head = current list head).
-__device__ __forceinline__ bool add_edge(const SeqView& v, Scal& sc, int32_t s, int32_t t,
-                                         int32_t head, int lane) {
-  if (sc.ne >= v.E) return false;
-  const int32_t e = sc.ne++;
-  if (lane == 0) {
-    v.ed[e] = make_int2(t, head);
-    reinterpret_cast<int32_t*>(&v.st[s])[3] = e;
+// Moves n tokens (n a multiple of 4; 16-byte aligned arrays) with int4 copies.
+__device__ __forceinline__ void pool_move(const SeqView& v, int32_t dst, int32_t src, int32_t n,
+                                          int lane) {
+  const int4* s4 = reinterpret_cast<const int4*>(v.pool + src);
+  int4* d4 = reinterpret_cast<int4*>(v.pool + dst);
+  const int32_t n4 = n >> 2;
+  constexpr int U = 4;
+  for (int32_t base = 0; base < n4; base += 32 * U) {
+    int4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int32_t k = base + u * 32 + lane;
+      if (k < n4) r[u] = s4[k];
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int32_t k = base + u * 32 + lane;
+      if (k < n4) d4[k] = r[u];
+    }
   }
   __syncwarp();
-  return true;
 }
 
-// Plain loads: every write to a sequence's arrays is made by the lanes of the
-// same warp and ordered by __syncwarp(), which is also a compiler barrier.
-__device__ __forceinline__ int4 load_state(const SeqView& v, int32_t s) { return v.st[s]; }
+// Appends token c to the out-token arrays of the states `s` of the lanes with
+// `want` set (records `r` as loaded), in parallel: full arrays move to arrays
+// of twice the capacity (at least 4), reserved from the pool in lane order.
+// Returns a status word.
+__device__ __forceinline__ int append_out(const SeqView& v, Scal& sc, int32_t s, int4 r,
+                                          int32_t c, bool want, int lane) {
+  const unsigned wm = __ballot_sync(kFullMask, want);
+  if (!wm) return SAMSPEC_ST_OK;
+  if (sc.ne + __popc(wm) > v.E) return SAMSPEC_ST_CAPACITY;
+  int32_t off = r.z, n = rec_nout(r), cap = rec_cap(r);
+  const bool grow = want && n == cap;
+  const int32_t ncap = grow ? (cap < 4 ? 4 : 2 * cap) : 0;
+  // exclusive prefix sum of the new capacities (lane order)
+  int32_t incl = ncap;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(kFullMask, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int32_t total = __shfl_sync(kFullMask, incl, 31);
+  if ((int64_t)sc.pool + total > v.P) return SAMSPEC_ST_CAPACITY;
+  const int32_t noff = sc.pool + incl - ncap;
+  sc.pool += total;
+  // arrays that hold tokens move, one warp-wide copy each (rare)
+  unsigned mv = __ballot_sync(kFullMask, grow && n > 0);
+  while (mv) {
+    const int l = __ffs(mv) - 1;
+    mv &= mv - 1;
+    pool_move(v, __shfl_sync(kFullMask, noff, l), __shfl_sync(kFullMask, off, l),
+              __shfl_sync(kFullMask, n, l), lane);
+  }
+  if (grow) {
+    off = noff;
+    cap = ncap;
+  }
+  if (want) {
+    v.pool[off + n] = c;
+    v.st[s] = make_int4(r.x, r.y, off, (n + 1) | (log2_pow2(cap) << 24));
+  }
+  sc.ne += __popc(wm);
+  __syncwarp();
+  return SAMSPEC_ST_OK;
+}
 
-// Appends token c (Blumer's online step).  Returns a status word.
-__device__ int extend_one(const SeqView& v, Scal& sc, int32_t c, int lane) {
+// Appends token c (Blumer's online step) when the suffix chain is not kept
+// (longer than kChainMax states).  Returns a status word.
+//
+// The link walk visits x_0 = last, x_1 = link(last), x_2, ... until a state
+// with a c-transition.  It runs in batches of 2, 4, ... 32 chain states, one
+// per lane: the links are chased first (cached, cheap), then every lane probes
+// its own (x_j, c) and loads its record at once, so a walk of k states costs k
+// link loads and about log2(k) hash round trips instead of k of each.
+__device__ int extend_chase(const SeqView& v, Scal& sc, int32_t c, int lane) {
   if (c < 0 || c >= v.V) return SAMSPEC_ST_TOKEN;
   if (sc.n >= v.C || sc.ns + 2 > v.S) return SAMSPEC_ST_CAPACITY;
   const int32_t i = sc.n;
   const int32_t cur = sc.ns++;
   if (lane == 0) {
     // position i ends only suffixes of S c and exceeds every earlier end
-    v.st[cur] = make_int4(sc.len_last + 1, -1, i, -1);
+    v.st[cur] = make_int4(sc.len_last + 1, i, -1, 0);
+    v.lk[cur] = -1;
     v.hist[i] = c;
   }
   __syncwarp();
-  uint32_t pos;
-  int32_t val;
-  // `last` never has an out-transition, so (last, c) is absent
-  int r = probe(v, sc.last, c, &pos, &val, lane);
-  if (r < 0) return SAMSPEC_ST_HASHFULL;
-  if (r > 0) return SAMSPEC_ST_LOOPCAP;
-  hash_write(v, pos, sc.last, c, cur, lane);
-  if (!add_edge(v, sc, sc.last, c, -1, lane)) return SAMSPEC_ST_CAPACITY;
 
-  int32_t p = sc.link_last;
+  int guard = sc.len_last + 2;      // chain states a walk may visit
+  int32_t x = sc.last;              // first chain state of the next batch
+  int W = 2;
   int32_t link_cur = 0;
-  int guard = sc.len_last + 2;
+  int32_t p = -1, q = -1;           // the state with a c-transition and its target
+  uint32_t p_pos = 0;               // slot of (p, c)
+  int32_t after_p = -1;             // link(p)
+  int32_t len_p = 0;
   for (;;) {
-    if (p == -1) {
-      link_cur = 0;
+    // chain states x_j of this batch to lanes j = 0 .. m-1; `x` ends as the
+    // last of them (its link is loaded below with the probes)
+    int32_t mine = lane == 0 ? x : -1;
+    int m = 1;
+    while (m < W) {
+      const int32_t y = v.lk[x];
+      if (y == -1) break;
+      x = y;
+      if (lane == m) mine = x;
+      ++m;
+    }
+    guard -= m;
+    if (guard < 0) return SAMSPEC_ST_LOOPCAP;
+    const bool has = lane < m;
+    const int4 rec = has ? v.st[mine] : make_int4(0, 0, -1, 0);
+    const int32_t nx = v.lk[x];
+    uint32_t pos = 0;
+    int32_t val = -1;
+    const int r = has ? lane_probe(v, mine, c, &pos, &val) : 0;
+    if (__any_sync(kFullMask, has && r < 0)) return SAMSPEC_ST_HASHFULL;
+    const unsigned fnd = __ballot_sync(kFullMask, has && r == 1);
+    const int kf = fnd ? __ffs(fnd) - 1 : m;
+    // (x_j, c) -> cur for the chain states before the first with a c-transition
+    const bool add = has && lane < kf;
+    if (!lane_place(v, pos, slot_value(mine, c, cur), add, lane)) return SAMSPEC_ST_HASHFULL;
+    const int st = append_out(v, sc, mine, rec, c, add, lane);
+    if (st != SAMSPEC_ST_OK) return st;
+    if (fnd) {
+      p = __shfl_sync(kFullMask, mine, kf);
+      q = __shfl_sync(kFullMask, val, kf);
+      p_pos = __shfl_sync(kFullMask, pos, kf);
+      len_p = __shfl_sync(kFullMask, rec.x, kf);
+      const int32_t nxt_lane = __shfl_sync(kFullMask, mine, (kf + 1) & 31);
+      after_p = kf + 1 < m ? nxt_lane : nx;
       break;
     }
-    if (--guard < 0) return SAMSPEC_ST_LOOPCAP;
-    const int4 sp = load_state(v, p);  // issued together with the probe's window
-    r = probe(v, p, c, &pos, &val, lane);
-    if (r < 0) return SAMSPEC_ST_HASHFULL;
-    if (r == 0) {
-      hash_write(v, pos, p, c, cur, lane);
-      if (!add_edge(v, sc, p, c, sp.w, lane)) return SAMSPEC_ST_CAPACITY;
-      p = sp.y;
-      continue;
-    }
-    const int32_t q = val;
-    const int4 sq = load_state(v, q);
-    if (sp.x + 1 == sq.x) {
-      link_cur = q;
-      break;
-    }
-    // split q: the clone copies q's transitions, link and min_endpos
-    if (sc.ns + 1 > v.S) return SAMSPEC_ST_CAPACITY;
-    const int32_t clone = sc.ns++;
-    if (lane == 0) v.st[clone] = make_int4(sp.x + 1, sq.y, sq.z, -1);
-    __syncwarp();
-    int32_t e = sq.w;
-    int32_t clone_head = -1;
-    int eguard = v.E + 1;
-    while (e != -1) {
-      if (--eguard < 0) return SAMSPEC_ST_LOOPCAP;
-      const int2 ed = v.ed[e];
-      int32_t to;
-      uint32_t qpos;
-      r = probe(v, q, ed.x, &qpos, &to, lane);
-      if (r != 1) return r < 0 ? SAMSPEC_ST_HASHFULL : SAMSPEC_ST_LOOPCAP;
-      uint32_t cpos;
-      int32_t dummy;
-      r = probe(v, clone, ed.x, &cpos, &dummy, lane);
-      if (r != 0) return r < 0 ? SAMSPEC_ST_HASHFULL : SAMSPEC_ST_LOOPCAP;
-      hash_write(v, cpos, clone, ed.x, to, lane);
-      if (sc.ne >= v.E) return SAMSPEC_ST_CAPACITY;
-      const int32_t ne = sc.ne++;
-      if (lane == 0) v.ed[ne] = make_int2(ed.x, clone_head);
-      __syncwarp();
-      clone_head = ne;
-      e = ed.y;
-    }
-    if (lane == 0) reinterpret_cast<int32_t*>(&v.st[clone])[3] = clone_head;
-    // redirect (p', c) -> q to the clone along p's suffix links
-    hash_write(v, pos, p, c, clone, lane);
-    int32_t pp = sp.y;
-    while (pp != -1) {
-      if (--guard < 0) return SAMSPEC_ST_LOOPCAP;
-      const int4 spp = load_state(v, pp);
-      uint32_t ppos;
-      int32_t pval;
-      r = probe(v, pp, c, &ppos, &pval, lane);
-      if (r < 0) return SAMSPEC_ST_HASHFULL;
-      if (r == 0 || pval != q) break;
-      hash_write(v, ppos, pp, c, clone, lane);
-      pp = spp.y;
-    }
-    if (lane == 0) reinterpret_cast<int32_t*>(&v.st[q])[1] = clone;
-    link_cur = clone;
-    break;
+    if (nx == -1) break;  // the root was the last chain state: link(cur) = root
+    x = nx;
+    W = W < 32 ? 2 * W : 32;
   }
-  if (lane == 0) reinterpret_cast<int32_t*>(&v.st[cur])[1] = link_cur;
+
+  if (q >= 0) {
+    const int4 sq = v.st[q];
+    const int32_t lq = v.lk[q];
+    if (len_p + 1 == sq.x) {
+      link_cur = q;
+    } else {
+      // split q: the clone takes q's transitions, link and min_endpos
+      if (sc.ns + 1 > v.S) return SAMSPEC_ST_CAPACITY;
+      const int32_t clone = sc.ns++;
+      const int32_t nq = rec_nout(sq);
+      if (sc.ne + nq > v.E) return SAMSPEC_ST_CAPACITY;
+      int32_t ccap = 4;
+      while (ccap < nq) ccap <<= 1;
+      if ((int64_t)sc.pool + ccap > v.P) return SAMSPEC_ST_CAPACITY;
+      const int32_t coff = sc.pool;
+      sc.pool += ccap;
+      if (lane == 0) {
+        v.st[clone] = make_int4(len_p + 1, sq.y, coff, nq | (log2_pow2(ccap) << 24));
+        v.lk[clone] = lq;
+      }
+      for (int32_t base = 0; base < nq; base += 32) {
+        const bool own = base + lane < nq;
+        const int32_t t = own ? v.pool[sq.z + base + lane] : 0;
+        uint32_t qpos = 0, cpos = 0;
+        int32_t to = -1, dummy = -1;
+        const int r1 = own ? lane_probe(v, q, t, &qpos, &to) : 1;
+        const int r2 = own ? lane_probe(v, clone, t, &cpos, &dummy) : 0;
+        if (__any_sync(kFullMask, r1 != 1 || r2 != 0))
+          return __any_sync(kFullMask, r1 < 0 || r2 < 0) ? SAMSPEC_ST_HASHFULL : SAMSPEC_ST_LOOPCAP;
+        if (own) v.pool[coff + base + lane] = t;
+        if (!lane_place(v, cpos, slot_value(clone, t, to), own, lane)) return SAMSPEC_ST_HASHFULL;
+      }
+      sc.ne += nq;
+      // (p, c) -> clone, then the states after p on the chain while their
+      // c-transition still leads to q (batched like the walk)
+      if (lane == 0) v.hs[p_pos] = slot_value(p, c, clone);
+      __syncwarp();
+      int32_t y = after_p;
+      W = 2;
+      while (y != -1) {
+        int32_t mine = lane == 0 ? y : -1;
+        int m = 1;
+        while (m < W) {
+          const int32_t z = v.lk[y];
+          if (z == -1) break;
+          y = z;
+          if (lane == m) mine = y;
+          ++m;
+        }
+        guard -= m;
+        if (guard < 0) return SAMSPEC_ST_LOOPCAP;
+        const bool has = lane < m;
+        const int32_t ny = v.lk[y];
+        uint32_t pos = 0;
+        int32_t val = -1;
+        const int r = has ? lane_probe(v, mine, c, &pos, &val) : 1;
+        if (__any_sync(kFullMask, has && r < 0)) return SAMSPEC_ST_HASHFULL;
+        const unsigned stop = __ballot_sync(kFullMask, has && (r == 0 || val != q));
+        const int ks = stop ? __ffs(stop) - 1 : m;
+        if (has && lane < ks) v.hs[pos] = slot_value(mine, c, clone);
+        __syncwarp();
+        if (stop) break;
+        y = ny;
+        W = W < 32 ? 2 * W : 32;
+      }
+      if (lane == 0) v.lk[q] = clone;
+      link_cur = clone;
+    }
+  }
+  if (lane == 0) v.lk[cur] = link_cur;
   __syncwarp();
   sc.last = cur;
   sc.len_last += 1;
@@ -254,29 +460,219 @@ __device__ int extend_one(const SeqView& v, Scal& sc, int32_t c, int lane) {
   return SAMSPEC_ST_OK;
 }
 
+template <typename T>
+__device__ __forceinline__ T sel(const T (&a)[kChR], int r) {
+  T x = a[0];
+#pragma unroll
+  for (int i = 1; i < kChR; ++i)
+    if (r == i) x = a[i];
+  return x;
+}
+
+// Appends token c (Blumer's online step) with the suffix chain of `last` in
+// registers: lane l holds chain states l, l + 32, ... (chr), m of them.
+// Every chain state's (x_j, c) key and record are fetched at once; the first
+// x_k with a c-transition ends the walk (x_j, j < k, gain c -> cur); the
+// targets of x_k .. x_{m-1} (q, or the clone where a split redirected them)
+// are, without repeats, the suffix chain of link(cur), so the new chain is
+// cur, those targets, root.  m becomes 0 if the new chain is longer than
+// kChainMax.  `sh` is this warp's scratch of kChainMax + 2 ints.
+__device__ int extend_chain(const SeqView& v, Scal& sc, int32_t c, int lane,
+                            int32_t (&chr)[kChR], int& m, int32_t* sh) {
+  if (c < 0 || c >= v.V) return SAMSPEC_ST_TOKEN;
+  if (sc.n >= v.C || sc.ns + 2 > v.S) return SAMSPEC_ST_CAPACITY;
+  const int32_t i = sc.n;
+  const int32_t cur = sc.ns++;
+  if (lane == 0) {
+    // position i ends only suffixes of S c and exceeds every earlier end
+    v.st[cur] = make_int4(sc.len_last + 1, i, -1, 0);
+    v.lk[cur] = -1;
+    v.hist[i] = c;
+  }
+  bool has[kChR];
+  int4 rec[kChR];
+  GroupLoad gl[kChR];
+#pragma unroll
+  for (int r = 0; r < kChR; ++r) {
+    has[r] = 32 * r + lane < m;
+    rec[r] = has[r] ? v.st[chr[r]] : make_int4(0, 0, -1, 0);
+    gl[r] = probe_issue(v, chr[r], c, has[r]);
+  }
+  uint32_t pos[kChR];
+  int32_t val[kChR];
+  int pr[kChR];
+#pragma unroll
+  for (int r = 0; r < kChR; ++r) {
+    pos[r] = 0;
+    val[r] = -1;
+    pr[r] = has[r] ? probe_finish(v, chr[r], c, gl[r], &pos[r], &val[r]) : 0;
+  }
+  bool full = false;
+  int k = m;
+#pragma unroll
+  for (int r = 0; r < kChR; ++r) {
+    full |= __any_sync(kFullMask, has[r] && pr[r] < 0);
+    const unsigned f = __ballot_sync(kFullMask, has[r] && pr[r] == 1);
+    if (k == m && f) k = 32 * r + __ffs(f) - 1;
+  }
+  if (full) return SAMSPEC_ST_HASHFULL;
+  // (x_j, c) -> cur for the chain states before x_k
+#pragma unroll
+  for (int r = 0; r < kChR; ++r) {
+    const bool want = has[r] && 32 * r + lane < k;
+    if (!__any_sync(kFullMask, want)) break;
+    if (!lane_place(v, pos[r], slot_value(chr[r], c, cur), want, lane, r == 0))
+      return SAMSPEC_ST_HASHFULL;
+    const int st = append_out(v, sc, chr[r], rec[r], c, want, lane);
+    if (st != SAMSPEC_ST_OK) return st;
+  }
+  int32_t link_cur = 0;
+  int mn = 2;  // length of the new chain
+  if (k < m) {
+    const int kr = k >> 5, kl = k & 31;
+    const int32_t p = __shfl_sync(kFullMask, sel(chr, kr), kl);
+    const int32_t q = __shfl_sync(kFullMask, sel(val, kr), kl);
+    const uint32_t p_pos = __shfl_sync(kFullMask, sel(pos, kr), kl);
+    int32_t lens[kChR];
+#pragma unroll
+    for (int r = 0; r < kChR; ++r) lens[r] = rec[r].x;
+    const int32_t len_p = __shfl_sync(kFullMask, sel(lens, kr), kl);
+    const int4 sq = v.st[q];
+    const int32_t lq = v.lk[q];
+    int32_t clone = -1;
+    if (len_p + 1 == sq.x) {
+      link_cur = q;
+    } else {
+      // split q: the clone takes q's transitions, link and min_endpos
+      if (sc.ns + 1 > v.S) return SAMSPEC_ST_CAPACITY;
+      clone = sc.ns++;
+      const int32_t nq = rec_nout(sq);
+      if (sc.ne + nq > v.E) return SAMSPEC_ST_CAPACITY;
+      int32_t ccap = 4;
+      while (ccap < nq) ccap <<= 1;
+      if ((int64_t)sc.pool + ccap > v.P) return SAMSPEC_ST_CAPACITY;
+      const int32_t coff = sc.pool;
+      sc.pool += ccap;
+      if (lane == 0) {
+        v.st[clone] = make_int4(len_p + 1, sq.y, coff, nq | (log2_pow2(ccap) << 24));
+        v.lk[clone] = lq;
+      }
+      for (int32_t base = 0; base < nq; base += 32) {
+        const bool own = base + lane < nq;
+        const int32_t t = own ? v.pool[sq.z + base + lane] : 0;
+        uint32_t qpos = 0, cpos = 0;
+        int32_t to = -1, dummy = -1;
+        const int r1 = own ? lane_probe(v, q, t, &qpos, &to) : 1;
+        const int r2 = own ? lane_probe(v, clone, t, &cpos, &dummy) : 0;
+        if (__any_sync(kFullMask, r1 != 1 || r2 != 0))
+          return __any_sync(kFullMask, r1 < 0 || r2 < 0) ? SAMSPEC_ST_HASHFULL : SAMSPEC_ST_LOOPCAP;
+        if (own) v.pool[coff + base + lane] = t;
+        if (!lane_place(v, cpos, slot_value(clone, t, to), own, lane)) return SAMSPEC_ST_HASHFULL;
+      }
+      sc.ne += nq;
+      // every chain state from x_k on whose c-transition leads to q (a run
+      // starting at x_k) now leads to the clone
+#pragma unroll
+      for (int r = 0; r < kChR; ++r) {
+        const int j = 32 * r + lane;
+        if (has[r] && j >= k && pr[r] == 1 && val[r] == q)
+          v.hs[pos[r]] = slot_value(chr[r], c, clone);
+      }
+      (void)p;
+      (void)p_pos;
+      __syncwarp();
+      if (lane == 0) v.lk[q] = clone;
+      link_cur = clone;
+    }
+    // the new chain: cur, the distinct targets of x_k .. x_{m-1}, root
+    bool lost = false;
+#pragma unroll
+    for (int r = 0; r < kChR; ++r) lost |= has[r] && 32 * r + lane >= k && pr[r] != 1;
+    if (__any_sync(kFullMask, lost)) return SAMSPEC_ST_LOOPCAP;  // a suffix without its c-transition
+    int cnt = 0;
+    int32_t prev_last = -1;  // target of the previous register's lane 31
+#pragma unroll
+    for (int r = 0; r < kChR; ++r) {
+      const int j = 32 * r + lane;
+      const bool in = has[r] && j >= k;
+      const int32_t t = (clone >= 0 && val[r] == q) ? clone : val[r];
+      int32_t prev = __shfl_up_sync(kFullMask, t, 1);
+      if (lane == 0) prev = prev_last;
+      const bool d = in && (j == k || t != prev);
+      const unsigned dm = __ballot_sync(kFullMask, d);
+      const int at = cnt + __popc(dm & ((1u << lane) - 1u)) + 1;
+      if (d && at <= kChainMax) sh[at] = t;
+      cnt += __popc(dm);
+      prev_last = __shfl_sync(kFullMask, t, 31);
+    }
+    mn = cnt + 2;
+  }
+  if (lane == 0) {
+    sh[0] = cur;
+    if (mn <= kChainMax + 1) sh[mn - 1] = 0;
+    v.lk[cur] = link_cur;
+  }
+  __syncwarp();
+  if (mn <= kChainMax) {
+#pragma unroll
+    for (int r = 0; r < kChR; ++r) chr[r] = 32 * r + lane < mn ? sh[32 * r + lane] : -1;
+    m = mn;
+  } else {
+    m = 0;
+  }
+  __syncwarp();
+  sc.last = cur;
+  sc.len_last += 1;
+  sc.link_last = link_cur;
+  sc.n += 1;
+  return SAMSPEC_ST_OK;
+}
+
+// After a chase-walk token: takes the chain up again if it is short enough
+// (it has at most len(link(last)) + 2 states).
+__device__ void chain_rebuild(const SeqView& v, const Scal& sc, int lane, int32_t (&chr)[kChR],
+                              int& m) {
+  m = 0;
+  const int32_t ll = sc.link_last;
+  const int32_t bound = (ll < 0 ? 0 : v.st[ll].x) + 2;
+  if (bound > kChainMax) return;
+  int32_t x = sc.last;
+  int n = 0;
+#pragma unroll
+  for (int r = 0; r < kChR; ++r) chr[r] = -1;
+  while (x != -1 && n < kChainMax) {
+#pragma unroll
+    for (int r = 0; r < kChR; ++r)
+      if (n == 32 * r + lane) chr[r] = x;
+    ++n;
+    x = v.lk[x];
+  }
+  if (x == -1) m = n;
+}
+
 __device__ void draft_one(const SeqView& v, const Scal& sc, int32_t K, int32_t* draft_row,
                           int32_t* dl_out, int32_t* ml_out, int32_t* me_out, int lane) {
   int32_t s = 0;
-  int4 rec = make_int4(0, -1, -1, -1);
+  int4 rec = make_int4(0, -1, -1, 0);
   if (sc.status == SAMSPEC_ST_OK && sc.n > 0) {
     // the state of S has no out-transition: start at its suffix link
     s = sc.link_last;
     int guard = sc.len_last + 1;
     while (s > 0) {
-      rec = load_state(v, s);
-      if (rec.w != -1) break;
+      rec = v.st[s];
+      if (rec_nout(rec) > 0) break;
       if (--guard < 0) {
         s = 0;
         break;
       }
-      s = rec.y;
+      s = v.lk[s];
     }
     if (s < 0) s = 0;
   }
   int32_t dl = 0, ml = 0, me = -1;
   if (s > 0) {
     ml = rec.x;
-    me = rec.z;
+    me = rec.y;
     dl = min(K, sc.n - 1 - me);
     if (dl < 0) dl = 0;
   }
@@ -298,6 +694,8 @@ __global__ void __launch_bounds__(64) sam_step_kernel(BatchView bv, const int32_
   const int lane = threadIdx.x & 31;
   if (b >= bv.B) return;
   const SeqView v = seq_view(bv, b);
+  __shared__ int32_t chain_sh[2][kChainMax + 2];
+  int32_t* sh = chain_sh[(threadIdx.x >> 5) & 1];
   Scal sc;
   sc.n = v.sc[SC_N];
   sc.last = v.sc[SC_LAST];
@@ -306,7 +704,14 @@ __global__ void __launch_bounds__(64) sam_step_kernel(BatchView bv, const int32_
   sc.status = v.sc[SC_STATUS];
   sc.link_last = v.sc[SC_LINKLAST];
   sc.len_last = v.sc[SC_LENLAST];
+  sc.pool = v.sc[SC_POOL];
+  int m = 0;
+  int32_t chr[kChR];
   if (kExtend && sc.status == SAMSPEC_ST_OK) {
+    m = v.sc[SC_CHAIN];
+    if (m < 0 || m > kChainMax) m = 0;
+#pragma unroll
+    for (int r = 0; r < kChR; ++r) chr[r] = 32 * r + lane < m ? v.chn[32 * r + lane] : -1;
     const int32_t nn = n_new[b];
     if (nn < 0 || nn > max_new) {
       sc.status = SAMSPEC_ST_BADDRAFT;
@@ -317,7 +722,13 @@ __global__ void __launch_bounds__(64) sam_step_kernel(BatchView bv, const int32_
         const int32_t mine = lane < cnt ? row[base + lane] : 0;
         for (int32_t k = 0; k < cnt; ++k) {
           const int32_t c = __shfl_sync(kFullMask, mine, k);
-          const int st = extend_one(v, sc, c, lane);
+          int st;
+          if (m > 0) {
+            st = extend_chain(v, sc, c, lane, chr, m, sh);
+          } else {
+            st = extend_chase(v, sc, c, lane);
+            if (st == SAMSPEC_ST_OK) chain_rebuild(v, sc, lane, chr, m);
+          }
           if (st != SAMSPEC_ST_OK) {
             sc.status = st;
             break;
@@ -338,6 +749,13 @@ __global__ void __launch_bounds__(64) sam_step_kernel(BatchView bv, const int32_
     v.sc[SC_STATUS] = sc.status;
     v.sc[SC_LINKLAST] = sc.link_last;
     v.sc[SC_LENLAST] = sc.len_last;
+    v.sc[SC_POOL] = sc.pool;
+    v.sc[SC_CHAIN] = sc.status == SAMSPEC_ST_OK ? m : 0;
+  }
+  if (kExtend && sc.status == SAMSPEC_ST_OK) {
+#pragma unroll
+    for (int r = 0; r < kChR; ++r)
+      if (32 * r + lane < m) v.chn[32 * r + lane] = chr[r];
   }
 }
 
@@ -359,8 +777,11 @@ __global__ void sam_reset_kernel(BatchView bv, const int32_t* __restrict__ mask)
     sc[SC_STATUS] = SAMSPEC_ST_OK;
     sc[SC_LINKLAST] = -1;
     sc[SC_LENLAST] = 0;
-    sc[7] = 0;
-    bv.st[(size_t)b * bv.S] = make_int4(0, -1, -1, -1);
+    sc[SC_POOL] = 0;
+    sc[SC_CHAIN] = 1;
+    bv.st[(size_t)b * bv.S] = make_int4(0, -1, -1, 0);
+    bv.lk[(size_t)b * bv.S] = -1;
+    bv.chn[(size_t)b * kChainMax] = 0;
   }
   }
 }
@@ -374,8 +795,8 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
   int32_t S, E;
-  int64_t H;
-  size_t off_states, off_edges, off_hash, off_hist, off_scal, total;
+  int64_t H, P;
+  size_t off_states, off_links, off_chain, off_pool, off_hash, off_hist, off_scal, total;
 };
 
 bool make_layout(int32_t B, int32_t C, Layout* L) {
@@ -386,11 +807,19 @@ bool make_layout(int32_t B, int32_t C, Layout* L) {
   int64_t H = 64;
   while (H < want) H <<= 1;
   L->H = H;
+  // every state's arrays together stay below 4 ints per transition: a state
+  // with n >= 1 out-tokens holds a final array of capacity <= max(4, 2n) and
+  // left behind arrays summing to less than that
+  L->P = 4 * (int64_t)L->E;
   size_t o = 0;
   L->off_states = o;
   o = align256(o + (size_t)B * L->S * sizeof(int4));
-  L->off_edges = o;
-  o = align256(o + (size_t)B * L->E * sizeof(int2));
+  L->off_links = o;
+  o = align256(o + (size_t)B * L->S * sizeof(int32_t));
+  L->off_chain = o;
+  o = align256(o + (size_t)B * kChainMax * sizeof(int32_t));
+  L->off_pool = o;
+  o = align256(o + (size_t)B * (size_t)L->P * sizeof(int32_t));
   L->off_hash = o;
   o = align256(o + (size_t)B * (size_t)L->H * sizeof(unsigned long long));
   L->off_hist = o;
@@ -404,7 +833,9 @@ bool make_layout(int32_t B, int32_t C, Layout* L) {
 BatchView view_of(const sam_batch* s) {
   BatchView v;
   v.st = reinterpret_cast<int4*>(s->ws + s->off_states);
-  v.ed = reinterpret_cast<int2*>(s->ws + s->off_edges);
+  v.lk = reinterpret_cast<int32_t*>(s->ws + s->off_links);
+  v.chn = reinterpret_cast<int32_t*>(s->ws + s->off_chain);
+  v.pool = reinterpret_cast<int32_t*>(s->ws + s->off_pool);
   v.hs = reinterpret_cast<unsigned long long*>(s->ws + s->off_hash);
   v.hist = reinterpret_cast<int32_t*>(s->ws + s->off_hist);
   v.sc = reinterpret_cast<int32_t*>(s->ws + s->off_scal);
@@ -414,6 +845,7 @@ BatchView view_of(const sam_batch* s) {
   v.C = s->C;
   v.V = s->V;
   v.H = s->H;
+  v.P = s->P;
   return v;
 }
 
@@ -467,10 +899,13 @@ int sam_batch_create(int32_t B, int32_t capacity_tokens, int32_t vocab, void* d_
   s->S = L.S;
   s->E = L.E;
   s->H = L.H;
+  s->P = L.P;
   s->ws_bytes = L.total;
   s->ws = static_cast<char*>(d_workspace);
   s->off_states = L.off_states;
-  s->off_edges = L.off_edges;
+  s->off_links = L.off_links;
+  s->off_chain = L.off_chain;
+  s->off_pool = L.off_pool;
   s->off_hash = L.off_hash;
   s->off_hist = L.off_hist;
   s->off_scal = L.off_scal;
@@ -562,11 +997,14 @@ int sam_dump_sequence(sam_batch* batch, int32_t b, int32_t* h_scalars, int32_t* 
           cudaSuccess ||
       cudaStreamSynchronize(st) != cudaSuccess)
     return SAMSPEC_ECUDA;
-  if (h_scalars) std::memcpy(h_scalars, sc, sizeof(sc));
+  if (h_scalars) std::memcpy(h_scalars, sc, 8 * sizeof(int32_t));
   const int32_t ns = std::min(sc[SC_NS], batch->S);
   std::vector<int4> states((size_t)ns);
+  std::vector<int32_t> links((size_t)ns);
   std::vector<unsigned long long> tab((size_t)batch->H);
   if (cudaMemcpyAsync(states.data(), v.st + (size_t)b * batch->S, (size_t)ns * sizeof(int4),
+                      cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemcpyAsync(links.data(), v.lk + (size_t)b * batch->S, (size_t)ns * sizeof(int32_t),
                       cudaMemcpyDeviceToHost, st) != cudaSuccess ||
       cudaMemcpyAsync(tab.data(), v.hs + (size_t)b * batch->H, tab.size() * sizeof(tab[0]),
                       cudaMemcpyDeviceToHost, st) != cudaSuccess ||
@@ -574,8 +1012,8 @@ int sam_dump_sequence(sam_batch* batch, int32_t b, int32_t* h_scalars, int32_t* 
     return SAMSPEC_ECUDA;
   for (int32_t i = 0; i < ns && i < max_states; ++i) {
     if (h_len) h_len[i] = states[i].x;
-    if (h_link) h_link[i] = states[i].y;
-    if (h_min_endpos) h_min_endpos[i] = states[i].z;
+    if (h_link) h_link[i] = links[i];
+    if (h_min_endpos) h_min_endpos[i] = states[i].y;
   }
   if (h_edges) {
     std::vector<int64_t> keys;

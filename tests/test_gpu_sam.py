@@ -202,3 +202,43 @@ def test_host_argument_errors(ss, cuda_device):
     batch = ss.SamBatch(2, 10, 10, device=cuda_device)
     with pytest.raises(ss.SamspecError):
         batch.draft(65)
+
+
+def test_long_suffix_chains(ss, cuda_device):
+    """Texts whose suffix chains grow past 128 states (long runs of one token,
+    short periods) and shrink again, built in bulk and in steps of 1-4
+    tokens: states, transitions and drafts stay bit-exact."""
+    rng = np.random.default_rng(77)
+    V = 50
+    texts = [
+        np.concatenate([np.full(400, 7), rng.integers(0, V, 300)]),
+        np.concatenate([np.tile([3, 4], 250), rng.integers(0, V, 200), np.tile([3, 4], 100)]),
+        np.concatenate([np.tile([1, 2, 3], 120), np.full(150, 9), np.tile([1, 2, 3], 60)]),
+        workloads.make_stream(rng, 900, V, 0.6, 64, 200),
+    ]
+    n = max(len(t) for t in texts)
+    B = len(texts)
+    hist = np.zeros((B, n), np.int32)
+    for b, t in enumerate(texts):
+        hist[b, :len(t)] = t
+    lens = np.array([len(t) for t in texts], np.int32)
+    sams = [oracle.Sam(V) for _ in range(B)]
+    for b in range(B):
+        sams[b].extend(texts[b])
+    bulk = ss.SamBatch(B, n, V, device=cuda_device)
+    bulk.extend(_i32(hist, cuda_device), _i32(lens, cuda_device))
+    _check_states(bulk, sams, range(B))
+    _check_drafts(bulk.draft(5), sams, 5, range(B))
+    step = ss.SamBatch(B, n, V, device=cuda_device)
+    ref = [oracle.Sam(V) for _ in range(B)]
+    pos = np.zeros(B, np.int64)
+    while (pos < lens).any():
+        k = np.minimum(rng.integers(1, 5, size=B), lens - pos).astype(np.int32)
+        toks = np.zeros((B, 4), np.int32)
+        for b in range(B):
+            toks[b, :k[b]] = texts[b][pos[b]:pos[b] + k[b]]
+            ref[b].extend(toks[b, :k[b]])
+        out = step.step(_i32(toks, cuda_device), _i32(k, cuda_device), 5)
+        _check_drafts(out, ref, 5, range(B))
+        pos += k
+    _check_states(step, ref, range(B))
