@@ -180,6 +180,22 @@ __device__ __forceinline__ DF df_add(DF x, DF y) {
   const float hi = s + lo;
   return {hi, lo - (hi - s)};
 }
+__device__ __forceinline__ DF df_neg(DF x) { return {-x.hi, -x.lo}; }
+__device__ __forceinline__ DF df_sub(DF x, DF y) { return df_add(x, df_neg(y)); }
+// x <= y for normalised pairs (|lo| at most half an ulp of hi)
+__device__ __forceinline__ bool df_le(DF x, DF y) {
+  return x.hi < y.hi || (x.hi == y.hi && x.lo <= y.lo);
+}
+// x * 2^k, exact while the parts stay normal
+__device__ __forceinline__ DF df_scale(DF x, int k) { return {ldexpf(x.hi, k), ldexpf(x.lo, k)}; }
+// x * a with the product's rounding error carried (FMA two-product)
+__device__ __forceinline__ DF df_mul_f(DF x, float a) {
+  const float p = x.hi * a;
+  const float e = fmaf(x.hi, a, -p) + x.lo * a;
+  const float hi = p + e;
+  return {hi, e - (hi - p)};
+}
+__device__ __forceinline__ float df_f(DF x) { return x.hi + x.lo; }
 __device__ __forceinline__ DF df_warp_sum(float v) {
   DF a = {v, 0.f};
 #pragma unroll
@@ -454,6 +470,15 @@ __device__ __forceinline__ float resid_elem(const Slice<TT, DT>& s, int i, int k
   return fmaxf(0.f, pe * invZ - qe * invZg);
 }
 
+// resid_elem for one logit pair (x target, g draft).
+__device__ __forceinline__ float resid_val(float x, float g, int smode, float RL, float RG,
+                                           float invZ, float invZg, float cT) {
+  const float pe = ex2_approx(fmaf(x, cT, -RL));
+  if (smode == 0) return pe;
+  const float qe = ex2_approx(fmaf(g, cT, -RG));
+  return fmaxf(0.f, pe * invZ - qe * invZg);
+}
+
 // residual-pass record: sum of r over the slice {r, 0, 0, 0}
 template <int TT, int DT, bool FULL>
 __device__ __forceinline__ float4 reduce_resid(const Slice<TT, DT>& s, int w, int lane, int nel,
@@ -489,15 +514,31 @@ __device__ void write_result(const VParams& P, int b, int L, int out, int st) {
 }
 
 // First lane in [0, n) whose inclusive running sum of v exceeds t, or -1;
-// *before receives the running sum ahead of that lane.
-__device__ __forceinline__ int warp_find(double v, double t, int n, int lane, double* before) {
-  const double x = lane < n ? v : 0.0;
-  const double incl = warp_incl_scan_d(x, lane);
-  const unsigned hit = __ballot_sync(kFullMask, lane < n && incl > t);
+// *before receives the running sum ahead of that lane.  Sums are carried as
+// float pairs (about 48 significant bits).
+__device__ __forceinline__ int warp_find(DF v, DF t, int n, int lane, DF* before) {
+  DF x = lane < n ? v : DF{0.f, 0.f};
+  DF incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF y = {__shfl_up_sync(kFullMask, incl.hi, o), __shfl_up_sync(kFullMask, incl.lo, o)};
+    if (lane >= o) incl = df_add(incl, y);
+  }
+  const unsigned hit = __ballot_sync(kFullMask, lane < n && !df_le(incl, t));
   if (!hit) return -1;
   const int src = __ffs(hit) - 1;
-  *before = __shfl_sync(kFullMask, incl, src) - __shfl_sync(kFullMask, x, src);
+  const DF bef = df_sub(incl, x);
+  *before = {__shfl_sync(kFullMask, bef.hi, src), __shfl_sync(kFullMask, bef.lo, src)};
   return src;
+}
+
+__device__ __forceinline__ float warp_incl_scan_f(float v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(kFullMask, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
 }
 
 // ---- control warp ------------------------------------------------------------
@@ -705,97 +746,105 @@ struct Control {
 
   // Resample scan of warp slice (c, w) of row L: the first token whose running
   // residual exceeds t (in the slice's own units: the expression its record
-  // summed, resid_elem, with token `excl` left out), ascending token order.
-  // Each lane sums its own contiguous elements; one warp scan finds the lane;
-  // that lane walks its elements.
-  __device__ int slice_scan(int b, int L, int c, int w, double t, int smode, int excl, float RL,
+  // summed, resid_val, with token `excl` left out), ascending token order.
+  // Each lane sums its own contiguous elements; a warp scan finds the lane;
+  // that lane's elements go one per lane and a second warp scan finds the
+  // token.
+  __device__ int slice_scan(int b, int L, int c, int w, float t, int smode, int excl, float RL,
                             float RG, float invZ, float invZg) {
     Slice<TT, DT> sl;
     const bool with_draft = DT >= 0 && smode == 1;
     const int n = load_slice_lanes<TT, DT>(sl, P, b, L, c, w, with_draft, lane);
     const int s0 = c * C::E_TILE + w * C::SL;
-    auto r_at = [&](int i, int k) -> float {
-      const int e = lane * EPL + i * C::VEC + k;
-      if (e >= n || s0 + e == excl) return 0.f;
-      return resid_elem<TT, DT>(sl, i, k, smode, RL, RG, invZ, invZg, P.cT);
-    };
     float tot = 0.f;
     int last_pos = -1;
 #pragma unroll
     for (int i = 0; i < C::VPL; ++i)
 #pragma unroll
       for (int k = 0; k < C::VEC; ++k) {
-        const float r = r_at(i, k);
+        const int e = lane * EPL + i * C::VEC + k;
+        float r = 0.f;
+        if (e < n && s0 + e != excl)
+          r = resid_val(sl.t[i].at(k), DT >= 0 ? sl.d[i].at(k) : 0.f, smode, RL, RG, invZ, invZg, P.cT);
         tot += r;
-        if (r > 0.f) last_pos = s0 + lane * EPL + i * C::VEC + k;
+        if (r > 0.f) last_pos = s0 + e;
       }
-    double before = 0.0;
-    const int ls = warp_find((double)tot, t, 32, lane, &before);
-    int token = -1;
-    if (ls >= 0) {
-      if (lane == ls) {
-        // the same values, recomputed in the same order
-        const float tl = (float)(t - before);
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < C::VPL; ++i)
-#pragma unroll
-          for (int k = 0; k < C::VEC; ++k) {
-            acc += r_at(i, k);
-            if (token < 0 && acc > tl) token = s0 + lane * EPL + i * C::VEC + k;
-          }
-        if (token < 0) token = last_pos;  // rounding: the lane's last positive entry
-      }
-      token = __shfl_sync(kFullMask, token, ls);
-    }
-    if (token < 0) {  // rounding put t past the slice: its last positive entry
+    const float incl = warp_incl_scan_f(tot, lane);
+    const unsigned hit = __ballot_sync(kFullMask, incl > t);
+    if (!hit) {  // rounding put t past the slice: its last positive entry
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1)
         last_pos = max(last_pos, __shfl_xor_sync(kFullMask, last_pos, o));
-      token = last_pos >= 0 ? last_pos : s0;
+      return last_pos >= 0 ? last_pos : s0;
     }
-    return token;
+    const int ls = __ffs(hit) - 1;
+    const float tl = t - __shfl_sync(kFullMask, incl - tot, ls);
+    // lane ls's elements, element q to lane q
+    float xe = 0.f, ge = 0.f;
+#pragma unroll
+    for (int i = 0; i < C::VPL; ++i)
+#pragma unroll
+      for (int k = 0; k < C::VEC; ++k) {
+        const int q = i * C::VEC + k;
+        const float xv = __shfl_sync(kFullMask, sl.t[i].at(k), ls);
+        float gv = 0.f;
+        if (DT >= 0 && with_draft) gv = __shfl_sync(kFullMask, sl.d[i].at(k), ls);
+        if (lane == q) {
+          xe = xv;
+          ge = gv;
+        }
+      }
+    const int e = ls * EPL + lane;
+    float re = 0.f;
+    if (lane < EPL && e < n && s0 + e != excl)
+      re = resid_val(xe, ge, smode, RL, RG, invZ, invZg, P.cT);
+    const float inc2 = warp_incl_scan_f(re, lane);
+    const unsigned h2 = __ballot_sync(kFullMask, lane < EPL && inc2 > tl);
+    if (h2) return s0 + ls * EPL + __ffs(h2) - 1;
+    // rounding: the lane's last positive entry
+    return __shfl_sync(kFullMask, last_pos, ls);
   }
 
   // The tile holding t: the last tile whose prefix mass (sm.pre, rescaled to
   // units of 2^ref_units) is <= t; then the warp slice from the tile's slice
-  // masses (slice_mass(c, w) -> double); then scan(c, w, t_w) inside it.
+  // masses (slice_mass(c, w) -> float, units 2^ref_units); then scan(c, w, t_w)
+  // inside it.
   template <typename SliceMass, typename Scan>
-  __device__ int resample(double t, float ref_units, SliceMass slice_mass, Scan scan) {
+  __device__ int resample(DF t, float ref_units, SliceMass slice_mass, Scan scan) {
     const int NC = P.NC;
     const float NEG_INF = -__int_as_float(0x7f800000);
     int cstar = 0;
-    double before = 0.0;
+    DF before = {0.f, 0.f};
 #pragma unroll
     for (int q = 1; q >= 0; --q) {
       const int c = q * 32 + lane;
-      double bc = 0.0;
+      DF bc = {0.f, 0.f};
       bool ok = false;
       if (c < NC) {
         const float4 pr = sm.pre[si][c][0];
         if (pr.z != NEG_INF && (pr.x != 0.f || pr.y != 0.f))
-          bc = ldexp((double)pr.x + (double)pr.y, (int)(pr.z - ref_units));
-        ok = bc <= t;
+          bc = df_scale(DF{pr.x, pr.y}, (int)(pr.z - ref_units));
+        ok = df_le(bc, t);
       }
       const unsigned h = __ballot_sync(kFullMask, ok);
       if (h) {
         const int src = 31 - __clz(h);
         cstar = q * 32 + src;
-        before = __shfl_sync(kFullMask, bc, src);
+        before = {__shfl_sync(kFullMask, bc.hi, src), __shfl_sync(kFullMask, bc.lo, src)};
         break;
       }
     }
-    const double tc = t - before;
-    const double sm_w = lane < kCW ? slice_mass(cstar, lane) : 0.0;
-    double bw = 0.0;
-    int wstar = warp_find(sm_w, tc, kCW, lane, &bw);
-    double tw;
+    const DF tc = df_sub(t, before);
+    const float sm_w = lane < kCW ? slice_mass(cstar, lane) : 0.f;
+    DF bw = {0.f, 0.f};
+    int wstar = warp_find(DF{sm_w, 0.f}, tc, kCW, lane, &bw);
+    DF tw;
     if (wstar < 0) {  // rounding put t past the tile: its last slice with mass
-      const unsigned pos = __ballot_sync(kFullMask, lane < kCW && sm_w > 0.0);
+      const unsigned pos = __ballot_sync(kFullMask, lane < kCW && sm_w > 0.f);
       wstar = pos ? 31 - __clz(pos) : 0;
-      tw = 1e300;
+      tw = {__int_as_float(0x7f800000), 0.f};
     } else {
-      tw = tc - bw;
+      tw = df_sub(tc, bw);
     }
     return scan(cstar, wstar, tw);
   }
@@ -837,26 +886,28 @@ struct Control {
       const int32_t d = j < nb ? S.dtok : -1;
       const float lm = run[0].nan ? __int_as_float(0x7fc00000) : run[0].mx;
       const float LM = run[0].ref;
-      const double zx = (double)run[0].sum.hi + (double)run[0].sum.lo;
-      float gm = NEG_INF, GM = NEG_INF;
-      double zg = 0.0, egd = 0.0;
+      const DF zx = run[0].sum;
+      float gm = NEG_INF, GM = NEG_INF, egd = 0.f;
+      DF zg = {0.f, 0.f};
       if (DT >= 0 && j < nb) {
         gm = run[1].nan ? __int_as_float(0x7fc00000) : run[1].mx;
         GM = run[1].ref;
-        zg = (double)run[1].sum.hi + (double)run[1].sum.lo;
-        egd = (double)exp_ref(S.gd, GM, P.cT, P.cTl);  // draft model's d, units 2^GM
+        zg = run[1].sum;
+        egd = exp_ref(S.gd, GM, P.cT, P.cTl);  // draft model's d, units 2^GM
       }
       // one-hot: the sums leave d out (zx), so that a rejection's residual is
       // exact; with draft logits they hold every token
-      const double ed = d >= 0 ? (double)exp_ref(S.xd, LM, P.cT, P.cTl) : 0.0;
-      const double zt = DT < 0 ? zx + ed : zx;
-      const bool bad_t = !(lm > NEG_INF) || isinf(lm) || !isfinite(zt) || !(zt > 0.0);
+      const float ed = d >= 0 ? exp_ref(S.xd, LM, P.cT, P.cTl) : 0.f;
+      const DF ztd = DT < 0 ? df_add(zx, DF{ed, 0.f}) : zx;
+      const float zt = df_f(ztd), zgf = df_f(zg);
+      const bool bad_t = !(lm > NEG_INF) || isinf(lm) || !isfinite(zt) || !(zt > 0.f);
       const bool bad_g = DT >= 0 && j < nb &&
-                         (!(gm > NEG_INF) || isinf(gm) || !isfinite(zg) || !(zg > 0.0));
+                         (!(gm > NEG_INF) || isinf(gm) || !isfinite(zgf) || !(zgf > 0.f));
       if (lane == 0) {
         if (P.dbg.row_m) P.dbg.row_m[ro] = lm / P.T;
         // Z relative to the row max: sum exp(x/T - m) = zt * 2^(LM - lm log2(e)/T)
-        if (P.dbg.row_z) P.dbg.row_z[ro] = (float)(zt * exp2((double)LM - (double)lm * P.cTd));
+        if (P.dbg.row_z)
+          P.dbg.row_z[ro] = (float)(((double)ztd.hi + (double)ztd.lo) * exp2((double)LM - (double)lm * P.cTd));
       }
       if (bad_t || bad_g) {
         finish(b, -1, -1, SAMSPEC_ST_BADROW);
@@ -864,14 +915,14 @@ struct Control {
         return;
       }
       if (j < nb) {
-        const double pd = ed / zt;
-        const double qd = DT >= 0 ? egd / zg : 1.0;
+        const float pd = ed / zt;
+        const float qd = DT >= 0 ? egd / zgf : 1.f;
         if (lane == 0) {
-          if (P.dbg.p_d) P.dbg.p_d[ro] = (float)pd;
-          if (P.dbg.q_d) P.dbg.q_d[ro] = (float)qd;
+          if (P.dbg.p_d) P.dbg.p_d[ro] = pd;
+          if (P.dbg.q_d) P.dbg.q_d[ro] = qd;
         }
         // accept iff u * q(d) <= p(d)  (eps <= alpha(x) with alpha = min(1, p/q))
-        if ((double)ua * qd <= pd) {
+        if (ua * qd <= pd) {
           post(kStats, j + 1);
           return;
         }
@@ -883,8 +934,8 @@ struct Control {
           S.L = j;
           S.lmax = LM;
           S.gmax = GM;
-          S.invZ = (float)(1.0 / zt);
-          S.invZg = (float)(1.0 / zg);
+          S.invZ = 1.f / zt;
+          S.invZg = 1.f / zgf;
           S.smode = 1;
         }
         __syncwarp();
@@ -893,24 +944,24 @@ struct Control {
       }
       // one-hot rejection: r = p without the rejected token, which the slice
       // sums already leave out; bonus row (no draft): r = p.  Units 2^LM.
-      if (j < nb && !(zx > 0.0)) {
+      if (j < nb && !(df_f(zx) > 0.f)) {
         // every other token has zero mass: p is concentrated on d itself
         if (lane == 0 && P.dbg.res_mass) P.dbg.res_mass[b] = 1.f;
         finish(b, j, d, 0);
         release();
         return;
       }
-      if (lane == 0 && P.dbg.res_mass) P.dbg.res_mass[b] = (float)(zx / zt);
-      const double tt = (double)ur * zx;
-      auto slice_mass = [&](int c, int w) -> double {
+      if (lane == 0 && P.dbg.res_mass) P.dbg.res_mass[b] = df_f(zx) / zt;
+      const DF tt = df_mul_f(zx, ur);
+      auto slice_mass = [&](int c, int w) -> float {
         const float4 r = R(c, w).a;
-        if (r.y == NEG_INF || r.z == 0.f) return 0.0;
-        return ldexp((double)r.z, (int)(r.y - LM));
+        if (r.y == NEG_INF || r.z == 0.f) return 0.f;
+        return ldexpf(r.z, (int)(r.y - LM));
       };
-      auto scan = [&](int c, int w, double tw) -> int {
+      auto scan = [&](int c, int w, DF tw) -> int {
         // the slice's own units: 2^R_w
         const float Rw = R(c, w).a.y;
-        return slice_scan(b, j, c, w, ldexp(tw, (int)(LM - Rw)), 0, d, Rw, 0.f, 0.f, 0.f);
+        return slice_scan(b, j, c, w, df_f(df_scale(tw, (int)(LM - Rw))), 0, d, Rw, 0.f, 0.f, 0.f);
       };
       const int out = resample(tt, LM, slice_mass, scan);
       finish(b, j, out, 0);
@@ -920,19 +971,19 @@ struct Control {
 
     // kResid: the running residual mass of row L and its tile prefixes
     const int L = S.L;
-    const double tot = (double)run[0].sum.hi + (double)run[0].sum.lo;
-    if (S.smode == 1 && (!(tot > 0.0) || !isfinite(tot))) {
+    const float tot = df_f(run[0].sum);
+    if (S.smode == 1 && (!(tot > 0.f) || !isfinite(tot))) {
       // zero residual (impossible in exact arithmetic): sample p instead
       if (lane == 0) S.smode = 0;
       __syncwarp();
       post(kResid, L);
       return;
     }
-    if (lane == 0 && P.dbg.res_mass) P.dbg.res_mass[b] = (float)(S.smode ? tot : 1.0);
-    const double tt = (double)ur * tot;
-    auto slice_mass = [&](int c, int w) -> double { return (double)R(c, w).a.x; };
-    auto scan = [&](int c, int w, double tw) -> int {
-      return slice_scan(b, L, c, w, tw, S.smode, -1, S.lmax, S.gmax, S.invZ, S.invZg);
+    if (lane == 0 && P.dbg.res_mass) P.dbg.res_mass[b] = S.smode ? tot : 1.f;
+    const DF tt = df_mul_f(run[0].sum, ur);
+    auto slice_mass = [&](int c, int w) -> float { return R(c, w).a.x; };
+    auto scan = [&](int c, int w, DF tw) -> int {
+      return slice_scan(b, L, c, w, df_f(tw), S.smode, -1, S.lmax, S.gmax, S.invZ, S.invZg);
     };
     const int out = resample(tt, 0.f, slice_mass, scan);
     finish(b, L, out, 0);
