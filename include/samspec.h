@@ -196,10 +196,10 @@ int sam_dump_sequence(sam_batch* batch, int32_t b, int32_t* h_scalars, int32_t* 
  * Workspace: d_workspace of spec_verify_workspace_bytes(B, K, V) bytes,
  * 256-byte aligned, zeroed once with spec_verify_workspace_init before first
  * use and not shared by two calls in flight.  Logits pointers must be 16-byte
- * aligned.  Limits: 1 <= B <= 2^24, 1 <= K <= 32, and V at most 64 tiles of
- * the kernel's 32 KB staging buffer: 524288 (fp32 target, greedy or one-hot
- * drafts), 1048576 (bf16 target, greedy or one-hot), 524288 (bf16 target and
- * bf16 draft logits), 262144 (any other pair with draft logits); larger V
+ * aligned.  Limits: 1 <= B <= 2^24, 1 <= K <= 32, and V at most 48 tiles of
+ * the kernel's 48 KB staging buffer: 589824 (fp32 target, greedy or one-hot
+ * drafts), 1179648 (bf16 target, greedy or one-hot), 589824 (bf16 target and
+ * bf16 draft logits), 294912 (any other pair with draft logits); larger V
  * returns SAMSPEC_ESIZE.  Asynchronous; one kernel launch. */
 typedef struct spec_verify_debug {
   float* row_m;

@@ -19,23 +19,27 @@
 // their accept chains itself, so rows after the first rejection are never read
 // and no inter-CTA merge is needed:
 //   warp 16 (producer) issues 1-D bulk copies (cp.async.bulk, the TMA engine)
-//       of 32 KB vocab tiles of the rows its sequence slots ask for into a
+//       of 48 KB vocab tiles of the rows its sequence slots ask for into a
 //       ring of shared-memory stages, completion counted on mbarriers;
-//   warps 0-15 (consumers) each reduce a 1/16 slice ("warp slice") of every
-//       tile from shared memory (16-byte vector reads) to a record -- the
-//       slice's max and sum of 2^((l - max) log2(e)/T), or its (max, first
-//       argmax) -- and release the stage;
+//   warps 0-15 (consumers) each take a 1/16 slice ("warp slice") of every
+//       tile into registers, release the stage, and reduce the slice to a
+//       record -- its max, an integer exponent reference R and the sum of
+//       2^(l log2(e)/T - R), or (greedy) its max -- then count the tile done;
 //   warps 17-19 (control, one per sequence slot) claim sequences from a
-//       global counter,
-//       merges the warp-slice records of a finished row in fp64, draws the
-//       Philox coins, decides accept/reject and posts the next row; after the
-//       final row it resamples: the slice records give the mass of every warp
-//       slice, so it finds the slice holding u' * sum(r) and scans just that
-//       2-8 KB slice, read again from L2, in ascending token order.
-// Several slots keep the producer streaming while a control warp decides.
-// Every wait is bounded by a global-timer deadline; a CTA that runs out of
-// time marks its sequences SAMSPEC_ST_TIMEOUT, lets its copies in flight land
-// and exits.
+//       global counter and merge each tile's 16 records as soon as they land
+//       (running max, reference and compensated float-pair mass, and the mass
+//       before each tile), so the row's statistics are ready when its last
+//       tile is; they draw the Philox coins, decide accept/reject and post the
+//       next row.  After the final row a control warp resamples: the tile
+//       prefix masses and slice records locate the warp slice holding
+//       u' * sum(r), and only that 3-6 KB slice is read again (from L2) and
+//       scanned in ascending token order.
+// Three slots keep the producer streaming while control warps decide.  Tiles
+// of 48 KB (4 ring stages) measured faster than 24-32 KB tiles with 16-28
+// consumer warps: the per-tile work of producer, consumers and control is
+// amortised over more logits.  Every wait is bounded by a global-timer
+// deadline; a CTA that runs out of time marks its sequences
+// SAMSPEC_ST_TIMEOUT, lets its copies in flight land and exits.
 
 #include <cstdint>
 #include <cstring>
@@ -55,10 +59,10 @@ constexpr int kProdWarp = kCW;       // producer warp
 constexpr int kCtrlWarp = kCW + 1;   // first control warp (one per slot)
 constexpr int kSlots = 3;
 constexpr int kThreads = (kCW + 1 + kSlots) * 32;
-constexpr int kStageBytes = 32768;
+constexpr int kStageBytes = 49152;
 constexpr int kMaxStages = 6;
 constexpr int kMinStages = 3;
-constexpr int kMaxChunks = 64;
+constexpr int kMaxChunks = 48;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 
 enum Kind : int32_t { kStats = 0, kResid = 1, kExit = 3 };
@@ -124,7 +128,6 @@ struct Smem {
   int32_t claim_lock;   // one control warp claims at a time
   int32_t tile_cnt[kSlots][kMaxChunks];  // consumer warps done with each tile of a job
   float4 pre[kSlots][kMaxChunks][2];     // control: mass before each tile {hi, lo, ref, 0}
-  float cmass[kSlots][kMaxChunks];  // control warp: tile masses per slot
 };
 
 __device__ __forceinline__ uint64_t gtimer() {
@@ -273,11 +276,12 @@ struct Cfg {
   static constexpr int SD = DT < 0 ? 0 : (DT ? 2 : 4);
   static constexpr int MAXS = ST > SD ? ST : SD;
   static constexpr int VEC = 16 / MAXS;
-  static constexpr int E_TILE = DT < 0 ? kStageBytes / ST : (ST == SD ? kStageBytes / (2 * ST) : 4096);
+  static constexpr int E_TILE = DT < 0 ? kStageBytes / ST : (ST == SD ? kStageBytes / (2 * ST) : kStageBytes / 8);
   static constexpr int SL = E_TILE / kCW;        // elements per warp slice
   static constexpr int VPL = SL / (32 * VEC);    // vectors per lane per array
   static constexpr int DOFF = E_TILE * ST;       // byte offset of the draft part
   static_assert(VPL >= 1 && VPL * 32 * VEC * kCW == E_TILE, "tile shape");
+  static_assert((VEC & (VEC - 1)) == 0, "vector length is a power of two");
   static_assert(E_TILE * (ST + SD) <= kStageBytes, "stage size");
 };
 
@@ -420,10 +424,11 @@ __device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, 
         for (int p = 0; p < h; ++p) v[p] = add2(v[p], v[p + h]);
       part[i] = v[0];
     }
+    // pairwise over the lane's VPL vectors (VPL need not be a power of two)
 #pragma unroll
-    for (int h = C::VPL / 2; h >= 1; h >>= 1)
+    for (int h = 1; h < C::VPL; h <<= 1)
 #pragma unroll
-      for (int i = 0; i < h; ++i) part[i] = add2(part[i], part[i + h]);
+      for (int i = 0; i + h < C::VPL; i += 2 * h) part[i] = add2(part[i], part[i + h]);
     float lo, hi;
     upk2(part[0], lo, hi);
     z = lo + hi;
@@ -445,9 +450,9 @@ __device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, 
       part[i] = v[0];
     }
 #pragma unroll
-    for (int h = C::VPL / 2; h >= 1; h >>= 1)
+    for (int h = 1; h < C::VPL; h <<= 1)
 #pragma unroll
-      for (int i = 0; i < h; ++i) part[i] += part[i + h];
+      for (int i = 0; i + h < C::VPL; i += 2 * h) part[i] += part[i + h];
     z = part[0];
   }
   // the slice's terms are summed in fp32 (its mass only has to locate a tile
@@ -778,29 +783,37 @@ struct Control {
       return last_pos >= 0 ? last_pos : s0;
     }
     const int ls = __ffs(hit) - 1;
-    const float tl = t - __shfl_sync(kFullMask, incl - tot, ls);
-    // lane ls's elements, element q to lane q
-    float xe = 0.f, ge = 0.f;
+    float tl = t - __shfl_sync(kFullMask, incl - tot, ls);
+    // lane ls's elements, 32 at a time in ascending order: element q to lane
+    // q % 32 of round q / 32
+    constexpr int kRounds = (EPL + 31) / 32;
 #pragma unroll
-    for (int i = 0; i < C::VPL; ++i)
+    for (int rd = 0; rd < kRounds; ++rd) {
+      float xe = 0.f, ge = 0.f;
 #pragma unroll
-      for (int k = 0; k < C::VEC; ++k) {
-        const int q = i * C::VEC + k;
-        const float xv = __shfl_sync(kFullMask, sl.t[i].at(k), ls);
-        float gv = 0.f;
-        if (DT >= 0 && with_draft) gv = __shfl_sync(kFullMask, sl.d[i].at(k), ls);
-        if (lane == q) {
-          xe = xv;
-          ge = gv;
+      for (int i = 0; i < C::VPL; ++i)
+#pragma unroll
+        for (int k = 0; k < C::VEC; ++k) {
+          const int q = i * C::VEC + k;
+          if (q / 32 != rd) continue;
+          const float xv = __shfl_sync(kFullMask, sl.t[i].at(k), ls);
+          float gv = 0.f;
+          if (DT >= 0 && with_draft) gv = __shfl_sync(kFullMask, sl.d[i].at(k), ls);
+          if (lane == q % 32) {
+            xe = xv;
+            ge = gv;
+          }
         }
-      }
-    const int e = ls * EPL + lane;
-    float re = 0.f;
-    if (lane < EPL && e < n && s0 + e != excl)
-      re = resid_val(xe, ge, smode, RL, RG, invZ, invZg, P.cT);
-    const float inc2 = warp_incl_scan_f(re, lane);
-    const unsigned h2 = __ballot_sync(kFullMask, lane < EPL && inc2 > tl);
-    if (h2) return s0 + ls * EPL + __ffs(h2) - 1;
+      const int q = rd * 32 + lane;
+      const int e = ls * EPL + q;
+      float re = 0.f;
+      if (q < EPL && e < n && s0 + e != excl)
+        re = resid_val(xe, ge, smode, RL, RG, invZ, invZg, P.cT);
+      const float inc2 = warp_incl_scan_f(re, lane);
+      const unsigned h2 = __ballot_sync(kFullMask, q < EPL && inc2 > tl);
+      if (h2) return s0 + ls * EPL + rd * 32 + __ffs(h2) - 1;
+      tl -= __shfl_sync(kFullMask, inc2, 31);
+    }
     // rounding: the lane's last positive entry
     return __shfl_sync(kFullMask, last_pos, ls);
   }

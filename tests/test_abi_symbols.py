@@ -56,10 +56,10 @@ def test_spec_verify_rejects_bad_arguments_on_the_host():
     assert call(dtype=7) == bd.EDTYPE
     assert call(ws_bytes=16) == bd.ESIZE
     assert call(target=ctypes.c_void_p(4100)) == bd.EALIGN
-    # V above 64 staging tiles: 8192 fp32 / 16384 bf16 logits per tile
-    assert call(dtype=bd.F32, V=64 * 8192 + 1) == bd.ESIZE
-    assert call(dtype=bd.BF16, V=64 * 16384 + 1) == bd.ESIZE
-    assert call(dtype=bd.F32, V=64 * 8192 + 1, T=0.0) == bd.ESIZE
+    # V above 48 staging tiles: 12288 fp32 / 24576 bf16 logits per tile
+    assert call(dtype=bd.F32, V=48 * 12288 + 1) == bd.ESIZE
+    assert call(dtype=bd.BF16, V=48 * 24576 + 1) == bd.ESIZE
+    assert call(dtype=bd.F32, V=48 * 12288 + 1, T=0.0) == bd.ESIZE
 
 
 def test_binding_refuses_missing_library(tmp_path):

@@ -215,3 +215,28 @@ def test_sweep_b1024_full_size_sampled(ss, cuda_device, K, dtype, T):
     compare_verify(gs, o, lambda i: rows[i], dr, None, T)
     # acceptance is low (drafts uniform among the top-5): most sequences stop early
     assert (g["accept_len"] <= K).all()
+
+
+@pytest.mark.parametrize("dtype,V,with_draft", [(torch.bfloat16, 48 * 24576, False),
+                                                (torch.float32, 48 * 12288, False),
+                                                (torch.float32, 48 * 6144, True)])
+def test_largest_vocabulary(ss, cuda_device, dtype, V, with_draft):
+    """The largest V each logits layout accepts (48 staging tiles), and one
+    more, which is refused."""
+    B, K = 2, 1
+    rng = np.random.default_rng(V)
+    logits = workloads.gaussian_logits(rng, (B, K + 1, V), 2.0)
+    draft = np.argsort(-logits[:, :K], axis=-1)[..., 3].astype(np.int32)
+    dlog = None
+    if with_draft:
+        dlog = (logits[:, :K] + workloads.gaussian_logits(rng, (B, K, V), 1.0)).astype(np.float32)
+    for T in (0.0, 1.0):
+        g, o, te, de = _run_both(ss, cuda_device, logits, draft, None, T=T, seed=3,
+                                 draft_logits=dlog if T > 0 else None, t_dtype=dtype)
+        _check(g, o, te, de, draft, None, T)
+    big = torch.zeros((1, K + 1, V + 64), dtype=dtype, device=cuda_device)
+    with pytest.raises(ss.SamspecError):
+        ss.spec_verify(big, torch.zeros((1, K), dtype=torch.int32, device=cuda_device), None,
+                       temperature=1.0,
+                       draft_logits=(torch.zeros((1, K, V + 64), dtype=torch.float32, device=cuda_device)
+                                     if with_draft else None))
