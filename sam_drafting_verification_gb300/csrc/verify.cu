@@ -199,8 +199,26 @@ __device__ __forceinline__ DF df_mul_f(DF x, float a) {
   return {hi, e - (hi - p)};
 }
 __device__ __forceinline__ float df_f(DF x) { return x.hi + x.lo; }
-__device__ __forceinline__ DF df_warp_sum(float v) {
-  DF a = {v, 0.f};
+// Warp sum of lane values in [0, 2^11) as a float pair: each value splits
+// into a multiple of 2^-10 (rounding by the 1.5 * 2^13 constant) and the
+// remainder (|r| <= 2^-11).  The multiples of 2^-10 sum exactly in fp32 (the
+// total stays below 2^11, 21 bits), the remainders in plain fp32 (error about
+// 2^-30 absolute), both halves of a packed pair per butterfly step.
+__device__ __forceinline__ DF split_warp_sum(float v) {
+  const float hi = (v + 12288.f) - 12288.f;
+  uint64_t p = pk2(hi, v - hi);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t q = ((uint64_t)__shfl_xor_sync(kFullMask, (uint32_t)(p >> 32), o) << 32) |
+                       __shfl_xor_sync(kFullMask, (uint32_t)p, o);
+    p = add2(p, q);
+  }
+  float sh, sl;
+  upk2(p, sh, sl);
+  const float s = sh + sl;  // |sl| is far below |sh| unless both are tiny
+  return {s, sl - (s - sh)};
+}
+__device__ __forceinline__ DF df_warp_sum(DF a) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const DF o2 = {__shfl_xor_sync(kFullMask, a.hi, o), __shfl_xor_sync(kFullMask, a.lo, o)};
@@ -361,15 +379,28 @@ template <int TT, int DT, bool FULL, bool DRAFT_ARRAY>
 __device__ __forceinline__ float lane_max(const Slice<TT, DT>& s, int w, int lane, int nel) {
   using C = Cfg<TT, DT>;
   float m = -__int_as_float(0x7f800000);
+  constexpr int ES = DRAFT_ARRAY ? C::SD : C::ST;
+  if constexpr (FULL && ES == 2) {
+    // bf16: packed maxima over every word of the lane, one unpack at the end
+    constexpr int W = C::VEC / 2;
+    uint32_t a = DRAFT_ARRAY ? s.d[0].w[0] : s.t[0].w[0];
 #pragma unroll
-  for (int i = 0; i < C::VPL; ++i) {
-    if (FULL) {
-      m = fmax_nan(m, DRAFT_ARRAY ? s.d[i].vmax() : s.t[i].vmax());
-    } else {
-      const int e = w * C::SL + (i * 32 + lane) * C::VEC;
+    for (int i = 0; i < C::VPL; ++i)
 #pragma unroll
-      for (int k = 0; k < C::VEC; ++k)
-        if (e + k < nel) m = fmax_nan(m, DRAFT_ARRAY ? s.d[i].at(k) : s.t[i].at(k));
+      for (int q = 0; q < W; ++q)
+        if (i > 0 || q > 0) a = bf16x2_max_nan(a, DRAFT_ARRAY ? s.d[i].w[q] : s.t[i].w[q]);
+    m = fmax_nan(bf16_lo(a), bf16_hi(a));
+  } else {
+#pragma unroll
+    for (int i = 0; i < C::VPL; ++i) {
+      if (FULL) {
+        m = fmax_nan(m, DRAFT_ARRAY ? s.d[i].vmax() : s.t[i].vmax());
+      } else {
+        const int e = w * C::SL + (i * 32 + lane) * C::VEC;
+#pragma unroll
+        for (int k = 0; k < C::VEC; ++k)
+          if (e + k < nel) m = fmax_nan(m, DRAFT_ARRAY ? s.d[i].at(k) : s.t[i].at(k));
+      }
     }
   }
   return m;
@@ -455,9 +486,9 @@ __device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, 
       for (int i = 0; i + h < C::VPL; i += 2 * h) part[i] += part[i + h];
     z = part[0];
   }
-  // the slice's terms are summed in fp32 (its mass only has to locate a tile
-  // and a slice; the control warp combines slices with compensated sums)
-  return make_float4(m, R, warp_sum(z), 0.f);
+  // lane sums in fp32; the warp's 32 lane sums as a float pair (z, w)
+  const DF zz = split_warp_sum(z);
+  return make_float4(m, R, zz.hi, zz.lo);
 }
 
 // Residual weight of one element, the same expression in the residual pass and
@@ -484,7 +515,7 @@ __device__ __forceinline__ float resid_val(float x, float g, int smode, float RL
   return fmaxf(0.f, pe * invZ - qe * invZg);
 }
 
-// residual-pass record: sum of r over the slice {r, 0, 0, 0}
+// residual-pass record: sum of r over the slice as a float pair {hi, lo, 0, 0}
 template <int TT, int DT, bool FULL>
 __device__ __forceinline__ float4 reduce_resid(const Slice<TT, DT>& s, int w, int lane, int nel,
                                                const Slot& S, float cT) {
@@ -500,7 +531,8 @@ __device__ __forceinline__ float4 reduce_resid(const Slice<TT, DT>& s, int w, in
         part += resid_elem<TT, DT>(s, i, k, S.smode, S.lmax, S.gmax, S.invZ, S.invZg, cT);
     acc += part;
   }
-  return make_float4(warp_sum(acc), 0.f, 0.f, 0.f);
+  const DF a = split_warp_sum(acc);
+  return make_float4(a.hi, a.lo, 0.f, 0.f);
 }
 
 // ---- outputs ---------------------------------------------------------------
@@ -687,8 +719,8 @@ struct Control {
     const bool nan = __any_sync(kFullMask, r.x != r.x || r.z != r.z);
     const float mc = warp_max(r.x);
     const float Rc = warp_max(r.y);
-    float v = 0.f;
-    if (Rc != NEG_INF && r.z != 0.f) v = ldexpf(r.z, (int)(r.y - Rc));
+    DF v = {0.f, 0.f};
+    if (Rc != NEG_INF && r.z != 0.f) v = df_scale(DF{r.z, r.w}, (int)(r.y - Rc));
     const DF t = df_warp_sum(v);  // the tile's mass over its 16 slices, units 2^Rc
     Run& R_ = run[f];
     if (lane == 0) sm.pre[si][c][f] = make_float4(R_.sum.hi, R_.sum.lo, R_.ref, 0.f);
@@ -723,7 +755,7 @@ struct Control {
       merge_softmax(c, 0);
       if (DT >= 0 && S.j < S.nb) merge_softmax(c, 1);
     } else {  // residual pass: plain running sum in units of p
-      const DF t = df_warp_sum(lane < kCW ? R(c, lane).a.x : 0.f);
+      const DF t = df_warp_sum(lane < kCW ? DF{R(c, lane).a.x, R(c, lane).a.y} : DF{0.f, 0.f});
       if (lane == 0) sm.pre[si][c][0] = make_float4(run[0].sum.hi, run[0].sum.lo, 0.f, 0.f);
       run[0].sum = df_add(run[0].sum, t);
       run[0].ref = 0.f;
@@ -820,7 +852,7 @@ struct Control {
 
   // The tile holding t: the last tile whose prefix mass (sm.pre, rescaled to
   // units of 2^ref_units) is <= t; then the warp slice from the tile's slice
-  // masses (slice_mass(c, w) -> float, units 2^ref_units); then scan(c, w, t_w)
+  // masses (slice_mass(c, w) -> float pair, units 2^ref_units); then scan(c, w, t_w)
   // inside it.
   template <typename SliceMass, typename Scan>
   __device__ int resample(DF t, float ref_units, SliceMass slice_mass, Scan scan) {
@@ -848,12 +880,12 @@ struct Control {
       }
     }
     const DF tc = df_sub(t, before);
-    const float sm_w = lane < kCW ? slice_mass(cstar, lane) : 0.f;
+    const DF sm_w = lane < kCW ? slice_mass(cstar, lane) : DF{0.f, 0.f};
     DF bw = {0.f, 0.f};
-    int wstar = warp_find(DF{sm_w, 0.f}, tc, kCW, lane, &bw);
+    int wstar = warp_find(sm_w, tc, kCW, lane, &bw);
     DF tw;
     if (wstar < 0) {  // rounding put t past the tile: its last slice with mass
-      const unsigned pos = __ballot_sync(kFullMask, lane < kCW && sm_w > 0.f);
+      const unsigned pos = __ballot_sync(kFullMask, lane < kCW && sm_w.hi > 0.f);
       wstar = pos ? 31 - __clz(pos) : 0;
       tw = {__int_as_float(0x7f800000), 0.f};
     } else {
@@ -966,10 +998,10 @@ struct Control {
       }
       if (lane == 0 && P.dbg.res_mass) P.dbg.res_mass[b] = df_f(zx) / zt;
       const DF tt = df_mul_f(zx, ur);
-      auto slice_mass = [&](int c, int w) -> float {
+      auto slice_mass = [&](int c, int w) -> DF {
         const float4 r = R(c, w).a;
-        if (r.y == NEG_INF || r.z == 0.f) return 0.f;
-        return ldexpf(r.z, (int)(r.y - LM));
+        if (r.y == NEG_INF || r.z == 0.f) return DF{0.f, 0.f};
+        return df_scale(DF{r.z, r.w}, (int)(r.y - LM));
       };
       auto scan = [&](int c, int w, DF tw) -> int {
         // the slice's own units: 2^R_w
@@ -994,7 +1026,7 @@ struct Control {
     }
     if (lane == 0 && P.dbg.res_mass) P.dbg.res_mass[b] = S.smode ? tot : 1.f;
     const DF tt = df_mul_f(run[0].sum, ur);
-    auto slice_mass = [&](int c, int w) -> float { return R(c, w).a.x; };
+    auto slice_mass = [&](int c, int w) -> DF { return DF{R(c, w).a.x, R(c, w).a.y}; };
     auto scan = [&](int c, int w, DF tw) -> int {
       return slice_scan(b, L, c, w, df_f(tw), S.smode, -1, S.lmax, S.gmax, S.invZ, S.invZg);
     };
@@ -1044,12 +1076,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
     int cs = 0;
     uint32_t cph = 0;
     for (;;) {
-      const uint64_t t0 = gtimer();
       bool ok = true;
-      while (!mbar_try_wait(&sm.full[cs], cph)) {
-        if (vload(&sm.abort) || gtimer() - t0 > kWaitNs) {
-          ok = false;
-          break;
+      if (!mbar_try_wait(&sm.full[cs], cph)) {
+        const uint64_t t0 = gtimer();
+        while (!mbar_try_wait(&sm.full[cs], cph)) {
+          if (vload(&sm.abort) || gtimer() - t0 > kWaitNs) {
+            ok = false;
+            break;
+          }
         }
       }
       if (!ok) {

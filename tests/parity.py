@@ -23,10 +23,13 @@ def rel_err(a, b):
     return np.abs(a - b) / np.maximum(np.abs(b), 1e-300)
 
 
-def compare_verify(g, o, target_rows, draft, draft_len, T, draft_rows=None, check_probs=True):
+def compare_verify(g, o, target_rows, draft, draft_len, T, draft_rows=None, check_probs=True,
+                   budget=True):
     """g: dict of numpy arrays from the GPU; o: oracle.verify output on the
     same inputs.  target_rows(b) -> [K+1, V] float32 rows of sequence b,
-    draft_rows(b) -> [K, V] or None.  Returns (decisions, excused)."""
+    draft_rows(b) -> [K, V] or None.  Returns (decisions, excused).  With
+    budget=False the 1e-4 share is left to the caller (counted over many
+    calls)."""
     B, K1 = o["row_m"].shape
     K = K1 - 1
     decisions = 0
@@ -69,7 +72,8 @@ def compare_verify(g, o, target_rows, draft, draft_len, T, draft_rows=None, chec
                 else:
                     assert g["row_m"][b, j] == o["row_m"][b, j]
                     assert g["row_arg"][b, j] == o["row_arg"][b, j]
-    assert excused <= int(1e-4 * max(decisions, 1)), f"{excused} excused of {decisions}"
+    if budget:
+        assert excused <= int(1e-4 * max(decisions, 1)), f"{excused} excused of {decisions}"
     return decisions, excused
 
 
