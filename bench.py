@@ -46,10 +46,10 @@ POOL = 16
 # workload, with the SHA-256 of verify.cu they were taken on: a changed kernel
 # reports null until it is captured again.
 VERIFY_TRAFFIC = {
-    "rs_bf16_b64": {"bytes": 19544192.0, "profile": "profiles/verify_kernel_rs_bf16_b64.md",
-                    "verify_cu_sha256": "9b8d7ccf5a3f87e5dc2be592ed0901ce44a9b9b9fd7635586796b575bf2b0393"},
-    "long_rollout_b256": {"bytes": 79012000.0, "profile": "profiles/launches_long_rollout_b256.md",
-                          "verify_cu_sha256": "9b8d7ccf5a3f87e5dc2be592ed0901ce44a9b9b9fd7635586796b575bf2b0393"},
+    "rs_bf16_b64": {"bytes": 19559680.0, "profile": "profiles/verify_kernel_rs_bf16_b64.md",
+                    "verify_cu_sha256": "e7722dba7a26453048c49c37f170930c98753fd413f9114ecbd6cb579588155e"},
+    "long_rollout_b256": {"bytes": 79019000.0, "profile": "profiles/launches_long_rollout_b256.md",
+                          "verify_cu_sha256": "e7722dba7a26453048c49c37f170930c98753fd413f9114ecbd6cb579588155e"},
 }
 
 
