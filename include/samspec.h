@@ -142,6 +142,19 @@ int sam_step(sam_batch* batch, const int32_t* d_tokens, const int32_t* d_n_new,
              int32_t max_new, int32_t K, int32_t* d_draft, int32_t* d_draft_len,
              int32_t* d_match_len, int32_t* d_min_endpos, samspec_stream_t stream);
 
+/* sam_step on n sequences of the batch: call index i (0 <= i < n) works on
+ * automaton d_rows[i] (d_rows NULL: automaton i, n <= B); d_tokens [n, max_new],
+ * d_n_new [n] and the draft outputs [n, K] / [n] follow the call index, so a
+ * caller can pass only its active sequences.  K = 0 extends without drafting
+ * (d_draft may be NULL; d_draft_len, if given, is set to 0; match_len and
+ * min_endpos are not written).
+ * Rows must be distinct within a call; a row outside [0, B) leaves no
+ * automaton changed and gets an empty draft. */
+int sam_step_rows(sam_batch* batch, const int32_t* d_rows, int32_t n, const int32_t* d_tokens,
+                  const int32_t* d_n_new, int32_t max_new, int32_t K, int32_t* d_draft,
+                  int32_t* d_draft_len, int32_t* d_match_len, int32_t* d_min_endpos,
+                  samspec_stream_t stream);
+
 /* Copies the B status words to h_status[B] (host memory) and synchronises
  * `stream`. */
 int sam_get_status(sam_batch* batch, int32_t* h_status, samspec_stream_t stream);
@@ -168,7 +181,8 @@ int sam_dump_sequence(sam_batch* batch, int32_t b, int32_t* h_scalars, int32_t* 
  *                  V contiguous; row j scores the token after draft j-1.
  *   d_draft_logits [B, K, V] logits of a draft model, or NULL for one-hot
  *                  drafts (a suffix automaton's draft has q = indicator).
- *   d_draft        [B, K] int32 draft tokens d_0 .. d_{K-1}.
+ *   d_draft        [B, K] int32 draft tokens d_0 .. d_{K-1} (may be NULL when
+ *                  K = 0: no drafts, the bonus row alone is sampled).
  *   d_draft_len    [B] int32 n_b in [0, K], or NULL (n_b = K).
  *   temperature    0 selects greedy verification: accept while d_j equals
  *                  the row's argmax (lowest id on ties); the emitted token is
@@ -196,7 +210,7 @@ int sam_dump_sequence(sam_batch* batch, int32_t b, int32_t* h_scalars, int32_t* 
  * Workspace: d_workspace of spec_verify_workspace_bytes(B, K, V) bytes,
  * 256-byte aligned, zeroed once with spec_verify_workspace_init before first
  * use and not shared by two calls in flight.  Logits pointers must be 16-byte
- * aligned.  Limits: 1 <= B <= 2^24, 1 <= K <= 32, and V at most 48 tiles of
+ * aligned.  Limits: 1 <= B <= 2^24, 0 <= K <= 32, and V at most 48 tiles of
  * the kernel's 48 KB staging buffer: 589824 (fp32 target, greedy or one-hot
  * drafts), 1179648 (bf16 target, greedy or one-hot), 589824 (bf16 target and
  * bf16 draft logits), 294912 (any other pair with draft logits); larger V
@@ -245,6 +259,31 @@ int spec_verify_noalloc(const void* d_target, int32_t target_dtype, const void* 
                         uint64_t step, int32_t* d_accept_len, int32_t* d_out_token,
                         int32_t* d_emit, int32_t* d_emit_len, int32_t* d_status,
                         const spec_verify_debug* dbg, samspec_stream_t stream);
+
+/* One decode step of model-free speculative decoding ([P1] §1.1: verify, then
+ * update each sequence's D-SAM with the verified tokens, then draft; [P1]
+ * §3.1.1: whether a step speculates at all is the caller's choice of K and
+ * K_next, e.g. only while the number of active sequences is at most a
+ * threshold):
+ *   1. spec_verify of n sequences (one-hot drafts: logits [n, K+1, V],
+ *      d_draft [n, K] with d_draft_len [n] or NULL; K = 0 verifies the bonus
+ *      row only, i.e. plain decoding) into accept_len / out_token / status
+ *      and the required d_emit [n, K+1] / d_emit_len [n];
+ *   2. sam_step_rows: automaton d_rows[i] (or i) is extended by its emitted
+ *      tokens (none for a sequence with a non-zero status) and drafts K_next
+ *      tokens into d_next_draft [n, K_next] / d_next_draft_len [n] (all 0
+ *      when K_next = 0; d_next_draft may then be NULL).
+ * d_next_draft may alias d_draft (the verification has read it by then).
+ * Two launches on `stream`; workspace as for spec_verify.  Errors as for the
+ * two calls. */
+int sam_spec_step(sam_batch* batch, const int32_t* d_rows, int32_t n, const void* d_target,
+                  int32_t target_dtype, const int32_t* d_draft, const int32_t* d_draft_len,
+                  int32_t K, int32_t V, float temperature, uint64_t seed, uint64_t step,
+                  int32_t* d_accept_len, int32_t* d_out_token, int32_t* d_emit,
+                  int32_t* d_emit_len, int32_t* d_status, const spec_verify_debug* dbg,
+                  int32_t K_next, int32_t* d_next_draft, int32_t* d_next_draft_len,
+                  int32_t* d_match_len, int32_t* d_min_endpos, void* d_workspace,
+                  size_t ws_bytes, samspec_stream_t stream);
 
 /* Philox4x32-10 uniforms exactly as spec_verify draws them, for inspection:
  * d_u[2 * (b * (K+1) + j) + {0,1}] = (u_j, u'_j) of sequence b, for

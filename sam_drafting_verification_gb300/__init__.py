@@ -7,6 +7,8 @@ the C entry points, over torch CUDA tensors:
     .extend(tokens, n_new)              -- sam_extend
     .draft(K)                           -- sam_draft
     .step(tokens, n_new, K)             -- sam_step (extend + draft, one launch)
+    .step_rows(rows, tokens, n_new, K)  -- sam_step_rows (a subset of the sequences)
+    .spec_step(target, draft, ...)      -- sam_spec_step (verify, extend, draft)
     .status(), .reset(mask), .dump(b), .export(), .import_(blob)
   spec_verify(target, draft, ...)       -- spec_verify
   spec_uniforms(B, K, seed, step)       -- spec_uniforms
@@ -117,6 +119,68 @@ class SamBatch:
                  "sam_step")
         return d, dl, ml, me
 
+    def step_rows(self, rows, tokens, n_new, K: int, out=None):
+        """sam_step on the automata `rows` (int32 [n], or None for 0..n-1)."""
+        _req(tokens, torch.int32, "tokens")
+        if tokens.dim() != 2:
+            raise ValueError("tokens must be [n, max_new]")
+        n = int(tokens.shape[0])
+        if rows is not None:
+            _req(rows, torch.int32, "rows", (n,))
+        _req(n_new, torch.int32, "n_new", (n,))
+        if out is None:
+            z = lambda *s: torch.empty(s, dtype=torch.int32, device=self.device)  # noqa: E731
+            out = (z(n, K), z(n), z(n), z(n))
+        d, dl, ml, me = out
+        _b.check(self.lib.sam_step_rows(self._h, _ptr(rows), n, _ptr(tokens), _ptr(n_new),
+                                        int(tokens.shape[1]), int(K), _ptr(d) if K > 0 else None,
+                                        _ptr(dl), _ptr(ml), _ptr(me), _stream(self.device)),
+                 "sam_step_rows")
+        return d, dl, ml, me
+
+    def spec_step(self, target, draft, draft_len=None, K_next: int = 3, rows=None,
+                  temperature: float = 0.0, seed: int = 0, step: int = 0, out=None,
+                  workspace=None):
+        """One decode step: verify `draft` ([n, K], one-hot) against `target`
+        ([n, K+1, V]), extend each automaton by its emitted tokens, draft
+        K_next tokens.  Returns a dict of CUDA tensors (accept_len, out_token,
+        emit, emit_len, status, next_draft, next_draft_len, match_len,
+        min_endpos)."""
+        if target.dim() != 3:
+            raise ValueError("target must be [n, K+1, V]")
+        n, K1, V = (int(x) for x in target.shape)
+        K = K1 - 1
+        dt = {torch.float32: F32, torch.bfloat16: BF16}.get(target.dtype)
+        if dt is None:
+            raise TypeError("target must be float32 or bfloat16")
+        _req(target, target.dtype, "target")
+        _req(draft, torch.int32, "draft", (n, K))
+        if draft_len is not None:
+            _req(draft_len, torch.int32, "draft_len", (n,))
+        if rows is not None:
+            _req(rows, torch.int32, "rows", (n,))
+        res = out if out is not None else {}
+
+        def need(key, shape):
+            if key not in res:
+                res[key] = torch.empty(shape, dtype=torch.int32, device=self.device)
+
+        for k in ("accept_len", "out_token", "emit_len", "status", "next_draft_len", "match_len",
+                  "min_endpos"):
+            need(k, (n,))
+        need("emit", (n, K1))
+        need("next_draft", (n, int(K_next)))
+        ws = workspace if workspace is not None else verify_workspace(n, K, V, self.device)
+        _b.check(self.lib.sam_spec_step(
+            self._h, _ptr(rows), n, _ptr(target), dt, _ptr(draft) if K > 0 else None,
+            _ptr(draft_len), K, V, float(temperature), int(seed) & (2**64 - 1),
+            int(step) & (2**64 - 1), _ptr(res["accept_len"]), _ptr(res["out_token"]),
+            _ptr(res["emit"]), _ptr(res["emit_len"]), _ptr(res["status"]), None, int(K_next),
+            _ptr(res["next_draft"]) if K_next > 0 else None, _ptr(res["next_draft_len"]),
+            _ptr(res["match_len"]), _ptr(res["min_endpos"]), _ptr(ws), ws.numel(),
+            _stream(self.device)), "sam_spec_step")
+        return res
+
     def status(self):
         import numpy as np
         out = np.empty(self.B, np.int32)
@@ -221,7 +285,8 @@ def spec_verify(target, draft, draft_len=None, temperature: float = 0.0, seed: i
         need("res_mass", (B,), torch.float32, float("nan"))
         dbg = _b.VerifyDebug(*[res[k].data_ptr() for k in ("row_m", "row_z", "p_d", "q_d", "row_arg", "res_mass")])
     ws = workspace if workspace is not None else verify_workspace(B, K, V, dev)
-    rc = lib.spec_verify(_ptr(target), dt, _ptr(draft_logits), ddt, _ptr(draft), _ptr(draft_len),
+    rc = lib.spec_verify(_ptr(target), dt, _ptr(draft_logits), ddt, _ptr(draft) if K > 0 else None,
+                         _ptr(draft_len),
                          B, K, V, float(temperature), int(seed) & (2**64 - 1), int(step) & (2**64 - 1),
                          _ptr(res["accept_len"]), _ptr(res["out_token"]), _ptr(res.get("emit")),
                          _ptr(res.get("emit_len")), _ptr(res.get("status")),

@@ -685,14 +685,29 @@ __device__ void draft_one(const SeqView& v, const Scal& sc, int32_t K, int32_t* 
 }
 
 template <bool kExtend, bool kDraft>
-__global__ void __launch_bounds__(64) sam_step_kernel(BatchView bv, const int32_t* __restrict__ tokens,
+__global__ void __launch_bounds__(64) sam_step_kernel(BatchView bv, const int32_t* __restrict__ rows,
+                                                      int32_t n_rows,
+                                                      const int32_t* __restrict__ tokens,
                                                       const int32_t* __restrict__ n_new,
                                                       int32_t max_new, int32_t K, int32_t* draft,
                                                       int32_t* draft_len, int32_t* match_len,
                                                       int32_t* min_endpos) {
-  const int b = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  // call index i (tokens, n_new and the draft outputs), automaton row b
+  const int i = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
-  if (b >= bv.B) return;
+  if (i >= n_rows) return;
+  const int b = rows ? rows[i] : i;
+  if (b < 0 || b >= bv.B) {  // no such automaton: an empty draft
+    if (kDraft) {
+      for (int t = lane; t < K; t += 32) draft[(size_t)i * K + t] = -1;
+      if (lane == 0) {
+        if (draft_len) draft_len[i] = 0;
+        if (match_len) match_len[i] = 0;
+        if (min_endpos) min_endpos[i] = -1;
+      }
+    }
+    return;
+  }
   const SeqView v = seq_view(bv, b);
   __shared__ int32_t chain_sh[2][kChainMax + 2];
   int32_t* sh = chain_sh[(threadIdx.x >> 5) & 1];
@@ -712,11 +727,11 @@ __global__ void __launch_bounds__(64) sam_step_kernel(BatchView bv, const int32_
     if (m < 0 || m > kChainMax) m = 0;
 #pragma unroll
     for (int r = 0; r < kChR; ++r) chr[r] = 32 * r + lane < m ? v.chn[32 * r + lane] : -1;
-    const int32_t nn = n_new[b];
+    const int32_t nn = n_new[i];
     if (nn < 0 || nn > max_new) {
       sc.status = SAMSPEC_ST_BADDRAFT;
     } else {
-      const int32_t* row = tokens + (size_t)b * max_new;
+      const int32_t* row = tokens + (size_t)i * max_new;
       for (int32_t base = 0; base < nn && sc.status == SAMSPEC_ST_OK; base += 32) {
         const int32_t cnt = min(32, nn - base);
         const int32_t mine = lane < cnt ? row[base + lane] : 0;
@@ -738,8 +753,8 @@ __global__ void __launch_bounds__(64) sam_step_kernel(BatchView bv, const int32_
     }
   }
   if (kDraft) {
-    draft_one(v, sc, K, draft + (size_t)b * K, draft_len ? draft_len + b : nullptr,
-              match_len ? match_len + b : nullptr, min_endpos ? min_endpos + b : nullptr, lane);
+    draft_one(v, sc, K, draft + (size_t)i * K, draft_len ? draft_len + i : nullptr,
+              match_len ? match_len + i : nullptr, min_endpos ? min_endpos + i : nullptr, lane);
   }
   if (kExtend && lane == 0) {
     v.sc[SC_N] = sc.n;
@@ -859,13 +874,14 @@ int launch_reset(sam_batch* s, const int32_t* mask, cudaStream_t stream) {
 }
 
 template <bool kExtend, bool kDraft>
-int launch_step(sam_batch* s, const int32_t* tokens, const int32_t* n_new, int32_t max_new,
-                int32_t K, int32_t* draft, int32_t* dl, int32_t* ml, int32_t* me,
-                cudaStream_t stream) {
+int launch_step(sam_batch* s, const int32_t* rows, int32_t n, const int32_t* tokens,
+                const int32_t* n_new, int32_t max_new, int32_t K, int32_t* draft, int32_t* dl,
+                int32_t* ml, int32_t* me, cudaStream_t stream) {
   constexpr int kWarpsPerBlock = 2;
-  const unsigned blocks = (unsigned)((s->B + kWarpsPerBlock - 1) / kWarpsPerBlock);
+  if (n < 1) return SAMSPEC_OK;
+  const unsigned blocks = (unsigned)((n + kWarpsPerBlock - 1) / kWarpsPerBlock);
   sam_step_kernel<kExtend, kDraft><<<blocks, 32 * kWarpsPerBlock, 0, stream>>>(
-      view_of(s), tokens, n_new, max_new, K, draft, dl, ml, me);
+      view_of(s), rows, n, tokens, n_new, max_new, K, draft, dl, ml, me);
   return cudaGetLastError() == cudaSuccess ? SAMSPEC_OK : SAMSPEC_ECUDA;
 }
 
@@ -932,16 +948,17 @@ int sam_reset(sam_batch* batch, const int32_t* d_seq_mask, samspec_stream_t stre
 int sam_extend(sam_batch* batch, const int32_t* d_tokens, const int32_t* d_n_new,
                int32_t max_new, samspec_stream_t stream) {
   if (!batch || !d_n_new || max_new < 0 || (max_new > 0 && !d_tokens)) return SAMSPEC_EINVAL;
-  return launch_step<true, false>(batch, d_tokens, d_n_new, max_new, 0, nullptr, nullptr,
-                                  nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
+  return launch_step<true, false>(batch, nullptr, batch->B, d_tokens, d_n_new, max_new, 0,
+                                  nullptr, nullptr, nullptr, nullptr,
+                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
 int sam_draft(sam_batch* batch, int32_t K, int32_t* d_draft, int32_t* d_draft_len,
               int32_t* d_match_len, int32_t* d_min_endpos, samspec_stream_t stream) {
   if (!batch || !d_draft) return SAMSPEC_EINVAL;
   if (K < 1 || K > 64) return SAMSPEC_ESIZE;
-  return launch_step<false, true>(batch, nullptr, nullptr, 0, K, d_draft, d_draft_len,
-                                  d_match_len, d_min_endpos,
+  return launch_step<false, true>(batch, nullptr, batch->B, nullptr, nullptr, 0, K, d_draft,
+                                  d_draft_len, d_match_len, d_min_endpos,
                                   reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -951,9 +968,31 @@ int sam_step(sam_batch* batch, const int32_t* d_tokens, const int32_t* d_n_new, 
   if (!batch || !d_n_new || !d_draft || max_new < 0 || (max_new > 0 && !d_tokens))
     return SAMSPEC_EINVAL;
   if (K < 1 || K > 64) return SAMSPEC_ESIZE;
-  return launch_step<true, true>(batch, d_tokens, d_n_new, max_new, K, d_draft, d_draft_len,
-                                 d_match_len, d_min_endpos,
+  return launch_step<true, true>(batch, nullptr, batch->B, d_tokens, d_n_new, max_new, K,
+                                 d_draft, d_draft_len, d_match_len, d_min_endpos,
                                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sam_step_rows(sam_batch* batch, const int32_t* d_rows, int32_t n, const int32_t* d_tokens,
+                  const int32_t* d_n_new, int32_t max_new, int32_t K, int32_t* d_draft,
+                  int32_t* d_draft_len, int32_t* d_match_len, int32_t* d_min_endpos,
+                  samspec_stream_t stream) {
+  if (!batch || n < 0 || (n > 0 && !d_n_new) || max_new < 0 || (max_new > 0 && !d_tokens))
+    return SAMSPEC_EINVAL;
+  if (!d_rows && n > batch->B) return SAMSPEC_ESIZE;
+  if (K < 0 || K > 64) return SAMSPEC_ESIZE;
+  if (K > 0 && !d_draft) return SAMSPEC_EINVAL;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    // no draft: draft_len reads 0 for every sequence of the call
+    if (d_draft_len && n > 0 &&
+        cudaMemsetAsync(d_draft_len, 0, (size_t)n * sizeof(int32_t), st) != cudaSuccess)
+      return SAMSPEC_ECUDA;
+    return launch_step<true, false>(batch, d_rows, n, d_tokens, d_n_new, max_new, 0, nullptr,
+                                    nullptr, nullptr, nullptr, st);
+  }
+  return launch_step<true, true>(batch, d_rows, n, d_tokens, d_n_new, max_new, K, d_draft,
+                                 d_draft_len, d_match_len, d_min_endpos, st);
 }
 
 int sam_get_status(sam_batch* batch, int32_t* h_status, samspec_stream_t stream) {

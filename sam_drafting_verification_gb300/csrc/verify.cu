@@ -1482,7 +1482,7 @@ int noalloc_scratch_address(void** out) {
 extern "C" {
 
 size_t spec_verify_workspace_bytes(int32_t B, int32_t K, int32_t V) {
-  if (B < 1 || K < 1 || V < 1) return 0;
+  if (B < 1 || K < 0 || V < 1) return 0;
   return 256;
 }
 
@@ -1500,8 +1500,9 @@ int spec_verify(const void* d_target, int32_t target_dtype, const void* d_draft_
                 int32_t* d_accept_len, int32_t* d_out_token, int32_t* d_emit, int32_t* d_emit_len,
                 int32_t* d_status, const spec_verify_debug* dbg, void* d_workspace,
                 size_t ws_bytes, samspec_stream_t stream) {
-  if (!d_target || !d_draft || !d_accept_len || !d_out_token || !d_workspace) return SAMSPEC_EINVAL;
-  if (B < 1 || B > (1 << 24) || K < 1 || K > 32 || V < 1 || V > (1 << 24)) return SAMSPEC_ESIZE;
+  if (!d_target || (K > 0 && !d_draft) || !d_accept_len || !d_out_token || !d_workspace)
+    return SAMSPEC_EINVAL;
+  if (B < 1 || B > (1 << 24) || K < 0 || K > 32 || V < 1 || V > (1 << 24)) return SAMSPEC_ESIZE;
   if (!(temperature >= 0.f) || temperature != temperature || temperature == __builtin_inff())
     return SAMSPEC_EINVAL;
   if (target_dtype != SAMSPEC_F32 && target_dtype != SAMSPEC_BF16) return SAMSPEC_EDTYPE;

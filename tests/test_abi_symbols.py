@@ -51,7 +51,7 @@ def test_spec_verify_rejects_bad_arguments_on_the_host():
                                None, None, None, None, p, ws_bytes, None)
 
     assert call(target=None) == bd.EINVAL
-    assert call(K=0) == bd.ESIZE and call(K=33) == bd.ESIZE
+    assert call(K=-1) == bd.ESIZE and call(K=33) == bd.ESIZE
     assert call(T=-1.0) == bd.EINVAL and call(T=float("nan")) == bd.EINVAL
     assert call(dtype=7) == bd.EDTYPE
     assert call(ws_bytes=16) == bd.ESIZE
