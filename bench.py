@@ -18,7 +18,7 @@ stream; max over ranks.  Under torchrun every rank runs its own batch (weak
 scaling, no collective on the data path).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                  [--workload rs_bf16_b64|sweep_b1024|long_rollout_b256]
+                  [--workload rs_bf16_b64|sweep_b1024|long_rollout_b256|rollout_toy_b64]
 """
 from __future__ import annotations
 
@@ -206,6 +206,8 @@ def run_gpu(args):
         return run_sweep(args, ws, rank, dev)
     if args.workload == "long_rollout_b256":
         return run_rollout(args, ws, rank, dev)
+    if args.workload == "rollout_toy_b64":
+        return run_rollout_toy(args, ws, rank, dev)
 
     B, V, K, T, n = 64, workloads.V_LARGE, 3, 1.0, 4096
     hist, cont = rs_inputs(rank, B, V, n, K)
@@ -615,6 +617,90 @@ def oracle_sam_rollout(streams, lens, toks, n_new, K, nseq):
 
 
 # --------------------------------------------------------------------------
+# toy-model rollout: the decode loop end to end, with and without speculation
+# --------------------------------------------------------------------------
+
+class ToyTarget:
+    """Stand-in for the target model: logits at (sequence b, new-token index p)
+    are a row of a seeded N(0, sd 2) pool plus `boost` on the stream's true
+    token, so greedy decoding reproduces the stream (Zipf tokens with copied
+    spans) and SAM drafts are accepted where the stream repeats itself."""
+
+    def __init__(self, truth, V, boost, dev, dtype, P=127, seed=4004):
+        import torch
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        self.noise = torch.empty((P, V), device=dev).normal_(0.0, 2.0, generator=g)
+        self.truth = torch.as_tensor(truth, dtype=torch.int64, device=dev)
+        self.boost, self.P, self.V, self.dtype = boost, P, V, dtype
+
+    def __call__(self, rows, n_done, draft, draft_len):
+        import torch
+        n, K = draft.shape
+        r = rows.long().repeat_interleave(K + 1)
+        p = (n_done.view(-1, 1) + torch.arange(K + 1, device=rows.device).view(1, -1)).reshape(-1)
+        x = self.noise[(r * 7919 + p) % self.P]
+        t = self.truth[r, p.clamp(max=self.truth.shape[1] - 1)]
+        x[torch.arange(x.shape[0], device=x.device), t] += self.boost
+        return x.to(self.dtype).view(n, K + 1, self.V).contiguous()
+
+
+def run_rollout_toy(args, ws, rank, dev):
+    """B=64 sequences with 4096-token Zipf(1.1) prompts (copy prob 0.3, spans
+    8-64) generating log-uniform [64, 1024] new tokens each (a long tail),
+    V=151936, bf16 logits from ToyTarget, greedy.  Three loops over the same
+    inputs: plain decoding (K=0), speculation at every step (K=3), and the
+    adaptive switch (K=3 only while at most 8 sequences are active).  Each
+    loop's tokens must equal the streams (lossless)."""
+    import torch
+
+    import sam_drafting_verification_gb300 as ss
+    from sam_drafting_verification_gb300.rollout import Rollout
+    B, V, K, n0, thr = 64, workloads.V_LARGE, 3, 4096, 8
+    rng = np.random.default_rng(1005 + 7919 * rank)
+    limits = workloads.log_uniform_lengths(rng, B, 64, 1024).astype(np.int64)
+    z = workloads.ZipfTokens(V, 1.1)
+    streams = [workloads.make_stream(rng, n0 + int(limits.max()) + 8, V, 0.3, 8, 64, z) for _ in range(B)]
+    prompts = np.stack([s[:n0] for s in streams]).astype(np.int32)
+    truth = np.stack([s[n0:] for s in streams]).astype(np.int64)
+    model = ToyTarget(truth, V, 40.0, dev, torch.bfloat16)
+    modes = {}
+    for name, k, t in (("plain", 0, None), ("speculate", K, None), ("adaptive", K, thr)):
+        batch = ss.SamBatch(B, n0 + int(limits.max()) + 64, V, device=dev)
+        batch.extend(torch.as_tensor(prompts, device=dev), torch.full((B,), n0, dtype=torch.int32, device=dev))
+        Rollout(batch, model, K=k, threshold=t).run(np.minimum(limits, 16))  # warm-up
+        batch.reset()
+        batch.extend(torch.as_tensor(prompts, device=dev), torch.full((B,), n0, dtype=torch.int32, device=dev))
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        res = Rollout(batch, model, K=k, threshold=t).run(limits)
+        torch.cuda.synchronize()
+        el = time.perf_counter() - t0
+        ok = all(res.tokens[b] == truth[b, :limits[b]].tolist() for b in range(B))
+        assert ok, f"{name}: rollout differs from plain decoding"
+        ntok = int(limits.sum())
+        modes[name] = {"steps": res.steps, "tokens": ntok, "seconds": round(el, 4),
+                       "tokens_per_s": round(ntok / el, 1),
+                       "tokens_per_step": round(ntok / res.steps, 3),
+                       "accepted_drafts": res.accepted,
+                       "speculative_steps": sum(1 for x in res.k_per_step if x > 0)}
+    line = {"metric": "generated tokens/s, toy-model rollout (decode loop through sam_spec_step)",
+            "value": modes["speculate"]["tokens_per_s"], "unit": "tokens/s", "n_gpus": ws,
+            "steps": modes["speculate"]["steps"], "warmup": 1, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32 (bf16 logits)",
+            "data": "synthetic",
+            "config": {"workload": "rollout_toy_b64", "B": B, "V": V, "K": K, "threshold": thr,
+                       "prompt": n0, "new_tokens": "log-uniform [64, 1024] per sequence",
+                       "target": "ToyTarget (seeded noise + 40 on the stream token), greedy",
+                       "timing": "wall clock of the whole loop, host bookkeeping and the toy "
+                                 "model's logits included"},
+            "modes": modes,
+            "lossless": True}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
 # verification sweep at B=1024
 # --------------------------------------------------------------------------
 
@@ -711,7 +797,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="rs_bf16_b64", choices=["rs_bf16_b64", "sweep_b1024", "long_rollout_b256"])
+    ap.add_argument("--workload", default="rs_bf16_b64", choices=["rs_bf16_b64", "sweep_b1024", "long_rollout_b256",
+                                                      "rollout_toy_b64"])
     ap.add_argument("--point", default="", help="sweep_b1024 only: one point 'K,f32|bf16,greedy|T=1|greedy-full-read'")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":
