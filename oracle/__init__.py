@@ -62,6 +62,9 @@ def _load():
         lib.osam_sizes.argtypes = [P, P]
         lib.osam_dump.argtypes = [P, P, P, P, P]
         lib.osam_step_batch.argtypes = [P, I32, P, P, I32, I32, P, P]
+        lib.osam_match.argtypes = [P, P, P, I64, I32, P, P]
+        lib.oselect_static.restype = I32
+        lib.oselect_static.argtypes = [I32, I32, I32]
         lib.ophilox4x32_10.argtypes = [P, P, P]
         lib.ouniforms.argtypes = [U64, U64, I64, I32, P]
         lib.over_verify.restype = I32
@@ -102,6 +105,17 @@ class Sam:
         info = np.empty(3, np.int32)
         self._lib.osam_draft(self._h, int(K), _ptr(out), _ptr(info))
         return out[:K].copy(), int(info[0]), int(info[1]), int(info[2])
+
+    def match(self, state, tokens, K: int):
+        """Static use: moves the matching state (v, l) of a generated text by
+        `tokens` and drafts K corpus tokens from the final state.  Returns
+        ((v, l), draft [K] (-1 padded), draft_len, min_endpos)."""
+        st = np.asarray(state, np.int32).copy()
+        tok = np.ascontiguousarray(tokens, dtype=np.int32)
+        out = np.empty(max(K, 1), np.int32)
+        info = np.empty(3, np.int32)
+        self._lib.osam_match(self._h, _ptr(st), _ptr(tok), tok.size, int(K), _ptr(out), _ptr(info))
+        return (int(st[0]), int(st[1])), out[:K].copy(), int(info[0]), int(info[2])
 
     def sizes(self):
         s = np.empty(5, np.int64)
@@ -193,3 +207,9 @@ def cdf_interval(target_row, temperature, rejected_token, token, draft_row=None)
     lib.over_cdf_interval(_ptr(t), _ptr(g), t.size, float(temperature), int(rejected_token),
                           int(token), _ptr(res))
     return float(res[0]), float(res[1]), float(res[2])
+
+
+def select_static(l_static: int, l_dynamic: int, l_bias: int) -> bool:
+    """Adaptive choice between a static and a dynamic automaton's drafts: the
+    static draft only when its match is longer by more than l_bias."""
+    return bool(_load().oselect_static(int(l_static), int(l_dynamic), int(l_bias)))

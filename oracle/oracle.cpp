@@ -133,6 +133,47 @@ struct Sam {
     for (int32_t t = dl; t < K; ++t) out[t] = -1;
     *draft_len = dl;
   }
+
+  // Static use ([P4] "Drafting with Suffix Automaton", "Update of Suffix
+  // Automaton"; [P1] §1.1 静态 SAM): this automaton holds a corpus and stays
+  // fixed; a generated text is followed by a matching state (v, l): v the
+  // state of the longest suffix of the generated text that occurs in the
+  // corpus, l its length.  A new token c moves it along c if v has that
+  // transition; otherwise shorter suffixes are tried by following links
+  // (their longest string, len(link)), and with none left the match is
+  // empty (root, 0).
+  void match(int32_t* v_io, int32_t* l_io, int32_t c) const {
+    int32_t v = *v_io, l = *l_io;
+    while (v != 0 && next[v].find(c) == next[v].end()) {
+      v = link[v];
+      l = len[v];
+    }
+    auto it = next[v].find(c);
+    if (it != next[v].end()) {
+      v = it->second;
+      l = l + 1;
+    } else {
+      v = 0;
+      l = 0;
+    }
+    *v_io = v;
+    *l_io = l;
+  }
+
+  // Draft from a matching state: the K corpus tokens after the first
+  // occurrence (min_endpos) of the matched suffix, cut at the corpus end.
+  void match_draft(int32_t v, int32_t l, int32_t K, int32_t* out, int32_t* draft_len) const {
+    const int32_t n = (int32_t)text.size();
+    int32_t dl = 0;
+    if (v != 0 && l > 0) {
+      const int32_t e = min_endpos[v];
+      dl = n - 1 - e;
+      if (dl > K) dl = K;
+      for (int32_t t = 0; t < dl; ++t) out[t] = text[e + 1 + t];
+    }
+    for (int32_t t = dl; t < K; ++t) out[t] = -1;
+    *draft_len = dl;
+  }
 };
 
 // ---------------------------------------------------------------------------
@@ -306,6 +347,26 @@ void osam_dump(void* s, int32_t* len, int32_t* link, int32_t* min_end, int32_t* 
       edges[3 * e + 2] = kv.second;
       ++e;
     }
+}
+
+// Static matching of one generated text: state[2] = {v, l} is moved by the n
+// tokens and the draft of the final state is written (info = {draft_len, l,
+// min_endpos of v or -1}).
+void osam_match(void* s, int32_t* state, const int32_t* tok, int64_t n, int32_t K, int32_t* draft,
+                int32_t* info) {
+  const Sam* sam = static_cast<Sam*>(s);
+  for (int64_t i = 0; i < n; ++i) sam->match(&state[0], &state[1], tok[i]);
+  sam->match_draft(state[0], state[1], K, draft, &info[0]);
+  info[1] = state[1];
+  info[2] = state[0] != 0 ? sam->min_endpos[state[0]] : -1;
+}
+
+// Adaptive draft selection between a dynamic and a static automaton ([P4]
+// "Drafting with Suffix Automaton"): the dynamic draft is preferred; the
+// static one is taken only when its match is longer by more than l_bias.
+// Returns 1 if the static draft is chosen.
+int32_t oselect_static(int32_t l_static, int32_t l_dynamic, int32_t l_bias) {
+  return l_static > l_dynamic + l_bias ? 1 : 0;
 }
 
 // Batch helper used for timing: B independent automata, each extended by
