@@ -155,6 +155,36 @@ int sam_step_rows(sam_batch* batch, const int32_t* d_rows, int32_t n, const int3
                   int32_t* d_draft_len, int32_t* d_match_len, int32_t* d_min_endpos,
                   samspec_stream_t stream);
 
+/* Static use of an automaton ([P4] "Drafting with Suffix Automaton",
+ * "Update of Suffix Automaton"; [P1] §1.1 静态 SAM): automaton `corpus_row` of
+ * `corpus` holds a corpus (documents joined by an end-of-sequence token,
+ * built with sam_extend) and is only read.  Call index i follows a generated
+ * text with the matching state d_state[2i], d_state[2i+1] = {state, length}
+ * of its longest suffix that occurs in the corpus ({0, 0} to start); the
+ * n_new[i] tokens d_tokens[i, :] move it along (a transition from the state,
+ * else from the first state on its suffix chain that has one, else to
+ * {0, 0}).  Then K corpus tokens after the state's min_endpos are drafted
+ * into d_draft [n, K] (-1 padded; d_draft_len [n]); d_match_len [n] and
+ * d_min_endpos [n] receive the length and that position (-1 at the root).
+ * A token outside [0, vocab) resets the state to {0, 0}.  The corpus is not
+ * modified, so any number of calls may read it at once.  One launch. */
+int ssam_match(const sam_batch* corpus, int32_t corpus_row, int32_t n, int32_t* d_state,
+               const int32_t* d_tokens, const int32_t* d_n_new, int32_t max_new, int32_t K,
+               int32_t* d_draft, int32_t* d_draft_len, int32_t* d_match_len,
+               int32_t* d_min_endpos, samspec_stream_t stream);
+
+/* Adaptive choice between a dynamic and a static automaton's drafts ([P4]
+ * "Drafting with Suffix Automaton": the dynamic draft is preferred): per
+ * sequence, the static draft (d_st_*) is taken when its match length exceeds
+ * the dynamic one (d_dyn_*) by more than l_bias, else the dynamic draft.
+ * Writes d_draft [n, K], d_draft_len [n] and, optionally, d_source [n]
+ * (1 = static).  One launch. */
+int sam_select_drafts(int32_t n, int32_t K, const int32_t* d_dyn_draft, const int32_t* d_dyn_len,
+                      const int32_t* d_dyn_match, const int32_t* d_st_draft,
+                      const int32_t* d_st_len, const int32_t* d_st_match, int32_t l_bias,
+                      int32_t* d_draft, int32_t* d_draft_len, int32_t* d_source,
+                      samspec_stream_t stream);
+
 /* Copies the B status words to h_status[B] (host memory) and synchronises
  * `stream`. */
 int sam_get_status(sam_batch* batch, int32_t* h_status, samspec_stream_t stream);

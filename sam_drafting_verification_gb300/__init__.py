@@ -9,6 +9,8 @@ the C entry points, over torch CUDA tensors:
     .step(tokens, n_new, K)             -- sam_step (extend + draft, one launch)
     .step_rows(rows, tokens, n_new, K)  -- sam_step_rows (a subset of the sequences)
     .spec_step(target, draft, ...)      -- sam_spec_step (verify, extend, draft)
+    .match(row, state, tokens, n_new, K) -- ssam_match (a corpus automaton, static use)
+  select_drafts(dynamic, static, l_bias) -- sam_select_drafts
     .status(), .reset(mask), .dump(b), .export(), .import_(blob)
   spec_verify(target, draft, ...)       -- spec_verify
   spec_uniforms(B, K, seed, step)       -- spec_uniforms
@@ -26,7 +28,8 @@ from . import _binding as _b
 from ._binding import (BF16, F32, ST_BADDRAFT, ST_BADROW, ST_CAPACITY, ST_HASHFULL,  # noqa: F401
                        ST_LOOPCAP, ST_OK, ST_TIMEOUT, ST_TOKEN, SamspecError)
 
-__all__ = ["SamBatch", "spec_verify", "spec_uniforms", "SamspecError", "library_path"]
+__all__ = ["SamBatch", "spec_verify", "spec_uniforms", "select_drafts", "SamspecError",
+           "library_path"]
 
 
 def library_path() -> str:
@@ -181,6 +184,29 @@ class SamBatch:
             _stream(self.device)), "sam_spec_step")
         return res
 
+    def match(self, row: int, state, tokens, n_new, K: int, out=None):
+        """Static use of automaton `row` (a corpus): moves the matching states
+        `state` (int32 [n, 2], in place) by tokens [n, max_new] / n_new [n] and
+        drafts K corpus tokens.  Returns (draft, draft_len, match_len,
+        min_endpos)."""
+        _req(state, torch.int32, "state")
+        if state.dim() != 2 or state.shape[1] != 2:
+            raise ValueError("state must be [n, 2]")
+        n = int(state.shape[0])
+        _req(tokens, torch.int32, "tokens")
+        if tokens.dim() != 2 or tokens.shape[0] != n:
+            raise ValueError("tokens must be [n, max_new]")
+        _req(n_new, torch.int32, "n_new", (n,))
+        if out is None:
+            z = lambda *s: torch.empty(s, dtype=torch.int32, device=self.device)  # noqa: E731
+            out = (z(n, K), z(n), z(n), z(n))
+        d, dl, ml, me = out
+        _b.check(self.lib.ssam_match(self._h, int(row), n, _ptr(state), _ptr(tokens), _ptr(n_new),
+                                     int(tokens.shape[1]), int(K), _ptr(d) if K > 0 else None,
+                                     _ptr(dl), _ptr(ml), _ptr(me), _stream(self.device)),
+                 "ssam_match")
+        return d, dl, ml, me
+
     def status(self):
         import numpy as np
         out = np.empty(self.B, np.int32)
@@ -294,6 +320,28 @@ def spec_verify(target, draft, draft_len=None, temperature: float = 0.0, seed: i
                          _ptr(ws), ws.numel(), _stream(dev))
     _b.check(rc, "spec_verify")
     return res
+
+
+def select_drafts(dynamic, static, l_bias: int):
+    """Per sequence, the static automaton's draft when its match is longer than
+    the dynamic one's by more than l_bias, else the dynamic draft.  dynamic /
+    static: (draft [n, K], draft_len [n], match_len [n]).  Returns (draft,
+    draft_len, source) with source 1 where the static draft was taken."""
+    dd, dl, dm = dynamic
+    sd, sl, sm = static
+    n, K = (int(x) for x in dd.shape)
+    for t, nm in ((dd, "dynamic draft"), (sd, "static draft")):
+        _req(t, torch.int32, nm, (n, K))
+    for t, nm in ((dl, "dynamic draft_len"), (dm, "dynamic match_len"), (sl, "static draft_len"),
+                  (sm, "static match_len")):
+        _req(t, torch.int32, nm, (n,))
+    od = torch.empty_like(dd)
+    ol = torch.empty_like(dl)
+    src = torch.empty_like(dl)
+    _b.check(_b.lib().sam_select_drafts(n, K, _ptr(dd), _ptr(dl), _ptr(dm), _ptr(sd), _ptr(sl),
+                                        _ptr(sm), int(l_bias), _ptr(od), _ptr(ol), _ptr(src),
+                                        _stream(dd.device)), "sam_select_drafts")
+    return od, ol, src
 
 
 def spec_uniforms(B: int, K: int, seed: int, step: int, device=None):

@@ -774,6 +774,121 @@ __global__ void __launch_bounds__(64) sam_step_kernel(BatchView bv, const int32_
   }
 }
 
+// Static use of an automaton (the volcengine.com SAM-Decoding article,
+// "Drafting with Suffix Automaton" / "Update of Suffix Automaton"): automaton
+// row `cb` holds a corpus and is only read; call index i follows a generated
+// text with the matching state state[2i..2i+1] = {v, l} (the state of the
+// longest suffix that occurs in the corpus, its length).  Each new token c
+// moves it along c from v, or from the first state on v's suffix chain that
+// has c (l becoming that state's len + 1), or to (root, 0).  The chain is
+// walked in batches of 2, 4, ... 32 states, one per lane, probed together.
+// The draft copies the K corpus tokens after min_endpos(v).
+__global__ void __launch_bounds__(64) ssam_match_kernel(BatchView bv, int32_t cb, int32_t n,
+                                                        int32_t* __restrict__ state,
+                                                        const int32_t* __restrict__ tokens,
+                                                        const int32_t* __restrict__ n_new,
+                                                        int32_t max_new, int32_t K, int32_t* draft,
+                                                        int32_t* draft_len, int32_t* match_len,
+                                                        int32_t* min_endpos) {
+  const int i = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (i >= n) return;
+  const SeqView v = seq_view(bv, cb);
+  const int32_t ns = v.sc[SC_NS];
+  const int32_t ntext = v.sc[SC_N];
+  int32_t s = state[2 * i], l = state[2 * i + 1];
+  if (s < 0 || s >= ns || l < 0) {  // not a state of this automaton: start over
+    s = 0;
+    l = 0;
+  }
+  const int32_t nn = n_new ? n_new[i] : 0;
+  for (int32_t t = 0; t < nn && t < max_new; ++t) {
+    const int32_t c = tokens[(size_t)i * max_new + t];
+    if (c < 0 || c >= v.V) {  // a token the corpus cannot hold
+      s = 0;
+      l = 0;
+      continue;
+    }
+    int32_t x = s;
+    int W = 2;
+    bool done = false, first = true;
+    int guard = v.S + 1;
+    while (!done) {
+      // chain states x_j of this batch to lanes j = 0 .. m-1
+      int32_t mine = lane == 0 ? x : -1;
+      int m = 1;
+      while (m < W) {
+        const int32_t y = v.lk[x];
+        if (y == -1) break;
+        x = y;
+        if (lane == m) mine = x;
+        ++m;
+      }
+      guard -= m;
+      const bool has = lane < m;
+      const int32_t len_m = has ? v.st[mine].x : 0;
+      const int32_t nx = v.lk[x];
+      uint32_t pos = 0;
+      int32_t val = -1;
+      const int r = has ? lane_probe(v, mine, c, &pos, &val) : 0;
+      const unsigned fnd = __ballot_sync(kFullMask, has && r == 1);
+      if (fnd) {
+        const int kf = __ffs(fnd) - 1;
+        const int32_t to = __shfl_sync(kFullMask, val, kf);
+        const int32_t lk = __shfl_sync(kFullMask, len_m, kf);
+        // found at the current state: the match grows by one; found further
+        // down the chain: the match is that state's longest string plus c
+        l = (first && kf == 0) ? l + 1 : lk + 1;
+        s = to;
+        done = true;
+      } else if (nx == -1 || guard < 0) {
+        s = 0;
+        l = 0;
+        done = true;
+      } else {
+        x = nx;
+        W = W < 32 ? 2 * W : 32;
+        first = false;
+      }
+    }
+  }
+  if (lane == 0) {
+    state[2 * i] = s;
+    state[2 * i + 1] = l;
+    if (match_len) match_len[i] = l;
+    if (min_endpos) min_endpos[i] = s != 0 ? v.st[s].y : -1;
+  }
+  int32_t dl = 0, e = -1;
+  if (s != 0 && l > 0) {
+    e = v.st[s].y;
+    dl = min(K, ntext - 1 - e);
+    if (dl < 0) dl = 0;
+  }
+  for (int t = lane; t < K; t += 32) draft[(size_t)i * K + t] = t < dl ? v.hist[e + 1 + t] : -1;
+  if (lane == 0 && draft_len) draft_len[i] = dl;
+}
+
+// Adaptive draft selection ([P4] "Drafting with Suffix Automaton"): the
+// dynamic automaton's draft unless the static match is longer by more than
+// l_bias.  One thread per (sequence, draft slot).
+__global__ void select_drafts_kernel(int32_t n, int32_t K, const int32_t* __restrict__ dd,
+                                     const int32_t* __restrict__ dl, const int32_t* __restrict__ dm,
+                                     const int32_t* __restrict__ sd, const int32_t* __restrict__ sl,
+                                     const int32_t* __restrict__ sm, int32_t l_bias,
+                                     int32_t* __restrict__ od, int32_t* __restrict__ ol,
+                                     int32_t* __restrict__ src) {
+  const int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (g >= (int64_t)n * (K + 1)) return;
+  const int i = (int)(g / (K + 1)), t = (int)(g % (K + 1));
+  const bool st = sm[i] > dm[i] + l_bias;
+  if (t < K) {
+    od[(size_t)i * K + t] = st ? sd[(size_t)i * K + t] : dd[(size_t)i * K + t];
+  } else {
+    ol[i] = st ? sl[i] : dl[i];
+    if (src) src[i] = st ? 1 : 0;
+  }
+}
+
 // Clears the hash tables of the selected sequences and empties their automata.
 __global__ void sam_reset_kernel(BatchView bv, const int32_t* __restrict__ mask) {
   for (int b = blockIdx.y; b < bv.B; b += gridDim.y) {
@@ -993,6 +1108,41 @@ int sam_step_rows(sam_batch* batch, const int32_t* d_rows, int32_t n, const int3
   }
   return launch_step<true, true>(batch, d_rows, n, d_tokens, d_n_new, max_new, K, d_draft,
                                  d_draft_len, d_match_len, d_min_endpos, st);
+}
+
+int ssam_match(const sam_batch* corpus, int32_t corpus_row, int32_t n, int32_t* d_state,
+               const int32_t* d_tokens, const int32_t* d_n_new, int32_t max_new, int32_t K,
+               int32_t* d_draft, int32_t* d_draft_len, int32_t* d_match_len,
+               int32_t* d_min_endpos, samspec_stream_t stream) {
+  if (!corpus || !d_state || n < 0 || max_new < 0 || (max_new > 0 && (!d_tokens || !d_n_new)) ||
+      (K > 0 && !d_draft))
+    return SAMSPEC_EINVAL;
+  if (corpus_row < 0 || corpus_row >= corpus->B || K < 0 || K > 64) return SAMSPEC_ESIZE;
+  if (n == 0) return SAMSPEC_OK;
+  constexpr int kWarpsPerBlock = 2;
+  const unsigned blocks = (unsigned)((n + kWarpsPerBlock - 1) / kWarpsPerBlock);
+  ssam_match_kernel<<<blocks, 32 * kWarpsPerBlock, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      view_of(corpus), corpus_row, n, d_state, d_tokens, max_new > 0 ? d_n_new : nullptr, max_new,
+      K, d_draft, d_draft_len, d_match_len, d_min_endpos);
+  return cudaGetLastError() == cudaSuccess ? SAMSPEC_OK : SAMSPEC_ECUDA;
+}
+
+int sam_select_drafts(int32_t n, int32_t K, const int32_t* d_dyn_draft, const int32_t* d_dyn_len,
+                      const int32_t* d_dyn_match, const int32_t* d_st_draft,
+                      const int32_t* d_st_len, const int32_t* d_st_match, int32_t l_bias,
+                      int32_t* d_draft, int32_t* d_draft_len, int32_t* d_source,
+                      samspec_stream_t stream) {
+  if (n < 0 || K < 0 || K > 64) return SAMSPEC_ESIZE;
+  if (n == 0) return SAMSPEC_OK;
+  if (!d_dyn_len || !d_dyn_match || !d_st_len || !d_st_match || !d_draft_len ||
+      (K > 0 && (!d_dyn_draft || !d_st_draft || !d_draft)))
+    return SAMSPEC_EINVAL;
+  const int64_t total = (int64_t)n * (K + 1);
+  select_drafts_kernel<<<(unsigned)((total + 255) / 256), 256, 0,
+                         reinterpret_cast<cudaStream_t>(stream)>>>(
+      n, K, d_dyn_draft, d_dyn_len, d_dyn_match, d_st_draft, d_st_len, d_st_match, l_bias, d_draft,
+      d_draft_len, d_source);
+  return cudaGetLastError() == cudaSuccess ? SAMSPEC_OK : SAMSPEC_ECUDA;
 }
 
 int sam_get_status(sam_batch* batch, int32_t* h_status, samspec_stream_t stream) {
