@@ -18,7 +18,7 @@ stream; max over ranks.  Under torchrun every rank runs its own batch (weak
 scaling, no collective on the data path).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                  [--workload rs_bf16_b64|sweep_b1024|long_rollout_b256|rollout_toy_b64]
+                  [--workload rs_bf16_b64|sweep_b1024|long_rollout_b256|rollout_toy_b64|static_match_b256]
 """
 from __future__ import annotations
 
@@ -208,6 +208,8 @@ def run_gpu(args):
         return run_rollout(args, ws, rank, dev)
     if args.workload == "rollout_toy_b64":
         return run_rollout_toy(args, ws, rank, dev)
+    if args.workload == "static_match_b256":
+        return run_static_match(args, ws, rank, dev)
 
     B, V, K, T, n = 64, workloads.V_LARGE, 3, 1.0, 4096
     hist, cont = rs_inputs(rank, B, V, n, K)
@@ -701,6 +703,113 @@ def run_rollout_toy(args, ws, rank, dev):
 
 
 # --------------------------------------------------------------------------
+# static corpus automaton: build and matching
+# --------------------------------------------------------------------------
+
+def run_static_match(args, ws, rank, dev):
+    """A corpus of ~1M tokens (documents of 200-4000 Zipf(1.1) tokens with
+    copied spans, V=151936, joined by an end-of-sequence token) built once on
+    the device; 256 generated texts (corpus passages of 16-256 tokens with
+    1-8 fresh tokens between them) followed 1-4 tokens per step for 512 steps
+    with K=3 corpus drafts, in one CUDA graph.  Reports the build rate and ns
+    per sequence-step of the matching, next to the oracle's matching of the
+    same texts on one host core."""
+    import torch
+
+    import oracle
+    import sam_drafting_verification_gb300 as ss
+    V, B, K, steps = workloads.V_LARGE, 256, 3, 512
+    eos = V - 1
+    rng = np.random.default_rng(1006 + 7919 * rank)
+    z = workloads.ZipfTokens(V, 1.1)
+    docs, total = [], 0
+    while total < 1_000_000:
+        d = workloads.make_stream(rng, int(rng.integers(200, 4000)), V, 0.3, 8, 64, z)
+        docs.append(np.concatenate([d, [eos]]))
+        total += len(docs[-1])
+    corpus = np.concatenate(docs).astype(np.int32)
+    n_new = rng.integers(1, 5, size=(steps, B)).astype(np.int32)
+    need = n_new.sum(axis=0)
+    gens = []
+    for b in range(B):
+        parts, n = [], 0
+        while n < need[b]:
+            a = int(rng.integers(0, len(corpus) - 300))
+            parts.append(corpus[a:a + int(rng.integers(16, 257))])
+            parts.append(z.draw(rng, int(rng.integers(1, 9))))
+            n += len(parts[-2]) + len(parts[-1])
+        gens.append(np.concatenate(parts)[:need[b]].astype(np.int32))
+    toks = np.zeros((steps, B, 4), np.int32)
+    for b in range(B):
+        pos = 0
+        for s in range(steps):
+            k = int(n_new[s, b])
+            toks[s, b, :k] = gens[b][pos:pos + k]
+            pos += k
+    cb = ss.SamBatch(1, len(corpus), V, device=dev)
+    cd = torch.as_tensor(corpus[None, :], device=dev)
+    cl = torch.tensor([len(corpus)], dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    cb.extend(cd, cl)
+    torch.cuda.synchronize()
+    build_s = time.perf_counter() - t0
+    assert cb.status()[0] == 0
+    state = torch.zeros((B, 2), dtype=torch.int32, device=dev)
+    td = torch.as_tensor(toks, device=dev)
+    nd = torch.as_tensor(n_new, device=dev)
+    outs = tuple(torch.empty(sz, dtype=torch.int32, device=dev) for sz in ((B, K), (B,), (B,), (B,)))
+    for s in range(3):  # warm-up
+        cb.match(0, state, td[s], nd[s], K, out=outs)
+    torch.cuda.synchronize()
+    cs = torch.cuda.Stream(device=dev)
+    g = torch.cuda.CUDAGraph()
+    cs.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(g, stream=cs):
+            for s in range(steps):
+                cb.match(0, state, td[s], nd[s], K, out=outs)
+    torch.cuda.synchronize()
+    state.zero_()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    ns_gpu = ms * 1e6 / (steps * B)
+    # the oracle on the same texts (corpus built untimed)
+    cpu = None
+    if rank == 0:
+        osam = oracle.Sam(V)
+        osam.extend(corpus)
+        ost = np.zeros((B, 2), np.int32)
+        t0 = time.perf_counter()
+        for s in range(steps):
+            oracle.match_batch(osam, ost, toks[s], n_new[s], K)
+        el = time.perf_counter() - t0
+        assert np.array_equal(ost, state.cpu().numpy()), "device and oracle matching states differ"
+        ns_cpu = el / (steps * B) * 1e9
+        cpu = {"value": round(ns_cpu, 1), "unit": "ns/seq-step (static matching + draft)", "cores": 1,
+               "kind": "oracle", "sample": f"the same {B} texts x {steps} steps, one C call per step "
+                                            f"for all {B} texts, {el:.2f} s"}
+    line = {"metric": "static-automaton matching ns/seq-step (K=3 corpus drafts)",
+            "value": round(ns_gpu, 2), "unit": "ns/seq-step", "n_gpus": ws, "steps": steps,
+            "warmup": 3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int32", "data": "synthetic",
+            "config": {"workload": "static_match_b256", "corpus_tokens": int(len(corpus)),
+                       "documents": len(docs), "B": B, "K": K, "V": V,
+                       "timing": "CUDA graph of the 512 matching launches"},
+            "cpu_baseline": cpu,
+            "breakdown": {"corpus_build_tokens_per_s": round(len(corpus) / build_s, 1),
+                          "corpus_build_s": round(build_s, 3),
+                          "speedup_vs_oracle": (round(cpu["value"] / ns_gpu, 1) if cpu else None)}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
 # verification sweep at B=1024
 # --------------------------------------------------------------------------
 
@@ -798,7 +907,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="rs_bf16_b64", choices=["rs_bf16_b64", "sweep_b1024", "long_rollout_b256",
-                                                      "rollout_toy_b64"])
+                                                      "rollout_toy_b64", "static_match_b256"])
     ap.add_argument("--point", default="", help="sweep_b1024 only: one point 'K,f32|bf16,greedy|T=1|greedy-full-read'")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":

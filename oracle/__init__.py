@@ -63,6 +63,7 @@ def _load():
         lib.osam_dump.argtypes = [P, P, P, P, P]
         lib.osam_step_batch.argtypes = [P, I32, P, P, I32, I32, P, P]
         lib.osam_match.argtypes = [P, P, P, I64, I32, P, P]
+        lib.osam_match_batch.argtypes = [P, I32, P, P, P, I32, I32, P, P]
         lib.oselect_static.restype = I32
         lib.oselect_static.argtypes = [I32, I32, I32]
         lib.ophilox4x32_10.argtypes = [P, P, P]
@@ -207,6 +208,21 @@ def cdf_interval(target_row, temperature, rejected_token, token, draft_row=None)
     lib.over_cdf_interval(_ptr(t), _ptr(g), t.size, float(temperature), int(rejected_token),
                           int(token), _ptr(res))
     return float(res[0]), float(res[1]), float(res[2])
+
+
+def match_batch(sam, state, tokens, n_new, K):
+    """sam.match for B texts in one C call (timing): state int32 [B, 2] is
+    updated in place; returns draft [B, K] and info [B, 3] (draft_len, match
+    length, min_endpos)."""
+    lib = _load()
+    tok = np.ascontiguousarray(tokens, dtype=np.int32)
+    nn = np.ascontiguousarray(n_new, dtype=np.int32)
+    B = len(nn)
+    draft = np.empty((B, max(K, 1)), np.int32)
+    info = np.empty((B, 3), np.int32)
+    lib.osam_match_batch(sam._h, B, _ptr(state), _ptr(tok), _ptr(nn), tok.shape[1], int(K),
+                         _ptr(draft), _ptr(info))
+    return draft[:, :K], info
 
 
 def select_static(l_static: int, l_dynamic: int, l_bias: int) -> bool:

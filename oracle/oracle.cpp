@@ -361,6 +361,17 @@ void osam_match(void* s, int32_t* state, const int32_t* tok, int64_t n, int32_t 
   info[2] = state[0] != 0 ? sam->min_endpos[state[0]] : -1;
 }
 
+// Timing helper: B generated texts matched against one corpus automaton in
+// one call (state [B, 2], tokens [B, max_new], n_new [B], draft [B, K],
+// info [B, 3]).
+void osam_match_batch(void* s, int32_t B, int32_t* state, const int32_t* tokens,
+                      const int32_t* n_new, int32_t max_new, int32_t K, int32_t* draft,
+                      int32_t* info) {
+  for (int32_t b = 0; b < B; ++b)
+    osam_match(s, state + 2 * (int64_t)b, tokens + (int64_t)b * max_new, n_new[b], K,
+               draft + (int64_t)b * K, info + 3 * (int64_t)b);
+}
+
 // Adaptive draft selection between a dynamic and a static automaton ([P4]
 // "Drafting with Suffix Automaton"): the dynamic draft is preferred; the
 // static one is taken only when its match is longer by more than l_bias.
