@@ -72,6 +72,8 @@ def _load():
         lib.over_verify.argtypes = [P, P, P, P, P, I32, I32, I32, D, U64, U64,
                                     P, P, P, P, P, P, P, P, P, P, P]
         lib.over_cdf_interval.argtypes = [P, P, I32, D, I32, I32, P]
+        lib.over_tree_verify.restype = I32
+        lib.over_tree_verify.argtypes = [P, P, P, P, I32, I32, I32, D, U64, U64, P, P, P, P, P, P]
         _lib = lib
         return lib
 
@@ -229,3 +231,25 @@ def select_static(l_static: int, l_dynamic: int, l_bias: int) -> bool:
     """Adaptive choice between a static and a dynamic automaton's drafts: the
     static draft only when its match is longer by more than l_bias."""
     return bool(_load().oselect_static(int(l_static), int(l_dynamic), int(l_bias)))
+
+
+def tree_verify(target, tok, first_child, next_sibling, temperature=0.0, seed=0, step=0):
+    """Verify a draft tree per sequence.  target [B, N, V] (row n: the token
+    after node n's path), tok / first_child / next_sibling [B, N] int (node 0
+    the verified context; -1 links: none).  Returns accept_len, out_token,
+    path [B, N] (accepted node indices, -1 after), status, u_res, res_mass."""
+    lib = _load()
+    t = np.ascontiguousarray(target, dtype=np.float32)
+    B, N, V = t.shape
+    tk = np.ascontiguousarray(tok, dtype=np.int32).reshape(B, N)
+    fc = np.ascontiguousarray(first_child, dtype=np.int32).reshape(B, N)
+    ns = np.ascontiguousarray(next_sibling, dtype=np.int32).reshape(B, N)
+    out = {k: np.empty(B, np.int32) for k in ("accept_len", "out_token", "status")}
+    out["path"] = np.empty((B, N), np.int32)
+    out["u_res"] = np.empty(B, np.float64)
+    out["res_mass"] = np.empty(B, np.float64)
+    lib.over_tree_verify(_ptr(t), _ptr(tk), _ptr(fc), _ptr(ns), B, N, V, float(temperature),
+                         int(seed) & (2**64 - 1), int(step) & (2**64 - 1), _ptr(out["accept_len"]),
+                         _ptr(out["out_token"]), _ptr(out["path"]), _ptr(out["status"]),
+                         _ptr(out["u_res"]), _ptr(out["res_mass"]))
+    return out

@@ -507,6 +507,125 @@ int32_t over_verify(const float* target, const float* draftlog, const int32_t* d
   return 0;
 }
 
+// Tree verification ([P3] SGLang 的实现: the candidates of a draft tree are
+// tried sibling by sibling, one coin per depth against the running sum of
+// their target probabilities; a rejected candidate's probability is removed
+// before the final sample; [P3] N-gram 的特殊情况: model-free candidates have
+// q = 0).  Sequence b's tree has N nodes: node 0 is the verified context,
+// node n >= 1 carries token tok[n]; first_child / next_sibling link them
+// (-1: none), each link pointing to a larger node index, each node n >= 1
+// linked exactly once, siblings carrying distinct tokens.  Row n of target
+// ([B, N, V]) scores the token after node n's path.
+//   greedy (T = 0): at node c follow the child whose token is the row's
+//     argmax; stop at the first node without such a child and emit that
+//     argmax;
+//   sampling: at node c with children k_1 .. k_m (in sibling order) draw
+//     u = U_acc(depth); take k_i for the first i with u <= p(k_1) + ... +
+//     p(k_i); if there is none, or c has no children, stop and emit a token
+//     drawn from p_c with the tried children's probabilities set to 0, by
+//     t = U_res(depth) * (remaining mass).  Whatever the tree, the emitted
+//     tokens follow the target distribution.
+// Outputs: accept_len (depth reached), out_token, path [B, N] (accepted node
+// indices, -1 after), status (BADDRAFT for a malformed tree, BADROW).
+int32_t over_tree_verify(const float* target, const int32_t* tok, const int32_t* first_child,
+                         const int32_t* next_sibling, int32_t B, int32_t N, int32_t V, double T,
+                         uint64_t seed, uint64_t step, int32_t* accept_len, int32_t* out_token,
+                         int32_t* path, int32_t* status, double* u_res, double* res_mass) {
+  std::vector<double> p, r;
+  std::vector<int32_t> refs;
+  for (int32_t b = 0; b < B; ++b) {
+    const float* rows = target + (int64_t)b * N * V;
+    const int32_t* tk = tok + (int64_t)b * N;
+    const int32_t* fc = first_child + (int64_t)b * N;
+    const int32_t* ns = next_sibling + (int64_t)b * N;
+    int32_t* pb = path + (int64_t)b * N;
+    for (int32_t n = 0; n < N; ++n) pb[n] = -1;
+    accept_len[b] = -1;
+    out_token[b] = -1;
+    if (u_res) u_res[b] = std::numeric_limits<double>::quiet_NaN();
+    if (res_mass) res_mass[b] = std::numeric_limits<double>::quiet_NaN();
+    // the tree's shape
+    bool bad = N < 1 || ns[0] != -1;
+    refs.assign(N, 0);
+    for (int32_t n = 0; !bad && n < N; ++n) {
+      if (n > 0 && (tk[n] < 0 || tk[n] >= V)) bad = true;
+      for (int32_t l : {fc[n], ns[n]}) {
+        if (l == -1) continue;
+        if (l <= n || l >= N) bad = true;
+        else ++refs[l];
+      }
+    }
+    for (int32_t n = 1; !bad && n < N; ++n) bad = refs[n] != 1;
+    for (int32_t n = 0; !bad && n < N; ++n)
+      for (int32_t a = fc[n]; !bad && a != -1; a = ns[a])
+        for (int32_t c = ns[a]; !bad && c != -1; c = ns[c]) bad = tk[a] == tk[c];
+    if (bad) {
+      status[b] = OV_BADDRAFT;
+      continue;
+    }
+    status[b] = OV_OK;
+    int32_t cur = 0, depth = 0;
+    if (T == 0.0) {
+      for (;;) {
+        int32_t a;
+        double mv;
+        if (!argmax_row(rows + (int64_t)cur * V, V, &a, &mv)) {
+          status[b] = OV_BADROW;
+          break;
+        }
+        int32_t next = -1;
+        for (int32_t c = fc[cur]; c != -1; c = ns[c])
+          if (tk[c] == a) next = c;
+        if (next == -1) {
+          accept_len[b] = depth;
+          out_token[b] = a;
+          break;
+        }
+        pb[depth++] = next;
+        cur = next;
+      }
+      continue;
+    }
+    for (;;) {
+      double m, z;
+      if (!softmax_row(rows + (int64_t)cur * V, V, T, p, &m, &z)) {
+        status[b] = OV_BADROW;
+        break;
+      }
+      double ua, ur;
+      uniforms(seed, step, b, depth, &ua, &ur);
+      int32_t next = -1;
+      double acc = 0.0;
+      r = p;
+      for (int32_t c = fc[cur]; c != -1; c = ns[c]) {
+        acc += p[tk[c]];
+        if (ua <= acc) {
+          next = c;
+          break;
+        }
+        r[tk[c]] = 0.0;  // tried and rejected: out of the final distribution
+      }
+      if (next != -1) {
+        pb[depth++] = next;
+        cur = next;
+        continue;
+      }
+      double mass = 0.0;
+      for (int32_t v = 0; v < V; ++v) mass += r[v];
+      if (!(mass > 0.0)) {  // cannot happen in exact arithmetic: fall back to p
+        r = p;
+        mass = 1.0;
+      }
+      accept_len[b] = depth;
+      out_token[b] = sample_cdf(r, ur * mass);
+      if (u_res) u_res[b] = ur;
+      if (res_mass) res_mass[b] = mass;
+      break;
+    }
+  }
+  return 0;
+}
+
 // Normalised CDF interval [lo, hi) of `token` under the residual of one row:
 // lo = C_{token-1} / sum r, hi = C_token / sum r.  Used by the parity tests to
 // decide whether a differing resample lies within a rounding band of a CDF
