@@ -72,6 +72,7 @@ def _load():
         lib.over_verify.argtypes = [P, P, P, P, P, I32, I32, I32, D, U64, U64,
                                     P, P, P, P, P, P, P, P, P, P, P]
         lib.over_cdf_interval.argtypes = [P, P, I32, D, I32, I32, P]
+        lib.over_tree_node_info.argtypes = [P, I32, D, P, I32, I32, P, P]
         lib.over_tree_verify.restype = I32
         lib.over_tree_verify.argtypes = [P, P, P, P, I32, I32, I32, D, U64, U64, P, P, P, P, P, P]
         _lib = lib
@@ -253,3 +254,17 @@ def tree_verify(target, tok, first_child, next_sibling, temperature=0.0, seed=0,
                          _ptr(out["out_token"]), _ptr(out["path"]), _ptr(out["status"]),
                          _ptr(out["u_res"]), _ptr(out["res_mass"]))
     return out
+
+
+def tree_node_info(row, temperature, children, token):
+    """At one tree node: cumulative probabilities of its children (sibling
+    order) and the [lo, hi) interval of `token` in the node's final-sample
+    distribution (children removed).  Returns (acc [n], lo, hi, mass)."""
+    lib = _load()
+    r = np.ascontiguousarray(row, dtype=np.float32)
+    ch = np.ascontiguousarray(children, dtype=np.int32)
+    acc = np.empty(max(len(ch), 1), np.float64)
+    lhm = np.empty(3, np.float64)
+    lib.over_tree_node_info(_ptr(r), r.size, float(temperature), _ptr(ch), len(ch), int(token),
+                            _ptr(acc), _ptr(lhm))
+    return acc[:len(ch)], float(lhm[0]), float(lhm[1]), float(lhm[2])

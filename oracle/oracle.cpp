@@ -626,6 +626,31 @@ int32_t over_tree_verify(const float* target, const int32_t* tok, const int32_t*
   return 0;
 }
 
+// For parity checks of tree verification at one node: acc[i] = p(k_1) + ...
+// + p(k_{i+1}) for the n children tokens (sibling order), and the interval
+// [lo, hi) of `token` in the node's final-sample distribution (the row
+// without the children, normalised) -- lo_hi_mass = {lo, hi, mass}.
+void over_tree_node_info(const float* trow, int32_t V, double T, const int32_t* children,
+                         int32_t n, int32_t token, double* acc, double* lo_hi_mass) {
+  std::vector<double> p;
+  double m, z;
+  softmax_row(trow, V, T, p, &m, &z);
+  double a = 0.0;
+  std::vector<double> r = p;
+  for (int32_t i = 0; i < n; ++i) {
+    a += p[children[i]];
+    acc[i] = a;
+    r[children[i]] = 0.0;
+  }
+  double mass = 0.0;
+  for (int32_t v = 0; v < V; ++v) mass += r[v];
+  double before = 0.0;
+  for (int32_t v = 0; v < token; ++v) before += r[v];
+  lo_hi_mass[0] = before / mass;
+  lo_hi_mass[1] = (before + r[token]) / mass;
+  lo_hi_mass[2] = mass;
+}
+
 // Normalised CDF interval [lo, hi) of `token` under the residual of one row:
 // lo = C_{token-1} / sum r, hi = C_token / sum r.  Used by the parity tests to
 // decide whether a differing resample lies within a rounding band of a CDF

@@ -116,3 +116,11 @@ def test_malformed_trees_are_refused():
     for t, f, n in cases:
         tr = oracle.tree_verify(logits, t[None], f[None], n[None], 1.0)
         assert tr["status"][0] == 6 and tr["accept_len"][0] == -1
+
+
+def test_node_info_closed_form():
+    # uniform row over 4 tokens, children {1, 2}: running sums 1/4, 1/2; the
+    # final distribution keeps tokens 0 and 3 with mass 1/2 each
+    acc, lo, hi, mass = oracle.tree_node_info(np.zeros(4, np.float32), 1.0, [1, 2], 3)
+    np.testing.assert_allclose(acc, [0.25, 0.5])
+    assert (lo, hi, mass) == (0.5, 1.0, 0.5)
