@@ -290,6 +290,37 @@ int spec_verify_noalloc(const void* d_target, int32_t target_dtype, const void* 
                         int32_t* d_emit, int32_t* d_emit_len, int32_t* d_status,
                         const spec_verify_debug* dbg, samspec_stream_t stream);
 
+/* Verification of a draft tree per sequence ([P3] SGLang 的实现: candidates
+ * are tried sibling by sibling; [P3] N-gram 的特殊情况: model-free drafts have
+ * q = 0).  Sequence b's tree has N nodes (1 <= N <= 32): node 0 is the
+ * verified context, node n >= 1 carries token d_tok[b, n]; d_first_child and
+ * d_next_sibling [B, N] link them (-1: none).  Every link must point to a
+ * larger index below N, every node n >= 1 must be linked exactly once, node 0
+ * has no sibling, tokens lie in [0, V) and siblings carry distinct tokens;
+ * otherwise the sequence gets ST_BADDRAFT.  d_target [B, N, V]: row n scores
+ * the token after node n's path.
+ *   T = 0: at each node the child whose token is the row's argmax is taken;
+ *          the first node without one emits its argmax.
+ *   T > 0: at depth t a coin u_t (Philox word 0 of counter (t, b, step))
+ *          takes the first child k_i (sibling order) with
+ *          u_t <= p(k_1) + ... + p(k_i); with none, or at a leaf, the emitted
+ *          token is drawn from p of the node with the tried children removed,
+ *          by u'_t (word 1) as in spec_verify.  A tree of one child per node
+ *          is the linear case of spec_verify.
+ * Outputs: d_accept_len [B] (depth reached), d_out_token [B], optional
+ * d_path [B, N] (accepted node indices, -1 after), d_emit [B, N] (their tokens,
+ * then the emitted token, -1 after), d_emit_len, d_status; dbg row_m / row_z /
+ * row_arg / res_mass as for spec_verify (rows indexed by node; p_d and q_d
+ * are not written).  Workspace as spec_verify_workspace_bytes(B, N - 1, V).
+ * V limits as spec_verify's one-hot case.  One kernel launch. */
+int spec_verify_tree(const void* d_target, int32_t target_dtype, const int32_t* d_tok,
+                     const int32_t* d_first_child, const int32_t* d_next_sibling, int32_t B,
+                     int32_t N, int32_t V, float temperature, uint64_t seed, uint64_t step,
+                     int32_t* d_accept_len, int32_t* d_out_token, int32_t* d_path,
+                     int32_t* d_emit, int32_t* d_emit_len, int32_t* d_status,
+                     const spec_verify_debug* dbg, void* d_workspace, size_t ws_bytes,
+                     samspec_stream_t stream);
+
 /* One decode step of model-free speculative decoding ([P1] §1.1: verify, then
  * update each sequence's D-SAM with the verified tokens, then draft; [P1]
  * §3.1.1: whether a step speculates at all is the caller's choice of K and

@@ -13,6 +13,7 @@ the C entry points, over torch CUDA tensors:
   select_drafts(dynamic, static, l_bias) -- sam_select_drafts
     .status(), .reset(mask), .dump(b), .export(), .import_(blob)
   spec_verify(target, draft, ...)       -- spec_verify
+  spec_verify_tree(target, tok, ...)    -- spec_verify_tree (draft trees)
   spec_uniforms(B, K, seed, step)       -- spec_uniforms
 
 Device memory (workspaces, inputs, outputs) comes from torch; each call is
@@ -28,8 +29,8 @@ from . import _binding as _b
 from ._binding import (BF16, F32, ST_BADDRAFT, ST_BADROW, ST_CAPACITY, ST_HASHFULL,  # noqa: F401
                        ST_LOOPCAP, ST_OK, ST_TIMEOUT, ST_TOKEN, SamspecError)
 
-__all__ = ["SamBatch", "spec_verify", "spec_uniforms", "select_drafts", "SamspecError",
-           "library_path"]
+__all__ = ["SamBatch", "spec_verify", "spec_verify_tree", "spec_uniforms", "select_drafts",
+           "SamspecError", "library_path"]
 
 
 def library_path() -> str:
@@ -342,6 +343,44 @@ def select_drafts(dynamic, static, l_bias: int):
                                         _ptr(sm), int(l_bias), _ptr(od), _ptr(ol), _ptr(src),
                                         _stream(dd.device)), "sam_select_drafts")
     return od, ol, src
+
+
+def spec_verify_tree(target, tok, first_child, next_sibling, temperature: float = 0.0,
+                     seed: int = 0, step: int = 0, debug: bool = False, workspace=None):
+    """Verify a draft tree per sequence: target [B, N, V] (row n: the token
+    after node n's path), tok / first_child / next_sibling int32 [B, N].
+    Returns a dict of CUDA tensors: accept_len, out_token, path [B, N], emit
+    [B, N], emit_len, status (+ row_m, row_z, row_arg, res_mass)."""
+    lib = _b.lib()
+    if target.dim() != 3:
+        raise ValueError("target must be [B, N, V]")
+    B, N, V = (int(x) for x in target.shape)
+    dt = {torch.float32: F32, torch.bfloat16: BF16}.get(target.dtype)
+    if dt is None:
+        raise TypeError("target must be float32 or bfloat16")
+    _req(target, target.dtype, "target")
+    for t, nm in ((tok, "tok"), (first_child, "first_child"), (next_sibling, "next_sibling")):
+        _req(t, torch.int32, nm, (B, N))
+    dev = target.device
+    z = lambda *s: torch.empty(s, dtype=torch.int32, device=dev)  # noqa: E731
+    res = {"accept_len": z(B), "out_token": z(B), "path": z(B, N), "emit": z(B, N),
+           "emit_len": z(B), "status": z(B)}
+    dbg = None
+    if debug:
+        for k in ("row_m", "row_z"):
+            res[k] = torch.full((B, N), float("nan"), dtype=torch.float32, device=dev)
+        res["row_arg"] = torch.full((B, N), -1, dtype=torch.int32, device=dev)
+        res["res_mass"] = torch.full((B,), float("nan"), dtype=torch.float32, device=dev)
+        dbg = _b.VerifyDebug(res["row_m"].data_ptr(), res["row_z"].data_ptr(), 0, 0,
+                             res["row_arg"].data_ptr(), res["res_mass"].data_ptr())
+    ws = workspace if workspace is not None else verify_workspace(B, N - 1, V, dev)
+    _b.check(lib.spec_verify_tree(_ptr(target), dt, _ptr(tok), _ptr(first_child), _ptr(next_sibling),
+                                  B, N, V, float(temperature), int(seed) & (2**64 - 1),
+                                  int(step) & (2**64 - 1), _ptr(res["accept_len"]), _ptr(res["out_token"]),
+                                  _ptr(res["path"]), _ptr(res["emit"]), _ptr(res["emit_len"]),
+                                  _ptr(res["status"]), ctypes.byref(dbg) if dbg is not None else None,
+                                  _ptr(ws), ws.numel(), _stream(dev)), "spec_verify_tree")
+    return res
 
 
 def spec_uniforms(B: int, K: int, seed: int, step: int, device=None):

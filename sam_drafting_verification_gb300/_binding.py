@@ -25,6 +25,7 @@ EXPORTED = [
     "sam_dump_sequence",
     "spec_verify_workspace_bytes", "spec_verify_workspace_init", "spec_verify", "spec_uniforms",
     "spec_verify_noalloc", "sam_step_rows", "sam_spec_step", "ssam_match", "sam_select_drafts",
+    "spec_verify_tree",
 ]
 
 
@@ -66,6 +67,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                                P, P, P, P, P, ctypes.POINTER(VerifyDebug), P]),
         "sam_step_rows": (ctypes.c_int, [P, P, I32, P, P, I32, I32, P, P, P, P, P]),
         "ssam_match": (ctypes.c_int, [P, I32, I32, P, P, P, I32, I32, P, P, P, P, P]),
+        "spec_verify_tree": (ctypes.c_int, [P, I32, P, P, P, I32, I32, I32, F, U64, U64, P, P, P,
+                                            P, P, P, ctypes.POINTER(VerifyDebug), P, SZ, P]),
         "sam_select_drafts": (ctypes.c_int, [I32, I32, P, P, P, P, P, P, I32, P, P, P, P]),
         "sam_spec_step": (ctypes.c_int, [P, P, I32, P, I32, P, P, I32, I32, F, U64, U64,
                                          P, P, P, P, P, ctypes.POINTER(VerifyDebug),

@@ -87,6 +87,11 @@ struct VParams {
   uint32_t* ws;  // [0] claim counter, [1] CTA exit counter, [2] error bits
   int32_t NC, NS;
   int32_t direct;  // 1: plain loads instead of bulk copies (unaligned rows)
+  // draft trees (K = N - 1, row n scores the token after node n's path)
+  const int32_t* ttok;  // [B, N] node tokens (node 0: the verified context)
+  const int32_t* tfc;   // [B, N] first child, -1: none
+  const int32_t* tns;   // [B, N] next sibling, -1: none
+  int32_t* path;        // [B, N] accepted node indices, -1 after
 };
 
 struct Tag {
@@ -105,6 +110,11 @@ struct Slot {
   int32_t dtok;   // draft token of the current row (-1 for the bonus row)
   float xd, gd;   // target / draft logit at dtok, captured by the consumers
   int32_t age;    // claim order inside the CTA: the producer serves the oldest first
+  // draft trees: depth of the current row, its children's tokens (sibling
+  // order; left out of the sums like a linear draft) and their logits
+  int32_t depth, nex;
+  int32_t ex[32];
+  float cx[32];
 };
 
 // One warp-slice record: softmax statistics of the target (a) and draft (b)
@@ -422,9 +432,10 @@ __device__ __forceinline__ float4 reduce_greedy(const Slice<TT, DT>& s, int w, i
 // per-record exponential enters the row's masses.  The element with tile index
 // `excl` (the row's draft token, added back exactly by the control warp) is
 // left out.  An all -inf slice gives {-inf, -inf, 0, 0}; NaN gives NaNs.
-template <int TT, int DT, bool FULL, bool DRAFT_ARRAY>
+template <int TT, int DT, bool FULL, bool DRAFT_ARRAY, bool MULTI = false>
 __device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, int lane, int nel,
-                                                 float cT, int excl) {
+                                                 float cT, int excl, const int32_t* exl = nullptr,
+                                                 int nex = 0, int elem0 = 0) {
   using C = Cfg<TT, DT>;
   const float NEG_INF = -__int_as_float(0x7f800000);
   const float QNAN = __int_as_float(0x7fc00000);
@@ -434,7 +445,13 @@ __device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, 
   if (m == NEG_INF) return make_float4(NEG_INF, NEG_INF, 0.f, 0.f);
   const float R = ceilf(m * cT);
   float z;
-  const bool has_excl = excl >= w * C::SL && excl < (w + 1) * C::SL;
+  bool has_excl = excl >= w * C::SL && excl < (w + 1) * C::SL;
+  if (MULTI) {  // a list of vocabulary ids (a tree node's children)
+    for (int k = 0; k < nex; ++k) {
+      const int o = exl[k] - elem0;
+      has_excl |= o >= w * C::SL && o < (w + 1) * C::SL;
+    }
+  }
   if (FULL && !has_excl) {
     // pairs of elements through packed FFMA / FADD, one MUFU ex2 each
     const uint64_t c2 = pk2(cT, cT), nr2 = pk2(-R, -R);
@@ -472,7 +489,10 @@ __device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, 
 #pragma unroll
       for (int k = 0; k < C::VEC; ++k) {
         const float x = DRAFT_ARRAY ? s.d[i].at(k) : s.t[i].at(k);
-        v[k] = (e + k < nel && e + k != excl) ? ex2_approx(fmaf(x, cT, -R)) : 0.f;
+        bool keep = e + k < nel && e + k != excl;
+        if (MULTI && keep && has_excl)
+          for (int q = 0; q < nex; ++q) keep &= exl[q] - elem0 != e + k;
+        v[k] = keep ? ex2_approx(fmaf(x, cT, -R)) : 0.f;
       }
 #pragma unroll
       for (int h = C::VEC / 2; h >= 1; h >>= 1)
@@ -537,6 +557,8 @@ __device__ __forceinline__ float4 reduce_resid(const Slice<TT, DT>& s, int w, in
 
 // ---- outputs ---------------------------------------------------------------
 __device__ void write_result(const VParams& P, int b, int L, int out, int st) {
+  if (P.path)
+    for (int t = 0; t <= P.K; ++t) P.path[(size_t)b * (P.K + 1) + t] = -1;
   P.accept_len[b] = st ? -1 : L;
   P.out_token[b] = st ? -1 : out;
   if (P.status) P.status[b] = st;
@@ -597,7 +619,7 @@ __device__ __forceinline__ float exp_ref(float x, float R, float cT, float cTl) 
   return ldexpf(exp2f((s - si) + (e1 + e2)), (int)fmaxf(si, -300.f));
 }
 
-template <int TT, int DT, bool GREEDY>
+template <int TT, int DT, bool GREEDY, bool TREE = false>
 struct Control {
   using C = Cfg<TT, DT>;
   static constexpr int EPL = C::SL / 32;  // slice elements per lane (lane-major loads)
@@ -607,10 +629,14 @@ struct Control {
   int lane, si;
   bool more;
   int32_t tok;        // lane t holds draft token t of the slot's sequence
+                      // (trees: the token of node t)
+  int32_t par_;       // trees: parent of node `lane`
+  int32_t pathv;      // trees: the node accepted at depth `lane`
   float ua, ur;       // coins of the row in flight (drawn while it streams)
 
   __device__ Control(const VParams& p, Smem& s, const Rec* r, int l, int slot)
-      : P(p), sm(s), rec(r), lane(l), si(slot), more(true), tok(-1), ua(0.f), ur(0.f) {
+      : P(p), sm(s), rec(r), lane(l), si(slot), more(true), tok(-1), par_(-1), pathv(-1),
+        ua(0.f), ur(0.f) {
     reset_row();
   }
 
@@ -619,7 +645,15 @@ struct Control {
   // Outputs of sequence b, written by the warp's lanes in parallel (lane t
   // holds draft token t).
   __device__ void finish(int b, int L, int out, int st) {
-    if (P.emit) {
+    if (TREE) {
+      // the accepted path's nodes, then their tokens and the final token
+      const int32_t pt = __shfl_sync(kFullMask, tok, pathv & 31);
+      if (lane <= P.K) {
+        if (P.path) P.path[(size_t)b * (P.K + 1) + lane] = (!st && lane < L) ? pathv : -1;
+        if (P.emit)
+          P.emit[(size_t)b * (P.K + 1) + lane] = st ? -1 : (lane < L ? pt : (lane == L ? out : -1));
+      }
+    } else if (P.emit) {
       int32_t* e = P.emit + (size_t)b * (P.K + 1);
       if (lane <= P.K) e[lane] = st ? -1 : (lane < L ? tok : (lane == L ? out : -1));
       if (P.K == 32 && lane == 0) e[32] = st ? -1 : (L == 32 ? out : -1);
@@ -641,6 +675,23 @@ struct Control {
   // Posts row j for the producer, then draws the row's coins while it streams.
   __device__ void post(int kind, int j) {
     Slot& S = sm.slot[si];
+    if (TREE) {
+      // row j is node j; its children (sibling order = index order) are the
+      // candidates, left out of the row's sums
+      const unsigned cm = __ballot_sync(kFullMask, lane <= P.K && par_ == j && lane > 0);
+      if ((cm >> lane) & 1u) S.ex[__popc(cm & ((1u << lane) - 1u))] = tok;
+      if (lane == 0) {
+        S.kind = kind;
+        S.j = j;
+        S.dtok = -1;
+        S.nex = kind == kStats ? __popc(cm) : 0;
+        __threadfence_block();
+        vstore(&S.state, kReady);
+      }
+      __syncwarp();
+      if (!GREEDY) verify_coins(P.seed, P.step, (uint32_t)S.b, (uint32_t)S.depth, &ua, &ur);
+      return;
+    }
     const int32_t dt = __shfl_sync(kFullMask, tok, j & 31);
     if (lane == 0) {
       S.kind = kind;
@@ -651,6 +702,38 @@ struct Control {
     }
     __syncwarp();
     if (!GREEDY) verify_coins(P.seed, P.step, (uint32_t)S.b, (uint32_t)j, &ua, &ur);
+  }
+
+  // Trees: node `lane` of sequence b into registers (token, parent), and the
+  // shape checks: every link points to a larger index below N, every node
+  // n >= 1 is linked exactly once, node 0 has no sibling, tokens lie in
+  // [0, V), siblings carry distinct tokens.
+  __device__ bool tree_load(int b) {
+    const int N = P.K + 1;
+    const bool in = lane < N;
+    const size_t o = (size_t)b * N + lane;
+    tok = in && lane > 0 ? P.ttok[o] : -1;
+    const int32_t fc = in ? P.tfc[o] : -1;
+    const int32_t ns = in ? P.tns[o] : -1;
+    bool bad = in && ((lane > 0 && (tok < 0 || tok >= P.V)) || (fc != -1 && (fc <= lane || fc >= N)) ||
+                      (ns != -1 && (ns <= lane || ns >= N)) || (lane == 0 && ns != -1));
+    if (__any_sync(kFullMask, bad)) return false;
+    // parents, in index order: node c is the first child of some n, or the
+    // next sibling of some s < c (whose parent is already known)
+    par_ = -1;
+    for (int c = 1; c < N; ++c) {
+      const unsigned f = __ballot_sync(kFullMask, in && fc == c);
+      const unsigned g = __ballot_sync(kFullMask, in && ns == c);
+      if (__popc(f) + __popc(g) != 1) return false;
+      const int32_t pc = f ? (__ffs(f) - 1) : __shfl_sync(kFullMask, par_, __ffs(g) - 1);
+      if (lane == c) par_ = pc;
+    }
+    // distinct tokens among siblings
+    const unsigned long long key = in && lane > 0
+                                       ? ((unsigned long long)(uint32_t)par_ << 32) | (uint32_t)tok
+                                       : (0xFFFFFFFFull << 32) | (uint32_t)lane;
+    const unsigned same = __match_any_sync(kFullMask, key);
+    return !__any_sync(kFullMask, in && lane > 0 && __popc(same) > 1);
   }
 
   // Claims sequences until one with valid drafts lands in the slot (or none
@@ -667,6 +750,23 @@ struct Control {
       if (b >= (uint32_t)P.B) {
         more = false;
         break;
+      }
+      if (TREE) {
+        if (!tree_load((int)b)) {
+          finish((int)b, -1, -1, SAMSPEC_ST_BADDRAFT);
+          continue;
+        }
+        pathv = -1;
+        if (lane == 0) {
+          S.b = (int32_t)b;
+          S.nb = 0;
+          S.L = 0;
+          S.depth = 0;
+          S.age = atomicAdd(&sm.claims, 1);
+        }
+        __syncwarp();
+        post(kStats, 0);
+        return;
       }
       const int nb = P.draft_len ? P.draft_len[b] : P.K;
       tok = (lane < P.K) ? P.draft[(size_t)b * P.K + lane] : -1;
@@ -788,7 +888,14 @@ struct Control {
   // that lane's elements go one per lane and a second warp scan finds the
   // token.
   __device__ int slice_scan(int b, int L, int c, int w, float t, int smode, int excl, float RL,
-                            float RG, float invZ, float invZg) {
+                            float RG, float invZ, float invZg, const int32_t* exl = nullptr,
+                            int nex = 0) {
+    auto out_of = [&](int v) {  // left out of the residual: `excl` or a listed id
+      if (v == excl) return true;
+      for (int q = 0; q < nex; ++q)
+        if (exl[q] == v) return true;
+      return false;
+    };
     Slice<TT, DT> sl;
     const bool with_draft = DT >= 0 && smode == 1;
     const int n = load_slice_lanes<TT, DT>(sl, P, b, L, c, w, with_draft, lane);
@@ -801,7 +908,7 @@ struct Control {
       for (int k = 0; k < C::VEC; ++k) {
         const int e = lane * EPL + i * C::VEC + k;
         float r = 0.f;
-        if (e < n && s0 + e != excl)
+        if (e < n && !out_of(s0 + e))
           r = resid_val(sl.t[i].at(k), DT >= 0 ? sl.d[i].at(k) : 0.f, smode, RL, RG, invZ, invZg, P.cT);
         tot += r;
         if (r > 0.f) last_pos = s0 + e;
@@ -839,7 +946,7 @@ struct Control {
       const int q = rd * 32 + lane;
       const int e = ls * EPL + q;
       float re = 0.f;
-      if (q < EPL && e < n && s0 + e != excl)
+      if (q < EPL && e < n && !out_of(s0 + e))
         re = resid_val(xe, ge, smode, RL, RG, invZ, invZg, P.cT);
       const float inc2 = warp_incl_scan_f(re, lane);
       const unsigned h2 = __ballot_sync(kFullMask, q < EPL && inc2 > tl);
@@ -894,6 +1001,85 @@ struct Control {
     return scan(cstar, wstar, tw);
   }
 
+  // Trees: node `node` accepted at the current depth; post its row.
+  __device__ void advance(int node) {
+    Slot& S = sm.slot[si];
+    const int depth = S.depth;
+    if (lane == depth) pathv = node;
+    __syncwarp();
+    if (lane == 0) S.depth = depth + 1;
+    __syncwarp();
+    post(kStats, node);
+  }
+
+  // Trees, T > 0: row j (node j) is complete.  Its children k_1 .. k_m were
+  // left out of the sums; p(k_i) from their captured logits; one coin u for
+  // this depth takes the first child with u <= p(k_1) + ... + p(k_i).  If
+  // none, or a leaf, the final token is drawn from the row without the
+  // children (the sums already leave them out).
+  __device__ void tree_step(int b, int j, size_t ro) {
+    Slot& S = sm.slot[si];
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    const int nex = S.nex;
+    const float lm = run[0].nan ? __int_as_float(0x7fc00000) : run[0].mx;
+    const float LM = run[0].ref;
+    const DF zx = run[0].sum;
+    const float ek = lane < nex ? exp_ref(S.cx[lane], LM, P.cT, P.cTl) : 0.f;
+    const DF ztd = df_add(zx, df_warp_sum(DF{ek, 0.f}));
+    const float zt = df_f(ztd);
+    const bool bad = !(lm > NEG_INF) || isinf(lm) || !isfinite(zt) || !(zt > 0.f);
+    if (lane == 0) {
+      if (P.dbg.row_m) P.dbg.row_m[ro] = lm / P.T;
+      if (P.dbg.row_z)
+        P.dbg.row_z[ro] = (float)(((double)ztd.hi + (double)ztd.lo) * exp2((double)LM - (double)lm * P.cTd));
+    }
+    if (bad) {
+      finish(b, -1, -1, SAMSPEC_ST_BADROW);
+      release();
+      return;
+    }
+    // running sum of the children's probabilities, in sibling order
+    float inc = ek;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(kFullMask, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const unsigned hit = __ballot_sync(kFullMask, lane < nex && ua * zt <= inc);
+    if (hit) {
+      const int k = __ffs(hit) - 1;
+      // the k-th child in sibling order
+      const unsigned cm = __ballot_sync(kFullMask, lane <= P.K && lane > 0 && par_ == j);
+      const bool mine = ((cm >> lane) & 1u) && __popc(cm & ((1u << lane) - 1u)) == k;
+      advance(__ffs(__ballot_sync(kFullMask, mine)) - 1);
+      return;
+    }
+    const int depth = S.depth;
+    if (!(df_f(zx) > 0.f)) {
+      // only the children carry mass (rounding): the child holding u' of it
+      const unsigned h2 = __ballot_sync(kFullMask, lane < nex && ur * zt <= inc);
+      const int k = h2 ? __ffs(h2) - 1 : nex - 1;
+      finish(b, depth, S.ex[k], 0);
+      release();
+      return;
+    }
+    if (lane == 0 && P.dbg.res_mass) P.dbg.res_mass[b] = df_f(zx) / zt;
+    const DF tt = df_mul_f(zx, ur);
+    auto slice_mass = [&](int c, int w) -> DF {
+      const float4 r = R(c, w).a;
+      if (r.y == NEG_INF || r.z == 0.f) return DF{0.f, 0.f};
+      return df_scale(DF{r.z, r.w}, (int)(r.y - LM));
+    };
+    auto scan = [&](int c, int w, DF tw) -> int {
+      const float Rw = R(c, w).a.y;
+      return slice_scan(b, j, c, w, df_f(df_scale(tw, (int)(LM - Rw))), 0, -1, Rw, 0.f, 0.f, 0.f,
+                        S.ex, nex);
+    };
+    const int out = resample(tt, LM, slice_mass, scan);
+    finish(b, depth, out, 0);
+    release();
+  }
+
   __device__ void handle() {
     Slot& S = sm.slot[si];
     const int b = S.b, j = S.j, nb = S.nb;
@@ -915,6 +1101,16 @@ struct Control {
         release();
         return;
       }
+      if (TREE) {  // follow the child holding the argmax, if there is one
+        const unsigned cm = __ballot_sync(kFullMask, lane <= P.K && lane > 0 && par_ == j && tok == idx);
+        if (cm) {
+          advance(__ffs(cm) - 1);
+          return;
+        }
+        finish(b, S.depth, idx, 0);
+        release();
+        return;
+      }
       const int32_t dj = __shfl_sync(kFullMask, tok, j & 31);
       if (j < nb && dj == idx) {
         post(kStats, j + 1);
@@ -922,6 +1118,11 @@ struct Control {
       }
       finish(b, j, idx, 0);
       release();
+      return;
+    }
+
+    if (TREE && S.kind == kStats) {
+      tree_step(b, j, ro);
       return;
     }
 
@@ -1036,7 +1237,7 @@ struct Control {
   }
 };
 
-template <int TT, int DT, bool GREEDY>
+template <int TT, int DT, bool GREEDY, bool TREE = false>
 __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
   using C = Cfg<TT, DT>;
   extern __shared__ __align__(1024) unsigned char dsm[];
@@ -1110,8 +1311,33 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
           // one-hot drafts: the row's draft token is left out of the sums
           // (tile index, or -1), so the residual of a rejection is exact
           const int ex = (DT < 0 && tg.dtok >= 0) ? tg.dtok - tg.elem0 : -1;
+          if (TREE) {  // a tree node's children: a list of ids left out
+            const int nex = S.nex;
+            r.a = full ? reduce_softmax<TT, DT, true, false, true>(sl, warp, lane, tg.nel, P.cT, -1,
+                                                                   S.ex, nex, tg.elem0)
+                       : reduce_softmax<TT, DT, false, false, true>(sl, warp, lane, tg.nel, P.cT, -1,
+                                                                    S.ex, nex, tg.elem0);
+            // the lanes holding the children keep their logits
+            for (int k = 0; k < nex; ++k) {
+              const int o = S.ex[k] - tg.elem0 - warp * C::SL;
+              if (o >= 0 && o < C::SL && o + warp * C::SL < tg.nel) {
+                const int v = o / C::VEC, kk = o % C::VEC;
+                if ((v & 31) == lane) {
+                  const int ii = v >> 5;
+                  float x = 0.f;
+#pragma unroll
+                  for (int i = 0; i < C::VPL; ++i)
+#pragma unroll
+                    for (int q = 0; q < C::VEC; ++q)
+                      if (i == ii && q == kk) x = sl.t[i].at(q);
+                  S.cx[k] = x;
+                }
+              }
+            }
+          } else {
           r.a = full ? reduce_softmax<TT, DT, true, false>(sl, warp, lane, tg.nel, P.cT, ex)
                      : reduce_softmax<TT, DT, false, false>(sl, warp, lane, tg.nel, P.cT, ex);
+          }
           if (DT >= 0 && tg.has_draft) {
             r.b = full ? reduce_softmax<TT, DT, true, true>(sl, warp, lane, tg.nel, P.cT, ex)
                        : reduce_softmax<TT, DT, false, true>(sl, warp, lane, tg.nel, P.cT, ex);
@@ -1277,7 +1503,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
     // while large ones keep four sequences in flight per CTA.
     const int si = warp - kCtrlWarp;
     Slot& S = sm.slot[si];
-    Control<TT, DT, GREEDY> ctl(P, sm, rec, lane, si);
+    Control<TT, DT, GREEDY, TREE> ctl(P, sm, rec, lane, si);
     int last_jobs = -1;
     uint64_t t_idle = gtimer();
     for (;;) {
@@ -1395,7 +1621,7 @@ __global__ void uniforms_kernel(int32_t B, int32_t K, uint64_t seed, uint64_t st
 }
 
 // ---- host launch --------------------------------------------------------------
-template <int TT, int DT, bool GREEDY>
+template <int TT, int DT, bool GREEDY, bool TREE = false>
 int launch(const VParams& P0, cudaStream_t stream) {
   using C = Cfg<TT, DT>;
   VParams P = P0;
@@ -1419,7 +1645,7 @@ int launch(const VParams& P0, cudaStream_t stream) {
       return SAMSPEC_ECUDA;
   }
   if (!attr_done[dev]) {
-    if (cudaFuncSetAttribute(verify_kernel<TT, DT, GREEDY>,
+    if (cudaFuncSetAttribute(verify_kernel<TT, DT, GREEDY, TREE>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem[dev]) !=
         cudaSuccess)
       return SAMSPEC_ECUDA;
@@ -1431,7 +1657,7 @@ int launch(const VParams& P0, cudaStream_t stream) {
   P.NS = ns;
   const size_t smem = head + (size_t)ns * kStageBytes;
   const int grid = P.B < sms[dev] ? P.B : sms[dev];
-  verify_kernel<TT, DT, GREEDY><<<grid, kThreads, smem, stream>>>(P);
+  verify_kernel<TT, DT, GREEDY, TREE><<<grid, kThreads, smem, stream>>>(P);
   return cudaGetLastError() == cudaSuccess ? SAMSPEC_OK : SAMSPEC_ECUDA;
 }
 
@@ -1545,6 +1771,60 @@ int spec_verify(const void* d_target, int32_t target_dtype, const void* d_draft_
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return greedy ? dispatch<true>(P, target_dtype, ddt, s)
                 : dispatch<false>(P, target_dtype, ddt, s);
+}
+
+int spec_verify_tree(const void* d_target, int32_t target_dtype, const int32_t* d_tok,
+                     const int32_t* d_first_child, const int32_t* d_next_sibling, int32_t B,
+                     int32_t N, int32_t V, float temperature, uint64_t seed, uint64_t step,
+                     int32_t* d_accept_len, int32_t* d_out_token, int32_t* d_path,
+                     int32_t* d_emit, int32_t* d_emit_len, int32_t* d_status,
+                     const spec_verify_debug* dbg, void* d_workspace, size_t ws_bytes,
+                     samspec_stream_t stream) {
+  if (!d_target || !d_tok || !d_first_child || !d_next_sibling || !d_accept_len ||
+      !d_out_token || !d_workspace)
+    return SAMSPEC_EINVAL;
+  if (B < 1 || B > (1 << 24) || N < 1 || N > 32 || V < 1 || V > (1 << 24)) return SAMSPEC_ESIZE;
+  if (!(temperature >= 0.f) || temperature != temperature || temperature == __builtin_inff())
+    return SAMSPEC_EINVAL;
+  if (target_dtype != SAMSPEC_F32 && target_dtype != SAMSPEC_BF16) return SAMSPEC_EDTYPE;
+  if (ws_bytes < spec_verify_workspace_bytes(B, N - 1, V)) return SAMSPEC_ESIZE;
+  if (reinterpret_cast<uintptr_t>(d_workspace) % 256 != 0) return SAMSPEC_EALIGN;
+  if (reinterpret_cast<uintptr_t>(d_target) % 16 != 0) return SAMSPEC_EALIGN;
+  const bool greedy = temperature == 0.f;
+  const int st = target_dtype == SAMSPEC_F32 ? 4 : 2;
+  VParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.target = static_cast<const unsigned char*>(d_target);
+  P.B = B;
+  P.K = N - 1;
+  P.V = V;
+  P.T = temperature;
+  P.Td = (double)temperature;
+  P.cTd = greedy ? 0.0 : 1.4426950408889634 / (double)temperature;
+  P.cT = (float)P.cTd;
+  P.cTl = (float)(P.cTd - (double)P.cT);
+  P.seed = seed;
+  P.step = step;
+  P.accept_len = d_accept_len;
+  P.out_token = d_out_token;
+  P.emit = d_emit;
+  P.emit_len = d_emit_len;
+  P.status = d_status;
+  if (dbg) {
+    P.dbg = *dbg;
+    P.dbg.p_d = nullptr;  // per-candidate probabilities are not reported for trees
+    P.dbg.q_d = nullptr;
+  }
+  P.ws = static_cast<uint32_t*>(d_workspace);
+  P.direct = ((size_t)V * st) % 16 != 0;
+  P.ttok = d_tok;
+  P.tfc = d_first_child;
+  P.tns = d_next_sibling;
+  P.path = d_path;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (greedy)
+    return target_dtype == SAMSPEC_F32 ? launch<0, -1, true, true>(P, s) : launch<1, -1, true, true>(P, s);
+  return target_dtype == SAMSPEC_F32 ? launch<0, -1, false, true>(P, s) : launch<1, -1, false, true>(P, s);
 }
 
 int spec_uniforms(int32_t B, int32_t K, uint64_t seed, uint64_t step, float* d_u,
