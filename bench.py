@@ -18,7 +18,7 @@ stream; max over ranks.  Under torchrun every rank runs its own batch (weak
 scaling, no collective on the data path).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                  [--workload rs_bf16_b64|sweep_b1024|long_rollout_b256|rollout_toy_b64|static_match_b256]
+                  [--workload rs_bf16_b64|sweep_b1024|long_rollout_b256|rollout_toy_b64|static_match_b256|tree_b256]
 """
 from __future__ import annotations
 
@@ -210,6 +210,8 @@ def run_gpu(args):
         return run_rollout_toy(args, ws, rank, dev)
     if args.workload == "static_match_b256":
         return run_static_match(args, ws, rank, dev)
+    if args.workload == "tree_b256":
+        return run_tree(args, ws, rank, dev)
 
     B, V, K, T, n = 64, workloads.V_LARGE, 3, 1.0, 4096
     hist, cont = rs_inputs(rank, B, V, n, K)
@@ -810,6 +812,150 @@ def run_static_match(args, ws, rank, dev):
 
 
 # --------------------------------------------------------------------------
+# tree-draft verification
+# --------------------------------------------------------------------------
+
+# node n's parent: a root with three candidates (nodes 1, 4, 7); nodes 1 and
+# 4 each carry a chain of two more drafts
+TREE_PARENT = (-1, 0, 1, 2, 0, 4, 5, 0)
+TREE_BOOST = (0.0, 14.0, 14.0, 14.0, 12.0, 12.0, 12.0, 11.0)
+TREE_REPLAYS = 10
+
+
+def tree_arrays(rng, B, V):
+    """tok / first_child / next_sibling [B, 8] of the fixed tree shape, with
+    random tokens (distinct among siblings)."""
+    N = len(TREE_PARENT)
+    fc = np.full(N, -1, np.int32)
+    ns = np.full(N, -1, np.int32)
+    last = {}
+    for n in range(1, N):
+        p = TREE_PARENT[n]
+        if p in last:
+            ns[last[p]] = n
+        else:
+            fc[p] = n
+        last[p] = n
+    tok = np.full((B, N), -1, np.int32)
+    for b in range(B):
+        t = rng.choice(V, N - 1, replace=False)
+        tok[b, 1:] = t
+    return tok, np.tile(fc, (B, 1)), np.tile(ns, (B, 1))
+
+
+def run_tree(args, ws, rank, dev):
+    """B=256 draft trees of 8 nodes (three candidates under the root, two of
+    them with chains of two more: up to 3 accepted drafts), V=151936, bf16
+    logits N(0, sd 2) with each node's token raised in its parent's row by
+    14 / 12 / 11 (first / second / third candidate branch), rejection sampling
+    at T=1.  Two step tensors of 622 MB alternate (each far above L2); the
+    timed region replays a CUDA graph of the verify launches ten times.  Algorithmic
+    bytes per launch: the rows the walk reads, sum over sequences of
+    (accepted depth + 1) x V x 2."""
+    import torch
+
+    import oracle
+    import sam_drafting_verification_gb300 as ss
+    B, V, T = 256, workloads.V_LARGE, 1.0
+    N = len(TREE_PARENT)
+    reps = min(max(args.steps, 1), 1000)
+    hbm, peak_kind = _peaks()
+    rng = np.random.default_rng(1007 + 7919 * rank)
+    pool = []
+    trees = []
+    for i in range(2):
+        tok, fc, ns = tree_arrays(rng, B, V)
+        g = torch.Generator(device=dev)
+        g.manual_seed(5000 + 31 * i + 7919 * rank)
+        lg = torch.empty((B, N, V), dtype=torch.bfloat16, device=dev)
+        for b0 in range(0, B, 64):
+            x = torch.empty((min(64, B - b0), N, V), dtype=torch.float32, device=dev).normal_(0.0, 2.0, generator=g)
+            lg[b0:b0 + 64] = x.to(torch.bfloat16)
+        par = np.array(TREE_PARENT[1:])
+        bb = np.repeat(np.arange(B), N - 1)
+        rows = np.tile(par, B)
+        cols = tok[:, 1:].reshape(-1)
+        boost = torch.tensor(np.tile(TREE_BOOST[1:], B), dtype=torch.float32, device=dev)
+        idx = tuple(torch.as_tensor(a, device=dev) for a in (bb, rows, cols))
+        lg.index_put_(idx, (lg[idx].float() + boost).to(torch.bfloat16))
+        pool.append(lg)
+        trees.append(tuple(torch.as_tensor(a, device=dev) for a in (tok, fc, ns)))
+    wsv = ss.verify_workspace(B, N - 1, V, dev)
+    res = ss.spec_verify_tree(pool[0], *trees[0], temperature=T, seed=11, step=0, workspace=wsv)
+    for w in range(max(args.warmup, 3)):
+        ss.spec_verify_tree(pool[w % 2], *trees[w % 2], temperature=T, seed=11, step=w, workspace=wsv, out=res)
+    torch.cuda.synchronize()
+    cs = torch.cuda.Stream(device=dev)
+    graph = torch.cuda.CUDAGraph()
+    cs.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(graph, stream=cs):
+            for r in range(reps):
+                ss.spec_verify_tree(pool[r % 2], *trees[r % 2], temperature=T, seed=11, step=r,
+                                    workspace=wsv, out=res)
+    torch.cuda.synchronize()
+    clk = ClockSampler(dev.index or 0)
+    clk.start()
+    _barrier(ws)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(cs):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(cs)
+        for _ in range(TREE_REPLAYS):
+            graph.replay()
+        e1.record(cs)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    clocks = clk.stop()
+    ms = _max_over_ranks(e0.elapsed_time(e1), ws, dev) / (reps * TREE_REPLAYS)
+    # the rows each launch read: the same calls again, untimed (same coins)
+    rows_read = 0
+    acc = np.zeros(N, np.int64)
+    st_bad = 0
+    for r in range(reps):
+        o = ss.spec_verify_tree(pool[r % 2], *trees[r % 2], temperature=T, seed=11, step=r, workspace=wsv,
+                                out=res)
+        L = o["accept_len"].cpu().numpy()
+        st_bad += int((o["status"].cpu().numpy() != 0).sum())
+        rows_read += int((L + 1).sum())
+        acc += np.bincount(L, minlength=N)[:N]
+    alg = rows_read / reps * V * 2
+    ach = alg / (ms / 1e3) / 1e9
+    cpu = None
+    if rank == 0:
+        # the oracle on a sample: 32 sequences of both step tensors, 2 steps each
+        nb = 32
+        host = [p[:nb].float().cpu().numpy() for p in pool]
+        htree = [tuple(a[:nb].cpu().numpy() for a in t) for t in trees]
+        t0 = time.perf_counter()
+        agree = 0
+        for r in range(4):
+            ob = oracle.tree_verify(host[r % 2], *htree[r % 2], temperature=T, seed=11, step=r)
+            gb = ss.spec_verify_tree(pool[r % 2], *trees[r % 2], temperature=T, seed=11, step=r,
+                                     workspace=wsv, out=res)
+            agree += int((gb["accept_len"][:nb].cpu().numpy() == ob["accept_len"]).sum())
+        el = time.perf_counter() - t0
+        cpu = {"value": round(4 * nb / el, 2), "unit": "seq-steps/s", "cores": 1, "kind": "oracle",
+               "sample": f"{nb} sequences x 4 steps of the same trees and coins ({el:.2f} s, fp64); "
+                         f"{agree}/{4 * nb} accepted depths equal to the device's"}
+    line = {"metric": "tree-draft verification seq-steps/s", "value": round(B / (ms / 1e3), 1),
+            "unit": "seq-steps/s", "n_gpus": ws, "steps": reps, "warmup": max(args.warmup, 3),
+            "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "tree_b256", "B": B, "N": N, "V": V, "temperature": T,
+                       "tree_parent": list(TREE_PARENT), "l2": "two 622 MB step tensors alternate",
+                       "timing": f"CUDA graph of {reps} verify launches, replayed {TREE_REPLAYS} times"},
+            "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(ach / hbm, 4), "traffic": None, "peak_source": peak_kind},
+            "cpu_baseline": cpu, "gpu_launches": reps * TREE_REPLAYS, "clocks": clocks,
+            "breakdown": {"mean_accept": round(float((acc * np.arange(N)).sum() / acc.sum()), 4),
+                          "accept_hist": acc.tolist(), "rows_per_seq": round(rows_read / reps / B, 4),
+                          "bad_status": st_bad}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
 # verification sweep at B=1024
 # --------------------------------------------------------------------------
 
@@ -907,7 +1053,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="rs_bf16_b64", choices=["rs_bf16_b64", "sweep_b1024", "long_rollout_b256",
-                                                      "rollout_toy_b64", "static_match_b256"])
+                                                      "rollout_toy_b64", "static_match_b256", "tree_b256"])
     ap.add_argument("--point", default="", help="sweep_b1024 only: one point 'K,f32|bf16,greedy|T=1|greedy-full-read'")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":

@@ -346,11 +346,12 @@ def select_drafts(dynamic, static, l_bias: int):
 
 
 def spec_verify_tree(target, tok, first_child, next_sibling, temperature: float = 0.0,
-                     seed: int = 0, step: int = 0, debug: bool = False, workspace=None):
+                     seed: int = 0, step: int = 0, debug: bool = False, workspace=None, out=None):
     """Verify a draft tree per sequence: target [B, N, V] (row n: the token
     after node n's path), tok / first_child / next_sibling int32 [B, N].
     Returns a dict of CUDA tensors: accept_len, out_token, path [B, N], emit
-    [B, N], emit_len, status (+ row_m, row_z, row_arg, res_mass)."""
+    [B, N], emit_len, status (+ row_m, row_z, row_arg, res_mass).  `out`: the
+    dict of an earlier call with the same sizes, written again in place."""
     lib = _b.lib()
     if target.dim() != 3:
         raise ValueError("target must be [B, N, V]")
@@ -363,8 +364,14 @@ def spec_verify_tree(target, tok, first_child, next_sibling, temperature: float 
         _req(t, torch.int32, nm, (B, N))
     dev = target.device
     z = lambda *s: torch.empty(s, dtype=torch.int32, device=dev)  # noqa: E731
-    res = {"accept_len": z(B), "out_token": z(B), "path": z(B, N), "emit": z(B, N),
-           "emit_len": z(B), "status": z(B)}
+    if out is not None:
+        res = out
+        for k, shp in (("accept_len", (B,)), ("out_token", (B,)), ("path", (B, N)), ("emit", (B, N)),
+                       ("emit_len", (B,)), ("status", (B,))):
+            _req(res[k], torch.int32, "out[" + k + "]", shp)
+    else:
+        res = {"accept_len": z(B), "out_token": z(B), "path": z(B, N), "emit": z(B, N),
+               "emit_len": z(B), "status": z(B)}
     dbg = None
     if debug:
         for k in ("row_m", "row_z"):

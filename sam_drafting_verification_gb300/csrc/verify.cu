@@ -432,10 +432,48 @@ __device__ __forceinline__ float4 reduce_greedy(const Slice<TT, DT>& s, int w, i
 // per-record exponential enters the row's masses.  The element with tile index
 // `excl` (the row's draft token, added back exactly by the control warp) is
 // left out.  An all -inf slice gives {-inf, -inf, 0, 0}; NaN gives NaNs.
+// Sum of 2^(x * cT - R) over a lane's elements of a full slice: pairs of
+// elements through packed FFMA / FADD, one MUFU ex2 each.  MASK: elements
+// whose bit i * VEC + k is set in xm count zero.
+template <int TT, int DT, bool DRAFT_ARRAY, bool MASK>
+__device__ __forceinline__ float packed_exp_sum(const Slice<TT, DT>& s, float cT, float R, uint64_t xm) {
+  using C = Cfg<TT, DT>;
+  const uint64_t c2 = pk2(cT, cT), nr2 = pk2(-R, -R);
+  uint64_t part[C::VPL];
+#pragma unroll
+  for (int i = 0; i < C::VPL; ++i) {
+    uint64_t v[C::VEC / 2];
+#pragma unroll
+    for (int p = 0; p < C::VEC / 2; ++p) {
+      const uint64_t y = fma2(DRAFT_ARRAY ? s.d[i].pair(p) : s.t[i].pair(p), c2, nr2);
+      float y0, y1;
+      upk2(y, y0, y1);
+      float e0 = ex2_approx(y0), e1 = ex2_approx(y1);
+      if (MASK) {
+        if ((xm >> (i * C::VEC + 2 * p)) & 1ull) e0 = 0.f;
+        if ((xm >> (i * C::VEC + 2 * p + 1)) & 1ull) e1 = 0.f;
+      }
+      v[p] = pk2(e0, e1);
+    }
+#pragma unroll
+    for (int h = C::VEC / 4; h >= 1; h >>= 1)
+#pragma unroll
+      for (int p = 0; p < h; ++p) v[p] = add2(v[p], v[p + h]);
+    part[i] = v[0];
+  }
+  // pairwise over the lane's VPL vectors (VPL need not be a power of two)
+#pragma unroll
+  for (int h = 1; h < C::VPL; h <<= 1)
+#pragma unroll
+    for (int i = 0; i + h < C::VPL; i += 2 * h) part[i] = add2(part[i], part[i + h]);
+  float lo, hi;
+  upk2(part[0], lo, hi);
+  return lo + hi;
+}
+
 template <int TT, int DT, bool FULL, bool DRAFT_ARRAY, bool MULTI = false>
 __device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, int lane, int nel,
-                                                 float cT, int excl, const int32_t* exl = nullptr,
-                                                 int nex = 0, int elem0 = 0) {
+                                                 float cT, int excl, uint64_t xm = 0) {
   using C = Cfg<TT, DT>;
   const float NEG_INF = -__int_as_float(0x7f800000);
   const float QNAN = __int_as_float(0x7fc00000);
@@ -445,41 +483,15 @@ __device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, 
   if (m == NEG_INF) return make_float4(NEG_INF, NEG_INF, 0.f, 0.f);
   const float R = ceilf(m * cT);
   float z;
-  bool has_excl = excl >= w * C::SL && excl < (w + 1) * C::SL;
-  if (MULTI) {  // a list of vocabulary ids (a tree node's children)
-    for (int k = 0; k < nex; ++k) {
-      const int o = exl[k] - elem0;
-      has_excl |= o >= w * C::SL && o < (w + 1) * C::SL;
-    }
-  }
+  // `excl`: one element left out (slice-relative id, or -1).  MULTI: xm marks
+  // the lane's elements left out (bit i * VEC + k), e.g. a tree node's
+  // children; the warp takes the masked path if any lane has one
+  const bool single = excl >= w * C::SL && excl < (w + 1) * C::SL;
+  const bool has_excl = single || (MULTI && __any_sync(kFullMask, xm != 0));
   if (FULL && !has_excl) {
-    // pairs of elements through packed FFMA / FADD, one MUFU ex2 each
-    const uint64_t c2 = pk2(cT, cT), nr2 = pk2(-R, -R);
-    uint64_t part[C::VPL];
-#pragma unroll
-    for (int i = 0; i < C::VPL; ++i) {
-      uint64_t v[C::VEC / 2];
-#pragma unroll
-      for (int p = 0; p < C::VEC / 2; ++p) {
-        const uint64_t y = fma2(DRAFT_ARRAY ? s.d[i].pair(p) : s.t[i].pair(p), c2, nr2);
-        float y0, y1;
-        upk2(y, y0, y1);
-        v[p] = pk2(ex2_approx(y0), ex2_approx(y1));
-      }
-#pragma unroll
-      for (int h = C::VEC / 4; h >= 1; h >>= 1)
-#pragma unroll
-        for (int p = 0; p < h; ++p) v[p] = add2(v[p], v[p + h]);
-      part[i] = v[0];
-    }
-    // pairwise over the lane's VPL vectors (VPL need not be a power of two)
-#pragma unroll
-    for (int h = 1; h < C::VPL; h <<= 1)
-#pragma unroll
-      for (int i = 0; i + h < C::VPL; i += 2 * h) part[i] = add2(part[i], part[i + h]);
-    float lo, hi;
-    upk2(part[0], lo, hi);
-    z = lo + hi;
+    z = packed_exp_sum<TT, DT, DRAFT_ARRAY, false>(s, cT, R, 0);
+  } else if (MULTI && FULL && !single) {
+    z = packed_exp_sum<TT, DT, DRAFT_ARRAY, true>(s, cT, R, xm);
   } else {
     float part[C::VPL];
 #pragma unroll
@@ -490,8 +502,7 @@ __device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, 
       for (int k = 0; k < C::VEC; ++k) {
         const float x = DRAFT_ARRAY ? s.d[i].at(k) : s.t[i].at(k);
         bool keep = e + k < nel && e + k != excl;
-        if (MULTI && keep && has_excl)
-          for (int q = 0; q < nex; ++q) keep &= exl[q] - elem0 != e + k;
+        if (MULTI) keep &= !((xm >> (i * C::VEC + k)) & 1ull);
         v[k] = keep ? ex2_approx(fmaf(x, cT, -R)) : 0.f;
       }
 #pragma unroll
@@ -890,16 +901,18 @@ struct Control {
   __device__ int slice_scan(int b, int L, int c, int w, float t, int smode, int excl, float RL,
                             float RG, float invZ, float invZg, const int32_t* exl = nullptr,
                             int nex = 0) {
-    auto out_of = [&](int v) {  // left out of the residual: `excl` or a listed id
-      if (v == excl) return true;
-      for (int q = 0; q < nex; ++q)
-        if (exl[q] == v) return true;
-      return false;
-    };
+    static_assert(EPL <= 64, "one mask bit per element of a lane");
     Slice<TT, DT> sl;
     const bool with_draft = DT >= 0 && smode == 1;
     const int n = load_slice_lanes<TT, DT>(sl, P, b, L, c, w, with_draft, lane);
     const int s0 = c * C::E_TILE + w * C::SL;
+    // the tokens left out of the residual (`excl` and the listed ids), as bits
+    // of the lane holding them (lane-major: lane l holds l * EPL .. + EPL - 1)
+    uint64_t xl = 0;
+    for (int q = -1; q < nex; ++q) {
+      const int o = (q < 0 ? excl : exl[q]) - s0;
+      if (o >= 0 && o < n && o / EPL == lane) xl |= 1ull << (o % EPL);
+    }
     float tot = 0.f;
     int last_pos = -1;
 #pragma unroll
@@ -908,7 +921,7 @@ struct Control {
       for (int k = 0; k < C::VEC; ++k) {
         const int e = lane * EPL + i * C::VEC + k;
         float r = 0.f;
-        if (e < n && !out_of(s0 + e))
+        if (e < n && !((xl >> (i * C::VEC + k)) & 1ull))
           r = resid_val(sl.t[i].at(k), DT >= 0 ? sl.d[i].at(k) : 0.f, smode, RL, RG, invZ, invZg, P.cT);
         tot += r;
         if (r > 0.f) last_pos = s0 + e;
@@ -922,6 +935,7 @@ struct Control {
       return last_pos >= 0 ? last_pos : s0;
     }
     const int ls = __ffs(hit) - 1;
+    const uint64_t xls = __shfl_sync(kFullMask, xl, ls);
     float tl = t - __shfl_sync(kFullMask, incl - tot, ls);
     // lane ls's elements, 32 at a time in ascending order: element q to lane
     // q % 32 of round q / 32
@@ -946,7 +960,7 @@ struct Control {
       const int q = rd * 32 + lane;
       const int e = ls * EPL + q;
       float re = 0.f;
-      if (q < EPL && e < n && !out_of(s0 + e))
+      if (q < EPL && e < n && !((xls >> q) & 1ull))
         re = resid_val(xe, ge, smode, RL, RG, invZ, invZg, P.cT);
       const float inc2 = warp_incl_scan_f(re, lane);
       const unsigned h2 = __ballot_sync(kFullMask, q < EPL && inc2 > tl);
@@ -1311,13 +1325,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
           // one-hot drafts: the row's draft token is left out of the sums
           // (tile index, or -1), so the residual of a rejection is exact
           const int ex = (DT < 0 && tg.dtok >= 0) ? tg.dtok - tg.elem0 : -1;
-          if (TREE) {  // a tree node's children: a list of ids left out
+          if (TREE) {
+            // a tree node's children are left out of the sums: the lane
+            // holding one keeps its logit and marks it in its mask
+            static_assert(C::VPL * C::VEC <= 64, "one mask bit per element of a lane");
             const int nex = S.nex;
-            r.a = full ? reduce_softmax<TT, DT, true, false, true>(sl, warp, lane, tg.nel, P.cT, -1,
-                                                                   S.ex, nex, tg.elem0)
-                       : reduce_softmax<TT, DT, false, false, true>(sl, warp, lane, tg.nel, P.cT, -1,
-                                                                    S.ex, nex, tg.elem0);
-            // the lanes holding the children keep their logits
+            uint64_t xm = 0;
             for (int k = 0; k < nex; ++k) {
               const int o = S.ex[k] - tg.elem0 - warp * C::SL;
               if (o >= 0 && o < C::SL && o + warp * C::SL < tg.nel) {
@@ -1331,9 +1344,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
                     for (int q = 0; q < C::VEC; ++q)
                       if (i == ii && q == kk) x = sl.t[i].at(q);
                   S.cx[k] = x;
+                  xm |= 1ull << (ii * C::VEC + kk);
                 }
               }
             }
+            r.a = full ? reduce_softmax<TT, DT, true, false, true>(sl, warp, lane, tg.nel, P.cT, -1, xm)
+                       : reduce_softmax<TT, DT, false, false, true>(sl, warp, lane, tg.nel, P.cT, -1, xm);
           } else {
           r.a = full ? reduce_softmax<TT, DT, true, false>(sl, warp, lane, tg.nel, P.cT, ex)
                      : reduce_softmax<TT, DT, false, false>(sl, warp, lane, tg.nel, P.cT, ex);
