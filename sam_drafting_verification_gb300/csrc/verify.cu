@@ -211,22 +211,28 @@ __device__ __forceinline__ DF df_mul_f(DF x, float a) {
 __device__ __forceinline__ float df_f(DF x) { return x.hi + x.lo; }
 // Warp sum of lane values in [0, 2^11) as a float pair: each value splits
 // into a multiple of 2^-10 (rounding by the 1.5 * 2^13 constant) and the
-// remainder (|r| <= 2^-11).  The multiples of 2^-10 sum exactly in fp32 (the
-// total stays below 2^11, 21 bits), the remainders in plain fp32 (error about
-// 2^-30 absolute), both halves of a packed pair per butterfly step.
+// remainder (|r| <= 2^-11).  The multiples sum exactly as integers (below
+// 2^26); the remainders sum as integers in units of 2^-34 (each rounded by at
+// most 2^-35, so the total is off by at most 2^-30).  One warp reduction
+// instruction each.
 __device__ __forceinline__ DF split_warp_sum(float v) {
   const float hi = (v + 12288.f) - 12288.f;
-  uint64_t p = pk2(hi, v - hi);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const uint64_t q = ((uint64_t)__shfl_xor_sync(kFullMask, (uint32_t)(p >> 32), o) << 32) |
-                       __shfl_xor_sync(kFullMask, (uint32_t)p, o);
-    p = add2(p, q);
-  }
-  float sh, sl;
-  upk2(p, sh, sl);
-  const float s = sh + sl;  // |sl| is far below |sh| unless both are tiny
-  return {s, sl - (s - sh)};
+  const float r = v - hi;
+  const uint32_t k1 = __reduce_add_sync(kFullMask, (uint32_t)(hi * 1024.f));
+  const int32_t k2 = (int32_t)__reduce_add_sync(kFullMask, (uint32_t)__float2int_rn(r * 0x1p34f));
+  const float a = __uint2float_rz(k1);               // k1 with its lowest bits cut (k1 < 2^26)
+  const float ea = (float)(k1 - __float2uint_rz(a));  // the cut bits, exact
+  const float ah = a * 0x1p-10f;
+  const float small = fmaf(ea, 0x1p-10f, (float)k2 * 0x1p-34f);
+  const float sum = ah + small;
+  const float bb = sum - ah;
+  return {sum, (ah - (sum - bb)) + (small - bb)};
+}
+// NaN-propagating warp maximum in one warp reduction instruction
+__device__ __forceinline__ float warp_max_nan(float v) {
+  float m;
+  asm("redux.sync.max.NaN.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(v));
+  return m;
 }
 __device__ __forceinline__ DF df_warp_sum(DF a) {
 #pragma unroll
@@ -420,18 +426,11 @@ __device__ __forceinline__ float lane_max(const Slice<TT, DT>& s, int w, int lan
 // maximum is found afterwards, in the one warp slice that holds it.
 template <int TT, int DT, bool FULL>
 __device__ __forceinline__ float4 reduce_greedy(const Slice<TT, DT>& s, int w, int lane, int nel) {
-  const float ml = lane_max<TT, DT, FULL, false>(s, w, lane, nel);
-  if (__any_sync(kFullMask, ml != ml)) return make_float4(0.f, 0.f, 1.f, 0.f);
-  return make_float4(warp_max(ml), 0.f, 0.f, 0.f);
+  const float m = warp_max_nan(lane_max<TT, DT, FULL, false>(s, w, lane, nel));
+  if (m != m) return make_float4(0.f, 0.f, 1.f, 0.f);
+  return make_float4(m, 0.f, 0.f, 0.f);
 }
 
-// Softmax record of one array of the slice: {m, R, z, 0} with m the slice
-// max, R = ceil(fl(m * cT)) an integer exponent reference and z the fp32 sum
-// of 2^fl(x * cT - R) over the slice (every term in (0, ~1]).
-// Records of one row combine by exact power-of-two scaling 2^(R - max R), so no
-// per-record exponential enters the row's masses.  The element with tile index
-// `excl` (the row's draft token, added back exactly by the control warp) is
-// left out.  An all -inf slice gives {-inf, -inf, 0, 0}; NaN gives NaNs.
 // Sum of 2^(x * cT - R) over a lane's elements of a full slice: pairs of
 // elements through packed FFMA / FADD, one MUFU ex2 each.  MASK: elements
 // whose bit i * VEC + k is set in xm count zero.
@@ -471,15 +470,21 @@ __device__ __forceinline__ float packed_exp_sum(const Slice<TT, DT>& s, float cT
   return lo + hi;
 }
 
+// Softmax record of one array of the slice: {m, R, z, 0} with m the slice
+// max, R = ceil(fl(m * cT)) an integer exponent reference and z the fp32 sum
+// of 2^fl(x * cT - R) over the slice (every term in (0, ~1]).
+// Records of one row combine by exact power-of-two scaling 2^(R - max R), so no
+// per-record exponential enters the row's masses.  The element with tile index
+// `excl` (the row's draft token, added back exactly by the control warp) is
+// left out.  An all -inf slice gives {-inf, -inf, 0, 0}; NaN gives NaNs.
 template <int TT, int DT, bool FULL, bool DRAFT_ARRAY, bool MULTI = false>
 __device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, int lane, int nel,
                                                  float cT, int excl, uint64_t xm = 0) {
   using C = Cfg<TT, DT>;
   const float NEG_INF = -__int_as_float(0x7f800000);
   const float QNAN = __int_as_float(0x7fc00000);
-  const float ml = lane_max<TT, DT, FULL, DRAFT_ARRAY>(s, w, lane, nel);
-  if (__any_sync(kFullMask, ml != ml)) return make_float4(QNAN, QNAN, QNAN, QNAN);
-  const float m = warp_max(ml);
+  const float m = warp_max_nan(lane_max<TT, DT, FULL, DRAFT_ARRAY>(s, w, lane, nel));
+  if (m != m) return make_float4(QNAN, QNAN, QNAN, QNAN);
   if (m == NEG_INF) return make_float4(NEG_INF, NEG_INF, 0.f, 0.f);
   const float R = ceilf(m * cT);
   float z;
