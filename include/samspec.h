@@ -241,10 +241,11 @@ int sam_dump_sequence(sam_batch* batch, int32_t b, int32_t* h_scalars, int32_t* 
  * 256-byte aligned, zeroed once with spec_verify_workspace_init before first
  * use and not shared by two calls in flight.  Logits pointers must be 16-byte
  * aligned.  Limits: 1 <= B <= 2^24, 0 <= K <= 32, and V at most 48 tiles of
- * the kernel's 48 KB staging buffer: 589824 (fp32 target, greedy or one-hot
- * drafts), 1179648 (bf16 target, greedy or one-hot), 589824 (bf16 target and
- * bf16 draft logits), 294912 (any other pair with draft logits); larger V
- * returns SAMSPEC_ESIZE.  Asynchronous; one kernel launch. */
+ * the kernel's 48 KB staging buffer with one-hot drafts (or greedy), 32 tiles
+ * with draft logits (T > 0): 589824 (fp32 target, greedy or one-hot drafts),
+ * 1179648 (bf16 target, greedy or one-hot), 393216 (bf16 target and bf16 draft
+ * logits), 196608 (any other pair with draft logits); larger V returns
+ * SAMSPEC_ESIZE.  Asynchronous; one kernel launch. */
 typedef struct spec_verify_debug {
   float* row_m;
   float* row_z;

@@ -18,15 +18,15 @@
 // a streaming reduction bound by HBM.  Each CTA owns whole sequences and walks
 // their accept chains itself, so rows after the first rejection are never read
 // and no inter-CTA merge is needed:
-//   warp 16 (producer) issues 1-D bulk copies (cp.async.bulk, the TMA engine)
+//   warp 24 (producer) issues 1-D bulk copies (cp.async.bulk, the TMA engine)
 //       of 48 KB vocab tiles of the rows its sequence slots ask for into a
 //       ring of shared-memory stages, completion counted on mbarriers;
-//   warps 0-15 (consumers) each take a 1/16 slice ("warp slice") of every
+//   warps 0-23 (consumers) each take a 1/24 slice ("warp slice") of every
 //       tile into registers, release the stage, and reduce the slice to a
 //       record -- its max, an integer exponent reference R and the sum of
 //       2^(l log2(e)/T - R), or (greedy) its max -- then count the tile done;
-//   warps 17-19 (control, one per sequence slot) claim sequences from a
-//       global counter and merge each tile's 16 records as soon as they land
+//   warps 25-27 (control, one per sequence slot) claim sequences from a
+//       global counter and merge each tile's 24 records as soon as they land
 //       (running max, reference and compensated float-pair mass, and the mass
 //       before each tile), so the row's statistics are ready when its last
 //       tile is; they draw the Philox coins, decide accept/reject and post the
@@ -35,9 +35,11 @@
 //       u' * sum(r), and only that 3-6 KB slice is read again (from L2) and
 //       scanned in ascending token order.
 // Three slots keep the producer streaming while control warps decide.  Tiles
-// of 48 KB (4 ring stages) measured faster than 24-32 KB tiles with 16-28
-// consumer warps: the per-tile work of producer, consumers and control is
-// amortised over more logits.  Every wait is bounded by a global-timer
+// of 48 KB (4 ring stages) measured faster than 24-32 KB tiles: the per-tile
+// work of producer, consumers and control is amortised over more logits.
+// 24 consumer warps measured faster than 8, 12 or 16: a warp's per-tile chain
+// (load, max, exponentials, warp reductions, record) is latency-bound, and
+// more warps overlap more chains.  Every wait is bounded by a global-timer
 // deadline; a CTA that runs out of time marks its sequences
 // SAMSPEC_ST_TIMEOUT, lets its copies in flight land and exits.
 
@@ -54,7 +56,7 @@
 namespace samspec {
 namespace {
 
-constexpr int kCW = 16;              // consumer warps
+constexpr int kCW = 24;              // consumer warps
 constexpr int kProdWarp = kCW;       // producer warp
 constexpr int kCtrlWarp = kCW + 1;   // first control warp (one per slot)
 constexpr int kSlots = 3;
@@ -63,6 +65,7 @@ constexpr int kStageBytes = 49152;
 constexpr int kMaxStages = 6;
 constexpr int kMinStages = 3;
 constexpr int kMaxChunks = 48;
+constexpr int kMaxChunksDraft = 32;  // with draft logits: both arrays' records must fit
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 
 enum Kind : int32_t { kStats = 0, kResid = 1, kExit = 3 };
@@ -119,9 +122,15 @@ struct Slot {
 
 // One warp-slice record: softmax statistics of the target (a) and draft (b)
 // rows; greedy {max, 0, NaN seen, 0} in a; residual pass {rh, rl, 0, 0} in a.
+// In shared memory the a parts of all slots, tiles and slices come first, then
+// (with draft logits only) the b parts in the same order.
 struct Rec {
   float4 a, b;
 };
+template <int DT>
+__host__ __device__ constexpr size_t rec_bytes_of(int NC) {
+  return (size_t)(DT >= 0 ? 2 : 1) * kSlots * NC * kCW * sizeof(float4);
+}
 
 struct Smem {
   Slot slot[kSlots];
@@ -617,9 +626,8 @@ __device__ __forceinline__ float warp_incl_scan_f(float v, int lane) {
 }
 
 // ---- control warp ------------------------------------------------------------
-// Records of a slot are indexed r = c * kCW + w (tile c, warp slice w); the
-// merges below give lane l the records r = q * 32 + l, so one pass of the
-// warp covers two tiles (lanes 0-15: tile 2q, lanes 16-31: tile 2q + 1).
+// Records of a slot are indexed r = c * kCW + w (tile c, warp slice w); a
+// merge of tile c gives lane w < kCW the record (c, w).
 
 // 2^(x * log2(e)/T - R) for one token (R an integer-valued reference),
 // accurate to a few fp32 ulp: log2(e)/T is carried as cT + cTl, x * cT and
@@ -641,7 +649,7 @@ struct Control {
   static constexpr int EPL = C::SL / 32;  // slice elements per lane (lane-major loads)
   const VParams& P;
   Smem& sm;
-  const Rec* rec;     // [kSlots][NC][kCW]
+  const float4* rec;  // a parts [kSlots][NC][kCW], then (draft logits) b parts
   int lane, si;
   bool more;
   int32_t tok;        // lane t holds draft token t of the slot's sequence
@@ -650,13 +658,19 @@ struct Control {
   int32_t pathv;      // trees: the node accepted at depth `lane`
   float ua, ur;       // coins of the row in flight (drawn while it streams)
 
-  __device__ Control(const VParams& p, Smem& s, const Rec* r, int l, int slot)
+  __device__ Control(const VParams& p, Smem& s, const float4* r, int l, int slot)
       : P(p), sm(s), rec(r), lane(l), si(slot), more(true), tok(-1), par_(-1), pathv(-1),
         ua(0.f), ur(0.f) {
     reset_row();
   }
 
-  __device__ const Rec& R(int c, int w) const { return rec[((size_t)si * P.NC + c) * kCW + w]; }
+  __device__ Rec R(int c, int w) const {
+    const size_t i = ((size_t)si * P.NC + c) * kCW + w;
+    Rec r;
+    r.a = rec[i];
+    r.b = DT >= 0 ? rec[(size_t)kSlots * P.NC * kCW + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    return r;
+  }
 
   // Outputs of sequence b, written by the warp's lanes in parallel (lane t
   // holds draft token t).
@@ -1262,8 +1276,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
   extern __shared__ __align__(1024) unsigned char dsm[];
   Smem& sm = *reinterpret_cast<Smem*>(dsm);
   const size_t rec_off = (sizeof(Smem) + 15) & ~(size_t)15;
-  Rec* rec = reinterpret_cast<Rec*>(dsm + rec_off);
-  const size_t rec_bytes = (size_t)kSlots * P.NC * kCW * sizeof(Rec);
+  float4* rec = reinterpret_cast<float4*>(dsm + rec_off);
+  const size_t rec_bytes = rec_bytes_of<DT>(P.NC);
   unsigned char* stages = dsm + ((rec_off + rec_bytes + 1023) & ~(size_t)1023);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1391,7 +1405,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       }
       __syncwarp();
       if (lane == 0) {
-        rec[((size_t)tg.slot * P.NC + tg.chunk) * kCW + warp] = r;
+        const size_t ri = ((size_t)tg.slot * P.NC + tg.chunk) * kCW + warp;
+        rec[ri] = r.a;
+        if (DT >= 0) rec[(size_t)kSlots * P.NC * kCW + ri] = r.b;
         __threadfence_block();  // the record (and captured logits) before the count
         atomicAdd(&sm.tile_cnt[tg.slot][tg.chunk], 1);
       }
@@ -1647,10 +1663,10 @@ int launch(const VParams& P0, cudaStream_t stream) {
   using C = Cfg<TT, DT>;
   VParams P = P0;
   P.NC = (P.V + C::E_TILE - 1) / C::E_TILE;
-  if (P.NC > kMaxChunks) return SAMSPEC_ESIZE;
+  if (P.NC > (DT >= 0 ? kMaxChunksDraft : kMaxChunks)) return SAMSPEC_ESIZE;
   const size_t rec_off = (sizeof(Smem) + 15) & ~(size_t)15;
   const size_t head =
-      (rec_off + (size_t)kSlots * P.NC * kCW * sizeof(Rec) + 1023) & ~(size_t)1023;
+      (rec_off + rec_bytes_of<DT>(P.NC) + 1023) & ~(size_t)1023;
   // Device properties and the kernel's shared-memory opt-in are set up once per
   // device, so that later launches make no runtime calls besides the launch
   // itself (safe inside stream capture).

@@ -46,8 +46,8 @@ def test_spec_verify_rejects_bad_arguments_on_the_host():
     lib = bd.lib()
     p = ctypes.c_void_p(4096)
 
-    def call(dtype=bd.F32, K=1, V=1000, T=1.0, ws_bytes=256, target=p):
-        return lib.spec_verify(target, dtype, None, bd.F32, p, None, 1, K, V, T, 0, 0, p, p,
+    def call(dtype=bd.F32, K=1, V=1000, T=1.0, ws_bytes=256, target=p, draft_logits=None):
+        return lib.spec_verify(target, dtype, draft_logits, bd.F32, p, None, 1, K, V, T, 0, 0, p, p,
                                None, None, None, None, p, ws_bytes, None)
 
     assert call(target=None) == bd.EINVAL
@@ -60,6 +60,8 @@ def test_spec_verify_rejects_bad_arguments_on_the_host():
     assert call(dtype=bd.F32, V=48 * 12288 + 1) == bd.ESIZE
     assert call(dtype=bd.BF16, V=48 * 24576 + 1) == bd.ESIZE
     assert call(dtype=bd.F32, V=48 * 12288 + 1, T=0.0) == bd.ESIZE
+    # with draft logits (T > 0) both rows share a tile: 32 tiles of 6144 fp32 pairs
+    assert call(dtype=bd.F32, V=32 * 6144 + 1, draft_logits=p, ws_bytes=1 << 20) == bd.ESIZE
 
 
 def test_binding_refuses_missing_library(tmp_path):

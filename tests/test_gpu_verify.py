@@ -219,10 +219,10 @@ def test_sweep_b1024_full_size_sampled(ss, cuda_device, K, dtype, T):
 
 @pytest.mark.parametrize("dtype,V,with_draft", [(torch.bfloat16, 48 * 24576, False),
                                                 (torch.float32, 48 * 12288, False),
-                                                (torch.float32, 48 * 6144, True)])
+                                                (torch.float32, 32 * 6144, True)])
 def test_largest_vocabulary(ss, cuda_device, dtype, V, with_draft):
-    """The largest V each logits layout accepts (48 staging tiles), and one
-    more, which is refused."""
+    """The largest V each logits layout accepts (48 staging tiles with one-hot
+    drafts, 32 with draft logits), and one more, which is refused."""
     B, K = 2, 1
     rng = np.random.default_rng(V)
     logits = workloads.gaussian_logits(rng, (B, K + 1, V), 2.0)
