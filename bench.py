@@ -46,10 +46,12 @@ POOL = 16
 # workload, with the SHA-256 of verify.cu they were taken on: a changed kernel
 # reports null until it is captured again.
 VERIFY_TRAFFIC = {
-    "rs_bf16_b64": {"bytes": 19559680.0, "profile": "profiles/verify_kernel_rs_bf16_b64.md",
-                    "verify_cu_sha256": "e7722dba7a26453048c49c37f170930c98753fd413f9114ecbd6cb579588155e"},
-    "long_rollout_b256": {"bytes": 79019000.0, "profile": "profiles/launches_long_rollout_b256.md",
-                          "verify_cu_sha256": "e7722dba7a26453048c49c37f170930c98753fd413f9114ecbd6cb579588155e"},
+    "rs_bf16_b64": {"bytes": 19538176.0, "profile": "profiles/verify_kernel_rs_bf16_b64.md",
+                    "verify_cu_sha256": "778ec0f73d36e26a115e4014cd7f73ef066ed28ae8ee284e5a580bd44b24fd9e"},
+    "long_rollout_b256": {"bytes": 78979955.0, "profile": "profiles/launches_long_rollout_b256.md",
+                          "verify_cu_sha256": "778ec0f73d36e26a115e4014cd7f73ef066ed28ae8ee284e5a580bd44b24fd9e"},
+    "tree_b256": {"bytes": 162061312.0, "profile": "profiles/verify_kernel_tree_b256.md",
+                  "verify_cu_sha256": "778ec0f73d36e26a115e4014cd7f73ef066ed28ae8ee284e5a580bd44b24fd9e"},
 }
 
 
@@ -946,7 +948,8 @@ def run_tree(args, ws, rank, dev):
                        "tree_parent": list(TREE_PARENT), "l2": "two 622 MB step tensors alternate",
                        "timing": f"CUDA graph of {reps} verify launches, replayed {TREE_REPLAYS} times"},
             "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
-                         "frac": round(ach / hbm, 4), "traffic": None, "peak_source": peak_kind},
+                         "frac": round(ach / hbm, 4), "traffic": _verify_traffic("tree_b256"),
+                         "peak_source": peak_kind, "algorithmic_bytes_per_launch": round(alg, 1)},
             "cpu_baseline": cpu, "gpu_launches": reps * TREE_REPLAYS, "clocks": clocks,
             "breakdown": {"mean_accept": round(float((acc * np.arange(N)).sum() / acc.sum()), 4),
                           "accept_hist": acc.tolist(), "rows_per_seq": round(rows_read / reps / B, 4),
