@@ -11,6 +11,9 @@ Function map (each function cites the page passage it follows in oracle.cpp):
   Sam                 -- dynamic suffix automaton, extend + draft + dump
   verify(...)         -- greedy / rejection-sampling verification of a batch
   cdf_interval(...)   -- normalised CDF interval of one token of a residual
+  tree_verify(...)    -- draft-tree verification (sibling-wise cumulative test)
+  truncate_row(...)   -- per-request temperature / top-k / top-p distribution
+  verify_sampling(...) -- verification against those truncated distributions
   philox4x32_10 / uniforms -- the counter-based generator behind the coins
 """
 from __future__ import annotations
@@ -33,6 +36,7 @@ OK = 0
 ETOKEN = 3
 BADROW = 5
 BADDRAFT = 6
+BADPARAM = 8
 
 
 def build(force: bool = False) -> str:
@@ -75,6 +79,11 @@ def _load():
         lib.over_tree_node_info.argtypes = [P, I32, D, P, I32, I32, P, P]
         lib.over_tree_verify.restype = I32
         lib.over_tree_verify.argtypes = [P, P, P, P, I32, I32, I32, D, U64, U64, P, P, P, P, P, P]
+        lib.over_verify_sampling.restype = I32
+        lib.over_verify_sampling.argtypes = [P, P, P, I32, I32, I32, P, P, P, U64, U64,
+                                             P, P, P, P, P, P, P, P]
+        lib.over_truncate_row.restype = I32
+        lib.over_truncate_row.argtypes = [P, I32, D, I32, D, P, P]
         _lib = lib
         return lib
 
@@ -268,3 +277,47 @@ def tree_node_info(row, temperature, children, token):
     lib.over_tree_node_info(_ptr(r), r.size, float(temperature), _ptr(ch), len(ch), int(token),
                             _ptr(acc), _ptr(lhm))
     return acc[:len(ch)], float(lhm[0]), float(lhm[1]), float(lhm[2])
+
+
+def truncate_row(row, temperature, top_k=0, top_p=1.0):
+    """One row's distribution under per-request sampling parameters:
+    softmax(l / T), top-k renormalisation, top-p renormalisation.  Returns
+    (p' [V] float64, tau) with tau the smallest kept logit; None for a bad
+    row."""
+    lib = _load()
+    r = np.ascontiguousarray(row, dtype=np.float32).reshape(-1)
+    pp = np.empty(r.size, np.float64)
+    tau = np.empty(1, np.float32)
+    rc = lib.over_truncate_row(_ptr(r), r.size, float(temperature), int(top_k), float(top_p),
+                               _ptr(pp), _ptr(tau))
+    return None if rc != 0 else (pp, float(tau[0]))
+
+
+def verify_sampling(target, draft, draft_len=None, temperature=None, top_k=None, top_p=None,
+                    seed=0, step=0):
+    """Verify one-hot drafts against per-request truncated distributions.
+    target [B, K+1, V]; draft [B, K]; temperature, top_k, top_p: [B] (top_k
+    <= 0 or >= V and top_p >= 1 disable truncation).  Returns accept_len,
+    out_token, status, p_d / u_acc / tau [B, K+1], u_res, res_mass."""
+    lib = _load()
+    t = np.ascontiguousarray(target, dtype=np.float32)
+    B, K1, V = t.shape
+    K = K1 - 1
+    d = np.ascontiguousarray(np.asarray(draft, dtype=np.int32).reshape(B, K))
+    dl = None if draft_len is None else np.ascontiguousarray(draft_len, dtype=np.int32)
+    T = np.ascontiguousarray(np.broadcast_to(1.0 if temperature is None else temperature, (B,)),
+                             dtype=np.float64)
+    tk = np.ascontiguousarray(np.broadcast_to(0 if top_k is None else top_k, (B,)), dtype=np.int32)
+    tp = np.ascontiguousarray(np.broadcast_to(1.0 if top_p is None else top_p, (B,)), dtype=np.float64)
+    out = {k: np.empty(B, np.int32) for k in ("accept_len", "out_token", "status")}
+    for k in ("p_d", "u_acc"):
+        out[k] = np.empty((B, K1), np.float64)
+    out["tau"] = np.empty((B, K1), np.float32)
+    out["u_res"] = np.empty(B, np.float64)
+    out["res_mass"] = np.empty(B, np.float64)
+    lib.over_verify_sampling(_ptr(t), _ptr(d), _ptr(dl), B, K, V, _ptr(T), _ptr(tk), _ptr(tp),
+                             int(seed) & (2**64 - 1), int(step) & (2**64 - 1),
+                             _ptr(out["accept_len"]), _ptr(out["out_token"]), _ptr(out["status"]),
+                             _ptr(out["p_d"]), _ptr(out["u_acc"]), _ptr(out["u_res"]),
+                             _ptr(out["res_mass"]), _ptr(out["tau"]))
+    return out

@@ -40,6 +40,7 @@
 //   CDF walked in ascending token id with a strict ">" test; if rounding leaves
 //   the whole CDF <= t, the largest token with positive residual is taken.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -224,6 +225,7 @@ enum : int32_t {
   OV_OK = 0,
   OV_BADROW = 5,    // NaN, +inf (T > 0) or an all -inf row
   OV_BADDRAFT = 6,  // draft length outside [0, K] or draft token outside [0, V)
+  OV_BADPARAM = 8,  // sampling parameters: T not > 0 and finite, or top_p not > 0
 };
 
 // Greedy: argmax with the lowest index on ties.  Returns false for a row the
@@ -262,6 +264,65 @@ bool softmax_row(const float* row, int32_t V, double T, std::vector<double>& p,
   for (int32_t v = 0; v < V; ++v) p[v] /= z;
   *m_out = m;
   *z_out = z;
+  return true;
+}
+
+// Per-request truncation of one target distribution, in the order of [P3]
+// SGLang 的实现 (_sampling_verify): p = softmax(l / T), then top-k
+// renormalisation, then top-p renormalisation.
+//   top-k (0 < k < V): keep the tokens whose logit is at least the k-th
+//     largest logit, counted with multiplicity (every token tied at that value
+//     is kept); k <= 0 or k >= V keeps everything;
+//   top-p (top_p < 1): of the tokens left, keep those whose renormalised mass
+//     strictly above their own probability is below top_p, i.e. the smallest
+//     top set whose mass reaches top_p, with ties at its edge kept;
+//     top_p >= 1 keeps everything;
+// then p' = p restricted to the kept set and renormalised.  Both steps keep a
+// set {v : l_v >= tau} (T > 0 keeps the logits' order), and tau, the smallest
+// kept logit, is returned.  False for a bad row (as softmax_row).
+bool truncate_row(const float* row, int32_t V, double T, int32_t top_k, double top_p,
+                  std::vector<double>& p, float* tau_out) {
+  double m, z;
+  if (!softmax_row(row, V, T, p, &m, &z)) return false;
+  std::vector<char> keep(V, 1);
+  if (top_k > 0 && top_k < V) {
+    std::vector<float> sorted(row, row + V);
+    std::sort(sorted.begin(), sorted.end(), [](float a, float b) { return a > b; });
+    const float tk = sorted[top_k - 1];
+    double s = 0.0;
+    for (int32_t v = 0; v < V; ++v) {
+      keep[v] = row[v] >= tk;
+      if (keep[v]) s += p[v];
+    }
+    for (int32_t v = 0; v < V; ++v) p[v] = keep[v] ? p[v] / s : 0.0;
+  }
+  if (top_p < 1.0) {
+    // kept tokens by descending logit; a group of equal logits shares the
+    // mass strictly above it
+    std::vector<int32_t> idx;
+    for (int32_t v = 0; v < V; ++v)
+      if (keep[v]) idx.push_back(v);
+    std::sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) { return row[a] > row[b]; });
+    double above = 0.0;
+    size_t i = 0;
+    while (i < idx.size()) {
+      size_t g = i;
+      double gm = 0.0;
+      while (g < idx.size() && row[idx[g]] == row[idx[i]]) gm += p[idx[g++]];
+      const bool k = above < top_p;
+      for (size_t t = i; t < g; ++t) keep[idx[t]] = k;
+      above += gm;
+      i = g;
+    }
+    double s = 0.0;
+    for (int32_t v = 0; v < V; ++v)
+      if (keep[v]) s += p[v];
+    for (int32_t v = 0; v < V; ++v) p[v] = keep[v] ? p[v] / s : 0.0;
+  }
+  float tau = std::numeric_limits<float>::infinity();
+  for (int32_t v = 0; v < V; ++v)
+    if (keep[v] && row[v] < tau) tau = row[v];
+  *tau_out = tau;
   return true;
 }
 
@@ -674,4 +735,89 @@ void over_cdf_interval(const float* trow, const float* drow, int32_t V, double T
   lo_hi_mass[2] = mass;
 }
 
+// Verification with per-request sampling parameters ([P3] SGLang 的实现,
+// _sampling_verify: per-request temperature, top_k and top_p applied to the
+// target probabilities before the drafts are tested; [P3] N-gram 的特殊情况:
+// one-hot drafts).  Row j's distribution is p'_j = truncate_row(row j, T_b,
+// k_b, top_p_b); d_j is accepted iff u_j <= p'_j(d_j); the final token is
+// drawn by u' from max(0, p'_L - 1[d_L]) after a rejection, or from p'_L for
+// the bonus row (the same residual rule as over_verify).
+// temp, top_k, top_p: [B].  Outputs as over_verify, plus tau [B, K+1] (the
+// smallest kept logit of each evaluated row, NaN otherwise; may be NULL).
+int32_t over_verify_sampling(const float* target, const int32_t* draft, const int32_t* draft_len,
+                             int32_t B, int32_t K, int32_t V, const double* temp,
+                             const int32_t* top_k, const double* top_p, uint64_t seed,
+                             uint64_t step, int32_t* accept_len, int32_t* out_token,
+                             int32_t* status, double* p_d, double* u_acc, double* u_res,
+                             double* res_mass, float* tau) {
+  const double nan = std::numeric_limits<double>::quiet_NaN();
+  std::vector<double> p, r;
+  for (int32_t b = 0; b < B; ++b) {
+    const float* trow0 = target + (int64_t)b * (K + 1) * V;
+    const int32_t* d = draft + (int64_t)b * K;
+    for (int32_t j = 0; j <= K; ++j) {
+      const int64_t o = (int64_t)b * (K + 1) + j;
+      if (p_d) p_d[o] = nan;
+      if (u_acc) u_acc[o] = nan;
+      if (tau) tau[o] = std::numeric_limits<float>::quiet_NaN();
+    }
+    if (u_res) u_res[b] = nan;
+    if (res_mass) res_mass[b] = nan;
+    accept_len[b] = -1;
+    out_token[b] = -1;
+    const int32_t nb = draft_len ? draft_len[b] : K;
+    bool bad = nb < 0 || nb > K;
+    for (int32_t j = 0; !bad && j < nb; ++j) bad = d[j] < 0 || d[j] >= V;
+    if (bad) { status[b] = OV_BADDRAFT; continue; }
+    const double T = temp[b], tp = top_p[b];
+    if (!(T > 0.0) || T == std::numeric_limits<double>::infinity() || !(tp > 0.0)) {
+      status[b] = OV_BADPARAM;
+      continue;
+    }
+    status[b] = OV_OK;
+    int32_t L = nb;
+    bool ok = true;
+    for (int32_t j = 0; j <= nb; ++j) {
+      const int64_t o = (int64_t)b * (K + 1) + j;
+      float tj;
+      if (!truncate_row(trow0 + (int64_t)j * V, V, T, top_k[b], tp, p, &tj)) { ok = false; break; }
+      if (tau) tau[o] = tj;
+      if (j == nb) { L = nb; break; }
+      double ua, ur;
+      uniforms(seed, step, b, j, &ua, &ur);
+      if (p_d) p_d[o] = p[d[j]];
+      if (u_acc) u_acc[o] = ua;
+      if (!(ua <= p[d[j]])) { L = j; break; }
+    }
+    if (!ok) { status[b] = OV_BADROW; continue; }
+    const bool rejected = L < nb;
+    residual(p, nullptr, rejected ? d[L] : -1, r);
+    double mass = 0.0;
+    for (int32_t v = 0; v < V; ++v) mass += r[v];
+    if (!(mass > 0.0)) {  // only the rejected token was kept: sample p' itself
+      r = p;
+      mass = 0.0;
+      for (int32_t v = 0; v < V; ++v) mass += r[v];
+    }
+    double ua, ur;
+    uniforms(seed, step, b, L, &ua, &ur);
+    accept_len[b] = L;
+    out_token[b] = sample_cdf(r, ur * mass);
+    if (u_res) u_res[b] = ur;
+    if (res_mass) res_mass[b] = mass;
+  }
+  return 0;
+}
+
+// One row through truncate_row: p' into p_out [V], the smallest kept logit
+// into tau_out[0]; returns 0, or OV_BADROW.
+int32_t over_truncate_row(const float* row, int32_t V, double T, int32_t top_k, double top_p,
+                          double* p_out, float* tau_out) {
+  std::vector<double> p;
+  if (!truncate_row(row, V, T, top_k, top_p, p, tau_out)) return OV_BADROW;
+  for (int32_t v = 0; v < V; ++v) p_out[v] = p[v];
+  return 0;
+}
+
 }  // extern "C"
+
