@@ -66,6 +66,8 @@ typedef struct CUstream_st* samspec_stream_t;
                                /* token outside [0, V); extend: n_new outside  */
                                /* [0, max_new]                                 */
 #define SAMSPEC_ST_TIMEOUT 7   /* verify: a bounded on-chip wait ran out       */
+#define SAMSPEC_ST_BADPARAM 8  /* verify with sampling parameters: temperature  */
+                               /* not > 0 and finite, or top_p not > 0         */
 
 /* logits element types */
 #define SAMSPEC_F32 0
@@ -321,6 +323,49 @@ int spec_verify_tree(const void* d_target, int32_t target_dtype, const int32_t* 
                      int32_t* d_emit, int32_t* d_emit_len, int32_t* d_status,
                      const spec_verify_debug* dbg, void* d_workspace, size_t ws_bytes,
                      samspec_stream_t stream);
+
+/* The cut of each target row under per-request sampling parameters ([P3]
+ * SGLang 的实现, _sampling_verify: p = softmax(l / T), then top-k
+ * renormalisation, then top-p renormalisation).  For row (b, r) of d_target
+ * [B, R, V] (1 <= R <= 33, V <= 2^22, 16-byte aligned) with d_temperature[b],
+ * d_top_k[b], d_top_p[b] ([B] each, device):
+ *   top-k (0 < k < V) keeps the tokens whose logit is at least the k-th
+ *   largest (ties kept); top-p (top_p < 1) keeps, of those, the ones whose
+ *   mass strictly above them is below top_p of their total (the smallest top
+ *   set reaching top_p, ties kept).  Both keep {v : l_v >= tau};
+ * d_tau [B, R] receives tau (fp32): -inf when nothing is cut (k <= 0 or
+ * k >= V, and top_p >= 1) or the row has NaN, +inf or only -inf logits; NaN
+ * when T is not > 0 and finite or top_p is not > 0.  Masses are taken in
+ * fixed point (units of 2^-42 of the row maximum's term), so a top-p cut whose
+ * mass lies within about 1e-7 of top_p may fall on either side.  One launch;
+ * asynchronous. */
+int spec_sampling_cut(const void* d_target, int32_t target_dtype, int32_t B, int32_t R, int32_t V,
+                      const float* d_temperature, const int32_t* d_top_k, const float* d_top_p,
+                      float* d_tau, samspec_stream_t stream);
+
+/* Verification with per-request sampling parameters ([P3] SGLang 的实现: the
+ * target probabilities are softmax(l / T_b), top-k renormalised, then top-p
+ * renormalised before the drafts are tested; [P3] N-gram 的特殊情况: one-hot
+ * drafts).  As spec_verify at T > 0 with one-hot drafts, except that
+ * sequence b uses d_temperature[b] and row j of it the truncated
+ * distribution p'_j (spec_sampling_cut's tau; logits below it have
+ * probability 0): d_j is accepted iff u_j <= p'_j(d_j); the final token is
+ * drawn from p'_L without d_L after a rejection, or from p'_L for the bonus
+ * row.  d_temperature, d_top_p: [B] fp32; d_top_k: [B] int32 (<= 0 or >= V:
+ * no top-k; top_p >= 1: no top-p).  A sequence with T_b not > 0 and finite
+ * or top_p_b not > 0 gets ST_BADPARAM.  Workspace:
+ * spec_verify_sampling_workspace_bytes(B, K, V) bytes, 256-byte aligned, its
+ * first 256 bytes zeroed once by spec_verify_workspace_init; the rest holds
+ * the cuts of the call.  dbg as spec_verify (row_z sums the kept tokens; q_d
+ * is not written).  V limits as spec_verify's one-hot case.  Two launches. */
+size_t spec_verify_sampling_workspace_bytes(int32_t B, int32_t K, int32_t V);
+int spec_verify_sampling(const void* d_target, int32_t target_dtype, const int32_t* d_draft,
+                         const int32_t* d_draft_len, int32_t B, int32_t K, int32_t V,
+                         const float* d_temperature, const int32_t* d_top_k,
+                         const float* d_top_p, uint64_t seed, uint64_t step,
+                         int32_t* d_accept_len, int32_t* d_out_token, int32_t* d_emit,
+                         int32_t* d_emit_len, int32_t* d_status, const spec_verify_debug* dbg,
+                         void* d_workspace, size_t ws_bytes, samspec_stream_t stream);
 
 /* One decode step of model-free speculative decoding ([P1] §1.1: verify, then
  * update each sequence's D-SAM with the verified tokens, then draft; [P1]

@@ -249,11 +249,13 @@ class SamBatch:
 _ws_cache = {}
 
 
-def verify_workspace(B: int, K: int, V: int, device=None):
-    """A zero-initialised verification workspace, cached per (device, stream)."""
+def verify_workspace(B: int, K: int, V: int, device=None, sampling: bool = False):
+    """A zero-initialised verification workspace, cached per (device, stream);
+    sampling=True sizes it for spec_verify_sampling."""
     lib = _b.lib()
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
-    need = int(lib.spec_verify_workspace_bytes(B, K, V))
+    need = int(lib.spec_verify_sampling_workspace_bytes(B, K, V) if sampling
+               else lib.spec_verify_workspace_bytes(B, K, V))
     key = (dev.index, torch.cuda.current_stream(dev).cuda_stream)
     ws = _ws_cache.get(key)
     if ws is None or ws.numel() < need:
@@ -387,6 +389,91 @@ def spec_verify_tree(target, tok, first_child, next_sibling, temperature: float 
                                   _ptr(res["path"]), _ptr(res["emit"]), _ptr(res["emit_len"]),
                                   _ptr(res["status"]), ctypes.byref(dbg) if dbg is not None else None,
                                   _ptr(ws), ws.numel(), _stream(dev)), "spec_verify_tree")
+    return res
+
+
+def _per_seq(x, B, dtype, dev, name):
+    """A [B] device tensor of `dtype` from a scalar or a [B] tensor."""
+    if isinstance(x, torch.Tensor):
+        return _req(x, dtype, name, (B,))
+    return torch.full((B,), x, dtype=dtype, device=dev)
+
+
+def sampling_cut(target, temperature, top_k, top_p):
+    """The cut of each row [B, R, V] under per-sequence (temperature, top_k,
+    top_p) ([B] tensors or scalars): [B, R] float32 tau, the smallest kept
+    logit (-inf: nothing cut; NaN: bad parameters)."""
+    lib = _b.lib()
+    if target.dim() != 3:
+        raise ValueError("target must be [B, R, V]")
+    B, R, V = (int(x) for x in target.shape)
+    dt = {torch.float32: F32, torch.bfloat16: BF16}.get(target.dtype)
+    if dt is None:
+        raise TypeError("target must be float32 or bfloat16")
+    _req(target, target.dtype, "target")
+    dev = target.device
+    T = _per_seq(temperature, B, torch.float32, dev, "temperature")
+    k = _per_seq(top_k, B, torch.int32, dev, "top_k")
+    p = _per_seq(top_p, B, torch.float32, dev, "top_p")
+    tau = torch.empty((B, R), dtype=torch.float32, device=dev)
+    _b.check(lib.spec_sampling_cut(_ptr(target), dt, B, R, V, _ptr(T), _ptr(k), _ptr(p), _ptr(tau),
+                                   _stream(dev)), "spec_sampling_cut")
+    return tau
+
+
+def spec_verify_sampling(target, draft, draft_len=None, temperature=1.0, top_k=0, top_p=1.0,
+                         seed: int = 0, step: int = 0, out=None, emit: bool = False,
+                         debug: bool = False, workspace=None):
+    """Verify one-hot drafts [B, K] against target logits [B, K+1, V] with
+    per-sequence temperature, top_k and top_p ([B] tensors or scalars).
+    Returns a dict of CUDA tensors: accept_len, out_token, status (+ emit,
+    emit_len, and the debug rows row_m, row_z, p_d, row_arg, res_mass)."""
+    lib = _b.lib()
+    if target.dim() != 3:
+        raise ValueError("target must be [B, K+1, V]")
+    B, K1, V = (int(x) for x in target.shape)
+    K = K1 - 1
+    dt = {torch.float32: F32, torch.bfloat16: BF16}.get(target.dtype)
+    if dt is None:
+        raise TypeError("target must be float32 or bfloat16")
+    _req(target, target.dtype, "target")
+    _req(draft, torch.int32, "draft", (B, K))
+    if draft_len is not None:
+        _req(draft_len, torch.int32, "draft_len", (B,))
+    dev = target.device
+    T = _per_seq(temperature, B, torch.float32, dev, "temperature")
+    k = _per_seq(top_k, B, torch.int32, dev, "top_k")
+    p = _per_seq(top_p, B, torch.float32, dev, "top_p")
+    res = out if out is not None else {}
+
+    def need(key, shape, dtype=torch.int32, fill=None):
+        if key not in res:
+            res[key] = (torch.empty(shape, dtype=dtype, device=dev) if fill is None
+                        else torch.full(shape, fill, dtype=dtype, device=dev))
+
+    need("accept_len", (B,))
+    need("out_token", (B,))
+    need("status", (B,))
+    if emit:
+        need("emit", (B, K1))
+        need("emit_len", (B,))
+    dbg = None
+    if debug:
+        for key in ("row_m", "row_z", "p_d"):
+            need(key, (B, K1), torch.float32, float("nan"))
+        need("row_arg", (B, K1), torch.int32, -1)
+        need("res_mass", (B,), torch.float32, float("nan"))
+        dbg = _b.VerifyDebug(res["row_m"].data_ptr(), res["row_z"].data_ptr(), res["p_d"].data_ptr(), 0,
+                             res["row_arg"].data_ptr(), res["res_mass"].data_ptr())
+    ws = workspace if workspace is not None else verify_workspace(B, K, V, dev, sampling=True)
+    rc = lib.spec_verify_sampling(_ptr(target), dt, _ptr(draft) if K > 0 else None, _ptr(draft_len),
+                                  B, K, V, _ptr(T), _ptr(k), _ptr(p), int(seed) & (2**64 - 1),
+                                  int(step) & (2**64 - 1), _ptr(res["accept_len"]),
+                                  _ptr(res["out_token"]), _ptr(res.get("emit")),
+                                  _ptr(res.get("emit_len")), _ptr(res["status"]),
+                                  ctypes.byref(dbg) if dbg is not None else None,
+                                  _ptr(ws), ws.numel(), _stream(dev))
+    _b.check(rc, "spec_verify_sampling")
     return res
 
 

@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libsamspec.so")
 
 # host-side return codes and per-sequence status words (include/samspec.h)
 OK, EINVAL, ESIZE, EDTYPE, ECUDA, EALIGN = 0, -1, -2, -3, -4, -5
-ST_OK, ST_CAPACITY, ST_HASHFULL, ST_TOKEN, ST_LOOPCAP, ST_BADROW, ST_BADDRAFT, ST_TIMEOUT = range(8)
+ST_OK, ST_CAPACITY, ST_HASHFULL, ST_TOKEN, ST_LOOPCAP, ST_BADROW, ST_BADDRAFT, ST_TIMEOUT, ST_BADPARAM = range(9)
 F32, BF16 = 0, 1
 
 EXPORTED = [
@@ -25,7 +25,8 @@ EXPORTED = [
     "sam_dump_sequence",
     "spec_verify_workspace_bytes", "spec_verify_workspace_init", "spec_verify", "spec_uniforms",
     "spec_verify_noalloc", "sam_step_rows", "sam_spec_step", "ssam_match", "sam_select_drafts",
-    "spec_verify_tree",
+    "spec_verify_tree", "spec_sampling_cut", "spec_verify_sampling_workspace_bytes",
+    "spec_verify_sampling",
 ]
 
 
@@ -70,6 +71,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "spec_verify_tree": (ctypes.c_int, [P, I32, P, P, P, I32, I32, I32, F, U64, U64, P, P, P,
                                             P, P, P, ctypes.POINTER(VerifyDebug), P, SZ, P]),
         "sam_select_drafts": (ctypes.c_int, [I32, I32, P, P, P, P, P, P, I32, P, P, P, P]),
+        "spec_sampling_cut": (ctypes.c_int, [P, I32, I32, I32, I32, P, P, P, P, P]),
+        "spec_verify_sampling_workspace_bytes": (SZ, [I32, I32, I32]),
+        "spec_verify_sampling": (ctypes.c_int, [P, I32, P, P, I32, I32, I32, P, P, P, U64, U64,
+                                                P, P, P, P, P, ctypes.POINTER(VerifyDebug), P, SZ, P]),
         "sam_spec_step": (ctypes.c_int, [P, P, I32, P, I32, P, P, I32, I32, F, U64, U64,
                                          P, P, P, P, P, ctypes.POINTER(VerifyDebug),
                                          I32, P, P, P, P, P, SZ, P]),

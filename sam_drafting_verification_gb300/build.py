@@ -13,7 +13,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 OBJ_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libsamspec.so")
-SOURCES = ["abi.cu", "sam.cu", "verify.cu"]
+SOURCES = ["abi.cu", "sam.cu", "sampling.cu", "verify.cu"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 

@@ -51,6 +51,7 @@
 
 #include "common.cuh"
 #include "philox.cuh"
+#include "sampling.cuh"
 #include "samspec.h"
 
 namespace samspec {
@@ -95,6 +96,10 @@ struct VParams {
   const int32_t* tfc;   // [B, N] first child, -1: none
   const int32_t* tns;   // [B, N] next sibling, -1: none
   int32_t* path;        // [B, N] accepted node indices, -1 after
+  // per-request sampling parameters: temperature [B] and the cut of each row
+  // [B, K+1] (logits below it are left out; -inf: none; NaN: bad parameters)
+  const float* seqT;
+  const float* tau;
 };
 
 struct Tag {
@@ -118,6 +123,9 @@ struct Slot {
   int32_t depth, nex;
   int32_t ex[32];
   float cx[32];
+  // per-request sampling: the sequence's temperature, log2(e)/T as cT + cTl,
+  // and the cut of the row in flight
+  float T, cT, cTl, tau;
 };
 
 // One warp-slice record: softmax statistics of the target (a) and draft (b)
@@ -443,8 +451,9 @@ __device__ __forceinline__ float4 reduce_greedy(const Slice<TT, DT>& s, int w, i
 // Sum of 2^(x * cT - R) over a lane's elements of a full slice: pairs of
 // elements through packed FFMA / FADD, one MUFU ex2 each.  MASK: elements
 // whose bit i * VEC + k is set in xm count zero.
-template <int TT, int DT, bool DRAFT_ARRAY, bool MASK>
-__device__ __forceinline__ float packed_exp_sum(const Slice<TT, DT>& s, float cT, float R, uint64_t xm) {
+template <int TT, int DT, bool DRAFT_ARRAY, bool MASK, bool THR = false>
+__device__ __forceinline__ float packed_exp_sum(const Slice<TT, DT>& s, float cT, float R, uint64_t xm,
+                                                float tau = 0.f) {
   using C = Cfg<TT, DT>;
   const uint64_t c2 = pk2(cT, cT), nr2 = pk2(-R, -R);
   uint64_t part[C::VPL];
@@ -453,10 +462,17 @@ __device__ __forceinline__ float packed_exp_sum(const Slice<TT, DT>& s, float cT
     uint64_t v[C::VEC / 2];
 #pragma unroll
     for (int p = 0; p < C::VEC / 2; ++p) {
-      const uint64_t y = fma2(DRAFT_ARRAY ? s.d[i].pair(p) : s.t[i].pair(p), c2, nr2);
+      const uint64_t xv = DRAFT_ARRAY ? s.d[i].pair(p) : s.t[i].pair(p);
+      const uint64_t y = fma2(xv, c2, nr2);
       float y0, y1;
       upk2(y, y0, y1);
       float e0 = ex2_approx(y0), e1 = ex2_approx(y1);
+      if (THR) {  // logits below the cut count zero
+        float x0, x1;
+        upk2(xv, x0, x1);
+        if (!(x0 >= tau)) e0 = 0.f;
+        if (!(x1 >= tau)) e1 = 0.f;
+      }
       if (MASK) {
         if ((xm >> (i * C::VEC + 2 * p)) & 1ull) e0 = 0.f;
         if ((xm >> (i * C::VEC + 2 * p + 1)) & 1ull) e1 = 0.f;
@@ -486,9 +502,10 @@ __device__ __forceinline__ float packed_exp_sum(const Slice<TT, DT>& s, float cT
 // per-record exponential enters the row's masses.  The element with tile index
 // `excl` (the row's draft token, added back exactly by the control warp) is
 // left out.  An all -inf slice gives {-inf, -inf, 0, 0}; NaN gives NaNs.
-template <int TT, int DT, bool FULL, bool DRAFT_ARRAY, bool MULTI = false>
+template <int TT, int DT, bool FULL, bool DRAFT_ARRAY, bool MULTI = false, bool THR = false>
 __device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, int lane, int nel,
-                                                 float cT, int excl, uint64_t xm = 0) {
+                                                 float cT, int excl, uint64_t xm = 0,
+                                                 float tau = 0.f) {
   using C = Cfg<TT, DT>;
   const float NEG_INF = -__int_as_float(0x7f800000);
   const float QNAN = __int_as_float(0x7fc00000);
@@ -502,8 +519,12 @@ __device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, 
   // children; the warp takes the masked path if any lane has one
   const bool single = excl >= w * C::SL && excl < (w + 1) * C::SL;
   const bool has_excl = single || (MULTI && __any_sync(kFullMask, xm != 0));
-  if (FULL && !has_excl) {
+  // THR: logits below tau (a per-request cut) are left out too
+  const bool cut = THR && tau > NEG_INF;
+  if (FULL && !has_excl && !cut) {
     z = packed_exp_sum<TT, DT, DRAFT_ARRAY, false>(s, cT, R, 0);
+  } else if (THR && FULL && !has_excl) {
+    z = packed_exp_sum<TT, DT, DRAFT_ARRAY, false, true>(s, cT, R, 0, tau);
   } else if (MULTI && FULL && !single) {
     z = packed_exp_sum<TT, DT, DRAFT_ARRAY, true>(s, cT, R, xm);
   } else {
@@ -517,6 +538,7 @@ __device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, 
         const float x = DRAFT_ARRAY ? s.d[i].at(k) : s.t[i].at(k);
         bool keep = e + k < nel && e + k != excl;
         if (MULTI) keep &= !((xm >> (i * C::VEC + k)) & 1ull);
+        if (THR) keep &= x >= tau;
         v[k] = keep ? ex2_approx(fmaf(x, cT, -R)) : 0.f;
       }
 #pragma unroll
@@ -643,7 +665,7 @@ __device__ __forceinline__ float exp_ref(float x, float R, float cT, float cTl) 
   return ldexpf(exp2f((s - si) + (e1 + e2)), (int)fmaxf(si, -300.f));
 }
 
-template <int TT, int DT, bool GREEDY, bool TREE = false>
+template <int TT, int DT, bool GREEDY, bool TREE = false, bool SAMP = false>
 struct Control {
   using C = Cfg<TT, DT>;
   static constexpr int EPL = C::SL / 32;  // slice elements per lane (lane-major loads)
@@ -663,6 +685,16 @@ struct Control {
         ua(0.f), ur(0.f) {
     reset_row();
   }
+
+  // temperature terms and the row's cut: per sequence with sampling
+  // parameters, else the launch's
+  __device__ float cT_() const { return SAMP ? sm.slot[si].cT : P.cT; }
+  __device__ float cTl_() const { return SAMP ? sm.slot[si].cTl : P.cTl; }
+  __device__ float T_() const { return SAMP ? sm.slot[si].T : P.T; }
+  __device__ double cTd_() const {
+    return SAMP ? (double)sm.slot[si].cT + (double)sm.slot[si].cTl : P.cTd;
+  }
+  __device__ float tau_() const { return SAMP ? sm.slot[si].tau : -__int_as_float(0x7f800000); }
 
   __device__ Rec R(int c, int w) const {
     const size_t i = ((size_t)si * P.NC + c) * kCW + w;
@@ -727,6 +759,7 @@ struct Control {
       S.kind = kind;
       S.j = j;
       S.dtok = (kind == kStats && j < S.nb) ? dt : -1;
+      if (SAMP) S.tau = P.tau[(size_t)S.b * (P.K + 1) + j];
       __threadfence_block();
       vstore(&S.state, kReady);
     }
@@ -805,6 +838,23 @@ struct Control {
         finish((int)b, -1, -1, SAMSPEC_ST_BADDRAFT);
         continue;
       }
+      if (SAMP) {
+        // the sequence's temperature, and every row's cut: a temperature not
+        // > 0 and finite, or a NaN cut (top_p not > 0), refuses the sequence
+        const float Tb = P.seqT[b];
+        const float tj = lane <= P.K ? P.tau[(size_t)b * (P.K + 1) + lane] : 0.f;
+        const bool nan_cut = __any_sync(kFullMask, tj != tj);
+        if (nan_cut || !(Tb > 0.f) || !(Tb < __int_as_float(0x7f800000))) {
+          finish((int)b, -1, -1, SAMSPEC_ST_BADPARAM);
+          continue;
+        }
+        if (lane == 0) {
+          const double cTd = 1.4426950408889634 / (double)Tb;
+          S.T = Tb;
+          S.cT = (float)cTd;
+          S.cTl = (float)(cTd - (double)S.cT);
+        }
+      }
       if (lane == 0) {
         S.b = (int32_t)b;
         S.nb = nb;
@@ -856,14 +906,17 @@ struct Control {
     if (lane == 0) sm.pre[si][c][f] = make_float4(R_.sum.hi, R_.sum.lo, R_.ref, 0.f);
     R_.nan |= nan;
     R_.mx = fmaxf(R_.mx, mc);
-    if (Rc != NEG_INF && (t.hi != 0.f || t.lo != 0.f)) {
-      if (Rc > R_.ref) {  // a larger reference: rescale what was summed so far
-        if (R_.ref != NEG_INF) {
-          const int sc = (int)(R_.ref - Rc);
-          R_.sum = DF{ldexpf(R_.sum.hi, sc), ldexpf(R_.sum.lo, sc)};
-        }
-        R_.ref = Rc;
+    // the reference follows every finite tile reference, with or without mass
+    // (a row whose only token left in the sums is the draft itself keeps a
+    // finite reference for the draft's exponential)
+    if (Rc != NEG_INF && Rc > R_.ref) {  // a larger reference: rescale what was summed so far
+      if (R_.ref != NEG_INF) {
+        const int sc = (int)(R_.ref - Rc);
+        R_.sum = DF{ldexpf(R_.sum.hi, sc), ldexpf(R_.sum.lo, sc)};
       }
+      R_.ref = Rc;
+    }
+    if (Rc != NEG_INF && (t.hi != 0.f || t.lo != 0.f)) {
       const int sc = (int)(Rc - R_.ref);
       R_.sum = df_add(R_.sum, DF{ldexpf(t.hi, sc), ldexpf(t.lo, sc)});
     }
@@ -941,7 +994,8 @@ struct Control {
         const int e = lane * EPL + i * C::VEC + k;
         float r = 0.f;
         if (e < n && !((xl >> (i * C::VEC + k)) & 1ull))
-          r = resid_val(sl.t[i].at(k), DT >= 0 ? sl.d[i].at(k) : 0.f, smode, RL, RG, invZ, invZg, P.cT);
+          r = resid_val(sl.t[i].at(k), DT >= 0 ? sl.d[i].at(k) : 0.f, smode, RL, RG, invZ, invZg, cT_());
+        if (SAMP && !(sl.t[i].at(k) >= tau_())) r = 0.f;
         tot += r;
         if (r > 0.f) last_pos = s0 + e;
       }
@@ -980,7 +1034,8 @@ struct Control {
       const int e = ls * EPL + q;
       float re = 0.f;
       if (q < EPL && e < n && !((xls >> q) & 1ull))
-        re = resid_val(xe, ge, smode, RL, RG, invZ, invZg, P.cT);
+        re = resid_val(xe, ge, smode, RL, RG, invZ, invZg, cT_());
+      if (SAMP && !(xe >= tau_())) re = 0.f;
       const float inc2 = warp_incl_scan_f(re, lane);
       const unsigned h2 = __ballot_sync(kFullMask, q < EPL && inc2 > tl);
       if (h2) return s0 + ls * EPL + rd * 32 + __ffs(h2) - 1;
@@ -1057,14 +1112,14 @@ struct Control {
     const float lm = run[0].nan ? __int_as_float(0x7fc00000) : run[0].mx;
     const float LM = run[0].ref;
     const DF zx = run[0].sum;
-    const float ek = lane < nex ? exp_ref(S.cx[lane], LM, P.cT, P.cTl) : 0.f;
+    const float ek = lane < nex ? exp_ref(S.cx[lane], LM, cT_(), cTl_()) : 0.f;
     const DF ztd = df_add(zx, df_warp_sum(DF{ek, 0.f}));
     const float zt = df_f(ztd);
     const bool bad = !(lm > NEG_INF) || isinf(lm) || !isfinite(zt) || !(zt > 0.f);
     if (lane == 0) {
-      if (P.dbg.row_m) P.dbg.row_m[ro] = lm / P.T;
+      if (P.dbg.row_m) P.dbg.row_m[ro] = lm / T_();
       if (P.dbg.row_z)
-        P.dbg.row_z[ro] = (float)(((double)ztd.hi + (double)ztd.lo) * exp2((double)LM - (double)lm * P.cTd));
+        P.dbg.row_z[ro] = (float)(((double)ztd.hi + (double)ztd.lo) * exp2((double)LM - (double)lm * cTd_()));
     }
     if (bad) {
       finish(b, -1, -1, SAMSPEC_ST_BADROW);
@@ -1172,21 +1227,22 @@ struct Control {
         gm = run[1].nan ? __int_as_float(0x7fc00000) : run[1].mx;
         GM = run[1].ref;
         zg = run[1].sum;
-        egd = exp_ref(S.gd, GM, P.cT, P.cTl);  // draft model's d, units 2^GM
+        egd = exp_ref(S.gd, GM, cT_(), cTl_());  // draft model's d, units 2^GM
       }
       // one-hot: the sums leave d out (zx), so that a rejection's residual is
       // exact; with draft logits they hold every token
-      const float ed = d >= 0 ? exp_ref(S.xd, LM, P.cT, P.cTl) : 0.f;
+      // (a draft below the row's cut has probability 0)
+      const float ed = (d >= 0 && (!SAMP || S.xd >= S.tau)) ? exp_ref(S.xd, LM, cT_(), cTl_()) : 0.f;
       const DF ztd = DT < 0 ? df_add(zx, DF{ed, 0.f}) : zx;
       const float zt = df_f(ztd), zgf = df_f(zg);
       const bool bad_t = !(lm > NEG_INF) || isinf(lm) || !isfinite(zt) || !(zt > 0.f);
       const bool bad_g = DT >= 0 && j < nb &&
                          (!(gm > NEG_INF) || isinf(gm) || !isfinite(zgf) || !(zgf > 0.f));
       if (lane == 0) {
-        if (P.dbg.row_m) P.dbg.row_m[ro] = lm / P.T;
+        if (P.dbg.row_m) P.dbg.row_m[ro] = lm / T_();
         // Z relative to the row max: sum exp(x/T - m) = zt * 2^(LM - lm log2(e)/T)
         if (P.dbg.row_z)
-          P.dbg.row_z[ro] = (float)(((double)ztd.hi + (double)ztd.lo) * exp2((double)LM - (double)lm * P.cTd));
+          P.dbg.row_z[ro] = (float)(((double)ztd.hi + (double)ztd.lo) * exp2((double)LM - (double)lm * cTd_()));
       }
       if (bad_t || bad_g) {
         finish(b, -1, -1, SAMSPEC_ST_BADROW);
@@ -1270,7 +1326,7 @@ struct Control {
   }
 };
 
-template <int TT, int DT, bool GREEDY, bool TREE = false>
+template <int TT, int DT, bool GREEDY, bool TREE = false, bool SAMP = false>
 __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
   using C = Cfg<TT, DT>;
   extern __shared__ __align__(1024) unsigned char dsm[];
@@ -1370,8 +1426,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
             r.a = full ? reduce_softmax<TT, DT, true, false, true>(sl, warp, lane, tg.nel, P.cT, -1, xm)
                        : reduce_softmax<TT, DT, false, false, true>(sl, warp, lane, tg.nel, P.cT, -1, xm);
           } else {
-          r.a = full ? reduce_softmax<TT, DT, true, false>(sl, warp, lane, tg.nel, P.cT, ex)
-                     : reduce_softmax<TT, DT, false, false>(sl, warp, lane, tg.nel, P.cT, ex);
+          if (SAMP) {  // the sequence's temperature; logits below the row's cut left out
+            const float cTs = S.cT, th = S.tau;
+            r.a = full ? reduce_softmax<TT, DT, true, false, false, true>(sl, warp, lane, tg.nel, cTs, ex, 0, th)
+                       : reduce_softmax<TT, DT, false, false, false, true>(sl, warp, lane, tg.nel, cTs, ex, 0, th);
+          } else {
+            r.a = full ? reduce_softmax<TT, DT, true, false>(sl, warp, lane, tg.nel, P.cT, ex)
+                       : reduce_softmax<TT, DT, false, false>(sl, warp, lane, tg.nel, P.cT, ex);
+          }
           }
           if (DT >= 0 && tg.has_draft) {
             r.b = full ? reduce_softmax<TT, DT, true, true>(sl, warp, lane, tg.nel, P.cT, ex)
@@ -1540,7 +1602,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
     // while large ones keep four sequences in flight per CTA.
     const int si = warp - kCtrlWarp;
     Slot& S = sm.slot[si];
-    Control<TT, DT, GREEDY, TREE> ctl(P, sm, rec, lane, si);
+    Control<TT, DT, GREEDY, TREE, SAMP> ctl(P, sm, rec, lane, si);
     int last_jobs = -1;
     uint64_t t_idle = gtimer();
     for (;;) {
@@ -1658,7 +1720,7 @@ __global__ void uniforms_kernel(int32_t B, int32_t K, uint64_t seed, uint64_t st
 }
 
 // ---- host launch --------------------------------------------------------------
-template <int TT, int DT, bool GREEDY, bool TREE = false>
+template <int TT, int DT, bool GREEDY, bool TREE = false, bool SAMP = false>
 int launch(const VParams& P0, cudaStream_t stream) {
   using C = Cfg<TT, DT>;
   VParams P = P0;
@@ -1682,7 +1744,7 @@ int launch(const VParams& P0, cudaStream_t stream) {
       return SAMSPEC_ECUDA;
   }
   if (!attr_done[dev]) {
-    if (cudaFuncSetAttribute(verify_kernel<TT, DT, GREEDY, TREE>,
+    if (cudaFuncSetAttribute(verify_kernel<TT, DT, GREEDY, TREE, SAMP>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem[dev]) !=
         cudaSuccess)
       return SAMSPEC_ECUDA;
@@ -1694,7 +1756,7 @@ int launch(const VParams& P0, cudaStream_t stream) {
   P.NS = ns;
   const size_t smem = head + (size_t)ns * kStageBytes;
   const int grid = P.B < sms[dev] ? P.B : sms[dev];
-  verify_kernel<TT, DT, GREEDY, TREE><<<grid, kThreads, smem, stream>>>(P);
+  verify_kernel<TT, DT, GREEDY, TREE, SAMP><<<grid, kThreads, smem, stream>>>(P);
   return cudaGetLastError() == cudaSuccess ? SAMSPEC_OK : SAMSPEC_ECUDA;
 }
 
@@ -1808,6 +1870,62 @@ int spec_verify(const void* d_target, int32_t target_dtype, const void* d_draft_
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return greedy ? dispatch<true>(P, target_dtype, ddt, s)
                 : dispatch<false>(P, target_dtype, ddt, s);
+}
+
+size_t spec_verify_sampling_workspace_bytes(int32_t B, int32_t K, int32_t V) {
+  if (B < 1 || K < 0 || V < 1) return 0;
+  return 256 + (((size_t)B * (K + 1) * sizeof(float) + 255) & ~(size_t)255);
+}
+
+int spec_verify_sampling(const void* d_target, int32_t target_dtype, const int32_t* d_draft,
+                         const int32_t* d_draft_len, int32_t B, int32_t K, int32_t V,
+                         const float* d_temperature, const int32_t* d_top_k,
+                         const float* d_top_p, uint64_t seed, uint64_t step,
+                         int32_t* d_accept_len, int32_t* d_out_token, int32_t* d_emit,
+                         int32_t* d_emit_len, int32_t* d_status, const spec_verify_debug* dbg,
+                         void* d_workspace, size_t ws_bytes, samspec_stream_t stream) {
+  if (!d_target || (K > 0 && !d_draft) || !d_temperature || !d_top_k || !d_top_p ||
+      !d_accept_len || !d_out_token || !d_workspace)
+    return SAMSPEC_EINVAL;
+  if (B < 1 || B > (1 << 24) || K < 0 || K > 32 || V < 1) return SAMSPEC_ESIZE;
+  if (target_dtype != SAMSPEC_F32 && target_dtype != SAMSPEC_BF16) return SAMSPEC_EDTYPE;
+  const int st = target_dtype == SAMSPEC_F32 ? 4 : 2;
+  if ((int64_t)V > (int64_t)kMaxChunks * (kStageBytes / st)) return SAMSPEC_ESIZE;
+  if (ws_bytes < spec_verify_sampling_workspace_bytes(B, K, V)) return SAMSPEC_ESIZE;
+  if (reinterpret_cast<uintptr_t>(d_workspace) % 256 != 0) return SAMSPEC_EALIGN;
+  if (reinterpret_cast<uintptr_t>(d_target) % 16 != 0) return SAMSPEC_EALIGN;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // each row's cut, into the workspace after the kernel's counters
+  float* tau = reinterpret_cast<float*>(static_cast<unsigned char*>(d_workspace) + 256);
+  const int rc = launch_sampling_cut(d_target, target_dtype, B, K + 1, V, d_temperature, d_top_k,
+                                     d_top_p, tau, s);
+  if (rc != SAMSPEC_OK) return rc;
+  VParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.target = static_cast<const unsigned char*>(d_target);
+  P.draft = d_draft;
+  P.draft_len = d_draft_len;
+  P.B = B;
+  P.K = K;
+  P.V = V;
+  P.T = 1.f;  // per sequence instead (seqT)
+  P.seed = seed;
+  P.step = step;
+  P.accept_len = d_accept_len;
+  P.out_token = d_out_token;
+  P.emit = d_emit;
+  P.emit_len = d_emit_len;
+  P.status = d_status;
+  if (dbg) {
+    P.dbg = *dbg;
+    P.dbg.q_d = nullptr;
+  }
+  P.ws = static_cast<uint32_t*>(d_workspace);
+  P.direct = ((size_t)V * st) % 16 != 0;
+  P.seqT = d_temperature;
+  P.tau = tau;
+  return target_dtype == SAMSPEC_F32 ? launch<0, -1, false, false, true>(P, s)
+                                     : launch<1, -1, false, false, true>(P, s);
 }
 
 int spec_verify_tree(const void* d_target, int32_t target_dtype, const int32_t* d_tok,

@@ -68,3 +68,30 @@ def test_binding_refuses_missing_library(tmp_path):
     import sam_drafting_verification_gb300._binding as bd
     with pytest.raises(bd.SamspecError):
         bd.load(str(tmp_path / "nope.so"))
+
+
+def test_sampling_entry_points_reject_bad_arguments_on_the_host():
+    """Argument checks of spec_sampling_cut and spec_verify_sampling, which
+    return before any device work (placeholders are never touched)."""
+    import sam_drafting_verification_gb300._binding as bd
+    lib = bd.lib()
+    p = ctypes.c_void_p(4096)
+    assert lib.spec_verify_sampling_workspace_bytes(4, 3, 100) >= 256 + 4 * 4 * 4
+    assert lib.spec_verify_sampling_workspace_bytes(0, 3, 100) == 0
+
+    def cut(target=p, dtype=bd.F32, B=2, R=2, V=100, temp=p):
+        return lib.spec_sampling_cut(target, dtype, B, R, V, temp, p, p, p, None)
+
+    assert cut(target=None) == bd.EINVAL and cut(temp=None) == bd.EINVAL
+    assert cut(R=34) == bd.ESIZE and cut(V=(1 << 22) + 1) == bd.ESIZE and cut(B=0) == bd.ESIZE
+    assert cut(dtype=9) == bd.EDTYPE
+    assert cut(target=ctypes.c_void_p(4100)) == bd.EALIGN
+
+    def ver(dtype=bd.BF16, K=2, V=1000, ws_bytes=1 << 16, draft=p, top_p=p):
+        return lib.spec_verify_sampling(p, dtype, draft, None, 2, K, V, p, p, top_p, 0, 0, p, p,
+                                        None, None, p, None, p, ws_bytes, None)
+
+    assert ver(draft=None) == bd.EINVAL and ver(top_p=None) == bd.EINVAL
+    assert ver(K=33) == bd.ESIZE and ver(ws_bytes=256) == bd.ESIZE
+    assert ver(V=48 * 24576 + 1) == bd.ESIZE and ver(dtype=bd.F32, V=48 * 12288 + 1) == bd.ESIZE
+    assert ver(dtype=5) == bd.EDTYPE

@@ -1,0 +1,212 @@
+"""Per-request temperature / top-k / top-p on the GPU against the oracle and
+the definitions: the cut of every row (top-k exactly; top-p exactly, or
+within 1e-6 of top_p in mass when the fixed-point sums put it on the other
+side), and verification decisions identical except where a coin falls within
+1e-6 of its threshold or CDF boundary (at most 1e-4 of the decisions)."""
+import numpy as np
+import pytest
+import torch
+from scipy import stats
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+BAND = 1e-6
+
+
+@pytest.fixture(scope="module")
+def ss(cuda_device):
+    import sam_drafting_verification_gb300 as ss
+    return ss
+
+
+def _probs(row, T):
+    x = row.astype(np.float64)
+    p = np.exp(x / T - (x / T).max())
+    return p / p.sum()
+
+
+def _cut_ok(row, T, k, top_p, tau_gpu, tau_oracle):
+    """(ok, excused): the GPU cut equals the oracle's, or lies within BAND of
+    the top-p boundary."""
+    if tau_gpu == tau_oracle or (np.isnan(tau_gpu) and np.isnan(tau_oracle)):
+        return True, False
+    if top_p >= 1.0:
+        return False, False
+    _, tau_k = oracle.truncate_row(row, T, k, 1.0)
+    x = row.astype(np.float64)
+    p = _probs(row, T)
+    kept_k = x >= tau_k
+    zk = p[kept_k].sum()
+    above = p[kept_k & (x > tau_gpu)].sum() / zk
+    incl = p[kept_k & (x >= tau_gpu)].sum() / zk
+    ok = tau_gpu >= tau_k and np.any(x == tau_gpu) and above < top_p + BAND and incl >= top_p - BAND
+    return bool(ok), True
+
+
+def _params(rng, B, V):
+    T = rng.choice([0.4, 0.7, 1.0, 1.7], B).astype(np.float32)
+    k = rng.choice([-1, 0, 1, 5, 50, 1000, V, V + 3], B).astype(np.int32)
+    p = rng.choice([0.1, 0.5, 0.9, 0.99, 1.0, 1.2], B).astype(np.float32)
+    return T, k, p
+
+
+@pytest.mark.parametrize("dtype,V", [(torch.float32, 3000), (torch.bfloat16, 40000),
+                                     (torch.bfloat16, 40001), (torch.float32, 2999)])
+def test_cut_matches_oracle(ss, cuda_device, dtype, V):
+    rng = np.random.default_rng(V)
+    B, R = 48, 3
+    logits = workloads.gaussian_logits(rng, (B, R, V), 2.0)
+    if dtype == torch.float32:
+        logits[::3] = np.round(logits[::3] * 4) / 4  # many exact ties
+    tl = torch.from_numpy(logits).to(dtype)
+    rows = tl.float().numpy()
+    T, k, p = _params(rng, B, V)
+    dev = cuda_device
+    tau = ss.sampling_cut(tl.to(dev), torch.from_numpy(T).to(dev), torch.from_numpy(k).to(dev),
+                          torch.from_numpy(p).to(dev)).cpu().numpy()
+    excused = 0
+    for b in range(B):
+        for r in range(R):
+            if not (0 < k[b] < V) and not (p[b] < 1.0):
+                assert tau[b, r] == -np.inf
+                continue
+            _, to = oracle.truncate_row(rows[b, r], float(T[b]), int(k[b]), float(p[b]))
+            ok, ex = _cut_ok(rows[b, r], float(T[b]), int(k[b]), float(p[b]), float(tau[b, r]), to)
+            assert ok, (b, r, T[b], k[b], p[b], tau[b, r], to)
+            excused += ex
+    assert excused <= 2, excused
+
+
+def test_cut_bad_parameters_and_rows(ss, cuda_device):
+    B, R, V = 6, 2, 64
+    logits = torch.randn((B, R, V), device=cuda_device)
+    logits[5, 1, 3] = float("nan")
+    T = torch.tensor([0.0, float("inf"), float("nan"), 1.0, 1.0, 1.0], device=cuda_device)
+    p = torch.tensor([0.9, 0.9, 0.9, 0.0, float("nan"), 0.9], device=cuda_device)
+    tau = ss.sampling_cut(logits, T, 5, p).cpu().numpy()
+    assert np.isnan(tau[:5]).all()
+    assert np.isfinite(tau[5, 0]) and tau[5, 1] == -np.inf
+
+
+def _compare(g, o, rows, draft, T, k, p, tau_g):
+    B, K1 = rows.shape[:2]
+    decisions = excused = 0
+    for b in range(B):
+        assert g["status"][b] == o["status"][b], b
+        if o["status"][b] != 0:
+            continue
+        Lg, Lo = int(g["accept_len"][b]), int(o["accept_len"][b])
+        # the emitted token is always inside the cut of its row
+        assert rows[b, Lg, g["out_token"][b]] >= tau_g[b, Lg], b
+        decisions += min(Lg, Lo) + 2
+        if Lg == Lo and g["out_token"][b] == o["out_token"][b]:
+            continue
+        other_side = False
+        for j in range(min(Lg, Lo) + 1):
+            ok, ex = _cut_ok(rows[b, j], float(T[b]), int(k[b]), float(p[b]), float(tau_g[b, j]),
+                             float(o["tau"][b, j]))
+            assert ok, (b, j)
+            other_side |= ex
+        if other_side:  # a top-p cut on the other side of its boundary
+            excused += 1
+            continue
+        if Lg != Lo:
+            j = min(Lg, Lo)
+            assert abs(o["u_acc"][b, j] - o["p_d"][b, j]) < BAND, (b, j, o["u_acc"][b, j], o["p_d"][b, j])
+        else:
+            pp, _ = oracle.truncate_row(rows[b, Lo], float(T[b]), int(k[b]), float(p[b]))
+            r = pp.copy()
+            if Lo < draft.shape[1]:
+                r[draft[b, Lo]] = max(0.0, r[draft[b, Lo]] - 1.0)
+            mass = r.sum()
+            tok = int(g["out_token"][b])
+            lo = r[:tok].sum() / mass
+            hi = lo + r[tok] / mass
+            assert r[tok] > 0 and lo - BAND <= o["u_res"][b] < hi + BAND, (b, tok, lo, hi, o["u_res"][b])
+        excused += 1
+    assert excused <= max(2, int(1e-4 * decisions) + 2), (excused, decisions)
+    return decisions, excused
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_verify_sampling_matches_oracle(ss, cuda_device, dtype):
+    rng = np.random.default_rng(11 if dtype == torch.float32 else 12)
+    B, K, V = 96, 3, 30000
+    logits = workloads.gaussian_logits(rng, (B, K + 1, V), 2.0)
+    top = np.argsort(-logits[:, :K], axis=-1)[..., :5]
+    draft = np.take_along_axis(top, rng.integers(0, 5, (B, K, 1)), -1)[..., 0].astype(np.int32)
+    tl = torch.from_numpy(logits).to(dtype)
+    rows = tl.float().numpy()
+    T, k, p = _params(rng, B, V)
+    dev = cuda_device
+    args = [torch.from_numpy(a).to(dev) for a in (T, k, p)]
+    g = ss.spec_verify_sampling(tl.to(dev), torch.from_numpy(draft).to(dev), None, *args,
+                                seed=17, step=5, emit=True)
+    g = {key: v.cpu().numpy() for key, v in g.items()}
+    tau_g = ss.sampling_cut(tl.to(dev), *args).cpu().numpy()
+    o = oracle.verify_sampling(rows, draft, None, T, k, p, seed=17, step=5)
+    _compare(g, o, rows, draft, T, k, p, tau_g)
+    assert (g["accept_len"] > 0).any()
+    # emitted tokens: the accepted drafts, then the final token
+    for b in range(B):
+        L = g["accept_len"][b]
+        assert list(g["emit"][b, :L + 1]) == list(draft[b, :L]) + [g["out_token"][b]]
+
+
+def test_no_truncation_equals_spec_verify(ss, cuda_device):
+    rng = np.random.default_rng(21)
+    B, K, V = 64, 4, 20000
+    for dtype in (torch.float32, torch.bfloat16):
+        logits = torch.from_numpy(workloads.gaussian_logits(rng, (B, K + 1, V), 2.0)).to(dtype).to(cuda_device)
+        draft = torch.argsort(logits[:, :K].float(), dim=-1, descending=True)[..., 1].to(torch.int32).contiguous()
+        for T in (0.6, 1.0):
+            a = ss.spec_verify(logits, draft, None, temperature=T, seed=3, step=1, emit=True)
+            s = ss.spec_verify_sampling(logits, draft, None, T, 0, 1.0, seed=3, step=1, emit=True)
+            for key in ("accept_len", "out_token", "emit", "status"):
+                assert torch.equal(a[key], s[key]), key
+
+
+def test_top1_equals_greedy(ss, cuda_device):
+    rng = np.random.default_rng(22)
+    B, K, V = 64, 4, 20000
+    logits = torch.from_numpy(workloads.gaussian_logits(rng, (B, K + 1, V), 2.0)).to(cuda_device)
+    am = torch.argmax(logits[:, :K], dim=-1).to(torch.int32)
+    draft = torch.where(torch.rand((B, K), device=cuda_device) < 0.7, am, (am + 1) % V).contiguous()
+    gr = ss.spec_verify(logits, draft, None, temperature=0.0)
+    for T in (0.3, 2.0):
+        s = ss.spec_verify_sampling(logits, draft, None, T, 1, 1.0, seed=5)
+        assert torch.equal(gr["accept_len"], s["accept_len"])
+        assert torch.equal(gr["out_token"], s["out_token"])
+
+
+def test_first_token_follows_the_truncated_distribution(ss, cuda_device):
+    """Losslessness on the device: identical rows, coins differing by
+    sequence; the first emitted token's frequencies follow p'."""
+    rng = np.random.default_rng(23)
+    V, B, T, k, p = 16, 200000, 0.8, 9, 0.9
+    row = workloads.gaussian_logits(rng, (V,), 1.0)
+    logits = torch.from_numpy(np.stack([row, row])).to(cuda_device).expand(B, 2, V).contiguous()
+    d = int(np.argsort(-row)[2])
+    draft = torch.full((B, 1), d, dtype=torch.int32, device=cuda_device)
+    g = ss.spec_verify_sampling(logits, draft, None, T, k, p, seed=29, step=0)
+    assert (g["status"] == 0).all()
+    first = torch.where(g["accept_len"] >= 1, draft[:, 0], g["out_token"]).cpu().numpy()
+    pp, tau = oracle.truncate_row(row, T, k, p)
+    counts = np.bincount(first, minlength=V)
+    keep = pp > 0
+    assert (counts[~keep] == 0).all()
+    assert stats.chisquare(counts[keep], pp[keep] * B).pvalue > 1e-3
+
+
+def test_bad_parameters(ss, cuda_device):
+    B, K, V = 6, 2, 100
+    logits = torch.randn((B, K + 1, V), device=cuda_device)
+    draft = torch.zeros((B, K), dtype=torch.int32, device=cuda_device)
+    T = torch.tensor([0.0, float("inf"), float("nan"), 1.0, 1.0, 1.0], device=cuda_device)
+    p = torch.tensor([0.9, 0.9, 0.9, 0.0, float("nan"), 0.9], device=cuda_device)
+    g = ss.spec_verify_sampling(logits, draft, None, T, 5, p)
+    assert g["status"].cpu().tolist() == [8, 8, 8, 8, 8, 0]
+    assert (g["accept_len"][:5] == -1).all()

@@ -240,3 +240,19 @@ def test_largest_vocabulary(ss, cuda_device, dtype, V, with_draft):
                        temperature=1.0,
                        draft_logits=(torch.zeros((1, K, V + 64), dtype=torch.float32, device=cuda_device)
                                      if with_draft else None))
+
+
+def test_only_the_draft_is_finite(ss, cuda_device):
+    """A row whose only finite logit is the draft token: p is one-hot on it, so
+    the draft is accepted (the sums without the draft are empty)."""
+    B, K, V = 4, 2, 1000
+    rng = np.random.default_rng(31)
+    logits = workloads.gaussian_logits(rng, (B, K + 1, V), 2.0)
+    draft = np.argsort(-logits[:, :K], axis=-1)[..., 2].astype(np.int32)
+    for b in range(B):
+        logits[b, 0, :] = -np.inf
+        logits[b, 0, draft[b, 0]] = 1.5
+    for T in (0.0, 1.0):
+        g, o, te, de = _run_both(ss, cuda_device, logits, draft, None, T=T, seed=2)
+        _check(g, o, te, de, draft, None, T)
+        assert (g["status"] == 0).all() and (g["accept_len"] >= 1).all()
