@@ -18,7 +18,7 @@ stream; max over ranks.  Under torchrun every rank runs its own batch (weak
 scaling, no collective on the data path).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                  [--workload rs_bf16_b64|sweep_b1024|long_rollout_b256|rollout_toy_b64|static_match_b256|tree_b256]
+                  [--workload rs_bf16_b64|sweep_b1024|long_rollout_b256|rollout_toy_b64|static_match_b256|tree_b256|sampling_b256]
 """
 from __future__ import annotations
 
@@ -214,6 +214,8 @@ def run_gpu(args):
         return run_static_match(args, ws, rank, dev)
     if args.workload == "tree_b256":
         return run_tree(args, ws, rank, dev)
+    if args.workload == "sampling_b256":
+        return run_sampling(args, ws, rank, dev)
 
     B, V, K, T, n = 64, workloads.V_LARGE, 3, 1.0, 4096
     hist, cont = rs_inputs(rank, B, V, n, K)
@@ -959,6 +961,125 @@ def run_tree(args, ws, rank, dev):
 
 
 # --------------------------------------------------------------------------
+# per-request sampling parameters
+# --------------------------------------------------------------------------
+
+SAMPLING_T = (0.6, 0.8, 1.0)
+SAMPLING_TOP_K = (0, 20, 50)
+SAMPLING_TOP_P = (0.9, 0.95, 1.0)
+
+
+def run_sampling(args, ws, rank, dev):
+    """B=256 sequences, K=3 one-hot drafts (uniform among each row's top 5),
+    V=151936, bf16 logits N(0, sd 2); per sequence a temperature from
+    {0.6, 0.8, 1.0}, top_k from {off, 20, 50} and top_p from {0.9, 0.95, 1.0}
+    (seeded).  One step = spec_verify_sampling: the cut of all 4 rows of every
+    sequence, then the verification with the cuts.  Two step tensors of 311 MB
+    alternate (each above L2); CUDA graphs of the steps, and of the cut alone
+    for its share."""
+    import torch
+
+    import oracle
+    import sam_drafting_verification_gb300 as ss
+    B, K, V = 256, 3, workloads.V_LARGE
+    reps = min(max(args.steps, 1), 1000)
+    hbm, peak_kind = _peaks()
+    rng = np.random.default_rng(1008 + 7919 * rank)
+    T = torch.tensor(rng.choice(SAMPLING_T, B), dtype=torch.float32, device=dev)
+    k = torch.tensor(rng.choice(SAMPLING_TOP_K, B), dtype=torch.int32, device=dev)
+    p = torch.tensor(rng.choice(SAMPLING_TOP_P, B), dtype=torch.float32, device=dev)
+    pool = [workloads.sweep_device(9000 + i + 100 * rank, B, K, V, torch.bfloat16, dev) for i in range(2)]
+    wsv = ss.verify_workspace(B, K, V, dev, sampling=True)
+    res = ss.spec_verify_sampling(pool[0][0], pool[0][1], None, T, k, p, seed=3, step=0, workspace=wsv)
+    tau = ss.sampling_cut(pool[0][0], T, k, p)
+    for w in range(max(args.warmup, 3)):
+        ss.spec_verify_sampling(pool[w % 2][0], pool[w % 2][1], None, T, k, p, seed=3, step=w,
+                                workspace=wsv, out=res)
+    torch.cuda.synchronize()
+    cs = torch.cuda.Stream(device=dev)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        cs.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(g, stream=cs):
+                for r in range(reps):
+                    fn(r)
+        torch.cuda.synchronize()
+        return g
+
+    g_all = capture(lambda r: ss.spec_verify_sampling(pool[r % 2][0], pool[r % 2][1], None, T, k, p, seed=3,
+                                                      step=r, workspace=wsv, out=res))
+    lib = ss._b.lib()
+    tau_ptr = tau.data_ptr()
+
+    def cut_only(r):
+        lg = pool[r % 2][0]
+        ss._b.check(lib.spec_sampling_cut(lg.data_ptr(), ss.BF16, B, K + 1, V, T.data_ptr(), k.data_ptr(),
+                                          p.data_ptr(), tau_ptr, cs.cuda_stream), "spec_sampling_cut")
+
+    g_cut = capture(cut_only)
+
+    def timed(g):
+        _barrier(ws)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(cs):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(cs)
+            g.replay()
+            e1.record(cs)
+        torch.cuda.synchronize()
+        _barrier(ws)
+        return _max_over_ranks(e0.elapsed_time(e1), ws, dev) / reps
+
+    clk = ClockSampler(dev.index or 0)
+    clk.start()
+    ms = timed(g_all)
+    clocks = clk.stop()
+    ms_cut = timed(g_cut)
+    # rows the verification read: the same calls again, untimed
+    rows_read = 0
+    for r in range(min(reps, 200)):
+        o = ss.spec_verify_sampling(pool[r % 2][0], pool[r % 2][1], None, T, k, p, seed=3, step=r,
+                                    workspace=wsv, out=res)
+        rows_read += int((o["accept_len"].cpu().numpy() + 1).sum())
+        assert (o["status"] == 0).all()
+    rows_per_seq = rows_read / min(reps, 200) / B
+    # cut: every row once from HBM; verification: the rows its chains needed
+    alg_cut = B * (K + 1) * V * 2
+    alg_ver = rows_per_seq * B * V * 2
+    ach = (alg_cut + alg_ver) / (ms / 1e3) / 1e9
+    cpu = None
+    if rank == 0:
+        nb = 16
+        host = [(pl[0][:nb].float().cpu().numpy(), pl[1][:nb].cpu().numpy()) for pl in pool]
+        Th, kh, ph = (x[:nb].cpu().numpy() for x in (T, k, p))
+        t0 = time.perf_counter()
+        for r in range(2):
+            oracle.verify_sampling(host[r][0], host[r][1], None, Th, kh, ph, seed=3, step=r)
+        el = time.perf_counter() - t0
+        cpu = {"value": round(2 * nb / el, 2), "unit": "seq-steps/s", "cores": 1, "kind": "oracle",
+               "sample": f"{nb} sequences x 2 steps of the same logits and parameters ({el:.2f} s, fp64)"}
+    line = {"metric": "sampling-parameter verification seq-steps/s", "value": round(B / (ms / 1e3), 1),
+            "unit": "seq-steps/s", "n_gpus": ws, "steps": reps, "warmup": max(args.warmup, 3),
+            "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "sampling_b256", "B": B, "K": K, "V": V,
+                       "temperature": list(SAMPLING_T), "top_k": list(SAMPLING_TOP_K),
+                       "top_p": list(SAMPLING_TOP_P), "l2": "two 311 MB step tensors alternate",
+                       "timing": f"CUDA graph of {reps} steps (cut + verify launches)"},
+            "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(ach / hbm, 4), "traffic": None, "peak_source": peak_kind,
+                         "algorithmic_bytes_per_step": round(alg_cut + alg_ver, 1)},
+            "cpu_baseline": cpu, "gpu_launches": 2 * reps, "clocks": clocks,
+            "breakdown": {"cut_us": round(ms_cut * 1e3, 2), "verify_us": round((ms - ms_cut) * 1e3, 2),
+                          "cut_GBps_one_read": round(alg_cut / (ms_cut / 1e3) / 1e9, 1),
+                          "rows_per_seq": round(rows_per_seq, 4)}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
 # verification sweep at B=1024
 # --------------------------------------------------------------------------
 
@@ -1056,7 +1177,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="rs_bf16_b64", choices=["rs_bf16_b64", "sweep_b1024", "long_rollout_b256",
-                                                      "rollout_toy_b64", "static_match_b256", "tree_b256"])
+                                                      "rollout_toy_b64", "static_match_b256", "tree_b256",
+                                                      "sampling_b256"])
     ap.add_argument("--point", default="", help="sweep_b1024 only: one point 'K,f32|bf16,greedy|T=1|greedy-full-read'")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":

@@ -327,7 +327,7 @@ int spec_verify_tree(const void* d_target, int32_t target_dtype, const int32_t* 
 /* The cut of each target row under per-request sampling parameters ([P3]
  * SGLang 的实现, _sampling_verify: p = softmax(l / T), then top-k
  * renormalisation, then top-p renormalisation).  For row (b, r) of d_target
- * [B, R, V] (1 <= R <= 33, V <= 2^22, 16-byte aligned) with d_temperature[b],
+ * [B, R, V] (1 <= R <= 33, V <= 2^21, 16-byte aligned) with d_temperature[b],
  * d_top_k[b], d_top_p[b] ([B] each, device):
  *   top-k (0 < k < V) keeps the tokens whose logit is at least the k-th
  *   largest (ties kept); top-p (top_p < 1) keeps, of those, the ones whose

@@ -25,8 +25,8 @@
 // log2(e)/T)) summed with integer atomics, so the sums are exact and the
 // result does not depend on the order of the additions; lanes of a warp that
 // hit the same bin are combined first (one warp reduction per distinct
-// digit).  Terms below 2^-43 of the row's maximum are dropped (at V = 2^22 at
-// most 2^-20 of the mass).
+// digit).  Terms below 2^-43 of the row's maximum are dropped (at V = 2^21 at
+// most 2^-21 of the mass).
 
 #include <cstdint>
 #include <cstring>
@@ -43,7 +43,7 @@ namespace {
 constexpr int kThr = 256;     // threads per CTA (one CTA per row)
 constexpr int kBins = 256;    // one 8-bit digit per level
 constexpr float kFix = 4398046511104.f;  // 2^42: mass units of 2^-42
-constexpr int kMaxV = 1 << 22;          // keeps every mass sum below 2^64
+constexpr int kMaxV = 1 << 21;          // keeps every mass sum below 2^63 (terms <= 2^42)
 
 // Order-preserving key of a logit: key(a) < key(b) iff a < b, equal iff
 // a == b (-0 is folded into +0 first).
@@ -55,17 +55,76 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
+constexpr int kLogBins = 1024;  // 32 per octave of the term, 32 octaves
+constexpr int kCap = 4096;     // boundary logits held in shared memory (a power of two:
+                               // the sort pads to one)
+
 struct CutSmem {
+  // radix levels over keys (the path for rows whose boundary bins overflow)
   uint32_t cnt[kBins];
   unsigned long long mass[kBins];
+  // log-scale bins of the term 2^(l cT - R): exact counts, and masses
+  // relative to each bin's upper edge in units of 2^-10 (lmassr; about 1e-3
+  // accurate: they only choose which bins to collect), turned into fp32
+  // masses (lmass) before the scans
+  uint32_t lcnt[kLogBins];
+  uint32_t lmassr[kLogBins];
+  float lmass[kLogBins];
+  // the logits of the boundary bins: keys and terms
+  uint32_t bkey[kCap];
+  float bmass[kCap];
+  double tsum[kThr];  // per-thread partial sums
   float red[kThr / 32];
-  // result of a bin scan
-  uint32_t digit;
-  uint32_t above_cnt;             // keys above the prefix (all levels so far)
-  unsigned long long above_mass;  // their mass
-  unsigned long long bin_mass;    // mass of the chosen bin
-  unsigned long long total;       // mass of every bin (first top-p level)
+  uint32_t nbuf;
+  uint32_t idx;
+  // broadcast of warp 0's choices
+  uint32_t dlo, dhi, nrange, above_in_range;
+  uint32_t key;
+  double dscr[4];  // broadcast scratch
 };
+
+// Log-scale bin (digit, higher = larger logit) of y = l cT - R <= ~0: 32 bins
+// per octave of the term 2^y, the last bin holding everything below 2^-32.
+__device__ __forceinline__ uint32_t log_digit(float y) {
+  const int b = __float2int_rz(-y * 32.f);
+  return (uint32_t)(kLogBins - 1 - min(max(b, 0), kLogBins - 1));
+}
+// The term 2^y relative to the upper edge 2^(-b/32) of its bin (digit d,
+// b = kLogBins - 1 - d), in units of 2^-10: between about 1002 and 1024 (0 for
+// the tiny terms of the last bin).
+__device__ __forceinline__ uint32_t rel_mass(float y, uint32_t d) {
+  const float b = (float)(kLogBins - 1 - (int)d);
+  return __float2uint_rn(ex2_approx(fmaf(b, 0.03125f, y)) * 1024.f);
+}
+// A running sum as a float pair (each addition's rounding error carried in
+// lo), read out in fp64.
+struct Acc {
+  float hi = 0.f, lo = 0.f;
+  __device__ __forceinline__ void add(float v) {
+    const float sm = hi + v;
+    const float bb = sm - hi;
+    lo += (hi - (sm - bb)) + (v - bb);
+    hi = sm;
+  }
+  __device__ __forceinline__ double get() const { return (double)hi + (double)lo; }
+};
+// Block sum of per-thread fp64 values in a fixed order (warps by xor tree,
+// then warp totals in index order); every thread gets the result.
+__device__ double block_sum(CutSmem& sh, double v, int lane, int warp) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFullMask, v, o);
+  __syncthreads();
+  if (lane == 0) sh.tsum[warp] = v;
+  __syncthreads();
+  double t = 0.0;
+  for (int w = 0; w < kThr / 32; ++w) t += sh.tsum[w];
+  __syncthreads();
+  return t;
+}
+// The term 2^y in fixed point, units of 2^-42.
+__device__ __forceinline__ unsigned long long fixed_mass(float y) {
+  return __float2ull_rn(ex2_approx(y) * kFix);
+}
 
 // Calls f(x, valid) for every logit of the row; every lane of the CTA makes
 // the same number of calls (valid = false past the end), so f may use
@@ -76,20 +135,29 @@ __device__ __forceinline__ void visit_row(const unsigned char* row, int V, F&& f
   constexpr int ES = TT ? 2 : 4;
   constexpr int VEC = 16 / ES;
   if (((size_t)V * ES) % 16 == 0) {
+    // kLoads vectors per thread in flight before any is processed
+    constexpr int kLoads = 4;
     const int nvec = V / VEC;
-    for (int base = 0; base < nvec; base += kThr) {
-      const int i = base + (int)threadIdx.x;
-      const bool ok = i < nvec;
-      uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (ok) w = *reinterpret_cast<const uint4*>(row + (size_t)i * 16);
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    for (int base = 0; base < nvec; base += kThr * kLoads) {
+      uint4 w[kLoads];
+      bool ok[kLoads];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (TT) {
-          f(bf16_lo(ws[q]), ok);
-          f(bf16_hi(ws[q]), ok);
-        } else {
-          f(__uint_as_float(ws[q]), ok);
+      for (int u = 0; u < kLoads; ++u) {
+        const int i = base + u * kThr + (int)threadIdx.x;
+        ok[u] = i < nvec;
+        w[u] = ok[u] ? *reinterpret_cast<const uint4*>(row + (size_t)i * 16) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kLoads; ++u) {
+        const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (TT) {
+            f(bf16_lo(ws[q]), ok[u]);
+            f(bf16_hi(ws[q]), ok[u]);
+          } else {
+            f(__uint_as_float(ws[q]), ok[u]);
+          }
         }
       }
     }
@@ -131,63 +199,70 @@ __device__ __forceinline__ void hist_add(CutSmem& sh, bool in, uint32_t digit,
   }
 }
 
-// Warp 0: the digit where the running sum over the bins from the top (255
-// down), added to what lies above the prefix, first reaches the target: a
-// count of k (BY_MASS false) or a mass (BY_MASS true; the target is
-// frac * total of this histogram when from_total, else need_mass).  The bins
-// above the chosen one are added to above_cnt / above_mass; the chosen bin's
-// mass goes to bin_mass.  If rounding keeps the sum below the target, the
-// lowest non-empty bin is taken (everything under the prefix is kept).
-template <bool BY_MASS>
-__device__ void scan_bins(CutSmem& sh, int lane, uint32_t k, double need_mass, bool from_total,
-                          double frac) {
-  uint32_t c[8];
-  unsigned long long ms[8];
+// Result of a bin scan (masses in the histogram's units, summed in fp64).
+struct ScanOut {
+  uint32_t digit;
+  uint32_t above_cnt;  // elements in the bins above the chosen one (plus above_c0)
+  double above_mass;   // their mass
+  double bin_mass;     // mass of the chosen bin
+  uint32_t bin_cnt;    // elements of the chosen bin
+  double total;        // mass of every bin
+};
+
+// Warp 0: over NB bins with counts cnt and masses mass, the bin where the
+// running sum from the top (bin NB - 1 down), added to what lies above
+// (above_c0 / above_m0), first reaches the target: a count of k (BY_MASS
+// false) or a mass (BY_MASS true; frac * total of these bins when
+// from_total, else need_mass).  If rounding keeps the sum below the target,
+// the lowest non-empty bin is taken (everything is kept).  Lane l owns bins
+// [NB/32 * l, NB/32 * (l + 1)); the bins are read from shared memory twice
+// rather than held in registers.
+template <int NB, bool BY_MASS, typename M>
+__device__ ScanOut scan_bins(const uint32_t* cnt, const M* mass, int lane, uint32_t above_c0,
+                             double above_m0, uint32_t k, double need_mass, bool from_total,
+                             double frac) {
+  constexpr int PL = NB / 32;  // bins per lane
+  const int base = PL * lane;
   uint32_t csum = 0;
-  unsigned long long msum = 0;
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    c[q] = sh.cnt[8 * lane + q];
-    ms[q] = sh.mass[8 * lane + q];
-    csum += c[q];
-    msum += ms[q];
+  double msum = 0.0;
+  for (int q = 0; q < PL; ++q) {
+    csum += cnt[base + q];
+    msum += (double)mass[base + q];
   }
   // sums over the lanes above (higher bins)
   uint32_t cs = csum;
-  unsigned long long mss = msum;
+  double mss = msum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t t = __shfl_down_sync(kFullMask, cs, o);
-    const unsigned long long u = __shfl_down_sync(kFullMask, mss, o);
+    const double u = __shfl_down_sync(kFullMask, mss, o);
     if (lane + o < 32) {
       cs += t;
       mss += u;
     }
   }
   const uint32_t cab = cs - csum;
-  const unsigned long long mab = mss - msum;
-  const unsigned long long total = __shfl_sync(kFullMask, mss, 0);
-  const uint32_t above_c0 = sh.above_cnt;
-  const unsigned long long above_m0 = sh.above_mass;
-  const double need = from_total ? frac * (double)total : need_mass;
-  // walk this lane's bins downwards
+  const double mab = mss - msum;
+  const double total = __shfl_sync(kFullMask, mss, 0);
+  const double need = from_total ? frac * total : need_mass;
   int found = -1;
-  uint32_t rc = cab;
-  unsigned long long rm = mab;
-  uint32_t fc = 0;
-  unsigned long long fm = 0;
-#pragma unroll
-  for (int q = 7; q >= 0; --q) {
-    const bool hit = BY_MASS ? (double)(above_m0 + rm + ms[q]) >= need : above_c0 + rc + c[q] >= k;
+  uint32_t rc = cab, fc = 0, fbc = 0;
+  double rm = mab, fm = 0.0, fbm = 0.0;
+  for (int q = PL - 1; q >= 0; --q) {
+    const uint32_t c = cnt[base + q];
+    const double m = (double)mass[base + q];
+    const bool hit = BY_MASS ? above_m0 + rm + m >= need : above_c0 + rc + c >= k;
     if (found < 0 && hit) {
       found = q;
       fc = rc;
       fm = rm;
+      fbc = c;
+      fbm = m;
     }
-    rc += c[q];
-    rm += ms[q];
+    rc += c;
+    rm += m;
   }
-  unsigned hitmask = __ballot_sync(kFullMask, found >= 0);
+  const unsigned hitmask = __ballot_sync(kFullMask, found >= 0);
   int src;
   if (hitmask) {
     src = 31 - __clz(hitmask);
@@ -195,15 +270,18 @@ __device__ void scan_bins(CutSmem& sh, int lane, uint32_t k, double need_mass, b
     found = -1;
     rc = cab;
     rm = mab;
-#pragma unroll
-    for (int q = 7; q >= 0; --q) {
-      if (c[q] > 0) {
+    for (int q = PL - 1; q >= 0; --q) {
+      const uint32_t c = cnt[base + q];
+      const double m = (double)mass[base + q];
+      if (c > 0) {
         found = q;
         fc = rc;
         fm = rm;
+        fbc = c;
+        fbm = m;
       }
-      rc += c[q];
-      rm += ms[q];
+      rc += c;
+      rm += m;
     }
     const unsigned ne = __ballot_sync(kFullMask, found >= 0);
     src = ne ? __ffs(ne) - 1 : 0;
@@ -213,17 +291,14 @@ __device__ void scan_bins(CutSmem& sh, int lane, uint32_t k, double need_mass, b
       fm = mab;
     }
   }
-  if (lane == src) {
-    sh.digit = (uint32_t)(8 * lane + found);
-    sh.above_cnt = above_c0 + fc;
-    sh.above_mass = above_m0 + fm;
-    unsigned long long bm = 0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      if (q == found) bm = ms[q];
-    sh.bin_mass = bm;
-    sh.total = total;
-  }
+  ScanOut o;
+  o.digit = (uint32_t)__shfl_sync(kFullMask, base + found, src);
+  o.above_cnt = __shfl_sync(kFullMask, above_c0 + fc, src);
+  o.above_mass = __shfl_sync(kFullMask, above_m0 + fm, src);
+  o.bin_mass = __shfl_sync(kFullMask, fbm, src);
+  o.bin_cnt = __shfl_sync(kFullMask, fbc, src);
+  o.total = total;
+  return o;
 }
 
 __device__ __forceinline__ float max_nan(float a, float b) {
@@ -232,13 +307,108 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   return d;
 }
 
+// The exact cut by radix levels over the keys, streaming the row once per
+// level (used when the boundary bins hold more logits than the buffer).
 template <int TT>
-__global__ void __launch_bounds__(kThr) cut_kernel(const unsigned char* target, int32_t R, int32_t V,
+__device__ uint32_t radix_cut(CutSmem& sh, const unsigned char* rp, int V, float cT, float Rf,
+                              bool use_k, bool use_p, int32_t k, float tp, int lane, int warp) {
+  constexpr int NLEV = TT ? 2 : 4;
+  uint32_t min_key = 0, key_k = 0, key_p = 0;
+  double zk = 0.0;  // mass of the keys >= tau_k, units 2^-42
+  for (int pass = 0; pass < 2; ++pass) {
+    if ((pass == 0 && !use_k) || (pass == 1 && !use_p)) continue;
+    uint32_t prefix = 0, above_c = 0;
+    double above_m = 0.0, bin_m = 0.0;
+    for (int lev = 0; lev < NLEV; ++lev) {
+      const int shift = 24 - 8 * lev;
+      const uint32_t hmask = lev == 0 ? 0u : (0xffffffffu << (shift + 8));
+      for (int i = threadIdx.x; i < kBins; i += kThr) {
+        sh.cnt[i] = 0;
+        sh.mass[i] = 0;
+      }
+      __syncthreads();
+      visit_row<TT>(rp, V, [&](float x, bool ok) {
+        const uint32_t u = order_key(x);
+        const bool in = ok && u >= min_key && (u & hmask) == (prefix & hmask);
+        const unsigned long long fx = in ? fixed_mass(fmaf(x, cT, -Rf)) : 0ull;
+        hist_add(sh, in, (u >> shift) & 0xffu, fx, lane);
+      });
+      __syncthreads();
+      if (warp == 0) {
+        const ScanOut o = pass == 0
+            ? scan_bins<kBins, false>(sh.cnt, sh.mass, lane, above_c, above_m, (uint32_t)k, 0.0,
+                                      false, 0.0)
+            : scan_bins<kBins, true>(sh.cnt, sh.mass, lane, above_c, above_m, 0u, (double)tp * zk,
+                                     !use_k && lev == 0, (double)tp);
+        if (lane == 0) {
+          sh.key = o.digit;
+          sh.nrange = o.above_cnt;
+          sh.dscr[0] = o.above_mass;
+          sh.dscr[1] = o.bin_mass;
+          sh.dscr[2] = o.total;
+        }
+      }
+      __syncthreads();
+      prefix |= sh.key << shift;
+      above_c = sh.nrange;
+      above_m = sh.dscr[0];
+      bin_m = sh.dscr[1];
+      if (pass == 1 && !use_k && lev == 0) zk = sh.dscr[2];
+      __syncthreads();
+    }
+    // bf16 keys: the low 16 bits follow from the sign
+    if (TT) prefix |= (prefix & 0x80000000u) ? 0u : 0xffffu;
+    if (pass == 0) {
+      key_k = prefix;
+      min_key = prefix;
+      zk = above_m + bin_m;
+    } else {
+      key_p = prefix;
+    }
+  }
+  return key_k > key_p ? key_k : key_p;
+}
+
+// Sorts the first n (<= kCap) entries of the buffer by key, descending
+// (bitonic network over the next power of two, at most kCap; padding keys are
+// 0, below every real key).
+__device__ void sort_buffer(CutSmem& sh, uint32_t n) {
+  static_assert((kCap & (kCap - 1)) == 0, "the sort pads to a power of two");
+  uint32_t np = 1;
+  while (np < n) np <<= 1;
+  for (uint32_t i = n + threadIdx.x; i < np; i += kThr) {
+    sh.bkey[i] = 0u;
+    sh.bmass[i] = 0ull;
+  }
+  __syncthreads();
+  for (uint32_t size = 2; size <= np; size <<= 1) {
+    for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
+      for (uint32_t i = threadIdx.x; i < np; i += kThr) {
+        const uint32_t j = i ^ stride;
+        if (j > i) {
+          const bool desc = (i & size) == 0;
+          const uint32_t a = sh.bkey[i], b = sh.bkey[j];
+          if (desc ? a < b : a > b) {
+            sh.bkey[i] = b;
+            sh.bkey[j] = a;
+            const float t = sh.bmass[i];
+            sh.bmass[i] = sh.bmass[j];
+            sh.bmass[j] = t;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+template <int TT>
+__global__ void __launch_bounds__(kThr, 4) cut_kernel(const unsigned char* target, int32_t R, int32_t V,
                                                    const float* temp, const int32_t* top_k,
                                                    const float* top_p, float* tau) {
   constexpr int ES = TT ? 2 : 4;
-  constexpr int NLEV = TT ? 2 : 4;
-  __shared__ CutSmem sh;
+  extern __shared__ __align__(16) unsigned char cut_dsm[];
+  CutSmem& sh = *reinterpret_cast<CutSmem*>(cut_dsm);
   const float INF = __int_as_float(0x7f800000);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t row = blockIdx.x;
@@ -257,7 +427,7 @@ __global__ void __launch_bounds__(kThr) cut_kernel(const unsigned char* target, 
     return;
   }
   const unsigned char* rp = target + (size_t)row * V * ES;
-  // the row maximum (NaN-propagating)
+  // 1. the row maximum (NaN-propagating)
   float m = -INF;
   visit_row<TT>(rp, V, [&](float x, bool ok) {
     if (ok) m = max_nan(m, x);
@@ -265,6 +435,10 @@ __global__ void __launch_bounds__(kThr) cut_kernel(const unsigned char* target, 
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max_nan(m, __shfl_xor_sync(kFullMask, m, o));
   if (lane == 0) sh.red[warp] = m;
+  for (int i = threadIdx.x; i < kLogBins; i += kThr) {
+    sh.lcnt[i] = 0;
+    sh.lmassr[i] = 0;
+  }
   __syncthreads();
   m = sh.red[0];
   for (int w = 1; w < kThr / 32; ++w) m = max_nan(m, sh.red[w]);
@@ -274,53 +448,185 @@ __global__ void __launch_bounds__(kThr) cut_kernel(const unsigned char* target, 
   }
   const float cT = (float)(1.4426950408889634 / (double)T);
   const float Rf = ceilf(m * cT);
-  uint32_t min_key = 0, key_k = 0, key_p = 0;
-  double zk = 0.0;  // mass of the keys >= tau_k, units 2^-42
-  for (int pass = 0; pass < 2; ++pass) {
-    if ((pass == 0 && !use_k) || (pass == 1 && !use_p)) continue;
-    uint32_t prefix = 0;
-    if (threadIdx.x == 0) {
-      sh.above_cnt = 0;
-      sh.above_mass = 0;
+  // 2. counts (exact) and masses (top-p only) of the log-scale bins; with
+  // top-p and no top-k, also the row's total as a float-pair sum
+  Acc s_all;
+  visit_row<TT>(rp, V, [&](float x, bool ok) {
+    if (!ok) return;
+    const float y = fmaf(x, cT, -Rf);
+    const uint32_t d = log_digit(y);
+    atomicAdd(&sh.lcnt[d], 1u);
+    if (use_p) {
+      atomicAdd(&sh.lmassr[d], rel_mass(y, d));
+      if (!use_k) s_all.add(ex2_approx(y));
     }
-    for (int lev = 0; lev < NLEV; ++lev) {
-      const int shift = 24 - 8 * lev;
-      const uint32_t hmask = lev == 0 ? 0u : (0xffffffffu << (shift + 8));
-      for (int i = threadIdx.x; i < kBins; i += kThr) {
-        sh.cnt[i] = 0;
-        sh.mass[i] = 0;
+  });
+  __syncthreads();
+  for (int d = threadIdx.x; d < kLogBins; d += kThr)
+    sh.lmass[d] = (float)sh.lmassr[d] * exp2f(-(float)(kLogBins - 1 - d) * 0.03125f - 10.f);
+  __syncthreads();
+  // 3. warp 0: the bins to collect, [dlo, dhi].  Top-k's bin dk is exact (from
+  // the counts).  Top-p's crossing is located with the fp32 masses, the range
+  // widened so that the exact crossing lies inside it barring a rounding
+  // corner, which step 5 detects.
+  if (warp == 0) {
+    uint32_t dlo, dhi, dk = 0, above_k = 0;
+    if (use_k) {
+      const ScanOut o = scan_bins<kLogBins, false>(sh.lcnt, sh.lmass, lane, 0u, 0.0, (uint32_t)k,
+                                                   0.0, false, 0.0);
+      dk = o.digit;
+      above_k = o.above_cnt;
+      dlo = dhi = dk;
+      if (use_p) {
+        // top_p * Z_k is at least top_p * (the mass above bin dk): its
+        // crossing is at or below the crossing of a little less than that
+        const ScanOut a = scan_bins<kLogBins, true>(sh.lcnt, sh.lmass, lane, 0u, 0.0, 0u,
+                                                    (double)tp * o.above_mass * (1.0 - 1e-4), false,
+                                                    0.0);
+        uint32_t d1 = a.digit;
+        uint32_t hi_ne = 0;  // a target of 0 is met at the top: the highest non-empty bin
+#pragma unroll
+        for (int q = 0; q < kLogBins / 32; ++q)
+          if (sh.lcnt[(kLogBins / 32) * lane + q] > 0) hi_ne = (kLogBins / 32) * lane + q;
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) hi_ne = max(hi_ne, __shfl_xor_sync(kFullMask, hi_ne, o2));
+        if (d1 > hi_ne) d1 = hi_ne;
+        dhi = d1 > dk ? d1 : dk;
       }
-      __syncthreads();
-      visit_row<TT>(rp, V, [&](float x, bool ok) {
-        const uint32_t u = order_key(x);
-        const bool in = ok && u >= min_key && (u & hmask) == (prefix & hmask);
-        const float e = ex2_approx(fmaf(x, cT, -Rf));
-        const unsigned long long fx = in ? __float2ull_rn(e * kFix) : 0ull;
-        hist_add(sh, in, (u >> shift) & 0xffu, fx, lane);
-      });
+    } else {
+      const ScanOut o = scan_bins<kLogBins, true>(sh.lcnt, sh.lmass, lane, 0u, 0.0, 0u, 0.0, true,
+                                                  (double)tp);
+      dlo = o.digit > 0 ? o.digit - 1 : 0;
+      dhi = o.digit < kLogBins - 1 ? o.digit + 1 : kLogBins - 1;
+    }
+    uint32_t nr = 0, nab = 0;
+#pragma unroll
+    for (int q = 0; q < kLogBins / 32; ++q) {
+      const uint32_t d = (kLogBins / 32) * lane + q;
+      if (d >= dlo && d <= dhi) nr += sh.lcnt[d];
+      if (d > dk && d <= dhi) nab += sh.lcnt[d];
+    }
+    nr = __reduce_add_sync(kFullMask, nr);
+    nab = __reduce_add_sync(kFullMask, nab);
+    if (lane == 0) {
+      sh.dlo = dlo;
+      sh.dhi = dhi;
+      sh.nrange = nr;
+      sh.above_in_range = nab;
+      sh.nbuf = 0;
+      sh.key = dk;
+      sh.idx = above_k;
+    }
+  }
+  __syncthreads();
+  const uint32_t dlo = sh.dlo, dhi = sh.dhi, nrange = sh.nrange;
+  const uint32_t dk = sh.key, above_k = sh.idx, nab = sh.above_in_range;
+  bool fallback = nrange > (uint32_t)kCap;
+  uint32_t key_k = 0, key_p = 0;
+  if (!fallback) {
+    __syncthreads();
+    // 4. the logits of bins [dlo, dhi] into the buffer; float-pair sums of the
+    // terms above dhi (top-p) and above dk (top-k); logits below the range
+    // need nothing
+    Acc s_hi, s_k;
+    visit_row<TT>(rp, V, [&](float x, bool ok) {
+      if (!ok) return;
+      const float y = fmaf(x, cT, -Rf);
+      const uint32_t d = log_digit(y);
+      if (d < dlo) return;
+      const float e = ex2_approx(y);
+      if (use_k && d > dk) s_k.add(e);
+      if (use_p && d > dhi) s_hi.add(e);
+      if (d <= dhi) {
+        const uint32_t pos = atomicAdd(&sh.nbuf, 1u);
+        if (pos < (uint32_t)kCap) {
+          sh.bkey[pos] = order_key(x);
+          sh.bmass[pos] = e;
+        }
+      }
+    });
+    const double base_mass = use_p ? block_sum(sh, s_hi.get(), lane, warp) : 0.0;
+    const double above_mk = use_k ? block_sum(sh, s_k.get(), lane, warp) : 0.0;
+    const double total = use_k ? 0.0 : block_sum(sh, s_all.get(), lane, warp);
+    const uint32_t n = min(sh.nbuf, (uint32_t)kCap);
+    __syncthreads();
+    sort_buffer(sh, n);
+    // 5. the cuts, from the sorted buffer
+    double zk = total;
+    if (use_k) {
+      key_k = sh.bkey[nab + (uint32_t)k - above_k - 1];
+      // Z_k: the mass above bin dk and that of bin dk's logits >= tau_k
+      double part = 0.0;
+      for (uint32_t i = nab + threadIdx.x; i < n; i += kThr)
+        if (sh.bkey[i] >= key_k) part += (double)sh.bmass[i];
+      zk = above_mk + block_sum(sh, part, lane, warp);
+    }
+    if (use_p) {
+      const double need = (double)tp * zk - base_mass;
+      // running mass over the sorted buffer (logits >= tau_k): per-thread
+      // chunks, their exclusive prefix by warp 0, then each chunk walked
+      const uint32_t chunk = (n + kThr - 1) / kThr;
+      const uint32_t i0 = min(n, threadIdx.x * chunk), i1 = min(n, i0 + chunk);
+      double own = 0.0;
+      for (uint32_t i = i0; i < i1; ++i)
+        if (sh.bkey[i] >= key_k) own += (double)sh.bmass[i];
+      sh.tsum[threadIdx.x] = own;
+      if (threadIdx.x == 0) sh.idx = 0xffffffffu;
       __syncthreads();
       if (warp == 0) {
-        if (pass == 0)
-          scan_bins<false>(sh, lane, (uint32_t)k, 0.0, false, 0.0);
-        else
-          scan_bins<true>(sh, lane, 0u, (double)tp * zk, !use_k && lev == 0, (double)tp);
+        constexpr int PT = kThr / 32;
+        double v[PT], t = 0.0;
+#pragma unroll
+        for (int q = 0; q < PT; ++q) {
+          v[q] = sh.tsum[PT * lane + q];
+          t += v[q];
+        }
+        double incl = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const double u = __shfl_up_sync(kFullMask, incl, o);
+          if (lane >= o) incl += u;
+        }
+        double run = incl - t;
+#pragma unroll
+        for (int q = 0; q < PT; ++q) {
+          sh.tsum[PT * lane + q] = run;
+          run += v[q];
+        }
       }
       __syncthreads();
-      prefix |= sh.digit << shift;
-      if (pass == 1 && !use_k && lev == 0) zk = (double)sh.total;
+      double run = sh.tsum[threadIdx.x];
+      for (uint32_t i = i0; i < i1; ++i) {
+        if (sh.bkey[i] < key_k) continue;
+        run += (double)sh.bmass[i];
+        if (run >= need) {
+          atomicMin(&sh.idx, i);
+          break;
+        }
+      }
+      __syncthreads();
+      const uint32_t ix = sh.idx;
+      if (!(need > 0.0)) {
+        fallback = true;  // the crossing lies above the collected bins
+      } else if (ix != 0xffffffffu) {
+        key_p = sh.bkey[ix];
+      } else if (use_k || dlo == 0) {
+        // no crossing inside: every logit >= tau_k (or the whole row) is kept
+        key_p = 0;
+      } else {
+        fallback = true;  // the crossing lies below the collected bins
+      }
     }
-    // bf16 keys: the low 16 bits follow from the sign
-    if (TT) prefix |= (prefix & 0x80000000u) ? 0u : 0xffffu;
-    if (pass == 0) {
-      key_k = prefix;
-      min_key = prefix;
-      zk = (double)(sh.above_mass + sh.bin_mass);
-    } else {
-      key_p = prefix;
-    }
-    __syncthreads();
   }
-  if (threadIdx.x == 0) tau[row] = key_value(key_k > key_p ? key_k : key_p);
+  if (fallback) {  // uniform over the CTA
+    __syncthreads();
+    const uint32_t key = radix_cut<TT>(sh, rp, V, cT, Rf, use_k, use_p, k, tp, lane, warp);
+    if (threadIdx.x == 0) tau[row] = key_value(key);
+    return;
+  }
+  // key 0: nothing cut (top-p keeps the whole row)
+  const uint32_t key = key_k > key_p ? key_k : key_p;
+  if (threadIdx.x == 0) tau[row] = key ? key_value(key) : -INF;
 }
 
 }  // namespace
@@ -330,10 +636,25 @@ int launch_sampling_cut(const void* target, int32_t dtype, int32_t B, int32_t R,
                         cudaStream_t stream) {
   const int64_t rows = (int64_t)B * R;
   const auto* t = static_cast<const unsigned char*>(target);
+  // the kernels' shared-memory opt-in, once per device (no runtime call
+  // besides the launch afterwards, so launches can be captured in graphs)
+  constexpr int kMaxDev = 64;
+  static bool attr_done[kMaxDev] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return SAMSPEC_ECUDA;
+  const int smem = (int)sizeof(CutSmem);
+  if (!attr_done[dev]) {
+    if (cudaFuncSetAttribute(cut_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(cut_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+      return SAMSPEC_ECUDA;
+    attr_done[dev] = true;
+  }
   if (dtype == SAMSPEC_F32)
-    cut_kernel<0><<<(unsigned)rows, kThr, 0, stream>>>(t, R, V, temp, top_k, top_p, tau);
+    cut_kernel<0><<<(unsigned)rows, kThr, smem, stream>>>(t, R, V, temp, top_k, top_p, tau);
   else
-    cut_kernel<1><<<(unsigned)rows, kThr, 0, stream>>>(t, R, V, temp, top_k, top_p, tau);
+    cut_kernel<1><<<(unsigned)rows, kThr, smem, stream>>>(t, R, V, temp, top_k, top_p, tau);
   return cudaGetLastError() == cudaSuccess ? SAMSPEC_OK : SAMSPEC_ECUDA;
 }
 

@@ -83,7 +83,7 @@ def test_sampling_entry_points_reject_bad_arguments_on_the_host():
         return lib.spec_sampling_cut(target, dtype, B, R, V, temp, p, p, p, None)
 
     assert cut(target=None) == bd.EINVAL and cut(temp=None) == bd.EINVAL
-    assert cut(R=34) == bd.ESIZE and cut(V=(1 << 22) + 1) == bd.ESIZE and cut(B=0) == bd.ESIZE
+    assert cut(R=34) == bd.ESIZE and cut(V=(1 << 21) + 1) == bd.ESIZE and cut(B=0) == bd.ESIZE
     assert cut(dtype=9) == bd.EDTYPE
     assert cut(target=ctypes.c_void_p(4100)) == bd.EALIGN
 
