@@ -64,7 +64,7 @@ struct CutSmem {
   uint32_t cnt[kBins];
   unsigned long long mass[kBins];
   // log-scale bins of the term 2^(l cT - R): exact counts, and masses
-  // relative to each bin's upper edge in units of 2^-10 (lmassr; about 1e-3
+  // relative to each bin's centre in units of 2^-10 (lmassr; about 1e-3
   // accurate: they only choose which bins to collect), turned into fp32
   // masses (lmass) before the scans
   uint32_t lcnt[kLogBins];
@@ -83,18 +83,26 @@ struct CutSmem {
   double dscr[4];  // broadcast scratch
 };
 
-// Log-scale bin (digit, higher = larger logit) of y = l cT - R <= ~0: 32 bins
-// per octave of the term 2^y, the last bin holding everything below 2^-32.
-__device__ __forceinline__ uint32_t log_digit(float y) {
-  const int b = __float2int_rz(-y * 32.f);
-  return (uint32_t)(kLogBins - 1 - min(max(b, 0), kLogBins - 1));
+// Log-scale bin of y = l cT - R <= ~0: b = round(-32 y) clamped to
+// [0, kLogBins - 1] (32 bins per octave of the term 2^y, the last holding
+// everything below about 2^-32), returned as the digit kLogBins - 1 - b
+// (higher = larger logit) and as the float bf = b.  The rounding goes through
+// the 1.5 * 2^23 shift on the FMA pipe, not a conversion instruction.
+__device__ __forceinline__ uint32_t log_digit(float y, float& bf) {
+  const float v = fminf(fmaxf(-32.f * y, 0.f), (float)(kLogBins - 1));
+  const float t = v + 12582912.f;
+  bf = t - 12582912.f;
+  return (uint32_t)(kLogBins - 1) - (__float_as_uint(t) - 0x4B400000u);
 }
-// The term 2^y relative to the upper edge 2^(-b/32) of its bin (digit d,
-// b = kLogBins - 1 - d), in units of 2^-10: between about 1002 and 1024 (0 for
-// the tiny terms of the last bin).
-__device__ __forceinline__ uint32_t rel_mass(float y, uint32_t d) {
-  const float b = (float)(kLogBins - 1 - (int)d);
-  return __float2uint_rn(ex2_approx(fmaf(b, 0.03125f, y)) * 1024.f);
+__device__ __forceinline__ uint32_t log_digit(float y) {
+  float bf;
+  return log_digit(y, bf);
+}
+// The term 2^y relative to its bin's centre 2^(-b/32), in units of 2^-10:
+// between about 1013 and 1035 (0 for the tiny terms of the last bin).
+__device__ __forceinline__ uint32_t rel_mass(float y, float bf) {
+  const float r = ex2_approx(fmaf(bf, 0.03125f, y));
+  return __float_as_uint(fmaf(r, 1024.f, 12582912.f)) - 0x4B400000u;
 }
 // A running sum as a float pair (each addition's rounding error carried in
 // lo), read out in fp64.
@@ -454,10 +462,11 @@ __global__ void __launch_bounds__(kThr, 4) cut_kernel(const unsigned char* targe
   visit_row<TT>(rp, V, [&](float x, bool ok) {
     if (!ok) return;
     const float y = fmaf(x, cT, -Rf);
-    const uint32_t d = log_digit(y);
+    float bf;
+    const uint32_t d = log_digit(y, bf);
     atomicAdd(&sh.lcnt[d], 1u);
     if (use_p) {
-      atomicAdd(&sh.lmassr[d], rel_mass(y, d));
+      atomicAdd(&sh.lmassr[d], rel_mass(y, bf));
       if (!use_k) s_all.add(ex2_approx(y));
     }
   });
