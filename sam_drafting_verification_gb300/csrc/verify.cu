@@ -153,6 +153,7 @@ struct Smem {
   int32_t claims;       // sequences claimed by this CTA
   int32_t pool_left;    // sequences not yet claimed, as of this CTA's last claim
   int32_t claim_lock;   // one control warp claims at a time
+  int32_t pool_done;    // a claim found no sequence left: idle slots leave
   int32_t tile_cnt[kSlots][kMaxChunks];  // consumer warps done with each tile of a job
   float4 pre[kSlots][kMaxChunks][2];     // control: mass before each tile {hi, lo, ref, 0}
 };
@@ -679,10 +680,11 @@ struct Control {
   int32_t par_;       // trees: parent of node `lane`
   int32_t pathv;      // trees: the node accepted at depth `lane`
   float ua, ur;       // coins of the row in flight (drawn while it streams)
+  bool first_;        // slot 0's first claim: sequence blockIdx.x, no atomic
 
   __device__ Control(const VParams& p, Smem& s, const float4* r, int l, int slot)
       : P(p), sm(s), rec(r), lane(l), si(slot), more(true), tok(-1), par_(-1), pathv(-1),
-        ua(0.f), ur(0.f) {
+        ua(0.f), ur(0.f), first_(slot == 0) {
     reset_row();
   }
 
@@ -742,6 +744,7 @@ struct Control {
       // candidates, left out of the row's sums
       const unsigned cm = __ballot_sync(kFullMask, lane <= P.K && par_ == j && lane > 0);
       if ((cm >> lane) & 1u) S.ex[__popc(cm & ((1u << lane) - 1u))] = tok;
+      __syncwarp();  // the lanes' entries before lane 0 publishes the job
       if (lane == 0) {
         S.kind = kind;
         S.j = j;
@@ -806,9 +809,13 @@ struct Control {
     while (more) {
       uint32_t b = 0;
       if (lane == 0) {
-        b = atomicAdd(&P.ws[0], 1u);
+        // CTA x's first sequence is x (grid <= B); later ones come from the
+        // shared counter, past the first gridDim.x
+        b = first_ ? blockIdx.x : gridDim.x + atomicAdd(&P.ws[0], 1u);
         vstore(&sm.pool_left, b >= (uint32_t)P.B ? 0 : P.B - 1 - (int)b);
+        if (b >= (uint32_t)P.B) vstore(&sm.pool_done, 1);
       }
+      first_ = false;
       b = __shfl_sync(kFullMask, b, 0);
       if (b >= (uint32_t)P.B) {
         more = false;
@@ -1355,6 +1362,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
     sm.claims = 0;
     sm.pool_left = P.B;
     sm.claim_lock = 0;
+    sm.pool_done = 0;
     for (int s = 0; s < kSlots; ++s)
       for (int c = 0; c < kMaxChunks; ++c) sm.tile_cnt[s][c] = 0;
     mbar_fence_init();
@@ -1609,6 +1617,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       if (vload(&sm.abort)) break;
       const int st = __shfl_sync(kFullMask, vload(&S.state), 0);
       if (st == kEmpty) {
+        // nothing left to claim (another slot found the pool empty)
+        if (__shfl_sync(kFullMask, vload(&sm.pool_done), 0)) break;
         // claim when this is the CTA's first sequence, or when no row is queued
         // and the producer has issued everything (its ring covers the claim)
         int go = 0;
@@ -1693,7 +1703,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         // this slot's sequence, and (slot 0) any nobody will claim now
         if (S.state != kEmpty) write_result(P, S.b, -1, -1, SAMSPEC_ST_TIMEOUT);
         if (si == 0)
-          for (uint32_t b = atomicAdd(&P.ws[0], 1u); b < (uint32_t)P.B; b = atomicAdd(&P.ws[0], 1u))
+          for (uint32_t b = gridDim.x + atomicAdd(&P.ws[0], 1u); b < (uint32_t)P.B;
+               b = gridDim.x + atomicAdd(&P.ws[0], 1u))
             write_result(P, (int)b, -1, -1, SAMSPEC_ST_TIMEOUT);
       }
       __threadfence_block();
