@@ -47,24 +47,31 @@ POOL = 16
 # reports null until it is captured again.
 VERIFY_TRAFFIC = {
     "rs_bf16_b64": {"bytes": 19538176.0, "profile": "profiles/verify_kernel_rs_bf16_b64.md",
-                    "verify_cu_sha256": "778ec0f73d36e26a115e4014cd7f73ef066ed28ae8ee284e5a580bd44b24fd9e"},
-    "long_rollout_b256": {"bytes": 78979955.0, "profile": "profiles/launches_long_rollout_b256.md",
-                          "verify_cu_sha256": "778ec0f73d36e26a115e4014cd7f73ef066ed28ae8ee284e5a580bd44b24fd9e"},
-    "tree_b256": {"bytes": 162061312.0, "profile": "profiles/verify_kernel_tree_b256.md",
-                  "verify_cu_sha256": "778ec0f73d36e26a115e4014cd7f73ef066ed28ae8ee284e5a580bd44b24fd9e"},
+                    "verify_cu_sha256": "501dfc92dfa938d5aaadc35a389107c2249f8a4a90a8c3e282f45d804219eb47"},
+    "long_rollout_b256": {"bytes": 78981542.0, "profile": "profiles/launches_long_rollout_b256.md",
+                          "verify_cu_sha256": "501dfc92dfa938d5aaadc35a389107c2249f8a4a90a8c3e282f45d804219eb47"},
+    "tree_b256": {"bytes": 161624064.0, "profile": "profiles/verify_kernel_tree_b256.md",
+                  "verify_cu_sha256": "501dfc92dfa938d5aaadc35a389107c2249f8a4a90a8c3e282f45d804219eb47"},
 }
+# the same for the sampling cut kernel (sampling.cu)
+CUT_TRAFFIC = {"sampling_b256": {"bytes": 715230720.0, "profile": "profiles/cut_kernel_sampling_b256.md",
+                                 "sampling_cu_sha256": "cb016df5c8130e13c893d8317ab5bb2dc2dc34ff38f2792725ca666fc4fac19a"}}
+
+
+def _traffic(table, workload, source):
+    import hashlib
+    t = table.get(workload)
+    if t is None:
+        return None
+    src = os.path.join(ROOT, "sam_drafting_verification_gb300", "csrc", source)
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != t[source.replace(".", "_") + "_sha256"]:
+            return None
+    return t["bytes"]
 
 
 def _verify_traffic(workload):
-    import hashlib
-    t = VERIFY_TRAFFIC.get(workload)
-    if t is None:
-        return None
-    src = os.path.join(ROOT, "sam_drafting_verification_gb300", "csrc", "verify.cu")
-    with open(src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != t["verify_cu_sha256"]:
-            return None
-    return t["bytes"]
+    return _traffic(VERIFY_TRAFFIC, workload, "verify.cu")
 
 
 def _peaks():
@@ -1048,7 +1055,7 @@ def run_sampling(args, ws, rank, dev):
     # cut: every row once from HBM; verification: the rows its chains needed
     alg_cut = B * (K + 1) * V * 2
     alg_ver = rows_per_seq * B * V * 2
-    ach = (alg_cut + alg_ver) / (ms / 1e3) / 1e9
+    ach = alg_cut / (ms_cut / 1e3) / 1e9  # the cut kernel: every row read once
     cpu = None
     if rank == 0:
         nb = 16
@@ -1068,8 +1075,10 @@ def run_sampling(args, ws, rank, dev):
                        "temperature": list(SAMPLING_T), "top_k": list(SAMPLING_TOP_K),
                        "top_p": list(SAMPLING_TOP_P), "l2": "two 311 MB step tensors alternate",
                        "timing": f"CUDA graph of {reps} steps (cut + verify launches)"},
-            "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
-                         "frac": round(ach / hbm, 4), "traffic": None, "peak_source": peak_kind,
+            "roofline": {"kernel": "cut_kernel<bf16>", "bound": "hbm", "achieved": round(ach, 1), "peak": hbm,
+                         "unit": "GB/s", "frac": round(ach / hbm, 4),
+                         "traffic": _traffic(CUT_TRAFFIC, "sampling_b256", "sampling.cu"),
+                         "peak_source": peak_kind, "algorithmic_bytes_per_launch": round(alg_cut, 1),
                          "algorithmic_bytes_per_step": round(alg_cut + alg_ver, 1)},
             "cpu_baseline": cpu, "gpu_launches": 2 * reps, "clocks": clocks,
             "breakdown": {"cut_us": round(ms_cut * 1e3, 2), "verify_us": round((ms - ms_cut) * 1e3, 2),
