@@ -1075,7 +1075,7 @@ def run_sampling(args, ws, rank, dev):
                        "temperature": list(SAMPLING_T), "top_k": list(SAMPLING_TOP_K),
                        "top_p": list(SAMPLING_TOP_P), "l2": "two 311 MB step tensors alternate",
                        "timing": f"CUDA graph of {reps} steps (cut + verify launches)"},
-            "roofline": {"kernel": "cut_kernel<bf16>", "bound": "hbm", "achieved": round(ach, 1), "peak": hbm,
+            "roofline": {"kernel": "cut_hist_kernel (bf16)", "bound": "hbm", "achieved": round(ach, 1), "peak": hbm,
                          "unit": "GB/s", "frac": round(ach / hbm, 4),
                          "traffic": _traffic(CUT_TRAFFIC, "sampling_b256", "sampling.cu"),
                          "peak_source": peak_kind, "algorithmic_bytes_per_launch": round(alg_cut, 1),

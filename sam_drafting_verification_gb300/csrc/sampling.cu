@@ -59,7 +59,8 @@ constexpr int kLogBins = 1024;  // 32 per octave of the term, 32 octaves
 constexpr int kCap = 4096;     // boundary logits held in shared memory (a power of two:
                                // the sort pads to one)
 
-struct CutSmem {
+template <int NT>
+struct CutSmemT {
   // radix levels over keys (the path for rows whose boundary bins overflow)
   uint32_t cnt[kBins];
   unsigned long long mass[kBins];
@@ -73,8 +74,8 @@ struct CutSmem {
   // the logits of the boundary bins: keys and terms
   uint32_t bkey[kCap];
   float bmass[kCap];
-  double tsum[kThr];  // per-thread partial sums
-  float red[kThr / 32];
+  double tsum[NT];  // per-thread partial sums
+  float red[NT / 32];
   uint32_t nbuf;
   uint32_t idx;
   // broadcast of warp 0's choices
@@ -82,6 +83,7 @@ struct CutSmem {
   uint32_t key;
   double dscr[4];  // broadcast scratch
 };
+using CutSmem = CutSmemT<kThr>;
 
 // Log-scale bin of y = l cT - R <= ~0: b = round(-32 y) clamped to
 // [0, kLogBins - 1] (32 bins per octave of the term 2^y, the last holding
@@ -138,7 +140,7 @@ __device__ __forceinline__ unsigned long long fixed_mass(float y) {
 // the same number of calls (valid = false past the end), so f may use
 // warp-wide collectives.  Rows whose byte length is a multiple of 16 are read
 // in 16-byte vectors.
-template <int TT, typename F>
+template <int TT, int NT = kThr, typename F>
 __device__ __forceinline__ void visit_row(const unsigned char* row, int V, F&& f) {
   constexpr int ES = TT ? 2 : 4;
   constexpr int VEC = 16 / ES;
@@ -146,12 +148,12 @@ __device__ __forceinline__ void visit_row(const unsigned char* row, int V, F&& f
     // kLoads vectors per thread in flight before any is processed
     constexpr int kLoads = 4;
     const int nvec = V / VEC;
-    for (int base = 0; base < nvec; base += kThr * kLoads) {
+    for (int base = 0; base < nvec; base += NT * kLoads) {
       uint4 w[kLoads];
       bool ok[kLoads];
 #pragma unroll
       for (int u = 0; u < kLoads; ++u) {
-        const int i = base + u * kThr + (int)threadIdx.x;
+        const int i = base + u * NT + (int)threadIdx.x;
         ok[u] = i < nvec;
         w[u] = ok[u] ? *reinterpret_cast<const uint4*>(row + (size_t)i * 16) : make_uint4(0u, 0u, 0u, 0u);
       }
@@ -170,7 +172,7 @@ __device__ __forceinline__ void visit_row(const unsigned char* row, int V, F&& f
       }
     }
   } else {
-    for (int base = 0; base < V; base += kThr) {
+    for (int base = 0; base < V; base += NT) {
       const int i = base + (int)threadIdx.x;
       const bool ok = i < V;
       float x = 0.f;
@@ -186,7 +188,8 @@ __device__ __forceinline__ void visit_row(const unsigned char* row, int V, F&& f
 // Adds one logit (when `in`) to bin `digit` of the histogram: the lanes of the
 // warp with the same digit are combined first, one warp reduction per
 // distinct digit present.
-__device__ __forceinline__ void hist_add(CutSmem& sh, bool in, uint32_t digit,
+template <int NT>
+__device__ __forceinline__ void hist_add(CutSmemT<NT>& sh, bool in, uint32_t digit,
                                          unsigned long long fixed, int lane) {
   unsigned todo = __ballot_sync(kFullMask, in);
   // parts of the fixed-point mass that sum without overflow over 32 lanes
@@ -317,8 +320,8 @@ __device__ __forceinline__ float max_nan(float a, float b) {
 
 // The exact cut by radix levels over the keys, streaming the row once per
 // level (used when the boundary bins hold more logits than the buffer).
-template <int TT>
-__device__ uint32_t radix_cut(CutSmem& sh, const unsigned char* rp, int V, float cT, float Rf,
+template <int TT, int NT = kThr>
+__device__ uint32_t radix_cut(CutSmemT<NT>& sh, const unsigned char* rp, int V, float cT, float Rf,
                               bool use_k, bool use_p, int32_t k, float tp, int lane, int warp) {
   constexpr int NLEV = TT ? 2 : 4;
   uint32_t min_key = 0, key_k = 0, key_p = 0;
@@ -330,12 +333,12 @@ __device__ uint32_t radix_cut(CutSmem& sh, const unsigned char* rp, int V, float
     for (int lev = 0; lev < NLEV; ++lev) {
       const int shift = 24 - 8 * lev;
       const uint32_t hmask = lev == 0 ? 0u : (0xffffffffu << (shift + 8));
-      for (int i = threadIdx.x; i < kBins; i += kThr) {
+      for (int i = threadIdx.x; i < kBins; i += NT) {
         sh.cnt[i] = 0;
         sh.mass[i] = 0;
       }
       __syncthreads();
-      visit_row<TT>(rp, V, [&](float x, bool ok) {
+      visit_row<TT, NT>(rp, V, [&](float x, bool ok) {
         const uint32_t u = order_key(x);
         const bool in = ok && u >= min_key && (u & hmask) == (prefix & hmask);
         const unsigned long long fx = in ? fixed_mass(fmaf(x, cT, -Rf)) : 0ull;
@@ -410,16 +413,19 @@ __device__ void sort_buffer(CutSmem& sh, uint32_t n) {
   }
 }
 
+// tau of a bf16 row left to the general path by the histogram kernel (a NaN
+// payload no other outcome writes)
+constexpr uint32_t kRetryBits = 0x7fc0a5a5u;
+
+// The cut of one row by the general path: the row maximum, log-scale bins,
+// the boundary bins collected and sorted, with radix selection behind them.
 template <int TT>
-__global__ void __launch_bounds__(kThr, 4) cut_kernel(const unsigned char* target, int32_t R, int32_t V,
-                                                   const float* temp, const int32_t* top_k,
-                                                   const float* top_p, float* tau) {
+__device__ void cut_row(CutSmem& sh, const unsigned char* target, int64_t row, int32_t R,
+                        int32_t V, const float* temp, const int32_t* top_k, const float* top_p,
+                        float* tau) {
   constexpr int ES = TT ? 2 : 4;
-  extern __shared__ __align__(16) unsigned char cut_dsm[];
-  CutSmem& sh = *reinterpret_cast<CutSmem*>(cut_dsm);
   const float INF = __int_as_float(0x7f800000);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t row = blockIdx.x;
   const int64_t b = row / R;
   const float T = temp[b];
   const int32_t k = top_k[b];
@@ -638,6 +644,396 @@ __global__ void __launch_bounds__(kThr, 4) cut_kernel(const unsigned char* targe
   if (threadIdx.x == 0) tau[row] = key ? key_value(key) : -INF;
 }
 
+// Rows blockIdx.x, blockIdx.x + gridDim.x, ... by the general path; with
+// only_marked, just the rows whose tau holds kRetryBits.
+template <int TT>
+__global__ void __launch_bounds__(kThr, 4) cut_kernel(const unsigned char* target, int64_t rows,
+                                                   int32_t R, int32_t V, const float* temp,
+                                                   const int32_t* top_k, const float* top_p,
+                                                   float* tau, int only_marked) {
+  extern __shared__ __align__(16) unsigned char cut_dsm[];
+  CutSmem& sh = *reinterpret_cast<CutSmem*>(cut_dsm);
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    if (only_marked && __float_as_uint(tau[row]) != kRetryBits) continue;
+    __syncthreads();  // the previous row is done with the shared memory
+    cut_row<TT>(sh, target, row, R, V, temp, top_k, top_p, tau);
+  }
+}
+
+// ---- bf16 rows: an exact count per bit pattern ------------------------------
+//
+// A bf16 logit is one of 65,536 bit patterns, so a count per pattern describes
+// the row exactly: the k-th largest value and every mass sum follow from the
+// counts, with no sort and no exponential per logit.  Counts are the 16-bit
+// halves of 32-bit shared-memory words (pattern p in word p >> 1, half p & 1;
+// 128 KB).  A row holding more than 65,535 copies of one value wraps a half;
+// the total count shows it, and such a row is marked for the general path (a
+// second launch that cuts only the marked rows).
+// Each row is streamed once, one shared atomic per logit.  A mass is computed
+// once per non-empty pattern, count x 2^((v - vmax) log2(e) / T) in fixed
+// point (units of 2^-42), so every prefix sum is exact and independent of the
+// order of the additions, and the top-p crossing is decided exactly.
+//
+// The patterns fall into 1024 chunks of 64 (32 words).  Chunks below 512 hold
+// positive values (larger with the index), the others negative ones (smaller
+// with the index), so in descending order of value they come as 511, 510,
+// ..., 0, 512, ..., 1023 (+0 and -0, patterns 0 and 0x8000, meet at the
+// seam).  After the pass, the warps reduce every chunk to a total (lanes read
+// consecutive words, so without bank conflicts), thread t scans chunk t's
+// total in that order, and the chunk where a running sum crosses its target
+// is walked by a warp, one word per lane.
+//
+// One persistent CTA of 1024 threads per SM takes rows blockIdx.x,
+// blockIdx.x + gridDim.x, ...; while it works on one, the bulk-copy engine
+// prefetches its next row into L2.
+
+constexpr int kHT = 1024;       // threads of the histogram kernel (one per chunk)
+constexpr int kHWords = 32768;  // 65,536 patterns, two counts per word
+constexpr int kChunks = 1024;   // 64 patterns, 32 words each
+static_assert(kChunks == kHT && kHWords == 32 * kChunks, "one chunk per thread");
+
+struct HistScratch {
+  unsigned long long wm[32];  // per-warp scan totals (masses), by rank
+  uint32_t wc[32];            // per-warp scan totals (counts), by rank
+  uint32_t wsp[32];           // per-warp flags
+  uint32_t wmax[32];          // per-warp largest value-order keys
+  unsigned long long kmrun, prun;
+  uint32_t krun, kchunk, pchunk;
+};
+
+// Value order of a pattern: okey16(a) > okey16(b) iff value(a) > value(b)
+// (NaN patterns aside; -0 sits just below +0).
+__device__ __forceinline__ uint32_t okey16(uint32_t p) {
+  return p < 0x8000u ? 0x8000u + p : 0xffffu - p;
+}
+// okey16 of both patterns of a word at once.
+__device__ __forceinline__ uint32_t okey16x2(uint32_t w) {
+  const uint32_t s2 = (w >> 15) & 0x00010001u;
+  return w ^ (s2 * 0x7fffu) ^ 0x80008000u;
+}
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float pattern_value(uint32_t p) { return __uint_as_float(p << 16); }
+__device__ __forceinline__ uint32_t half_count(uint32_t w, uint32_t p) {
+  return (p & 1u) ? (w >> 16) : (w & 0xffffu);
+}
+// Exclusive prefixes, in descending order of the threads' chunks, of the
+// per-thread counts c and masses m (the masses only when with_mass), with
+// their totals, and the OR of the flags f.  One barrier; called by every
+// thread.
+struct ChunkScan {
+  uint32_t c_ex, c_tot, flags;
+  unsigned long long m_ex, m_tot;
+};
+__device__ ChunkScan chunk_scan(HistScratch& hs, uint32_t c, unsigned long long m, uint32_t f,
+                                bool with_mass, int lane, int warp) {
+  const bool rev = warp < kHT / 64;  // positive chunks: higher lanes come first
+  uint32_t ci = c;
+  unsigned long long mi = with_mass ? m : 0ull;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const bool take = rev ? lane + o < 32 : lane >= o;
+    const uint32_t uc = rev ? __shfl_down_sync(kFullMask, ci, o) : __shfl_up_sync(kFullMask, ci, o);
+    if (take) ci += uc;
+    if (with_mass) {
+      const unsigned long long um =
+          rev ? __shfl_down_sync(kFullMask, mi, o) : __shfl_up_sync(kFullMask, mi, o);
+      if (take) mi += um;
+    }
+  }
+  const uint32_t wf = __reduce_or_sync(kFullMask, f);
+  const int wr = rev ? kHT / 64 - 1 - warp : warp;
+  if (lane == (rev ? 0 : 31)) {
+    hs.wc[wr] = ci;
+    hs.wm[wr] = mi;
+    hs.wsp[wr] = wf;
+  }
+  __syncthreads();
+  ChunkScan o;
+  o.flags = __reduce_or_sync(kFullMask, hs.wsp[lane]);
+  const uint32_t tc = hs.wc[lane];
+  uint32_t tci = tc;
+#pragma unroll
+  for (int q = 1; q < 32; q <<= 1) {
+    const uint32_t u = __shfl_up_sync(kFullMask, tci, q);
+    if (lane >= q) tci += u;
+  }
+  o.c_ex = __shfl_sync(kFullMask, tci - tc, wr) + ci - c;
+  o.c_tot = __shfl_sync(kFullMask, tci, 31);
+  o.m_ex = o.m_tot = 0;
+  if (with_mass) {
+    const unsigned long long tm = hs.wm[lane];
+    unsigned long long tmi = tm;
+#pragma unroll
+    for (int q = 1; q < 32; q <<= 1) {
+      const unsigned long long u = __shfl_up_sync(kFullMask, tmi, q);
+      if (lane >= q) tmi += u;
+    }
+    o.m_ex = __shfl_sync(kFullMask, tmi - tm, wr) + mi - m;
+    o.m_tot = __shfl_sync(kFullMask, tmi, 31);
+  }
+  return o;
+}
+
+// Walks chunk c in descending order of value, one word per lane, from `run`
+// (the weight of everything above the chunk) and returns the first pattern at
+// which the running weight reaches `target` (the chunk's last non-empty one
+// if it never does).  weight(c, p): the weight of the c logits of pattern p.
+template <typename U, typename Wt>
+__device__ uint32_t chunk_step(const uint32_t* hist, uint32_t c, int lane, U run, U target,
+                               Wt&& weight) {
+  const bool pos = c < kChunks / 2;
+  const uint32_t word = 32 * c + (pos ? 31 - lane : lane);
+  const uint32_t w = hist[word];
+  const uint32_t pf = pos ? 2 * word + 1 : 2 * word;  // the larger value of the two
+  const uint32_t ps = pf ^ 1u;
+  const U a = weight(half_count(w, pf), pf);
+  const U b = weight(half_count(w, ps), ps);
+  U inc = a + b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const U u = __shfl_up_sync(kFullMask, inc, o);
+    if (lane >= o) inc += u;
+  }
+  const U before = run + inc - a - b;
+  unsigned hit = __ballot_sync(kFullMask, before + a + b >= target);
+  uint32_t res = before + a >= target ? pf : ps;
+  if (!hit) {  // not reached: the last pattern with weight
+    hit = __ballot_sync(kFullMask, a + b > 0);
+    res = b > 0 ? ps : pf;
+    return hit ? __shfl_sync(kFullMask, res, 31 - __clz(hit)) : pf;
+  }
+  return __shfl_sync(kFullMask, res, __ffs(hit) - 1);
+}
+
+// ceil(tp * Z) for a float tp in (0, 1) and Z < 2^63, exactly.
+__device__ __forceinline__ unsigned long long mul_ceil(unsigned long long Z, float tp) {
+  const uint32_t bits = __float_as_uint(tp);
+  uint32_t e = bits >> 23;
+  unsigned long long m = bits & 0x7fffffu;
+  if (e) m |= 0x800000u;
+  else e = 1;
+  const int s = 150 - (int)e;  // tp = m 2^-s, s >= 24
+  const unsigned long long lo = Z * m, hi = __umul64hi(Z, m);
+  unsigned long long q;
+  bool rem;
+  if (s < 64) {
+    q = (lo >> s) | (hi << (64 - s));
+    rem = (lo & ((1ull << s) - 1)) != 0;
+  } else if (s < 128) {
+    const int r = s - 64;
+    q = r ? hi >> r : hi;
+    rem = lo != 0 || (r && (hi & ((1ull << r) - 1)) != 0);
+  } else {
+    q = 0;
+    rem = lo != 0 || hi != 0;
+  }
+  return q + (rem ? 1ull : 0ull);
+}
+
+// floor(t 2^42) for t in [0, 1], from the float's fields (no conversion
+// instruction).
+__device__ __forceinline__ unsigned long long fixed42(float t) {
+  const uint32_t bits = __float_as_uint(t);
+  const int e = (int)(bits >> 23);
+  const uint32_t m = (bits & 0x7fffffu) | 0x800000u;
+  if (e >= 108) return (unsigned long long)m << ((e - 108) & 63);
+  return e > 84 ? (unsigned long long)(m >> (108 - e)) : 0ull;
+}
+
+// Sum over the warp of values below 2^63 (three 21-bit parts through
+// redux.sync).
+__device__ __forceinline__ unsigned long long warp_sum63(unsigned long long v) {
+  const uint32_t p0 = __reduce_add_sync(kFullMask, (uint32_t)(v & 0x1fffffu));
+  const uint32_t p1 = __reduce_add_sync(kFullMask, (uint32_t)((v >> 21) & 0x1fffffu));
+  const uint32_t p2 = __reduce_add_sync(kFullMask, (uint32_t)(v >> 42));
+  return (unsigned long long)p0 + ((unsigned long long)p1 << 21) + ((unsigned long long)p2 << 42);
+}
+
+// Prefetches bytes [a, b) of global memory into L2 (16-byte aligned inside),
+// in 32 KB pieces spread over the lanes of one warp.
+__device__ __forceinline__ void prefetch_l2(const unsigned char* a, const unsigned char* b,
+                                            int lane) {
+  const uintptr_t a0 = ((uintptr_t)a + 15) & ~(uintptr_t)15;
+  const uintptr_t a1 = (uintptr_t)b & ~(uintptr_t)15;
+  constexpr uintptr_t kPiece = 32768;
+  for (uintptr_t o = a0 + (uintptr_t)lane * kPiece; o < a1; o += 32 * kPiece) {
+    const uint32_t n = (uint32_t)(a1 - o < kPiece ? a1 - o : kPiece);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(o), "r"(n) : "memory");
+  }
+}
+
+// Adds the two bf16 patterns of word w to the histogram.
+__device__ __forceinline__ void count_pair(uint32_t* hist, uint32_t w) {
+  atomicAdd(&hist[(w >> 1) & 0x7fffu], (w & 1u) * 0xffffu + 1u);
+  atomicAdd(&hist[w >> 17], ((w >> 16) & 1u) * 0xffffu + 1u);
+}
+
+__global__ void __launch_bounds__(kHT, 1)
+    cut_hist_kernel(const unsigned char* target, int64_t rows, int32_t R, int32_t V,
+                    const float* temp, const int32_t* top_k, const float* top_p, float* tau) {
+  extern __shared__ __align__(16) unsigned char hist_dsm[];
+  uint32_t* hist = reinterpret_cast<uint32_t*>(hist_dsm);
+  HistScratch& hs = *reinterpret_cast<HistScratch*>(hist_dsm + (size_t)kHWords * 4);
+  const float INF = __int_as_float(0x7f800000);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const size_t row_bytes = (size_t)V * 2;
+  if (warp == 0 && (int64_t)blockIdx.x < rows) {
+    const unsigned char* r0 = target + (size_t)blockIdx.x * row_bytes;
+    prefetch_l2(r0, r0 + row_bytes, lane);
+  }
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const int64_t b = row / R;
+    const float T = temp[b];
+    const int32_t k = top_k[b];
+    const float tp = top_p[b];
+    if (!(T > 0.f) || !(T < INF) || !(tp > 0.f)) {
+      if (tid == 0) tau[row] = __int_as_float(0x7fc00000);
+      continue;
+    }
+    const bool use_k = k > 0 && k < V;
+    const bool use_p = tp < 1.f;
+    if (!use_k && !use_p) {
+      if (tid == 0) tau[row] = -INF;
+      continue;
+    }
+    const unsigned char* rp = target + (size_t)row * row_bytes;
+    if (warp == 0 && row + gridDim.x < rows) {
+      const unsigned char* rn = rp + (size_t)gridDim.x * row_bytes;
+      prefetch_l2(rn, rn + row_bytes, lane);
+    }
+    __syncthreads();  // the previous row's readers are done
+    for (int i = tid; i < kHWords / 4; i += kHT)
+      reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    // 1. one pass over the row: a count per bit pattern, and the largest
+    // value-order key
+    uint32_t kmax2 = 0;
+    if ((row_bytes & 15) == 0) {
+      const uint4* rv = reinterpret_cast<const uint4*>(rp);
+      const int nvec = V >> 3;
+      constexpr int kLoads = 4;
+      for (int base = 0; base < nvec; base += kHT * kLoads) {
+        uint4 w[kLoads];
+#pragma unroll
+        for (int u = 0; u < kLoads; ++u) {
+          const int i = base + u * kHT + tid;
+          if (i < nvec) w[u] = __ldcs(rv + i);
+        }
+#pragma unroll
+        for (int u = 0; u < kLoads; ++u) {
+          if (base + u * kHT + tid < nvec) {
+            count_pair(hist, w[u].x);
+            count_pair(hist, w[u].y);
+            count_pair(hist, w[u].z);
+            count_pair(hist, w[u].w);
+            kmax2 = max_u16x2(kmax2, max_u16x2(max_u16x2(okey16x2(w[u].x), okey16x2(w[u].y)),
+                                               max_u16x2(okey16x2(w[u].z), okey16x2(w[u].w))));
+          }
+        }
+      }
+    } else {
+      const uint16_t* rs = reinterpret_cast<const uint16_t*>(rp);
+      for (int i = tid; i < V; i += kHT) {
+        const uint32_t p = rs[i];
+        atomicAdd(&hist[p >> 1], (p & 1u) * 0xffffu + 1u);
+        kmax2 = max(kmax2, okey16(p));
+      }
+    }
+    {
+      const uint32_t km = __reduce_max_sync(kFullMask, max(kmax2 & 0xffffu, kmax2 >> 16));
+      if (lane == 0) hs.wmax[warp] = km;
+    }
+    __syncthreads();
+    const uint32_t kmax = __reduce_max_sync(kFullMask, hs.wmax[lane]);
+    const float vmax = pattern_value(kmax >= 0x8000u ? kmax - 0x8000u : 0xffffu - kmax);
+    const float cT = 1.44269504088896341f / T;
+    // a pattern's mass, count x 2^((v - vmax) log2(e) / T), units of 2^-42
+    const auto mass = [=](uint32_t c, uint32_t p) -> unsigned long long {
+      return (unsigned long long)c * fixed42(ex2_approx((pattern_value(p) - vmax) * cT));
+    };
+    // 2. thread t: the count and (top-p) the mass of chunk t; lanes start at
+    // different words of their chunks, so a warp's reads hit distinct banks.
+    // Chunks 510, 511 and 1023 hold only +inf and NaN patterns, chunk 1022
+    // -inf (pattern 0xff80, the low half of its first word) and NaNs.
+    uint32_t cnt = 0;
+    unsigned long long m0 = 0, m1 = 0;
+#pragma unroll 4
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t word = 32 * tid + ((j + lane) & 31);
+      const uint32_t w = hist[word];
+      cnt += (w & 0xffffu) + (w >> 16);
+      if (use_p && w) {
+        m0 += mass(w & 0xffffu, 2 * word);
+        m1 += mass(w >> 16, 2 * word + 1);
+      }
+    }
+    uint32_t special = 0;
+    if (tid == 510 || tid == 511 || tid == 1023) special = cnt != 0;
+    else if (tid == 1022) special = cnt != (hist[0x7fc0] & 0xffffu);
+    const unsigned long long mine = m0 + m1;
+    const ChunkScan sc = chunk_scan(hs, cnt, mine, special, use_p, lane, warp);
+    if (sc.c_tot != (uint32_t)V) {
+      // a count wrapped: the row goes to the general path (a second launch)
+      if (tid == 0) tau[row] = __uint_as_float(kRetryBits);
+      continue;
+    }
+    // the verifier refuses rows with a NaN or +inf, and rows of -inf only
+    if (sc.flags || kmax >= 0xff80u || kmax <= okey16(0xff80u)) {
+      if (tid == 0) tau[row] = -INF;
+      continue;
+    }
+    // 3. the crossing chunks: top-k's where the count from the top reaches k;
+    // top-p's where the mass from the top reaches ceil(top_p * Z_k), Z_k the
+    // mass of the patterns >= tau_k
+    float cut = -INF;
+    unsigned long long need = 0;
+    if (use_k) {
+      if (sc.c_ex < (uint32_t)k && sc.c_ex + cnt >= (uint32_t)k) {
+        hs.kchunk = tid;
+        hs.krun = sc.c_ex;
+        hs.kmrun = sc.m_ex;
+      }
+    } else {
+      need = mul_ceil(sc.m_tot, tp);
+      if (sc.m_ex < need && sc.m_ex + mine >= need) {
+        hs.pchunk = tid;
+        hs.prun = sc.m_ex;
+      }
+    }
+    __syncthreads();
+    if (use_k) {
+      const uint32_t kc = hs.kchunk;
+      cut = pattern_value(chunk_step<uint32_t>(hist, kc, lane, hs.krun, (uint32_t)k,
+                                               [](uint32_t c, uint32_t) { return c; }));
+      if (use_p) {
+        // Z_k: the mass above chunk kc and that of kc's patterns >= tau_k
+        const uint32_t word = 32 * kc + lane;
+        const uint32_t w = hist[word];
+        unsigned long long part = 0;
+        if (pattern_value(2 * word) >= cut) part += mass(w & 0xffffu, 2 * word);
+        if (pattern_value(2 * word + 1) >= cut) part += mass(w >> 16, 2 * word + 1);
+        // tau_k = +0 keeps the -0 logits too (pattern 0x8000, chunk 512)
+        if (kc == 0 && lane == 0) part += mass(hist[0x4000] & 0xffffu, 0x8000u);
+        need = mul_ceil(hs.kmrun + warp_sum63(part), tp);
+        if (sc.m_ex < need && sc.m_ex + mine >= need) {
+          hs.pchunk = tid;
+          hs.prun = sc.m_ex;
+        }
+        __syncthreads();
+      }
+    }
+    // 4. top-p: the pattern of its crossing chunk where the mass reaches need
+    // (at or above tau_k: the inclusive mass at tau_k is Z_k)
+    if (use_p) cut = pattern_value(chunk_step<unsigned long long>(hist, hs.pchunk, lane, hs.prun,
+                                                                  need, mass));
+    if (tid == 0) tau[row] = cut;
+  }
+}
+
 }  // namespace
 
 int launch_sampling_cut(const void* target, int32_t dtype, int32_t B, int32_t R, int32_t V,
@@ -645,25 +1041,40 @@ int launch_sampling_cut(const void* target, int32_t dtype, int32_t B, int32_t R,
                         cudaStream_t stream) {
   const int64_t rows = (int64_t)B * R;
   const auto* t = static_cast<const unsigned char*>(target);
-  // the kernels' shared-memory opt-in, once per device (no runtime call
-  // besides the launch afterwards, so launches can be captured in graphs)
+  // the kernels' shared-memory opt-in and the SM count, once per device (no
+  // runtime call besides the launch afterwards, so launches can be captured
+  // in graphs)
   constexpr int kMaxDev = 64;
   static bool attr_done[kMaxDev] = {false};
+  static int sm_count[kMaxDev] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return SAMSPEC_ECUDA;
   const int smem = (int)sizeof(CutSmem);
+  const int hsmem = kHWords * 4 + (int)sizeof(HistScratch);
   if (!attr_done[dev]) {
     if (cudaFuncSetAttribute(cut_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
             cudaSuccess ||
         cudaFuncSetAttribute(cut_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
+            cudaSuccess ||
+        cudaFuncSetAttribute(cut_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             hsmem) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev) !=
+            cudaSuccess ||
+        sm_count[dev] < 1)
       return SAMSPEC_ECUDA;
     attr_done[dev] = true;
   }
-  if (dtype == SAMSPEC_F32)
-    cut_kernel<0><<<(unsigned)rows, kThr, smem, stream>>>(t, R, V, temp, top_k, top_p, tau);
-  else
-    cut_kernel<1><<<(unsigned)rows, kThr, smem, stream>>>(t, R, V, temp, top_k, top_p, tau);
+  if (dtype == SAMSPEC_F32) {
+    cut_kernel<0><<<(unsigned)rows, kThr, smem, stream>>>(t, rows, R, V, temp, top_k, top_p, tau,
+                                                          0);
+  } else {
+    const int64_t grid = rows < sm_count[dev] ? rows : sm_count[dev];
+    cut_hist_kernel<<<(unsigned)grid, kHT, hsmem, stream>>>(t, rows, R, V, temp, top_k, top_p,
+                                                            tau);
+    if (cudaGetLastError() != cudaSuccess) return SAMSPEC_ECUDA;
+    const int64_t g2 = rows < 4 * (int64_t)sm_count[dev] ? rows : 4 * (int64_t)sm_count[dev];
+    cut_kernel<1><<<(unsigned)g2, kThr, smem, stream>>>(t, rows, R, V, temp, top_k, top_p, tau, 1);
+  }
   return cudaGetLastError() == cudaSuccess ? SAMSPEC_OK : SAMSPEC_ECUDA;
 }
 

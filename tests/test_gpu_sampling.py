@@ -210,3 +210,110 @@ def test_bad_parameters(ss, cuda_device):
     g = ss.spec_verify_sampling(logits, draft, None, T, 5, p)
     assert g["status"].cpu().tolist() == [8, 8, 8, 8, 8, 0]
     assert (g["accept_len"][:5] == -1).all()
+
+
+def _check_cuts(ss, dev, rows_bf16, T, k, p):
+    """Cuts of bf16 rows [B, R, V] against the oracle; returns the number of
+    excused top-p boundary rows."""
+    tl = torch.from_numpy(rows_bf16.astype(np.float32)).to(torch.bfloat16)
+    rows = tl.float().numpy()
+    B, R, V = rows.shape
+    tau = ss.sampling_cut(tl.to(dev), torch.from_numpy(T).to(dev), torch.from_numpy(k).to(dev),
+                          torch.from_numpy(p).to(dev)).cpu().numpy()
+    excused = 0
+    for b in range(B):
+        for r in range(R):
+            res = oracle.truncate_row(rows[b, r], float(T[b]), int(k[b]), float(p[b]))
+            if res is None:  # a row the verifier refuses
+                assert tau[b, r] == -np.inf, (b, r)
+                continue
+            ok, ex = _cut_ok(rows[b, r], float(T[b]), int(k[b]), float(p[b]), float(tau[b, r]), res[1])
+            assert ok, (b, r, T[b], k[b], p[b], tau[b, r], res[1])
+            excused += ex
+    return excused
+
+
+def test_cut_bf16_signed_zeros_infinities_and_ties(ss, cuda_device):
+    """Rows whose cut falls among +0 and -0 (equal values on both sides of the
+    sign), rows with -inf logits (counted by top-k, massless for top-p), rows
+    of few distinct values, and refused rows (NaN, +inf, only -inf)."""
+    rng = np.random.default_rng(31)
+    V = 4096
+    base = []
+    zeros = np.zeros(V, np.float32)
+    zeros[: V // 2] = -0.0
+    zeros[rng.choice(V, 12, replace=False)] = rng.uniform(0.5, 2.0, 12)
+    base.append(zeros)
+    ninf = workloads.gaussian_logits(rng, (V,), 2.0)
+    ninf[rng.choice(V, V - 30, replace=False)] = -np.inf
+    base.append(ninf)
+    few = rng.choice(np.array([-1.0, 0.0, 0.5, 1.0, 3.0], np.float32), V)
+    base.append(few)
+    mixed = workloads.gaussian_logits(rng, (V,), 2.0)
+    mixed[rng.choice(V, 200, replace=False)] = -np.inf
+    mixed[rng.choice(V, 300, replace=False)] = 0.0
+    mixed[rng.choice(V, 300, replace=False)] = -0.0
+    base.append(mixed)
+    params = [(1.0, 5, 1.0), (1.0, 13, 1.0), (0.7, 0, 0.5), (1.0, 40, 0.95), (2.0, 0, 0.999),
+              (1.0, 1000, 1.0), (0.5, 2500, 0.9)]
+    rows = np.stack([np.stack(base)] * len(params))  # [P, 4, V]
+    T = np.array([q[0] for q in params], np.float32)
+    k = np.array([q[1] for q in params], np.int32)
+    p = np.array([q[2] for q in params], np.float32)
+    assert _check_cuts(ss, cuda_device, rows, T, k, p) <= 2
+    bad = workloads.gaussian_logits(rng, (3, 1, V), 2.0)
+    bad[0, 0, 7] = np.nan
+    bad[1, 0, 9] = np.inf
+    bad[2, 0, :] = -np.inf
+    ones = np.ones(3, np.float32)
+    tau = ss.sampling_cut(torch.from_numpy(bad).to(torch.bfloat16).to(cuda_device),
+                          torch.from_numpy(ones).to(cuda_device), 5, 0.9).cpu().numpy()
+    assert (tau == -np.inf).all()
+
+
+@pytest.mark.parametrize("value", [1.0, 1.0078125, -np.inf])
+def test_cut_bf16_many_equal_logits(ss, cuda_device, value):
+    """More than 65,535 logits of one value (bf16 patterns of both parities,
+    and -inf) take the radix path; 65,535 exactly does not.  Both agree with
+    the oracle."""
+    rng = np.random.default_rng(32)
+    V = 151936
+    rows = workloads.gaussian_logits(rng, (3, 2, V), 2.0)
+    for i, n in enumerate((65535, 65536, 120000)):
+        for r in range(2):
+            rows[i, r, rng.choice(V, n, replace=False)] = value
+    T = np.array([1.0, 0.8, 1.0], np.float32)
+    k = np.array([50, 0, 70000], np.int32)
+    p = np.array([0.9, 0.95, 1.0], np.float32)
+    assert _check_cuts(ss, cuda_device, rows, T, k, p) <= 1
+    const = np.full((2, 1, V), value if np.isfinite(value) else 0.5, np.float32)
+    assert _check_cuts(ss, cuda_device, const, np.ones(2, np.float32), np.array([10, 0], np.int32),
+                       np.array([0.5, 0.3], np.float32)) == 0
+
+
+def test_cut_full_vocab_sampled(ss, cuda_device):
+    """The benchmark's shape (V = 151936 bf16, 4 rows per sequence, mixed
+    parameters, more rows than SMs): every row cut on the device, 24 sampled
+    rows checked against the oracle."""
+    rng = np.random.default_rng(33)
+    B, R, V = 96, 4, 151936
+    logits = workloads.gaussian_logits(rng, (B, R, V), 2.0)
+    tl = torch.from_numpy(logits).to(torch.bfloat16)
+    rows = tl.float().numpy()
+    T = rng.choice([0.6, 0.8, 1.0], B).astype(np.float32)
+    k = rng.choice([0, 20, 50], B).astype(np.int32)
+    p = rng.choice([0.9, 0.95, 1.0], B).astype(np.float32)
+    dev = cuda_device
+    tau = ss.sampling_cut(tl.to(dev), torch.from_numpy(T).to(dev), torch.from_numpy(k).to(dev),
+                          torch.from_numpy(p).to(dev)).cpu().numpy()
+    excused = 0
+    for i in rng.choice(B * R, 24, replace=False):
+        b, r = divmod(int(i), R)
+        if k[b] == 0 and p[b] >= 1.0:
+            assert tau[b, r] == -np.inf
+            continue
+        _, to = oracle.truncate_row(rows[b, r], float(T[b]), int(k[b]), float(p[b]))
+        ok, ex = _cut_ok(rows[b, r], float(T[b]), int(k[b]), float(p[b]), float(tau[b, r]), to)
+        assert ok, (b, r, tau[b, r], to)
+        excused += ex
+    assert excused <= 1
