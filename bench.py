@@ -54,8 +54,8 @@ VERIFY_TRAFFIC = {
                   "verify_cu_sha256": "501dfc92dfa938d5aaadc35a389107c2249f8a4a90a8c3e282f45d804219eb47"},
 }
 # the same for the sampling cut kernel (sampling.cu)
-CUT_TRAFFIC = {"sampling_b256": {"bytes": 715230720.0, "profile": "profiles/cut_kernel_sampling_b256.md",
-                                 "sampling_cu_sha256": "cb016df5c8130e13c893d8317ab5bb2dc2dc34ff38f2792725ca666fc4fac19a"}}
+CUT_TRAFFIC = {"sampling_b256": {"bytes": 277739520.0, "profile": "profiles/cut_hist_kernel_sampling_b256.md",
+                                 "sampling_cu_sha256": "2eb93d6d233d24b2139c22ec6f469c8bd9654118c6da981b652bf86e4329af42"}}
 
 
 def _traffic(table, workload, source):
@@ -1052,10 +1052,13 @@ def run_sampling(args, ws, rank, dev):
         rows_read += int((o["accept_len"].cpu().numpy() + 1).sum())
         assert (o["status"] == 0).all()
     rows_per_seq = rows_read / min(reps, 200) / B
-    # cut: every row once from HBM; verification: the rows its chains needed
-    alg_cut = B * (K + 1) * V * 2
+    # cut: once from HBM every row that has a truncation (no top-k and top_p
+    # >= 1 leave a row unread); verification: the rows its chains needed
+    kh_all, ph_all = k.cpu().numpy(), p.cpu().numpy()
+    cut_seqs = int((((kh_all > 0) & (kh_all < V)) | (ph_all < 1.0)).sum())
+    alg_cut = cut_seqs * (K + 1) * V * 2
     alg_ver = rows_per_seq * B * V * 2
-    ach = alg_cut / (ms_cut / 1e3) / 1e9  # the cut kernel: every row read once
+    ach = alg_cut / (ms_cut / 1e3) / 1e9  # the cut kernel: each truncated row read once
     cpu = None
     if rank == 0:
         nb = 16

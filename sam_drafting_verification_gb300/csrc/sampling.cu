@@ -14,19 +14,27 @@
 // and tau = max(tau_k, tau_p).  The verifier then masks every logit below
 // tau out of its sums, so the truncated distribution is never materialised.
 //
-// One CTA per row finds tau exactly by radix selection over order-preserving
-// 32-bit keys of the logits (8-bit digits from the top: two levels for bf16
-// rows, whose low 16 key bits are fixed by the sign, four for fp32): each
-// level streams the row (from L2 after the first pass) and builds a 256-bin
-// histogram of counts and masses of the keys that share the prefix chosen so
-// far; one warp then scans the bins from the top for the digit where the
-// running count reaches k (or the running mass reaches top_p * Z_k).  Masses
-// are 2^(l log2(e)/T - R) in fixed point (units of 2^-42, R = ceil(max l
-// log2(e)/T)) summed with integer atomics, so the sums are exact and the
-// result does not depend on the order of the additions; lanes of a warp that
-// hit the same bin are combined first (one warp reduction per distinct
-// digit).  Terms below 2^-43 of the row's maximum are dropped (at V = 2^21 at
-// most 2^-21 of the mass).
+// Two kernels find tau exactly.
+//
+// bf16 rows (cut_hist_kernel): a count per bit pattern in shared memory, one
+// streaming pass per row; the cuts follow from the counts and from fixed-point
+// masses computed once per non-empty pattern (details above that kernel).
+//
+// fp32 rows, and bf16 rows whose 16-bit counts wrap (cut_kernel, one CTA of
+// 256 threads per row): the row maximum; counts and approximate masses in
+// 1,024 log-scale bins of the term; the logits of the bins that hold the cuts
+// copied to shared memory and sorted.  Where those bins hold too many logits,
+// radix selection over order-preserving 32-bit keys of the logits (8-bit
+// digits from the top: two levels for bf16 rows, whose low 16 key bits are
+// fixed by the sign, four for fp32): each level streams the row and builds a
+// 256-bin histogram of counts and masses of the keys that share the prefix
+// chosen so far; one warp then scans the bins from the top for the digit where
+// the running count reaches k (or the running mass reaches top_p * Z_k).
+// Masses there are 2^(l log2(e)/T - R) in fixed point (units of 2^-42, R =
+// ceil(max l log2(e)/T)) summed with integer atomics, so the sums are exact
+// and the result does not depend on the order of the additions; lanes of a
+// warp that hit the same bin are combined first.  Terms below 2^-43 of the
+// row's maximum are dropped (at V = 2^21 at most 2^-21 of the mass).
 
 #include <cstdint>
 #include <cstring>
@@ -59,8 +67,7 @@ constexpr int kLogBins = 1024;  // 32 per octave of the term, 32 octaves
 constexpr int kCap = 4096;     // boundary logits held in shared memory (a power of two:
                                // the sort pads to one)
 
-template <int NT>
-struct CutSmemT {
+struct CutSmem {
   // radix levels over keys (the path for rows whose boundary bins overflow)
   uint32_t cnt[kBins];
   unsigned long long mass[kBins];
@@ -74,8 +81,8 @@ struct CutSmemT {
   // the logits of the boundary bins: keys and terms
   uint32_t bkey[kCap];
   float bmass[kCap];
-  double tsum[NT];  // per-thread partial sums
-  float red[NT / 32];
+  double tsum[kThr];  // per-thread partial sums
+  float red[kThr / 32];
   uint32_t nbuf;
   uint32_t idx;
   // broadcast of warp 0's choices
@@ -83,7 +90,6 @@ struct CutSmemT {
   uint32_t key;
   double dscr[4];  // broadcast scratch
 };
-using CutSmem = CutSmemT<kThr>;
 
 // Log-scale bin of y = l cT - R <= ~0: b = round(-32 y) clamped to
 // [0, kLogBins - 1] (32 bins per octave of the term 2^y, the last holding
@@ -140,7 +146,7 @@ __device__ __forceinline__ unsigned long long fixed_mass(float y) {
 // the same number of calls (valid = false past the end), so f may use
 // warp-wide collectives.  Rows whose byte length is a multiple of 16 are read
 // in 16-byte vectors.
-template <int TT, int NT = kThr, typename F>
+template <int TT, typename F>
 __device__ __forceinline__ void visit_row(const unsigned char* row, int V, F&& f) {
   constexpr int ES = TT ? 2 : 4;
   constexpr int VEC = 16 / ES;
@@ -148,12 +154,12 @@ __device__ __forceinline__ void visit_row(const unsigned char* row, int V, F&& f
     // kLoads vectors per thread in flight before any is processed
     constexpr int kLoads = 4;
     const int nvec = V / VEC;
-    for (int base = 0; base < nvec; base += NT * kLoads) {
+    for (int base = 0; base < nvec; base += kThr * kLoads) {
       uint4 w[kLoads];
       bool ok[kLoads];
 #pragma unroll
       for (int u = 0; u < kLoads; ++u) {
-        const int i = base + u * NT + (int)threadIdx.x;
+        const int i = base + u * kThr + (int)threadIdx.x;
         ok[u] = i < nvec;
         w[u] = ok[u] ? *reinterpret_cast<const uint4*>(row + (size_t)i * 16) : make_uint4(0u, 0u, 0u, 0u);
       }
@@ -172,7 +178,7 @@ __device__ __forceinline__ void visit_row(const unsigned char* row, int V, F&& f
       }
     }
   } else {
-    for (int base = 0; base < V; base += NT) {
+    for (int base = 0; base < V; base += kThr) {
       const int i = base + (int)threadIdx.x;
       const bool ok = i < V;
       float x = 0.f;
@@ -188,8 +194,7 @@ __device__ __forceinline__ void visit_row(const unsigned char* row, int V, F&& f
 // Adds one logit (when `in`) to bin `digit` of the histogram: the lanes of the
 // warp with the same digit are combined first, one warp reduction per
 // distinct digit present.
-template <int NT>
-__device__ __forceinline__ void hist_add(CutSmemT<NT>& sh, bool in, uint32_t digit,
+__device__ __forceinline__ void hist_add(CutSmem& sh, bool in, uint32_t digit,
                                          unsigned long long fixed, int lane) {
   unsigned todo = __ballot_sync(kFullMask, in);
   // parts of the fixed-point mass that sum without overflow over 32 lanes
@@ -320,8 +325,8 @@ __device__ __forceinline__ float max_nan(float a, float b) {
 
 // The exact cut by radix levels over the keys, streaming the row once per
 // level (used when the boundary bins hold more logits than the buffer).
-template <int TT, int NT = kThr>
-__device__ uint32_t radix_cut(CutSmemT<NT>& sh, const unsigned char* rp, int V, float cT, float Rf,
+template <int TT>
+__device__ uint32_t radix_cut(CutSmem& sh, const unsigned char* rp, int V, float cT, float Rf,
                               bool use_k, bool use_p, int32_t k, float tp, int lane, int warp) {
   constexpr int NLEV = TT ? 2 : 4;
   uint32_t min_key = 0, key_k = 0, key_p = 0;
@@ -333,12 +338,12 @@ __device__ uint32_t radix_cut(CutSmemT<NT>& sh, const unsigned char* rp, int V, 
     for (int lev = 0; lev < NLEV; ++lev) {
       const int shift = 24 - 8 * lev;
       const uint32_t hmask = lev == 0 ? 0u : (0xffffffffu << (shift + 8));
-      for (int i = threadIdx.x; i < kBins; i += NT) {
+      for (int i = threadIdx.x; i < kBins; i += kThr) {
         sh.cnt[i] = 0;
         sh.mass[i] = 0;
       }
       __syncthreads();
-      visit_row<TT, NT>(rp, V, [&](float x, bool ok) {
+      visit_row<TT>(rp, V, [&](float x, bool ok) {
         const uint32_t u = order_key(x);
         const bool in = ok && u >= min_key && (u & hmask) == (prefix & hmask);
         const unsigned long long fx = in ? fixed_mass(fmaf(x, cT, -Rf)) : 0ull;
@@ -668,24 +673,26 @@ __global__ void __launch_bounds__(kThr, 4) cut_kernel(const unsigned char* targe
 // halves of 32-bit shared-memory words (pattern p in word p >> 1, half p & 1;
 // 128 KB).  A row holding more than 65,535 copies of one value wraps a half;
 // the total count shows it, and such a row is marked for the general path (a
-// second launch that cuts only the marked rows).
-// Each row is streamed once, one shared atomic per logit.  A mass is computed
-// once per non-empty pattern, count x 2^((v - vmax) log2(e) / T) in fixed
-// point (units of 2^-42), so every prefix sum is exact and independent of the
-// order of the additions, and the top-p crossing is decided exactly.
+// second launch that cuts only the marked rows).  Each row is streamed once,
+// one shared atomic per logit, with the row maximum (as a value-order key)
+// tracked on the way.  A mass is computed once per non-empty pattern,
+// count x 2^((v - vmax) log2(e) / T) in fixed point (units of 2^-42), so
+// every prefix sum is exact and independent of the order of the additions,
+// and the top-p crossing is decided exactly.
 //
-// The patterns fall into 1024 chunks of 64 (32 words).  Chunks below 512 hold
-// positive values (larger with the index), the others negative ones (smaller
-// with the index), so in descending order of value they come as 511, 510,
-// ..., 0, 512, ..., 1023 (+0 and -0, patterns 0 and 0x8000, meet at the
-// seam).  After the pass, the warps reduce every chunk to a total (lanes read
-// consecutive words, so without bank conflicts), thread t scans chunk t's
-// total in that order, and the chunk where a running sum crosses its target
-// is walked by a warp, one word per lane.
+// The patterns fall into 1024 chunks of 64 (32 words), chunk t owned by
+// thread t.  Chunks below 512 hold positive values (larger with the index),
+// the others negative ones (smaller with the index), so in descending order
+// of value they come as 511, 510, ..., 0, 512, ..., 1023 (+0 and -0, patterns
+// 0 and 0x8000, meet at the seam).  After the pass each thread sums its
+// chunk's counts and masses (lane l starting at word l of its chunk, so a
+// warp's reads hit distinct banks), one block scan in that order locates the
+// chunks where the running count reaches k and the running mass reaches
+// ceil(top_p * Z_k), and a warp walks each of those chunks, one word per lane.
 //
 // One persistent CTA of 1024 threads per SM takes rows blockIdx.x,
-// blockIdx.x + gridDim.x, ...; while it works on one, the bulk-copy engine
-// prefetches its next row into L2.
+// blockIdx.x + gridDim.x, ...; each row's parameters are loaded while the
+// previous row is cut.
 
 constexpr int kHT = 1024;       // threads of the histogram kernel (one per chunk)
 constexpr int kHWords = 32768;  // 65,536 patterns, two counts per word
@@ -853,19 +860,6 @@ __device__ __forceinline__ unsigned long long warp_sum63(unsigned long long v) {
   return (unsigned long long)p0 + ((unsigned long long)p1 << 21) + ((unsigned long long)p2 << 42);
 }
 
-// Prefetches bytes [a, b) of global memory into L2 (16-byte aligned inside),
-// in 32 KB pieces spread over the lanes of one warp.
-__device__ __forceinline__ void prefetch_l2(const unsigned char* a, const unsigned char* b,
-                                            int lane) {
-  const uintptr_t a0 = ((uintptr_t)a + 15) & ~(uintptr_t)15;
-  const uintptr_t a1 = (uintptr_t)b & ~(uintptr_t)15;
-  constexpr uintptr_t kPiece = 32768;
-  for (uintptr_t o = a0 + (uintptr_t)lane * kPiece; o < a1; o += 32 * kPiece) {
-    const uint32_t n = (uint32_t)(a1 - o < kPiece ? a1 - o : kPiece);
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(o), "r"(n) : "memory");
-  }
-}
-
 // Adds the two bf16 patterns of word w to the histogram.
 __device__ __forceinline__ void count_pair(uint32_t* hist, uint32_t w) {
   atomicAdd(&hist[(w >> 1) & 0x7fffu], (w & 1u) * 0xffffu + 1u);
@@ -881,15 +875,23 @@ __global__ void __launch_bounds__(kHT, 1)
   const float INF = __int_as_float(0x7f800000);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const size_t row_bytes = (size_t)V * 2;
-  if (warp == 0 && (int64_t)blockIdx.x < rows) {
-    const unsigned char* r0 = target + (size_t)blockIdx.x * row_bytes;
-    prefetch_l2(r0, r0 + row_bytes, lane);
+  float nT = 0.f, ntp = 0.f;
+  int32_t nk = 0;
+  if ((int64_t)blockIdx.x < rows) {
+    const int64_t b = blockIdx.x / R;
+    nT = temp[b];
+    nk = top_k[b];
+    ntp = top_p[b];
   }
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
-    const int64_t b = row / R;
-    const float T = temp[b];
-    const int32_t k = top_k[b];
-    const float tp = top_p[b];
+    const float T = nT, tp = ntp;
+    const int32_t k = nk;
+    if (row + gridDim.x < rows) {  // the next row's parameters, used next iteration
+      const int64_t b = (row + gridDim.x) / R;
+      nT = temp[b];
+      nk = top_k[b];
+      ntp = top_p[b];
+    }
     if (!(T > 0.f) || !(T < INF) || !(tp > 0.f)) {
       if (tid == 0) tau[row] = __int_as_float(0x7fc00000);
       continue;
@@ -901,10 +903,6 @@ __global__ void __launch_bounds__(kHT, 1)
       continue;
     }
     const unsigned char* rp = target + (size_t)row * row_bytes;
-    if (warp == 0 && row + gridDim.x < rows) {
-      const unsigned char* rn = rp + (size_t)gridDim.x * row_bytes;
-      prefetch_l2(rn, rn + row_bytes, lane);
-    }
     __syncthreads();  // the previous row's readers are done
     for (int i = tid; i < kHWords / 4; i += kHT)
       reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -960,21 +958,31 @@ __global__ void __launch_bounds__(kHT, 1)
     // Chunks 510, 511 and 1023 hold only +inf and NaN patterns, chunk 1022
     // -inf (pattern 0xff80, the low half of its first word) and NaNs.
     uint32_t cnt = 0;
-    unsigned long long m0 = 0, m1 = 0;
-#pragma unroll 4
+#pragma unroll 8
     for (int j = 0; j < 32; ++j) {
-      const uint32_t word = 32 * tid + ((j + lane) & 31);
-      const uint32_t w = hist[word];
+      const uint32_t w = hist[32 * tid + ((j + lane) & 31)];
       cnt += (w & 0xffffu) + (w >> 16);
-      if (use_p && w) {
-        m0 += mass(w & 0xffffu, 2 * word);
-        m1 += mass(w >> 16, 2 * word + 1);
+    }
+    unsigned long long mine = 0;
+    if (use_p) {
+      // four words at a time: eight independent exponentials in flight
+      for (int j = 0; j < 32; j += 4) {
+        uint32_t wd[4], w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          wd[u] = 32 * tid + ((j + u + lane) & 31);
+          w[u] = hist[wd[u]];
+        }
+        if (w[0] | w[1] | w[2] | w[3]) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            mine += mass(w[u] & 0xffffu, 2 * wd[u]) + mass(w[u] >> 16, 2 * wd[u] + 1);
+        }
       }
     }
     uint32_t special = 0;
     if (tid == 510 || tid == 511 || tid == 1023) special = cnt != 0;
     else if (tid == 1022) special = cnt != (hist[0x7fc0] & 0xffffu);
-    const unsigned long long mine = m0 + m1;
     const ChunkScan sc = chunk_scan(hs, cnt, mine, special, use_p, lane, warp);
     if (sc.c_tot != (uint32_t)V) {
       // a count wrapped: the row goes to the general path (a second launch)
