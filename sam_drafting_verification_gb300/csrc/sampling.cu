@@ -700,6 +700,8 @@ constexpr int kChunks = 1024;   // 64 patterns, 32 words each
 static_assert(kChunks == kHT && kHWords == 32 * kChunks, "one chunk per thread");
 
 struct HistScratch {
+  unsigned long long cmass[kChunks];  // per-chunk masses
+  uint32_t ccnt[kChunks];             // per-chunk counts
   unsigned long long wm[32];  // per-warp scan totals (masses), by rank
   uint32_t wc[32];            // per-warp scan totals (counts), by rank
   uint32_t wsp[32];           // per-warp flags
@@ -953,33 +955,46 @@ __global__ void __launch_bounds__(kHT, 1)
     const auto mass = [=](uint32_t c, uint32_t p) -> unsigned long long {
       return (unsigned long long)c * fixed42(ex2_approx((pattern_value(p) - vmax) * cT));
     };
-    // 2. thread t: the count and (top-p) the mass of chunk t; lanes start at
-    // different words of their chunks, so a warp's reads hit distinct banks.
-    // Chunks 510, 511 and 1023 hold only +inf and NaN patterns, chunk 1022
-    // -inf (pattern 0xff80, the low half of its first word) and NaNs.
-    uint32_t cnt = 0;
-#pragma unroll 8
-    for (int j = 0; j < 32; ++j) {
-      const uint32_t w = hist[32 * tid + ((j + lane) & 31)];
-      cnt += (w & 0xffffu) + (w >> 16);
-    }
-    unsigned long long mine = 0;
-    if (use_p) {
-      // four words at a time: eight independent exponentials in flight
-      for (int j = 0; j < 32; j += 4) {
+    // 2. the count and (top-p) the mass of every chunk.  Four lanes share a
+    // chunk, 8 words each, so a warp covers 8 chunks per round and the dense
+    // chunks of a row (consecutive) spread over several warps; lane l starts
+    // at word (l / 4) of its quarter, so a warp's 32 reads hit 32 banks.
+    for (int rd = 0; rd < kChunks / kHT * 4; ++rd) {
+      const int c = 8 * (rd * (kHT / 32) + warp) + (lane >> 2);
+      const int w0 = 32 * c + 8 * (lane & 3);
+      uint32_t cc = 0;
+      unsigned long long cm = 0;
+#pragma unroll
+      for (int i = 0; i < 8; i += 4) {
         uint32_t wd[4], w[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          wd[u] = 32 * tid + ((j + u + lane) & 31);
+          wd[u] = w0 + ((i + u + (lane >> 2)) & 7);
           w[u] = hist[wd[u]];
+          cc += (w[u] & 0xffffu) + (w[u] >> 16);
         }
-        if (w[0] | w[1] | w[2] | w[3]) {
+        if (use_p && (w[0] | w[1] | w[2] | w[3])) {
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            mine += mass(w[u] & 0xffffu, 2 * wd[u]) + mass(w[u] >> 16, 2 * wd[u] + 1);
+            cm += mass(w[u] & 0xffffu, 2 * wd[u]) + mass(w[u] >> 16, 2 * wd[u] + 1);
         }
       }
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {
+        cc += __shfl_xor_sync(kFullMask, cc, o);
+        if (use_p) cm += __shfl_xor_sync(kFullMask, cm, o);
+      }
+      if ((lane & 3) == 0) {
+        hs.ccnt[c] = cc;
+        hs.cmass[c] = cm;
+      }
     }
+    __syncthreads();
+    // thread t: chunk t.  Chunks 510, 511 and 1023 hold only +inf and NaN
+    // patterns, chunk 1022 -inf (pattern 0xff80, the low half of its first
+    // word) and NaNs.
+    const uint32_t cnt = hs.ccnt[tid];
+    const unsigned long long mine = use_p ? hs.cmass[tid] : 0ull;
     uint32_t special = 0;
     if (tid == 510 || tid == 511 || tid == 1023) special = cnt != 0;
     else if (tid == 1022) special = cnt != (hist[0x7fc0] & 0xffffu);
