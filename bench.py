@@ -54,8 +54,8 @@ VERIFY_TRAFFIC = {
                   "verify_cu_sha256": "501dfc92dfa938d5aaadc35a389107c2249f8a4a90a8c3e282f45d804219eb47"},
 }
 # the same for the sampling cut kernel (sampling.cu)
-CUT_TRAFFIC = {"sampling_b256": {"bytes": 277739520.0, "profile": "profiles/cut_hist_kernel_sampling_b256.md",
-                                 "sampling_cu_sha256": "2eb93d6d233d24b2139c22ec6f469c8bd9654118c6da981b652bf86e4329af42"}}
+CUT_TRAFFIC = {"sampling_b256": {"bytes": 277559040.0, "profile": "profiles/cut_hist_kernel_sampling_b256.md",
+                                 "sampling_cu_sha256": "78f29c9034b75bbbe1bded1e886e3e513b3184c3ee3411e7902190e5669d7d55"}}
 
 
 def _traffic(table, workload, source):
