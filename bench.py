@@ -383,33 +383,54 @@ def run_gpu(args):
 
 def e2e_rs(batch, snap, pool, emit, emit_len, draft, dlen, mlen, mend, out, wsv, B, K, V, T, steps, dev):
     """Same metric through the public API with host buffers: every step copies
-    its logits from pinned host memory and reads the emitted tokens back."""
+    its logits from pinned host memory and reads the emitted tokens back.  The
+    copy of step s + 1 runs on a copy stream into a second device buffer while
+    step s computes (the host link, about 200 GB/s, bounds the loop)."""
     import torch
 
     import sam_drafting_verification_gb300 as ss
     host_pool = [p.cpu().pin_memory() for p in pool[:4]]
-    dev_buf = torch.empty_like(pool[0])
+    dev_buf = [torch.empty_like(pool[0]) for _ in range(2)]
     host_emit = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
     host_len = torch.empty(B, dtype=torch.int32).pin_memory()
     batch.import_(snap)
     emit_len.zero_()
     torch.cuda.synchronize()
+    cur = torch.cuda.current_stream(dev)
+    cps = torch.cuda.Stream(device=dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    freed = [torch.cuda.Event() for _ in range(2)]
+
+    def issue_copy(s):
+        i = s % 2
+        if s >= 2:  # the buffer's previous step has verified
+            cps.wait_event(freed[i])
+        with torch.cuda.stream(cps):
+            dev_buf[i].copy_(host_pool[s % len(host_pool)], non_blocking=True)
+        copied[i].record(cps)
+
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
+    e0.record(cur)
+    cps.wait_stream(cur)
+    issue_copy(0)
     for s in range(steps):
-        dev_buf.copy_(host_pool[s % len(host_pool)], non_blocking=True)
+        if s + 1 < steps:
+            issue_copy(s + 1)
+        cur.wait_event(copied[s % 2])
         batch.step(emit, emit_len, K, out=(draft, dlen, mlen, mend))
-        ss.spec_verify(dev_buf, draft, dlen, temperature=T, seed=1002, step=s, out=out, emit=True,
-                       status=True, workspace=wsv)
+        ss.spec_verify(dev_buf[s % 2], draft, dlen, temperature=T, seed=1002, step=s, out=out,
+                       emit=True, status=True, workspace=wsv)
+        freed[s % 2].record(cur)
         host_emit.copy_(emit, non_blocking=True)
         host_len.copy_(emit_len, non_blocking=True)
-    e1.record()
+    e1.record(cur)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     return {"value": round(B / (ms / 1e3), 1), "unit": "seq-steps/s",
-            "h2d_bytes_per_step": int(dev_buf.numel() * dev_buf.element_size()),
+            "h2d_bytes_per_step": int(dev_buf[0].numel() * dev_buf[0].element_size()),
             "d2h_bytes_per_step": int(host_emit.numel() * 4 + host_len.numel() * 4),
-            "ms_per_step": round(ms, 4), "steps": steps}
+            "ms_per_step": round(ms, 4), "steps": steps,
+            "overlap": "step s + 1's copy on a second stream while step s computes"}
 
 
 class OracleLoop:
