@@ -1104,7 +1104,7 @@ def run_sampling(args, ws, rank, dev):
                          "traffic": _traffic(CUT_TRAFFIC, "sampling_b256", "sampling.cu"),
                          "peak_source": peak_kind, "algorithmic_bytes_per_launch": round(alg_cut, 1),
                          "algorithmic_bytes_per_step": round(alg_cut + alg_ver, 1)},
-            "cpu_baseline": cpu, "gpu_launches": 2 * reps, "clocks": clocks,
+            "cpu_baseline": cpu, "gpu_launches": 3 * reps, "clocks": clocks,
             "breakdown": {"cut_us": round(ms_cut * 1e3, 2), "verify_us": round((ms - ms_cut) * 1e3, 2),
                           "cut_GBps_one_read": round(alg_cut / (ms_cut / 1e3) / 1e9, 1),
                           "rows_per_seq": round(rows_per_seq, 4)}}
