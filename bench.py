@@ -46,8 +46,8 @@ POOL = 16
 # workload, with the SHA-256 of verify.cu they were taken on: a changed kernel
 # reports null until it is captured again.
 VERIFY_TRAFFIC = {
-    "rs_bf16_b64": {"bytes": 19538176.0, "profile": "profiles/verify_kernel_rs_bf16_b64.md",
-                    "verify_cu_sha256": "501dfc92dfa938d5aaadc35a389107c2249f8a4a90a8c3e282f45d804219eb47"},
+    "rs_bf16_b64": {"bytes": 19537920.0, "profile": "profiles/verify_kernel_rs_bf16_b64.md",
+                    "verify_cu_sha256": "bbb652d498d8e15843e7c24655bb1eb7a46a9b7e25e1c39905f50390e090f3fe"},
     "long_rollout_b256": {"bytes": 78981542.0, "profile": "profiles/launches_long_rollout_b256.md",
                           "verify_cu_sha256": "501dfc92dfa938d5aaadc35a389107c2249f8a4a90a8c3e282f45d804219eb47"},
     "tree_b256": {"bytes": 161624064.0, "profile": "profiles/verify_kernel_tree_b256.md",

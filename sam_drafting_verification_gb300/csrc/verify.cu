@@ -810,8 +810,10 @@ struct Control {
       uint32_t b = 0;
       if (lane == 0) {
         // CTA x's first sequence is x (grid <= B); later ones come from the
-        // shared counter, past the first gridDim.x
-        b = first_ ? blockIdx.x : gridDim.x + atomicAdd(&P.ws[0], 1u);
+        // shared counter, past the first gridDim.x (none when the grid
+        // covers the batch: the counter is then never touched)
+        b = first_ ? blockIdx.x
+                   : gridDim.x >= (uint32_t)P.B ? (uint32_t)P.B : gridDim.x + atomicAdd(&P.ws[0], 1u);
         vstore(&sm.pool_left, b >= (uint32_t)P.B ? 0 : P.B - 1 - (int)b);
         if (b >= (uint32_t)P.B) vstore(&sm.pool_done, 1);
       }
@@ -1702,7 +1704,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       if (vload(&sm.abort)) {
         // this slot's sequence, and (slot 0) any nobody will claim now
         if (S.state != kEmpty) write_result(P, S.b, -1, -1, SAMSPEC_ST_TIMEOUT);
-        if (si == 0)
+        if (si == 0 && gridDim.x < (uint32_t)P.B)
           for (uint32_t b = gridDim.x + atomicAdd(&P.ws[0], 1u); b < (uint32_t)P.B;
                b = gridDim.x + atomicAdd(&P.ws[0], 1u))
             write_result(P, (int)b, -1, -1, SAMSPEC_ST_TIMEOUT);
@@ -1712,7 +1714,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && gridDim.x < (uint32_t)P.B) {  // the claim counter was used
     __threadfence();
     if (atomicAdd(&P.ws[1], 1u) == gridDim.x - 1) {
       // last CTA out: reset the counters for the next launch on this workspace
