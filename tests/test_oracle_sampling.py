@@ -119,3 +119,47 @@ def test_bad_parameters_are_refused():
     s = oracle.verify_sampling(logits, draft, None, T, 5, p)
     assert list(s["status"]) == [8, 8, 8, 8, 8, 0]
     assert (s["accept_len"][:5] == -1).all()
+
+
+def test_signed_zeros_are_one_value():
+    """+0 and -0 compare equal, so a row mixing them truncates exactly as the
+    row with every zero positive (ties at a cut are kept on both sides of the
+    sign), checked against the brute-force definition."""
+    row = np.zeros(9, np.float32)
+    row[:4] = -0.0
+    row[[6, 8]] = [1.5, 0.75]
+    pos = np.abs(row)
+    for T, k, top_p in ((1.0, 3, 1.0), (1.0, 0, 0.6), (0.7, 5, 0.9), (1.3, 2, 0.99)):
+        pa, ta = oracle.truncate_row(row, T, k, top_p)
+        pb, tb = oracle.truncate_row(pos, T, k, top_p)
+        np.testing.assert_array_equal(pa, pb)
+        assert ta == tb
+        pbr, keep = _brute(pos, T, k, top_p)
+        np.testing.assert_allclose(pa, pbr, rtol=1e-12, atol=0)
+        assert ta == pos[keep].min()
+
+
+def test_negative_infinity_logits():
+    """-inf logits have zero probability: top-k still counts them (a k beyond
+    the finite logits cuts at -inf and keeps every finite one), and top-p
+    never needs them."""
+    row = np.array([2.0, -np.inf, 0.5, -np.inf, 1.0, -np.inf], np.float32)
+    p, tau = oracle.truncate_row(row, 1.0, 5, 1.0)
+    assert tau == -np.inf
+    assert (p[np.isfinite(row)] > 0).all() and (p[~np.isfinite(row)] == 0).all()
+    np.testing.assert_allclose(p.sum(), 1.0, rtol=1e-15)
+    p, tau = oracle.truncate_row(row, 1.0, 0, 0.999999)
+    assert tau == 0.5 and (p[~np.isfinite(row)] == 0).all()
+    p, tau = oracle.truncate_row(row, 1.0, 2, 1.0)
+    assert tau == 1.0 and np.count_nonzero(p) == 2
+
+
+def test_constant_row_keeps_everything():
+    """Every logit equal: any top-k keeps all of them (ties at the k-th), any
+    top-p keeps all of them (nothing lies strictly above), and the result is
+    uniform."""
+    row = np.full(7, 0.25, np.float32)
+    for k, top_p in ((1, 1.0), (3, 0.5), (0, 0.01), (6, 0.99)):
+        p, tau = oracle.truncate_row(row, 0.8, k, top_p)
+        assert tau == np.float32(0.25)
+        np.testing.assert_allclose(p, np.full(7, 1 / 7), rtol=1e-14)
