@@ -223,6 +223,9 @@ def _check_cuts(ss, dev, rows_bf16, T, k, p):
     excused = 0
     for b in range(B):
         for r in range(R):
+            if not (0 < k[b] < V) and not (p[b] < 1.0):  # no truncation: nothing cut
+                assert tau[b, r] == -np.inf, (b, r)
+                continue
             res = oracle.truncate_row(rows[b, r], float(T[b]), int(k[b]), float(p[b]))
             if res is None:  # a row the verifier refuses
                 assert tau[b, r] == -np.inf, (b, r)
@@ -317,3 +320,15 @@ def test_cut_full_vocab_sampled(ss, cuda_device):
         assert ok, (b, r, tau[b, r], to)
         excused += ex
     assert excused <= 1
+
+
+@pytest.mark.parametrize("V", [1, 2, 7, 8, 9])
+def test_cut_bf16_tiny_vocabularies(ss, cuda_device, V):
+    """Vocabularies of a few logits (row lengths that are and are not whole
+    16-byte vectors), with ties, against the oracle."""
+    rng = np.random.default_rng(50 + V)
+    rows = np.round(workloads.gaussian_logits(rng, (6, 2, V), 2.0) * 2) / 2
+    T = np.array([1.0, 0.5, 2.0, 1.0, 0.7, 1.0], np.float32)
+    k = np.array([1, 2, 0, 3, 1, 0], np.int32)
+    p = np.array([1.0, 0.9, 0.5, 0.3, 0.99, 0.01], np.float32)
+    assert _check_cuts(ss, cuda_device, rows, T, k, p) <= 1
