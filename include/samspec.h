@@ -335,10 +335,12 @@ int spec_verify_tree(const void* d_target, int32_t target_dtype, const int32_t* 
  *   set reaching top_p, ties kept).  Both keep {v : l_v >= tau};
  * d_tau [B, R] receives tau (fp32): -inf when nothing is cut (k <= 0 or
  * k >= V, and top_p >= 1) or the row has NaN, +inf or only -inf logits; NaN
- * when T is not > 0 and finite or top_p is not > 0.  Masses are taken in
- * fixed point (units of 2^-42 of the row maximum's term), so a top-p cut whose
- * mass lies within about 1e-7 of top_p may fall on either side.  One launch;
- * asynchronous. */
+ * when T is not > 0 and finite or top_p is not > 0.  Masses are summed
+ * exactly in fixed point, each term floored to units of 2^-42 of the row
+ * maximum's term, so a top-p cut whose mass lies within V * 2^-42 of top_p
+ * (under 5e-7 at V = 2^21) may fall on either side.  fp32 rows: one launch;
+ * bf16 rows: two (the second cuts only rows holding more than 65,535 equal
+ * logits).  Asynchronous. */
 int spec_sampling_cut(const void* d_target, int32_t target_dtype, int32_t B, int32_t R, int32_t V,
                       const float* d_temperature, const int32_t* d_top_k, const float* d_top_p,
                       float* d_tau, samspec_stream_t stream);
@@ -357,7 +359,8 @@ int spec_sampling_cut(const void* d_target, int32_t target_dtype, int32_t B, int
  * spec_verify_sampling_workspace_bytes(B, K, V) bytes, 256-byte aligned, its
  * first 256 bytes zeroed once by spec_verify_workspace_init; the rest holds
  * the cuts of the call.  dbg as spec_verify (row_z sums the kept tokens; q_d
- * is not written).  V limits as spec_verify's one-hot case.  Two launches. */
+ * is not written).  V limits as spec_verify's one-hot case.  The cut and the
+ * verification: two launches (three with bf16 targets). */
 size_t spec_verify_sampling_workspace_bytes(int32_t B, int32_t K, int32_t V);
 int spec_verify_sampling(const void* d_target, int32_t target_dtype, const int32_t* d_draft,
                          const int32_t* d_draft_len, int32_t B, int32_t K, int32_t V,
