@@ -1,0 +1,41 @@
+"""Host logic of bench.py that needs no GPU: the DRAM-traffic tables that
+feed the roofline's `traffic` field are well formed, point at committed ncu
+summaries, and are used only while the kernel source still hashes to the
+one the counters were taken on."""
+import hashlib
+import os
+import re
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _entries():
+    for table, source in ((bench.VERIFY_TRAFFIC, "verify.cu"), (bench.CUT_TRAFFIC, "sampling.cu")):
+        for workload, entry in table.items():
+            yield table, source, workload, entry
+
+
+def test_traffic_tables_are_well_formed():
+    seen = 0
+    for _, source, workload, entry in _entries():
+        assert entry["bytes"] > 0, workload
+        assert os.path.isfile(os.path.join(ROOT, entry["profile"])), entry["profile"]
+        assert re.fullmatch(r"[0-9a-f]{64}", entry[source.replace(".", "_") + "_sha256"]), workload
+        seen += 1
+    assert seen >= 4
+
+
+def test_traffic_only_for_the_captured_source():
+    for table, source, workload, entry in _entries():
+        path = os.path.join(ROOT, "sam_drafting_verification_gb300", "csrc", source)
+        with open(path, "rb") as f:
+            current = hashlib.sha256(f.read()).hexdigest()
+        key = source.replace(".", "_") + "_sha256"
+        same = {workload: dict(entry, **{key: current})}
+        other = {workload: dict(entry, **{key: "0" * 64})}
+        assert bench._traffic(same, workload, source) == entry["bytes"]
+        assert bench._traffic(other, workload, source) is None
+        assert bench._traffic(table, "no_such_workload", source) is None
+
