@@ -1,29 +1,42 @@
 """Benchmark of the SAM-drafting + lossless-verification hot path on GB300.
 
-One step = one pass of the per-step hot path over a batch: the device suffix
-automata are extended with the tokens the previous verification emitted and
-queried for K drafts (sam_step, one launch), then the drafts are verified
-against that step's target logits (spec_verify, one launch).  The emitted
-tokens feed the next step, as in a decode loop.
+Default line (workload verify_b1024): lossless verification of B=1024
+sequences per GPU, K=3 one-hot drafts each, V=151936, bf16 target logits
+N(0, sd 2) with every draft drawn uniformly among its row's top 5, rejection
+sampling at T=1.0.  One step = one spec_verify launch over the whole batch:
+row statistics, the accept chain, the resample or bonus token and the Philox
+coins, in one kernel.  Logits rotate through three step tensors of 1.25 GB
+each (far above the 129 MB L2), and the timed region replays a CUDA graph of
+exactly --steps steps, each replay bracketed by a barrier and a device
+synchronisation and timed with CUDA events on the capture stream; the line
+reports the median replay (max over ranks), over enough replays for at least
+half a second of timed work.
 
-Default workload (rs_bf16_b64): B=64 sequences per GPU, V=151936, Zipf(1.1)
-histories of 4096 tokens (copy prob 0.3, spans 8-64), K=3 SAM drafts,
-rejection sampling at T=1.0 on bf16 logits N(0, sd 2) + 4 on the stream's
-true continuation.  Logits come from a rotating pool of 16 step tensors
-(1.24 GB, far above the 129 MB L2), so no step finds its rows in L2.
-
-The timed region replays a CUDA graph of exactly --steps steps, bracketed by a
-barrier and a device synchronisation, timed with CUDA events on the capture
-stream; max over ranks.  Under torchrun every rank runs its own batch (weak
-scaling, no collective on the data path).
+The same run measures the rest of the path and puts it under `breakdown`:
+  step_b64          the full decode step at B=64 (device suffix automata
+                    extended by the emitted tokens and drafting K=3, then
+                    verification at T=1 of bf16 logits with the continuation
+                    boosted), beside the oracle on one host core and on all;
+  sam_rollout_b256  the automata alone on 256 histories of 16k-32k tokens:
+                    prefill tokens/s and ns per sequence-step of 512 steps of
+                    extend (1-4 tokens) + draft, beside the oracle's build and
+                    step on one core and on all;
+  sweep_b1024       K in {1,3,5,8} x fp32/bf16 x {greedy, T=1, every row read};
+  draft_model_b32   verification with draft-model logits (B=32, K=5, fp32,
+                    T=0.7, residual resampling).
+Under torchrun every rank runs its own batches (weak scaling, no collective on
+the data path).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                  [--workload rs_bf16_b64|sweep_b1024|long_rollout_b256|rollout_toy_b64|static_match_b256|tree_b256|sampling_b256]
+                  [--workload verify_b1024|rs_bf16_b64|sweep_b1024|long_rollout_b256|
+                              draft_model_b32|rollout_toy_b64|static_match_b256|
+                              tree_b256|sampling_b256]
 """
 from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -41,20 +54,27 @@ import workloads  # noqa: E402
 METRIC = "verified sequence-steps/s and spec_verify HBM GB/s vs 8 TB/s; SAM ns/seq-step"
 POOL = 16
 
+# the default line's workload
+HEAD_B, HEAD_K, HEAD_T = 1024, 3, 1.0
+HEAD_POOL = 3
+HEAD_SEED = 7303
+HEAD_COIN_SEED = 5
+HEAD_WORKLOAD = "verify_b1024_k3_bf16_t1"
+HEAD_MIN_TIMED_MS = 500.0
+
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
-# verify kernel, from the ncu captures summarised under profiles/, keyed by
-# workload, with the SHA-256 of verify.cu they were taken on: a changed kernel
-# reports null until it is captured again.
+# verify kernel from one ncu capture of each workload, with the SHA-256 of
+# verify.cu it was taken on: a changed kernel reports null until captured again.
 VERIFY_TRAFFIC = {
-    "rs_bf16_b64": {"bytes": 19537920.0, "profile": "profiles/verify_kernel_rs_bf16_b64.md",
+    "rs_bf16_b64": {"bytes": 19537920.0,
                     "verify_cu_sha256": "bbb652d498d8e15843e7c24655bb1eb7a46a9b7e25e1c39905f50390e090f3fe"},
-    "long_rollout_b256": {"bytes": 78981542.0, "profile": "profiles/launches_long_rollout_b256.md",
+    "long_rollout_b256": {"bytes": 78981542.0,
                           "verify_cu_sha256": "501dfc92dfa938d5aaadc35a389107c2249f8a4a90a8c3e282f45d804219eb47"},
-    "tree_b256": {"bytes": 161624064.0, "profile": "profiles/verify_kernel_tree_b256.md",
+    "tree_b256": {"bytes": 161624064.0,
                   "verify_cu_sha256": "501dfc92dfa938d5aaadc35a389107c2249f8a4a90a8c3e282f45d804219eb47"},
 }
 # the same for the sampling cut kernel (sampling.cu)
-CUT_TRAFFIC = {"sampling_b256": {"bytes": 277559040.0, "profile": "profiles/cut_hist_kernel_sampling_b256.md",
+CUT_TRAFFIC = {"sampling_b256": {"bytes": 277559040.0,
                                  "sampling_cu_sha256": "78f29c9034b75bbbe1bded1e886e3e513b3184c3ee3411e7902190e5669d7d55"}}
 
 
@@ -81,6 +101,13 @@ def _peaks():
         return float(p["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def _nproc() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
 
 
 class ClockSampler:
@@ -165,7 +192,265 @@ def _sum_over_ranks(x, ws, device):
 
 
 # --------------------------------------------------------------------------
-# inputs of the default workload
+# graphs and their timing
+# --------------------------------------------------------------------------
+
+def _capture(dev, fn, n):
+    """A CUDA graph of fn(0) .. fn(n - 1), captured on a side stream."""
+    import torch
+    cs = torch.cuda.Stream(device=dev)
+    g = torch.cuda.CUDAGraph()
+    cs.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(g, stream=cs):
+            for i in range(n):
+                fn(i)
+    torch.cuda.synchronize(dev)
+    return g, cs
+
+
+def _replay_ms(g, cs, ws, pre=None):
+    """One replay of g on its stream, bracketed by a barrier and a device
+    synchronisation on both sides, timed with events on that stream."""
+    import torch
+    if pre is not None:
+        pre()
+    torch.cuda.synchronize()
+    _barrier(ws)
+    with torch.cuda.stream(cs):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(cs)
+        g.replay()
+        e1.record(cs)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    return e0.elapsed_time(e1)
+
+
+def _timed_replays(g, cs, ws, dev, min_ms, min_reps=3, max_reps=2000, pre=None):
+    """Replays g (after one untimed replay) until about min_ms of timed work;
+    every rank makes the same number of replays."""
+    est = _max_over_ranks(_replay_ms(g, cs, ws, pre), ws, dev)
+    reps = int(min(max_reps, max(min_reps, math.ceil(min_ms / max(est, 1e-3)))))
+    return [_replay_ms(g, cs, ws, pre) for _ in range(reps)]
+
+
+# --------------------------------------------------------------------------
+# the oracle on the host cores
+# --------------------------------------------------------------------------
+
+def _threads_rate(work, nthreads, seconds):
+    """work(t, i) -> units done (thread t, its i-th call; the oracle's C calls
+    release the interpreter lock).  Every thread calls until `seconds` have
+    passed; returns (units per second over the wall clock, units, wall s)."""
+    counts = [0] * nthreads
+    start = threading.Barrier(nthreads + 1)
+    t_end = [0.0]
+
+    def run(t):
+        start.wait()
+        i = 0
+        while time.perf_counter() < t_end[0]:
+            counts[t] += work(t, i)
+            i += 1
+
+    ths = [threading.Thread(target=run, args=(t,)) for t in range(nthreads)]
+    for th in ths:
+        th.start()
+    t0 = time.perf_counter()
+    t_end[0] = t0 + seconds
+    start.wait()
+    for th in ths:
+        th.join()
+    el = time.perf_counter() - t0
+    return sum(counts) / el, sum(counts), el
+
+
+def oracle_verify_rate(rows, drafts, T, seed, one_core_s, all_core_s, draft_logits=None,
+                       seq_index=None):
+    """The oracle's verification of a host sample (rows [n, K+1, V], drafts
+    [n, K]) repeated over steps: seq-steps/s on one thread, then on every
+    host core (each thread verifying the whole sample with its own steps)."""
+    import oracle
+    n = rows.shape[0]
+    si = np.arange(n) if seq_index is None else seq_index
+
+    def work(t, i):
+        oracle.verify(rows, drafts, None, temperature=T, seed=seed, step=1000 * t + i,
+                      draft_logits=draft_logits, seq_index=si)
+        return n
+
+    one, units1, el1 = _threads_rate(work, 1, one_core_s)
+    nc = _nproc()
+    alln, units_n, el_n = _threads_rate(work, nc, all_core_s)
+    return {"one_core": round(one, 2), "all_cores": round(alln, 2), "nproc": nc,
+            "ideal_all_cores": round(one * nc, 2),
+            "sample": f"{n} sequences per call; one thread {units1} seq-steps in {el1:.2f} s, "
+                      f"{nc} threads {units_n} seq-steps in {el_n:.2f} s"}
+
+
+# --------------------------------------------------------------------------
+# default line: verification at B=1024, K=3, bf16, T=1
+# --------------------------------------------------------------------------
+
+def head_config(ws, npool=HEAD_POOL):
+    return {"workload": HEAD_WORKLOAD, "B_per_gpu": HEAD_B, "V": workloads.V_LARGE, "K": HEAD_K,
+            "temperature": HEAD_T, "logits": "bf16 N(0, sd 2)",
+            "drafts": "one-hot, each uniform among its row's top 5",
+            "parallelism": f"dp{ws} (independent batches)",
+            "l2": f"inputs larger than L2: {npool} rotating logits tensors of "
+                  f"{HEAD_B * (HEAD_K + 1) * workloads.V_LARGE * 2 / 1e9:.2f} GB",
+            "timing": "CUDA graph of exactly `steps` verify launches, replayed for >= "
+                      f"{HEAD_MIN_TIMED_MS:.0f} ms; median replay; events on the capture stream"}
+
+
+def run_verify_b1024(args, ws, rank, dev):
+    import torch
+
+    import sam_drafting_verification_gb300 as ss
+    B, K, V, T = HEAD_B, HEAD_K, workloads.V_LARGE, HEAD_T
+    steps, warm = args.steps, args.warmup
+    hbm, peak_kind = _peaks()
+    npool = max(1, args.pool)
+    pool = [workloads.sweep_device(HEAD_SEED + 31 * i + 7919 * rank, B, K, V, torch.bfloat16, dev)
+            for i in range(npool)]
+    wsv = ss.verify_workspace(B, K, V, dev)
+    res = {k: torch.empty(B, dtype=torch.int32, device=dev) for k in ("accept_len", "out_token", "status")}
+
+    def step(s):
+        lg, dr = pool[s % npool]
+        ss.spec_verify(lg, dr, temperature=T, seed=HEAD_COIN_SEED, step=s, out=res, status=True,
+                       workspace=wsv)
+
+    for s in range(warm):
+        step(s)
+    torch.cuda.synchronize()
+    g, cs = _capture(dev, lambda i: step(warm + i), steps)
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    time.sleep(0.3)
+    times = _timed_replays(g, cs, ws, dev, HEAD_MIN_TIMED_MS)
+    clk = clocks.stop()
+    assert (res["status"] == 0).all(), "verification error"
+    ms_step = _max_over_ranks(statistics.median(times) / steps, ws, dev)
+    seqs = _sum_over_ranks(float(B), ws, dev)
+
+    # rows each launch read (the chains' lengths): the same launches again, eagerly
+    rows, acc = 0, 0
+    for i in range(steps):
+        step(warm + i)
+        L = res["accept_len"].cpu().numpy().astype(np.int64)
+        rows += int((L + 1).sum())
+        acc += int(L.sum())
+    alg = rows / steps * V * 2
+    achieved = alg / (ms_step / 1e3) / 1e9
+    roof = {"kernel": "verify_kernel<bf16, one-hot, T>0>", "bound": "hbm", "achieved": round(achieved, 1),
+            "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+            "traffic": _verify_traffic(HEAD_WORKLOAD),
+            "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
+            "algorithmic_bytes_per_launch": round(alg, 1),
+            "algorithmic_bytes": "sum over sequences of (accepted drafts + 1) rows x V x 2 B",
+            "kernel_ms": round(ms_step, 5)}
+
+    cpu = None
+    if rank == 0:
+        nb = 16
+        host_rows = pool[0][0][:nb].float().cpu().numpy()
+        host_dr = pool[0][1][:nb].cpu().numpy()
+        c = oracle_verify_rate(host_rows, host_dr, T, HEAD_COIN_SEED, 10.0, 5.0)
+        cpu = {"value": c["one_core"], "unit": "seq-steps/s", "cores": 1, "kind": "oracle",
+               "nproc": c["nproc"], "all_cores": c["all_cores"], "ideal_all_cores": c["ideal_all_cores"],
+               "sample": "fp64 verification of 16 sequences of the same workload (bf16 rows widened), "
+                         + c["sample"]}
+    e2e = e2e_verify(pool[:2] if npool > 1 else pool * 2, B, K, V, T, steps, dev)
+    del pool
+    torch.cuda.empty_cache()
+
+    breakdown = {"verify_b1024": {"mean_accept": round(acc / (steps * B), 5),
+                                  "rows_per_seq": round(rows / (steps * B), 5),
+                                  "replays": len(times),
+                                  "replay_ms_min_median_max": [round(min(times), 4),
+                                                               round(statistics.median(times), 4),
+                                                               round(max(times), 4)]}}
+    if not args.no_breakdown:
+        breakdown["step_b64"] = measure_step_b64(dev, ws, rank, cpu=rank == 0)
+        torch.cuda.empty_cache()
+        breakdown["sam_rollout_b256"] = measure_rollout(dev, ws, rank, cpu=rank == 0)
+        torch.cuda.empty_cache()
+        breakdown["draft_model_b32"] = measure_draft_model(dev, ws, rank, cpu=rank == 0)
+        torch.cuda.empty_cache()
+        breakdown["sweep_b1024"] = measure_sweep(dev, ws, rank)
+
+    line = {
+        "metric": METRIC, "value": round(seqs / (ms_step / 1e3), 1), "unit": "seq-steps/s", "n_gpus": ws,
+        "steps": steps, "warmup": warm, "ms_per_step": round(ms_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 (bf16 logits)", "data": "synthetic",
+        "config": head_config(ws, npool),
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": len(times) * steps, "clocks": clk, "breakdown": breakdown,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def e2e_verify(pool, B, K, V, T, steps, dev):
+    """The default line's metric through the public API with host buffers:
+    every step copies its logits and drafts from pinned host memory, verifies
+    and reads the accept lengths and emitted tokens back.  Step s + 1's copy
+    runs on a copy stream into a second device buffer while step s verifies."""
+    import torch
+
+    import sam_drafting_verification_gb300 as ss
+    host = [(pool[i][0].cpu().pin_memory(), pool[i][1].cpu().pin_memory()) for i in range(2)]
+    dev_buf = [(torch.empty_like(pool[0][0]), torch.empty_like(pool[0][1])) for _ in range(2)]
+    out = [{k: torch.empty(B, dtype=torch.int32, device=dev) for k in ("accept_len", "out_token", "status")}
+           for _ in range(2)]
+    h_acc = torch.empty((steps, B), dtype=torch.int32).pin_memory()
+    h_tok = torch.empty((steps, B), dtype=torch.int32).pin_memory()
+    wsv = ss.verify_workspace(B, K, V, dev)
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream(dev)
+    cps = torch.cuda.Stream(device=dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    freed = [torch.cuda.Event() for _ in range(2)]
+
+    def issue_copy(s):
+        i = s % 2
+        if s >= 2:  # the buffer's previous step has verified
+            cps.wait_event(freed[i])
+        with torch.cuda.stream(cps):
+            dev_buf[i][0].copy_(host[s % 2][0], non_blocking=True)
+            dev_buf[i][1].copy_(host[s % 2][1], non_blocking=True)
+        copied[i].record(cps)
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    cps.wait_stream(cur)
+    issue_copy(0)
+    for s in range(steps):
+        if s + 1 < steps:
+            issue_copy(s + 1)
+        cur.wait_event(copied[s % 2])
+        o = out[s % 2]
+        ss.spec_verify(dev_buf[s % 2][0], dev_buf[s % 2][1], temperature=T, seed=HEAD_COIN_SEED, step=s,
+                       out=o, status=True, workspace=wsv)
+        freed[s % 2].record(cur)
+        h_acc[s].copy_(o["accept_len"], non_blocking=True)
+        h_tok[s].copy_(o["out_token"], non_blocking=True)
+    e1.record(cur)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    assert (h_acc >= 0).all()
+    h2d = int(dev_buf[0][0].numel() * 2 + dev_buf[0][1].numel() * 4)
+    return {"value": round(B / (ms / 1e3), 1), "unit": "seq-steps/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": int(2 * B * 4),
+            "ms_per_step": round(ms, 4), "steps": steps, "h2d_GBps": round(h2d / (ms / 1e3) / 1e9, 1),
+            "overlap": "step s + 1's copy on a second stream while step s verifies"}
+
+
+# --------------------------------------------------------------------------
+# the full decode step at B=64 (automata + verification)
 # --------------------------------------------------------------------------
 
 def rs_inputs(rank: int, B: int = 64, V: int = workloads.V_LARGE, n: int = 4096, K: int = 3):
@@ -195,44 +480,86 @@ def rs_logits_pool(device, B, K, V, cont, seed):
     return pool
 
 
-# --------------------------------------------------------------------------
-# GPU arm
-# --------------------------------------------------------------------------
+class OracleLoop:
+    """The oracle as it stands, on a sample of the B=64 workload: sequences
+    [b0, b1) get their automata built over their histories (untimed); a step
+    extends one with its previously emitted tokens, drafts K and verifies the
+    draft in fp64 against that step's logits (host-generated, same
+    distribution, bf16-rounded)."""
 
-def run_gpu(args):
+    def __init__(self, hist, cont, b0, b1, npool=4, seed=77):
+        import oracle
+        self.oracle = oracle
+        V, K = workloads.V_LARGE, 3
+        self.K, self.T, self.b0, self.b1, self.npool = K, 1.0, b0, b1, npool
+        rng = np.random.default_rng(seed + b0)
+        self.rows = []
+        for p in range(npool):
+            x = workloads.gaussian_logits(rng, (b1 - b0, K + 1, V), 2.0)
+            workloads.boost_truth(x, cont[b0:b1, p * (K + 1):(p + 1) * (K + 1)], 4.0)
+            self.rows.append(workloads.to_bf16(x).float().numpy())
+        self.sams = [oracle.Sam(V) for _ in range(b1 - b0)]
+        for i in range(b1 - b0):
+            self.sams[i].extend(hist[b0 + i])
+        self.emit = [[] for _ in range(b1 - b0)]
+
+    def seq_step(self, i, s):
+        K = self.K
+        self.sams[i].extend(self.emit[i])
+        d, dl, _, _ = self.sams[i].draft(K)
+        d = np.maximum(d, 0)[None]
+        rows = self.rows[s % self.npool][i:i + 1]
+        r = self.oracle.verify(rows, d, np.array([dl], np.int32), temperature=self.T, seed=1002,
+                               step=s, seq_index=np.array([self.b0 + i]))
+        L = int(r["accept_len"][0])
+        self.emit[i] = list(d[0, :L]) + [int(r["out_token"][0])]
+
+
+def oracle_step_rate(hist, cont, one_core_s, all_core_s):
+    """Decode steps of the oracle on the B=64 workload: one thread over 16
+    sequences, then every host core, each thread with its own sequences."""
+    nc = _nproc()
+    one = OracleLoop(hist, cont, 0, 16)
+
+    def w1(t, i):
+        for b in range(16):
+            one.seq_step(b, i)
+        return 16
+
+    r1, u1, el1 = _threads_rate(w1, 1, one_core_s)
+    per = max(1, hist.shape[0] // nc)
+    loops = [OracleLoop(hist, cont, (t * per) % hist.shape[0], (t * per) % hist.shape[0] + per)
+             for t in range(nc)]
+
+    def wn(t, i):
+        for b in range(per):
+            loops[t].seq_step(b, i)
+        return per
+
+    rn, un, eln = _threads_rate(wn, nc, all_core_s)
+    return {"one_core": round(r1, 2), "all_cores": round(rn, 2), "nproc": nc,
+            "ideal_all_cores": round(r1 * nc, 2),
+            "sample": f"one thread: 16 sequences, {u1} seq-steps in {el1:.2f} s; {nc} threads x "
+                      f"{per} sequences, {un} seq-steps in {eln:.2f} s (extend + draft + fp64 verify)"}
+
+
+def measure_step_b64(dev, ws, rank, cpu=True, steps=64, warm=3, min_ms=300.0):
+    """The full decode step at B=64: sam_step (extend by the previous step's
+    emitted tokens, draft K=3), then spec_verify at T=1 on that step's
+    logits; the emitted tokens feed the next step.  Verification is also
+    timed alone on the drafts each step produced."""
     import torch
 
     import sam_drafting_verification_gb300 as ss
-
-    ws, rank, local = _dist()
-    if ws > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local if ws > 1 else 0)
-    torch.cuda.set_device(dev)
-    if args.workload == "sweep_b1024":
-        return run_sweep(args, ws, rank, dev)
-    if args.workload == "long_rollout_b256":
-        return run_rollout(args, ws, rank, dev)
-    if args.workload == "rollout_toy_b64":
-        return run_rollout_toy(args, ws, rank, dev)
-    if args.workload == "static_match_b256":
-        return run_static_match(args, ws, rank, dev)
-    if args.workload == "tree_b256":
-        return run_tree(args, ws, rank, dev)
-    if args.workload == "sampling_b256":
-        return run_sampling(args, ws, rank, dev)
-
     B, V, K, T, n = 64, workloads.V_LARGE, 3, 1.0, 4096
     hist, cont = rs_inputs(rank, B, V, n, K)
-    steps, warm = args.steps, args.warmup
     cap = n + (K + 1) * (steps + warm + 8) + 64
     batch = ss.SamBatch(B, cap, V, device=dev)
     hist_d = torch.as_tensor(hist, device=dev)
     nfull = torch.full((B,), n, dtype=torch.int32, device=dev)
-
-    # S1: prefill build (one launch), timed on its own
+    batch.extend(hist_d, nfull)  # untimed build, then the timed one
+    torch.cuda.synchronize()
+    batch.reset()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
@@ -242,267 +569,103 @@ def run_gpu(args):
     prefill_ms = e0.elapsed_time(e1)
     assert (batch.status() == 0).all()
     snap = batch.export()
-
     pool = rs_logits_pool(dev, B, K, V, cont, 4242 + rank)
     emit = torch.zeros((B, K + 1), dtype=torch.int32, device=dev)
     emit_len = torch.zeros(B, dtype=torch.int32, device=dev)
-    draft = torch.empty((B, K), dtype=torch.int32, device=dev)
-    dlen = torch.empty(B, dtype=torch.int32, device=dev)
-    mlen = torch.empty(B, dtype=torch.int32, device=dev)
-    mend = torch.empty(B, dtype=torch.int32, device=dev)
+    dlog = torch.empty((steps + warm, B, K), dtype=torch.int32, device=dev)
+    llog = torch.empty((steps + warm, B), dtype=torch.int32, device=dev)
+    aux = (torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev))
     out = {"accept_len": torch.empty(B, dtype=torch.int32, device=dev),
            "out_token": torch.empty(B, dtype=torch.int32, device=dev),
            "emit": emit, "emit_len": emit_len,
            "status": torch.empty(B, dtype=torch.int32, device=dev)}
-    acc_log = torch.zeros((max(min(steps, 2000), 1), B), dtype=torch.int32, device=dev)
+    acc_log = torch.zeros((steps, B), dtype=torch.int32, device=dev)
     wsv = ss.verify_workspace(B, K, V, dev)
 
-    def step(s, log_row=None, only_verify=False):
-        if not only_verify:
-            batch.step(emit, emit_len, K, out=(draft, dlen, mlen, mend))
-        ss.spec_verify(pool[s % POOL], draft, dlen, temperature=T, seed=1002, step=s, out=out,
+    def step(s, verify_only=False, log=False):
+        if not verify_only:
+            batch.step(emit, emit_len, K, out=(dlog[s], llog[s], aux[0], aux[1]))
+        ss.spec_verify(pool[s % POOL], dlog[s], llog[s], temperature=T, seed=1002, step=s, out=out,
                        emit=True, status=True, workspace=wsv)
-        if log_row is not None:
-            log_row.copy_(out["accept_len"])
+        if log:
+            acc_log[s - warm].copy_(out["accept_len"])
 
-    # warm-up (eager), then restore the automata to the post-prefill snapshot
+    def restore():
+        batch.import_(snap)
+        emit_len.zero_()
+
     for s in range(warm):
         step(s)
     torch.cuda.synchronize()
-    batch.import_(snap)
-    emit_len.zero_()
+    restore()
+    g_full, cs = _capture(dev, lambda i: step(warm + i), steps)
+    restore()
+    # one eager pass of the same steps: accept lengths, and the drafts each
+    # step produced (logged in dlog) for the verify-only graph
+    for i in range(steps):
+        step(warm + i, log=True)
+    torch.cuda.synchronize()
+    st_ok = bool((out["status"] == 0).all()) and bool((batch.status() == 0).all())
+    g_ver, cs2 = _capture(dev, lambda i: step(warm + i, verify_only=True), steps)
+    full = _timed_replays(g_full, cs, ws, dev, min_ms, pre=restore)
+    ver = _timed_replays(g_ver, cs2, ws, dev, min_ms / 2)
+    ms_full = _max_over_ranks(statistics.median(full) / steps, ws, dev)
+    ms_ver = _max_over_ranks(statistics.median(ver) / steps, ws, dev)
+    L = acc_log.cpu().numpy().astype(np.int64)
+    hbm, _ = _peaks()
+    vbytes = float((L + 1).sum()) / steps * V * 2
+    r = {"B": B, "K": K, "V": V, "temperature": T, "history": n, "steps_per_replay": steps,
+         "seq_steps_per_s": round(_sum_over_ranks(float(B), ws, dev) / (ms_full / 1e3), 1),
+         "ms_per_step": round(ms_full, 5), "verify_us": round(ms_ver * 1e3, 2),
+         "sam_ns_per_seq_step": round(max(ms_full - ms_ver, 0.0) * 1e6 / B, 1),
+         "verify_frac_of_peak": round(vbytes / (ms_ver / 1e3) / 1e9 / hbm, 4),
+         "verify_algorithmic_bytes_per_launch": round(vbytes, 1),
+         "verify_traffic": _verify_traffic("rs_bf16_b64"),
+         "mean_accept_len": round(float(L.mean()), 4),
+         "prefill_tokens_per_s": round(B * n / (prefill_ms / 1e3), 1),
+         "statuses_ok": st_ok}
+    if cpu:
+        c = oracle_step_rate(hist, cont, 5.0, 4.0)
+        r["oracle_seq_steps_per_s"] = c
+        r["vs_oracle_one_core"] = round(r["seq_steps_per_s"] / c["one_core"], 1)
+        r["vs_oracle_all_cores"] = round(r["seq_steps_per_s"] / c["all_cores"], 1)
+    return r
 
-    # capture exactly `steps` steps (2 kernels each) in one graph
-    cs = torch.cuda.Stream(device=dev)
-    g = torch.cuda.CUDAGraph()
-    cs.wait_stream(torch.cuda.current_stream(dev))
-    with torch.cuda.stream(cs):
-        with torch.cuda.graph(g, stream=cs):
-            for s in range(steps):
-                step(warm + s)
-    torch.cuda.synchronize()
-    batch.import_(snap)
-    emit_len.zero_()
-    torch.cuda.synchronize()
 
-    clocks = ClockSampler(dev.index)
-    clocks.start()
-    time.sleep(0.3)
-    _barrier(ws)
-    torch.cuda.synchronize()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.nvtx.range_push("timed")
-    t0.record()
-    g.replay()
-    t1.record()
-    torch.cuda.synchronize()
-    torch.cuda.nvtx.range_pop()
-    _barrier(ws)
-    total_ms = t0.elapsed_time(t1)
-    clk = clocks.stop()
-    st = out["status"].cpu().numpy()
-    assert (st == 0).all() and (batch.status() == 0).all(), "verification or automaton error"
-
-    # acceptance of the first timed steps (eager re-run of the same steps, outside timing)
-    n_acc = min(steps, 2000)
-    batch.import_(snap)
-    emit_len.zero_()
-    for s in range(n_acc):
-        step(warm + s, log_row=acc_log[s])
-    torch.cuda.synchronize()
-    L = acc_log[:n_acc].cpu().numpy().astype(np.int64)
-
-    # attribution: the verify launches alone, replayed as a graph on the same inputs
-    n_att = min(steps, 2000)
-    gv = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(cs):
-        with torch.cuda.graph(gv, stream=cs):
-            for s in range(n_att):
-                step(warm + s, only_verify=True)
-    torch.cuda.synchronize()
-    v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    v0.record()
-    gv.replay()
-    v1.record()
-    torch.cuda.synchronize()
-    verify_ms = v0.elapsed_time(v1) / n_att
-    Lv = out["accept_len"].cpu().numpy().astype(np.int64)  # last verify's lengths (same drafts each launch)
-
-    ms_step = _max_over_ranks(total_ms / steps, ws, dev)
-    seqs = _sum_over_ranks(float(B), ws, dev)
-    value = seqs / (ms_step / 1e3)
-    sam_ms = max(ms_step - verify_ms, 0.0)
-
-    # verify roofline: algorithmic bytes = rows the accept chains need
-    row_bytes = V * 2
-    verify_bytes = float((Lv + 1).sum()) * row_bytes
+def run_rs(args, ws, rank, dev):
+    r = measure_step_b64(dev, ws, rank, cpu=rank == 0, steps=args.steps, warm=args.warmup)
     hbm, peak_kind = _peaks()
-    achieved = verify_bytes / (verify_ms / 1e3) / 1e9
-    roof = {"kernel": "verify_kernel<bf16, one-hot, T>0>", "bound": "hbm",
-            "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-            "frac": round(achieved / hbm, 4), "traffic": _verify_traffic("rs_bf16_b64"),
-            "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
-            "algorithmic_bytes_per_launch": verify_bytes,
-            "kernel_ms": round(verify_ms, 5)}
-
-    cpu = cpu_baseline_rs(hist, cont) if rank == 0 else None
-    e2e = e2e_rs(batch, snap, pool, emit, emit_len, draft, dlen, mlen, mend, out, wsv, B, K, V, T,
-                 steps=min(steps, 200), dev=dev)
-
-    line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "seq-steps/s", "n_gpus": ws,
-        "steps": steps, "warmup": warm, "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32 (bf16 logits)", "data": "synthetic",
-        "config": {"workload": "rs_bf16_b64", "B_per_gpu": B, "V": V, "K": K, "temperature": T,
-                   "history": n, "logits": "bf16 N(0, sd 2) + 4 on the true continuation",
-                   "drafts": "device SAM (K=3)", "parallelism": f"dp{ws} (independent batches)",
-                   "l2": f"inputs larger than L2: rotating pool of {POOL} logits tensors "
-                         f"({POOL * B * (K + 1) * V * 2 / 1e9:.2f} GB)",
-                   "timing": "CUDA graph of exactly `steps` steps, events on the capture stream"},
-        "roofline": roof,
-        "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": 2 * steps,
-        "clocks": clk,
-        "breakdown": {
-            "sam_step_ns_per_seq_step": round(sam_ms * 1e6 / B, 1),
-            "verify_us_per_step": round(verify_ms * 1e3, 2),
-            "verify_algorithmic_GBps": round(achieved, 1),
-            "prefill_tokens_per_s": round(B * n / (prefill_ms / 1e3), 1),
-            "mean_accept_len": round(float(L.mean()), 4),
-            "mean_emitted_per_step": round(float(L.mean()) + 1, 4),
-        },
-    }
+    c = r.get("oracle_seq_steps_per_s")
+    ver_ms = r["verify_us"] / 1e3
+    line = {"metric": METRIC, "value": r["seq_steps_per_s"], "unit": "seq-steps/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32 (bf16 logits)", "data": "synthetic",
+            "config": {"workload": "rs_bf16_b64", "B_per_gpu": 64, "V": r["V"], "K": 3, "temperature": 1.0,
+                       "history": 4096, "logits": "bf16 N(0, sd 2) + 4 on the true continuation",
+                       "drafts": "device SAM (K=3)", "l2": f"rotating pool of {POOL} logits tensors",
+                       "timing": "CUDA graph of exactly `steps` steps, median replay"},
+            "roofline": {"kernel": "verify_kernel<bf16, one-hot, T>0>", "bound": "hbm",
+                         "achieved": round(r["verify_algorithmic_bytes_per_launch"] / ver_ms / 1e6, 1),
+                         "peak": hbm, "unit": "GB/s", "frac": r["verify_frac_of_peak"],
+                         "traffic": r["verify_traffic"], "peak_source": peak_kind,
+                         "algorithmic_bytes_per_launch": r["verify_algorithmic_bytes_per_launch"]},
+            "cpu_baseline": ({"value": c["one_core"], "unit": "seq-steps/s", "cores": 1, "kind": "oracle",
+                              "nproc": c["nproc"], "all_cores": c["all_cores"], "sample": c["sample"]}
+                             if c else None),
+            "gpu_launches": 2 * args.steps, "breakdown": r}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
-
-
-def e2e_rs(batch, snap, pool, emit, emit_len, draft, dlen, mlen, mend, out, wsv, B, K, V, T, steps, dev):
-    """Same metric through the public API with host buffers: every step copies
-    its logits from pinned host memory and reads the emitted tokens back.  The
-    copy of step s + 1 runs on a copy stream into a second device buffer while
-    step s computes (the host link, about 200 GB/s, bounds the loop)."""
-    import torch
-
-    import sam_drafting_verification_gb300 as ss
-    host_pool = [p.cpu().pin_memory() for p in pool[:4]]
-    dev_buf = [torch.empty_like(pool[0]) for _ in range(2)]
-    host_emit = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
-    host_len = torch.empty(B, dtype=torch.int32).pin_memory()
-    batch.import_(snap)
-    emit_len.zero_()
-    torch.cuda.synchronize()
-    cur = torch.cuda.current_stream(dev)
-    cps = torch.cuda.Stream(device=dev)
-    copied = [torch.cuda.Event() for _ in range(2)]
-    freed = [torch.cuda.Event() for _ in range(2)]
-
-    def issue_copy(s):
-        i = s % 2
-        if s >= 2:  # the buffer's previous step has verified
-            cps.wait_event(freed[i])
-        with torch.cuda.stream(cps):
-            dev_buf[i].copy_(host_pool[s % len(host_pool)], non_blocking=True)
-        copied[i].record(cps)
-
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(cur)
-    cps.wait_stream(cur)
-    issue_copy(0)
-    for s in range(steps):
-        if s + 1 < steps:
-            issue_copy(s + 1)
-        cur.wait_event(copied[s % 2])
-        batch.step(emit, emit_len, K, out=(draft, dlen, mlen, mend))
-        ss.spec_verify(dev_buf[s % 2], draft, dlen, temperature=T, seed=1002, step=s, out=out,
-                       emit=True, status=True, workspace=wsv)
-        freed[s % 2].record(cur)
-        host_emit.copy_(emit, non_blocking=True)
-        host_len.copy_(emit_len, non_blocking=True)
-    e1.record(cur)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
-    return {"value": round(B / (ms / 1e3), 1), "unit": "seq-steps/s",
-            "h2d_bytes_per_step": int(dev_buf[0].numel() * dev_buf[0].element_size()),
-            "d2h_bytes_per_step": int(host_emit.numel() * 4 + host_len.numel() * 4),
-            "ms_per_step": round(ms, 4), "steps": steps,
-            "overlap": "step s + 1's copy on a second stream while step s computes"}
-
-
-class OracleLoop:
-    """The oracle as it stands, on a sample of the same workload: each sampled
-    sequence's automaton is built over its history (untimed); a step extends it
-    with the previously emitted tokens, drafts K and verifies the draft in fp64
-    against that step's logits (host-generated, same distribution, bf16-rounded)."""
-
-    def __init__(self, hist, cont, nseq, npool=4, seed=77):
-        import torch
-
-        import oracle
-        self.oracle = oracle
-        V, K = workloads.V_LARGE, 3
-        self.K, self.T, self.nseq, self.npool = K, 1.0, nseq, npool
-        rng = np.random.default_rng(seed)
-        self.rows = []
-        for p in range(npool):
-            x = workloads.gaussian_logits(rng, (nseq, K + 1, V), 2.0)
-            workloads.boost_truth(x, cont[:nseq, p * (K + 1):(p + 1) * (K + 1)], 4.0)
-            self.rows.append(workloads.to_bf16(x).float().numpy())
-        self.sams = [oracle.Sam(V) for _ in range(nseq)]
-        for b in range(nseq):
-            self.sams[b].extend(hist[b])
-        self.emit = [[] for _ in range(nseq)]
-
-    def seq_step(self, b, s):
-        K = self.K
-        self.sams[b].extend(self.emit[b])
-        d, dl, _, _ = self.sams[b].draft(K)
-        d = np.maximum(d, 0)[None]
-        rows = self.rows[s % self.npool][b:b + 1]
-        r = self.oracle.verify(rows, d, np.array([dl], np.int32), temperature=self.T, seed=1002,
-                               step=s, seq_index=np.array([b]))
-        L = int(r["accept_len"][0])
-        self.emit[b] = list(d[0, :L]) + [int(r["out_token"][0])]
-
-
-def cpu_baseline_rs(hist, cont, nseq=64, min_steps=40, target_s=10.0, max_steps=1000):
-    """The oracle's decode steps over nseq sequences, repeated until about
-    target_s seconds of host work (at least min_steps steps)."""
-    loop = OracleLoop(hist, cont, nseq)
-    t0 = time.perf_counter()
-    nsteps = 0
-    while nsteps < max_steps and (nsteps < min_steps or time.perf_counter() - t0 < target_s):
-        for b in range(nseq):
-            loop.seq_step(b, nsteps)
-        nsteps += 1
-    el = time.perf_counter() - t0
-    return {"value": round(nseq * nsteps / el, 2), "unit": "seq-steps/s", "cores": 1, "kind": "oracle",
-            "sample": f"{nseq} sequences x {nsteps} decode steps of the same workload "
-                      f"(extend + draft + fp64 verify, single thread), {el:.2f} s"}
 
 
 # --------------------------------------------------------------------------
-# long-tail rollout: B=256 long histories, 512 decode steps
+# the automata alone: long-tail rollout, B=256 histories of 16k-32k tokens
 # --------------------------------------------------------------------------
 
-def run_rollout(args, ws, rank, dev):
-    """B=256 histories log-uniform in [16k, 32k] tokens (Zipf(1.1), copy prob
-    0.5, spans 16-256), V=151936: one prefill build, then 512 steps of
-    (extend by the stream's next U{1..4} tokens + draft K=3, greedy verify of
-    the drafts on bf16 logits [256, 4, V] ~ N(0, sd 2)).  The SAM step is also
-    timed alone (ns per sequence-step) next to the oracle's extend + draft on
-    a sample of the same sequences."""
-    import torch
-
-    import sam_drafting_verification_gb300 as ss
+def _rollout_inputs(rank):
     w = workloads.long_rollout(seed=1004 + 7919 * rank)
-    B, V, K, steps = w["B"], w["V"], w["K"], w["steps"]
+    B, steps = w["B"], w["steps"]
     lens, n_new, streams = w["lens"], w["n_new"], w["streams"]
-    cap = int(max(len(x) for x in streams))
     maxlen = int(lens.max())
     pre = np.zeros((B, maxlen), np.int32)
     toks = np.zeros((steps, B, 4), np.int32)
@@ -513,13 +676,93 @@ def run_rollout(args, ws, rank, dev):
             k = int(n_new[s, b])
             toks[s, b, :k] = streams[b][pos:pos + k]
             pos += k
+    return w, pre, toks
+
+
+def oracle_rollout_rates(streams, lens, toks, n_new, K, one_core_seqs=16):
+    """The oracle's automata on samples of the rollout: the prefill build
+    (tokens/s) and 512 steps of extend + draft (ns per sequence-step), on
+    one thread over `one_core_seqs` sequences, then on every host core with
+    the same number of sequences per thread."""
+    import oracle
+    V = workloads.V_LARGE
+    nc = _nproc()
+    steps = toks.shape[0]
+
+    def build_and_step(seqs):
+        sams = [oracle.Sam(V) for _ in seqs]
+        t0 = time.perf_counter()
+        for i, b in enumerate(seqs):
+            sams[i].extend(streams[b][:lens[b]])
+        t1 = time.perf_counter()
+        for s in range(steps):
+            oracle.step_batch(sams, toks[s, seqs], n_new[s, seqs], K)
+        t2 = time.perf_counter()
+        return t1 - t0, t2 - t1
+
+    seqs1 = list(range(one_core_seqs))
+    b1, s1 = build_and_step(seqs1)
+    tok1 = int(sum(int(lens[b]) for b in seqs1))
+    per = one_core_seqs
+    B = len(lens)
+    groups = [[(t * per + i) % B for i in range(per)] for t in range(nc)]
+    res = [None] * nc
+    gate = threading.Barrier(nc)
+    walls = {}
+
+    def run(t):
+        import oracle as o
+        sams = [o.Sam(V) for _ in groups[t]]
+        gate.wait()
+        if t == 0:
+            walls["b0"] = time.perf_counter()
+        for i, b in enumerate(groups[t]):
+            sams[i].extend(streams[b][:lens[b]])
+        gate.wait()
+        if t == 0:
+            walls["b1"] = time.perf_counter()
+        for s in range(steps):
+            o.step_batch(sams, toks[s, groups[t]], n_new[s, groups[t]], K)
+        gate.wait()
+        if t == 0:
+            walls["s1"] = time.perf_counter()
+        res[t] = True
+
+    ths = [threading.Thread(target=run, args=(t,)) for t in range(nc)]
+    for th in ths:
+        th.start()
+    for th in ths:
+        th.join()
+    tokn = int(sum(int(lens[b]) for g in groups for b in g))
+    bn, sn = walls["b1"] - walls["b0"], walls["s1"] - walls["b1"]
+    return {"nproc": nc,
+            "prefill_tokens_per_s": {"one_core": round(tok1 / b1, 1), "all_cores": round(tokn / bn, 1),
+                                     "ideal_all_cores": round(tok1 / b1 * nc, 1)},
+            "ns_per_seq_step": {"one_core": round(s1 / (steps * per) * 1e9, 1),
+                                "all_cores": round(sn / (steps * per * nc) * 1e9, 1),
+                                "ideal_all_cores": round(s1 / (steps * per) * 1e9 / nc, 1)},
+            "sample": f"one thread: {per} sequences ({tok1} history tokens, build {b1:.2f} s, "
+                      f"{steps} steps {s1:.2f} s); {nc} threads x {per} sequences ({tokn} tokens, "
+                      f"build {bn:.2f} s, steps {sn:.2f} s)"}
+
+
+def measure_rollout(dev, ws, rank, cpu=True, min_ms=400.0):
+    """B=256 histories log-uniform in [16k, 32k] tokens (Zipf(1.1), copy prob
+    0.5, spans 16-256), V=151936: the prefill build, then 512 steps of
+    (extend by the stream's next U{1..4} tokens + draft K=3), timed alone and
+    with greedy verification of bf16 logits N(0, sd 2) [256, 4, V]."""
+    import torch
+
+    import sam_drafting_verification_gb300 as ss
+    w, pre, toks = _rollout_inputs(rank)
+    B, V, K, steps = w["B"], w["V"], w["K"], w["steps"]
+    lens, n_new, streams = w["lens"], w["n_new"], w["streams"]
+    cap = int(max(len(x) for x in streams))
     batch = ss.SamBatch(B, cap, V, device=dev)
     pre_d = torch.as_tensor(pre, device=dev)
     lens_d = torch.as_tensor(lens, device=dev)
     toks_d = torch.as_tensor(toks, device=dev)
     nn_d = torch.as_tensor(n_new, device=dev)
-
-    # S1: prefill (one launch), timed after one untimed build
     batch.extend(pre_d, lens_d)
     torch.cuda.synchronize()
     batch.reset()
@@ -531,8 +774,7 @@ def run_rollout(args, ws, rank, dev):
     prefill_ms = e0.elapsed_time(e1)
     assert (batch.status() == 0).all()
     snap = batch.export()
-
-    npool = 4  # 4 x 311 MB of bf16 logits: each step's rows are not in L2
+    npool = 4
     g = torch.Generator(device=dev)
     g.manual_seed(4004 + rank)
     pool = []
@@ -550,110 +792,220 @@ def run_rollout(args, ws, rank, dev):
            "status": torch.empty(B, dtype=torch.int32, device=dev)}
     wsv = ss.verify_workspace(B, K, V, dev)
 
-    def step(s, sam=True, verify=True):
-        if sam:
-            batch.step(toks_d[s], nn_d[s], K, out=(draft, dlen, mlen, mend))
+    def step(s, verify=True):
+        batch.step(toks_d[s], nn_d[s], K, out=(draft, dlen, mlen, mend))
         if verify:
             ss.spec_verify(pool[s % npool], draft, dlen, temperature=0.0, out=out, status=True,
                            workspace=wsv)
 
-    def graph(**kw):
-        cs = torch.cuda.Stream(device=dev)
-        gr = torch.cuda.CUDAGraph()
-        cs.wait_stream(torch.cuda.current_stream(dev))
-        with torch.cuda.stream(cs):
-            with torch.cuda.graph(gr, stream=cs):
-                for s in range(steps):
-                    step(s, **kw)
-        torch.cuda.synchronize()
-        return gr
-
-    def timed(gr):
+    def restore():
         batch.import_(snap)
-        torch.cuda.synchronize()
-        _barrier(ws)
-        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        gr.replay()
-        b_.record()
-        torch.cuda.synchronize()
-        _barrier(ws)
-        return a.elapsed_time(b_)
 
-    for s in range(max(args.warmup, 3)):  # eager warm-up
+    for s in range(3):
         step(s)
     torch.cuda.synchronize()
-    batch.import_(snap)
-    g_full = graph()
-    g_sam = graph(verify=False)
-    timed(g_full)  # graph warm-up
-    clocks = ClockSampler(dev.index)
-    clocks.start()
-    time.sleep(0.3)
-    full_ms = timed(g_full)
-    clk = clocks.stop()
+    restore()
+    g_full, cs1 = _capture(dev, lambda s: step(s), steps)
+    g_sam, cs2 = _capture(dev, lambda s: step(s, verify=False), steps)
+    full = _timed_replays(g_full, cs1, ws, dev, min_ms, pre=restore)
+    sam = _timed_replays(g_sam, cs2, ws, dev, min_ms, pre=restore)
     assert (out["status"].cpu() == 0).all() and (batch.status() == 0).all()
-    sam_ms = timed(g_sam)
-    # drafts of the last step: the automata followed the streams exactly
-    st_ms = _max_over_ranks(full_ms / steps, ws, dev)
-    sam_ns = _max_over_ranks(sam_ms / steps / B * 1e6, ws, dev)
-    seqs = _sum_over_ranks(float(B), ws, dev)
-    verify_ms = max(full_ms - sam_ms, 1e-9) / steps
-    Lh = out["accept_len"].cpu().numpy().astype(np.int64)
-    hbm, peak_kind = _peaks()
-    vbytes = float((Lh + 1).sum()) * V * 2
-    achieved = vbytes / (verify_ms / 1e3) / 1e9
+    # the automata followed the streams: the last drafts equal a fresh query
+    st_ms = _max_over_ranks(statistics.median(full) / steps, ws, dev)
+    sam_ns = _max_over_ranks(statistics.median(sam) / steps / B * 1e6, ws, dev)
+    r = {"B": B, "K": K, "V": V, "steps": steps, "prefill_tokens": int(lens.sum()),
+         "sam_ns_per_seq_step": round(sam_ns, 1),
+         "step_with_greedy_verify_us": round(st_ms * 1e3, 2),
+         "seq_steps_per_s_with_verify": round(_sum_over_ranks(float(B), ws, dev) / (st_ms / 1e3), 1),
+         "prefill_tokens_per_s": round(float(lens.sum()) / (prefill_ms / 1e3), 1),
+         "prefill_ms": round(prefill_ms, 3),
+         "replays": [len(full), len(sam)]}
+    if cpu:
+        c = oracle_rollout_rates(streams, lens, toks, n_new, K)
+        r["oracle"] = c
+        r["sam_vs_oracle_one_core"] = round(c["ns_per_seq_step"]["one_core"] / sam_ns, 1)
+        r["sam_vs_oracle_all_cores"] = round(c["ns_per_seq_step"]["all_cores"] / sam_ns, 1)
+        r["prefill_vs_oracle_one_core"] = round(r["prefill_tokens_per_s"] / c["prefill_tokens_per_s"]["one_core"], 1)
+        r["prefill_vs_oracle_all_cores"] = round(r["prefill_tokens_per_s"] / c["prefill_tokens_per_s"]["all_cores"], 1)
+    return r
 
-    cpu = None
-    if rank == 0:
-        cpu = oracle_sam_rollout(streams, lens, toks, n_new, K, nseq=B)
-    line = {
-        "metric": METRIC, "value": round(seqs / (st_ms / 1e3), 1), "unit": "seq-steps/s",
-        "n_gpus": ws, "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": round(st_ms, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32 (SAM), f32 (bf16 logits)",
-        "data": "synthetic",
-        "config": {"workload": "long_rollout_b256", "B_per_gpu": B, "V": V, "K": K, "steps": steps,
-                   "history": "log-uniform [16384, 32768]", "prefill_tokens": int(lens.sum()),
-                   "verify": "greedy, bf16 N(0, sd 2)",
-                   "l2": f"inputs larger than L2: {npool} logits tensors of {B * (K + 1) * V * 2 / 1e6:.0f} MB",
-                   "timing": "CUDA graph of the 512 steps, events on the capture stream"},
-        "roofline": {"kernel": "verify_kernel<bf16, greedy>", "bound": "hbm", "achieved": round(achieved, 1),
-                     "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                     "traffic": _verify_traffic("long_rollout_b256"),
-                     "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
-                     "algorithmic_bytes_per_launch": vbytes,
-                     "note": "verify time = (full step - SAM-only step) / steps"},
-        "cpu_baseline": cpu,
-        "gpu_launches": 2 * steps,
-        "clocks": clk,
-        "breakdown": {
-            "sam_step_ns_per_seq_step": round(sam_ns, 1),
-            "sam_vs_oracle": (round(cpu["value"] / sam_ns, 1) if cpu else None),
-            "verify_us_per_step": round(verify_ms * 1e3, 2),
-            "prefill_tokens_per_s": round(float(lens.sum()) / (prefill_ms / 1e3), 1),
-            "prefill_ms": round(prefill_ms, 3),
-        },
-    }
+
+def run_rollout(args, ws, rank, dev):
+    r = measure_rollout(dev, ws, rank, cpu=rank == 0)
+    c = r.get("oracle")
+    line = {"metric": METRIC, "value": r["sam_ns_per_seq_step"], "unit": "ns/seq-step (SAM extend + draft)",
+            "n_gpus": ws, "steps": r["steps"], "warmup": 3,
+            "ms_per_step": round(r["sam_ns_per_seq_step"] * r["B"] / 1e6, 5),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+            "data": "synthetic",
+            "config": {"workload": "long_rollout_b256", "B_per_gpu": r["B"], "V": r["V"], "K": r["K"],
+                       "steps": r["steps"], "history": "log-uniform [16384, 32768]",
+                       "prefill_tokens": r["prefill_tokens"],
+                       "timing": "CUDA graph of the 512 SAM steps, median replay"},
+            "cpu_baseline": ({"value": c["ns_per_seq_step"]["one_core"], "unit": "ns/seq-step", "cores": 1,
+                              "kind": "oracle", "nproc": c["nproc"],
+                              "all_cores": c["ns_per_seq_step"]["all_cores"], "sample": c["sample"]}
+                             if c else None),
+            "gpu_launches": r["steps"], "breakdown": r}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
-def oracle_sam_rollout(streams, lens, toks, n_new, K, nseq):
-    """The oracle's extend + draft (one C call per step for the sample), on
-    the first nseq sequences of the rollout; the builds are untimed."""
-    import oracle
-    V = workloads.V_LARGE
-    sams = [oracle.Sam(V) for _ in range(nseq)]
-    for b in range(nseq):
-        sams[b].extend(streams[b][:lens[b]])
-    steps = toks.shape[0]
-    t0 = time.perf_counter()
-    for s in range(steps):
-        oracle.step_batch(sams, toks[s, :nseq], n_new[s, :nseq], K)
-    el = time.perf_counter() - t0
-    return {"value": round(el / (steps * nseq) * 1e9, 1), "unit": "ns/seq-step (SAM extend + draft)",
-            "cores": 1, "kind": "oracle",
-            "sample": f"{nseq} of the 256 sequences x {steps} steps, single thread, {el:.2f} s"}
+# --------------------------------------------------------------------------
+# verification with draft-model logits: B=32, K=5, fp32, T=0.7
+# --------------------------------------------------------------------------
+
+DM_POOL = 4
+
+
+def measure_draft_model(dev, ws, rank, cpu=True, reps=20, min_ms=200.0):
+    """Target N(0, sd 2) [32, 6, V] fp32, draft logits = target + N(0, 1)
+    [32, 5, V] fp32, drafts sampled from softmax(draft / 0.7), T=0.7:
+    accept with min(1, p/q), resample from norm(max(0, p - q)).  Four input
+    sets rotate (856 MB).  Algorithmic bytes of a launch: per sequence the
+    (L + 1) target rows and min(L + 1, n) draft rows its chain scored, plus
+    one residual pass over the final target and draft rows after a
+    rejection."""
+    import torch
+
+    import sam_drafting_verification_gb300 as ss
+    B, K, V, T = 32, 5, workloads.V_LARGE, 0.7
+    hbm, peak_kind = _peaks()
+    pool = [workloads.draft_model_device(1003 + 17 * i + 7919 * rank, B, K, V, T, dev) for i in range(DM_POOL)]
+    wsv = ss.verify_workspace(B, K, V, dev)
+    res = {k: torch.empty(B, dtype=torch.int32, device=dev) for k in ("accept_len", "out_token", "status")}
+
+    def step(s):
+        tg, dl, dr = pool[s % DM_POOL]
+        ss.spec_verify(tg, dr, draft_logits=dl, temperature=T, seed=3, step=s, out=res, status=True,
+                       workspace=wsv)
+
+    for s in range(3):
+        step(s)
+    torch.cuda.synchronize()
+    g, cs = _capture(dev, step, reps)
+    times = _timed_replays(g, cs, ws, dev, min_ms)
+    ms = _max_over_ranks(statistics.median(times) / reps, ws, dev)
+    acc, rows_t, rows_d, resid = 0, 0, 0, 0
+    for s in range(reps):
+        step(s)
+        L = res["accept_len"].cpu().numpy().astype(np.int64)
+        assert (res["status"] == 0).all()
+        acc += int(L.sum())
+        rows_t += int((L + 1).sum())
+        rows_d += int(np.minimum(L + 1, K).sum())
+        resid += int((L < K).sum())
+    alg = (rows_t + rows_d + 2 * resid) / reps * V * 4
+    ach = alg / (ms / 1e3) / 1e9
+    r = {"B": B, "K": K, "V": V, "temperature": T, "us_per_launch": round(ms * 1e3, 2),
+         "seq_steps_per_s": round(_sum_over_ranks(float(B), ws, dev) / (ms / 1e3), 1),
+         "acceptance": round(acc / (reps * B * K), 4), "mean_accept_len": round(acc / (reps * B), 4),
+         "algorithmic_bytes_per_launch": round(alg, 1), "achieved_GBps": round(ach, 1),
+         "frac": round(ach / hbm, 4), "peak_source": peak_kind,
+         "traffic": _verify_traffic("draft_model_b32")}
+    if cpu:
+        nb = 4
+        tg, dl, dr = pool[0]
+        c = oracle_verify_rate(tg[:nb].cpu().numpy(), dr[:nb].cpu().numpy(), T, 3, 5.0, 4.0,
+                               draft_logits=dl[:nb].cpu().numpy())
+        r["oracle_seq_steps_per_s"] = c
+    return r
+
+
+def run_draft_model(args, ws, rank, dev):
+    r = measure_draft_model(dev, ws, rank, cpu=rank == 0, reps=args.steps)
+    hbm, peak_kind = _peaks()
+    c = r.get("oracle_seq_steps_per_s")
+    line = {"metric": METRIC, "value": r["seq_steps_per_s"], "unit": "seq-steps/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": 3, "ms_per_step": round(r["us_per_launch"] / 1e3, 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": "draft_model_b32", "B_per_gpu": r["B"], "V": r["V"], "K": r["K"],
+                       "temperature": r["temperature"], "logits": "fp32 target N(0, sd 2), draft = target + N(0, 1)",
+                       "drafts": "sampled from softmax(draft / 0.7)", "l2": f"{DM_POOL} rotating input sets (856 MB)",
+                       "timing": "CUDA graph of `steps` launches, median replay"},
+            "roofline": {"kernel": "verify_kernel<f32, f32 draft logits, T>0>", "bound": "hbm",
+                         "achieved": r["achieved_GBps"], "peak": hbm, "unit": "GB/s", "frac": r["frac"],
+                         "traffic": r["traffic"], "peak_source": peak_kind,
+                         "algorithmic_bytes_per_launch": r["algorithmic_bytes_per_launch"]},
+            "cpu_baseline": ({"value": c["one_core"], "unit": "seq-steps/s", "cores": 1, "kind": "oracle",
+                              "nproc": c["nproc"], "all_cores": c["all_cores"], "sample": c["sample"]}
+                             if c else None),
+            "gpu_launches": args.steps, "breakdown": r}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# verification sweep at B=1024
+# --------------------------------------------------------------------------
+
+def measure_sweep(dev, ws, rank, reps=10, only=None):
+    """B=1024, V=151936, K in {1,3,5,8} x fp32/bf16 x {greedy, T=1, greedy
+    with drafts = each row's argmax (every row read)}; logits N(0, sd 2),
+    drafts uniform among each row's top 5.  Each point: a graph of `reps`
+    launches on one input (above L2 at every point: each launch reads at
+    least 1024 rows), median of three replays."""
+    import torch
+
+    import sam_drafting_verification_gb300 as ss
+    B, V = 1024, workloads.V_LARGE
+    hbm, _ = _peaks()
+    points = []
+    for K in (1, 3, 5, 8):
+        for dtype in (torch.float32, torch.bfloat16):
+            if only and (only[0] != K or only[1] != dtype):
+                continue
+            logits, draft = workloads.sweep_device(7000 + K + 100 * rank, B, K, V, dtype, dev)
+            full_draft = torch.argmax(logits[:, :K].float(), dim=-1).to(torch.int32).contiguous()
+            for T, name, dr in ((0.0, "greedy", draft), (1.0, "T=1", draft), (0.0, "greedy-full-read", full_draft)):
+                if only and only[2] != name:
+                    continue
+                wsv = ss.verify_workspace(B, K, V, dev)
+                res = ss.spec_verify(logits, dr, None, temperature=T, seed=5, step=0, workspace=wsv)
+                for w in range(3):
+                    ss.spec_verify(logits, dr, None, temperature=T, seed=5, step=w, out=res, workspace=wsv)
+                torch.cuda.synchronize()
+                g, cs = _capture(dev, lambda r: ss.spec_verify(logits, dr, None, temperature=T, seed=5, step=r,
+                                                               out=res, workspace=wsv), reps)
+                times = [_replay_ms(g, cs, ws) for _ in range(4)][1:]
+                ms = _max_over_ranks(statistics.median(times) / reps, ws, dev)
+                Lh = res["accept_len"].cpu().numpy().astype(np.int64)
+                alg = float((Lh + 1).sum()) * V * logits.element_size()
+                points.append({"K": K, "dtype": str(dtype).split(".")[-1], "mode": name,
+                               "us": round(ms * 1e3, 2), "seq_steps_per_s": round(B / (ms / 1e3), 1),
+                               "mean_accept": round(float(Lh.mean()), 4),
+                               "alg_GBps": round(alg / (ms / 1e3) / 1e9, 1),
+                               "frac": round(alg / (ms / 1e3) / 1e9 / hbm, 4)})
+                del g
+            del logits, draft, full_draft
+            torch.cuda.empty_cache()
+    return points
+
+
+def run_sweep(args, ws, rank, dev):
+    import torch
+    only = None
+    if args.point:  # "K,dtype,mode", e.g. "3,bf16,T=1": one sweep point (profiling)
+        k_s, d_s, m_s = args.point.split(",")
+        only = (int(k_s), {"f32": torch.float32, "bf16": torch.bfloat16}[d_s], m_s)
+    hbm, peak_kind = _peaks()
+    points = measure_sweep(dev, ws, rank, reps=max(args.steps, 1), only=only)
+    head = points[0]
+    for p in points:  # the default line's point when present
+        if (p["K"], p["dtype"], p["mode"]) == (HEAD_K, "bfloat16", "T=1"):
+            head = p
+    line = {"metric": METRIC, "value": head["seq_steps_per_s"], "unit": "seq-steps/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": 3, "ms_per_step": head["us"] / 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": "sweep_b1024", "B": 1024, "V": workloads.V_LARGE,
+                       "point": {k: head[k] for k in ("K", "dtype", "mode")}},
+            "roofline": {"bound": "hbm", "achieved": head["alg_GBps"], "peak": hbm, "unit": "GB/s",
+                         "frac": head["frac"], "traffic": None, "peak_source": peak_kind},
+            "points": points}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 # --------------------------------------------------------------------------
@@ -1120,106 +1472,80 @@ def run_sampling(args, ws, rank, dev):
 
 
 # --------------------------------------------------------------------------
-# verification sweep at B=1024
-# --------------------------------------------------------------------------
-
-def run_sweep(args, ws, rank, dev):
-    import torch
-
-    import sam_drafting_verification_gb300 as ss
-    B, V = 1024, workloads.V_LARGE
-    hbm, peak_kind = _peaks()
-    points = []
-    reps = max(args.steps, 1)
-    only = None
-    if args.point:  # "K,dtype,mode", e.g. "3,bf16,T=1": one sweep point (profiling)
-        k_s, d_s, m_s = args.point.split(",")
-        only = (int(k_s), {"f32": torch.float32, "bf16": torch.bfloat16}[d_s], m_s)
-    for K in (1, 3, 5, 8):
-        for dtype in (torch.float32, torch.bfloat16):
-            if only and (only[0] != K or only[1] != dtype):
-                continue
-            logits, draft = workloads.sweep_device(7000 + K + 100 * rank, B, K, V, dtype, dev)
-            full_draft = torch.argmax(logits[:, :K].float(), dim=-1).to(torch.int32).contiguous()
-            for T, name, dr in ((0.0, "greedy", draft), (1.0, "T=1", draft), (0.0, "greedy-full-read", full_draft)):
-                if only and only[2] != name:
-                    continue
-                wsv = ss.verify_workspace(B, K, V, dev)
-                res = ss.spec_verify(logits, dr, None, temperature=T, seed=5, step=0, workspace=wsv)
-                for _ in range(args.warmup):
-                    ss.spec_verify(logits, dr, None, temperature=T, seed=5, step=0, out=res, workspace=wsv)
-                torch.cuda.synchronize()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                for r in range(reps):
-                    ss.spec_verify(logits, dr, None, temperature=T, seed=5, step=r, out=res, workspace=wsv)
-                e1.record()
-                torch.cuda.synchronize()
-                ms = e0.elapsed_time(e1) / reps
-                Lh = res["accept_len"].cpu().numpy().astype(np.int64)
-                alg = float((Lh + 1).sum()) * V * logits.element_size()
-                points.append({"K": K, "dtype": str(dtype).split(".")[-1], "mode": name,
-                               "us": round(ms * 1e3, 2), "seq_steps_per_s": round(B / (ms / 1e3), 1),
-                               "mean_accept": round(float(Lh.mean()), 4),
-                               "alg_GBps": round(alg / (ms / 1e3) / 1e9, 1),
-                               "frac": round(alg / (ms / 1e3) / 1e9 / hbm, 4)})
-            del logits, draft, full_draft
-            torch.cuda.empty_cache()
-    head = max(points, key=lambda p: p["frac"])
-    line = {"metric": METRIC, "value": head["seq_steps_per_s"], "unit": "seq-steps/s", "n_gpus": ws,
-            "steps": reps, "warmup": args.warmup, "ms_per_step": head["us"] / 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": {"workload": "sweep_b1024", "B": B, "V": V},
-            "roofline": {"bound": "hbm", "achieved": head["alg_GBps"], "peak": hbm, "unit": "GB/s",
-                         "frac": head["frac"], "traffic": None, "peak_source": peak_kind},
-            "points": points}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-
-
-# --------------------------------------------------------------------------
 # reference arm: the oracle
 # --------------------------------------------------------------------------
 
+REF_SEQS = 16
+
+
 def run_reference(args):
-    """The oracle arm: one step = one sequence's decode step (extend + draft +
-    fp64 verification) of the same workload, single-threaded on the host."""
+    """The oracle arm on the default line's workload: one step = the oracle's
+    fp64 verification of 16 sequences of B=1024, K=3, bf16, T=1 inputs (same
+    distributions, drawn on the host), single-threaded."""
+    import oracle
     ws, rank, local = _dist()
     if rank != 0:
         return
-    hist, cont = rs_inputs(0)
-    nseq = 8
-    loop = OracleLoop(hist, cont, nseq)
+    rows, drafts = workloads.sweep_host_bf16(HEAD_SEED, REF_SEQS, HEAD_K)
+    si = np.arange(REF_SEQS)
     for s in range(max(args.warmup, 0)):
-        loop.seq_step(s % nseq, s // nseq)
+        oracle.verify(rows, drafts, None, temperature=HEAD_T, seed=HEAD_COIN_SEED, step=s, seq_index=si)
     t0 = time.perf_counter()
     for s in range(args.steps):
-        loop.seq_step(s % nseq, 1000 + s // nseq)
+        oracle.verify(rows, drafts, None, temperature=HEAD_T, seed=HEAD_COIN_SEED, step=1000 + s, seq_index=si)
     el = time.perf_counter() - t0
-    v = args.steps / el if el > 0 else 0.0
+    v = REF_SEQS * args.steps / el if el > 0 else 0.0
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": "seq-steps/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(1e3 / v, 3) if v else None, "higher_is_better": True,
+            "ms_per_step": round(el / max(args.steps, 1) * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "rs_bf16_b64", "B_per_gpu": 64, "V": workloads.V_LARGE, "K": 3,
-                       "temperature": 1.0, "history": 4096},
+            "config": head_config(1),
             "cpu_baseline": {"value": round(v, 2), "unit": "seq-steps/s", "cores": 1, "kind": "oracle",
-                             "sample": f"each step: one sequence's decode step, {nseq} sequences in turn"},
+                             "nproc": _nproc(),
+                             "sample": f"each step: fp64 verification of {REF_SEQS} sequences of the "
+                                       f"workload (host-drawn, same distributions), one thread"},
             "e2e": {"value": round(v, 2), "unit": "seq-steps/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
+def run_gpu(args):
+    import torch
+
+    import sam_drafting_verification_gb300  # noqa: F401  (fails loudly without the library)
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    run = {"verify_b1024": run_verify_b1024, "rs_bf16_b64": run_rs, "sweep_b1024": run_sweep,
+           "long_rollout_b256": run_rollout, "draft_model_b32": run_draft_model,
+           "rollout_toy_b64": run_rollout_toy, "static_match_b256": run_static_match,
+           "tree_b256": run_tree, "sampling_b256": run_sampling}[args.workload]
+    run(args, ws, rank, dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+WORKLOADS = ["verify_b1024", "rs_bf16_b64", "sweep_b1024", "long_rollout_b256", "draft_model_b32",
+             "rollout_toy_b64", "static_match_b256", "tree_b256", "sampling_b256"]
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="rs_bf16_b64", choices=["rs_bf16_b64", "sweep_b1024", "long_rollout_b256",
-                                                      "rollout_toy_b64", "static_match_b256", "tree_b256",
-                                                      "sampling_b256"])
+    ap.add_argument("--workload", default="verify_b1024", choices=WORKLOADS)
     ap.add_argument("--point", default="", help="sweep_b1024 only: one point 'K,f32|bf16,greedy|T=1|greedy-full-read'")
+    ap.add_argument("--pool", type=int, default=HEAD_POOL,
+                    help="verify_b1024 only: logits tensors the steps rotate through")
+    ap.add_argument("--no-breakdown", action="store_true",
+                    help="verify_b1024 only: the default line without the other configurations")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":
         args.warmup = 3

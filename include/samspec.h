@@ -276,12 +276,17 @@ int spec_verify(const void* d_target, int32_t target_dtype, const void* d_draft_
  * Same arguments, outputs and limits as spec_verify, without the workspace:
  * its scratch (the kernel's work counters) is a fixed 256-byte array inside
  * the library, present on every device that loads it until the process
- * exits.  Sizes whose workspace would not fit it return SAMSPEC_ESIZE.  The
- * call allocates nothing: it clears the array with cudaMemsetAsync on
- * `stream` and launches the same kernel as spec_verify.
+ * exits.  Every size spec_verify takes fits that array, so the limits are
+ * spec_verify's (1 <= B <= 2^24, 0 <= K <= 32, V within the tile limits
+ * above); anything beyond them returns SAMSPEC_ESIZE, and every argument
+ * error is returned before anything is enqueued.  The call allocates
+ * nothing: it clears the array with cudaMemsetAsync on `stream` and launches
+ * the same kernel as spec_verify.
  *   - The first call on a device looks the array's device address up (with
  *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     stream capture.  After cudaDeviceReset of a device the cached address
+ *     is stale: do not call this entry point on that device again in the
+ *     same process.
  *   - All calls on a device share the one array: two calls whose kernels
  *     overlap on the GPU (different streams, no ordering between them) race
  *     on it and give wrong results.  Serialise them, or use spec_verify with

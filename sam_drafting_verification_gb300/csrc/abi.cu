@@ -21,6 +21,7 @@ const char* samspec_strerror(int code) {
     case SAMSPEC_ST_BADROW: return "sequence: logits row with NaN, +inf or all -inf";
     case SAMSPEC_ST_BADDRAFT: return "sequence: draft length, draft token or n_new out of range";
     case SAMSPEC_ST_TIMEOUT: return "sequence: a bounded on-chip wait ran out";
+    case SAMSPEC_ST_BADPARAM: return "sequence: temperature not > 0 and finite, or top_p not > 0";
     default: return "unknown code";
   }
 }

@@ -68,6 +68,7 @@ constexpr int kMinStages = 3;
 constexpr int kMaxChunks = 48;
 constexpr int kMaxChunksDraft = 32;  // with draft logits: both arrays' records must fit
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
+constexpr size_t kVerifyWorkspaceBytes = 256;  // work counters: claims, exits, error bits
 
 enum Kind : int32_t { kStats = 0, kResid = 1, kExit = 3 };
 enum State : int32_t { kEmpty = 0, kReady = 1, kIssued = 2 };
@@ -1798,7 +1799,10 @@ namespace {
 
 // Device address of noalloc_scratch on the current device.  On the host the
 // array's name only stands in for the symbol, so the address is looked up
-// once per device (with that device current) and cached.
+// once per device (with that device current) and cached for the life of the
+// process.  cudaDeviceReset destroys the context that address belongs to:
+// after a reset of a device, this entry point must not be called on it again
+// in the same process.
 int noalloc_scratch_address(void** out) {
   constexpr int kMaxDev = 64;
   static std::mutex mu;
@@ -1815,31 +1819,25 @@ int noalloc_scratch_address(void** out) {
   return SAMSPEC_OK;
 }
 
-}  // namespace
 
-extern "C" {
-
-size_t spec_verify_workspace_bytes(int32_t B, int32_t K, int32_t V) {
-  if (B < 1 || K < 0 || V < 1) return 0;
-  return 256;
+// Logits per staging tile of the kernel instantiated for (target, draft)
+// element types (draft -1: one-hot drafts or greedy).
+int tile_elems(int tdt, int ddt) {
+  if (ddt < 0) return tdt == SAMSPEC_F32 ? Cfg<0, -1>::E_TILE : Cfg<1, -1>::E_TILE;
+  if (tdt == SAMSPEC_F32) return ddt == SAMSPEC_F32 ? Cfg<0, 0>::E_TILE : Cfg<0, 1>::E_TILE;
+  return ddt == SAMSPEC_F32 ? Cfg<1, 0>::E_TILE : Cfg<1, 1>::E_TILE;
 }
 
-int spec_verify_workspace_init(void* d_workspace, size_t ws_bytes, samspec_stream_t stream) {
-  if (!d_workspace || ws_bytes < 256) return SAMSPEC_EINVAL;
-  return cudaMemsetAsync(d_workspace, 0, 256, reinterpret_cast<cudaStream_t>(stream)) ==
-                 cudaSuccess
-             ? SAMSPEC_OK
-             : SAMSPEC_ECUDA;
-}
-
-int spec_verify(const void* d_target, int32_t target_dtype, const void* d_draft_logits,
-                int32_t draft_dtype, const int32_t* d_draft, const int32_t* d_draft_len,
-                int32_t B, int32_t K, int32_t V, float temperature, uint64_t seed, uint64_t step,
-                int32_t* d_accept_len, int32_t* d_out_token, int32_t* d_emit, int32_t* d_emit_len,
-                int32_t* d_status, const spec_verify_debug* dbg, void* d_workspace,
-                size_t ws_bytes, samspec_stream_t stream) {
-  if (!d_target || (K > 0 && !d_draft) || !d_accept_len || !d_out_token || !d_workspace)
-    return SAMSPEC_EINVAL;
+// spec_verify's host-side argument checks and kernel parameters, without the
+// workspace.  Enqueues nothing; every size the kernel cannot take is refused
+// here, so a caller may check before touching device memory.
+int verify_params(const void* d_target, int32_t target_dtype, const void* d_draft_logits,
+                  int32_t draft_dtype, const int32_t* d_draft, const int32_t* d_draft_len,
+                  int32_t B, int32_t K, int32_t V, float temperature, uint64_t seed, uint64_t step,
+                  int32_t* d_accept_len, int32_t* d_out_token, int32_t* d_emit,
+                  int32_t* d_emit_len, int32_t* d_status, const spec_verify_debug* dbg,
+                  VParams* out, int* ddt_out) {
+  if (!d_target || (K > 0 && !d_draft) || !d_accept_len || !d_out_token) return SAMSPEC_EINVAL;
   if (B < 1 || B > (1 << 24) || K < 0 || K > 32 || V < 1 || V > (1 << 24)) return SAMSPEC_ESIZE;
   if (!(temperature >= 0.f) || temperature != temperature || temperature == __builtin_inff())
     return SAMSPEC_EINVAL;
@@ -1850,13 +1848,13 @@ int spec_verify(const void* d_target, int32_t target_dtype, const void* d_draft_
     if (draft_dtype != SAMSPEC_F32 && draft_dtype != SAMSPEC_BF16) return SAMSPEC_EDTYPE;
     ddt = draft_dtype;
   }
-  if (ws_bytes < spec_verify_workspace_bytes(B, K, V)) return SAMSPEC_ESIZE;
-  if (reinterpret_cast<uintptr_t>(d_workspace) % 256 != 0) return SAMSPEC_EALIGN;
+  const int64_t nc = ((int64_t)V + tile_elems(target_dtype, ddt) - 1) / tile_elems(target_dtype, ddt);
+  if (nc > (ddt >= 0 ? kMaxChunksDraft : kMaxChunks)) return SAMSPEC_ESIZE;
   const int st = target_dtype == SAMSPEC_F32 ? 4 : 2;
   const int sd = ddt < 0 ? 0 : (ddt == SAMSPEC_F32 ? 4 : 2);
   if (reinterpret_cast<uintptr_t>(d_target) % 16 != 0) return SAMSPEC_EALIGN;
   if (ddt >= 0 && reinterpret_cast<uintptr_t>(d_draft_logits) % 16 != 0) return SAMSPEC_EALIGN;
-  VParams P;
+  VParams& P = *out;
   std::memset(&P, 0, sizeof(P));
   P.target = static_cast<const unsigned char*>(d_target);
   P.draftl = static_cast<const unsigned char*>(d_draft_logits);
@@ -1878,11 +1876,47 @@ int spec_verify(const void* d_target, int32_t target_dtype, const void* d_draft_
   P.emit_len = d_emit_len;
   P.status = d_status;
   if (dbg) P.dbg = *dbg;
-  P.ws = static_cast<uint32_t*>(d_workspace);
   P.direct = ((size_t)V * st) % 16 != 0 || (sd && ((size_t)V * sd) % 16 != 0);
+  *ddt_out = ddt;
+  return SAMSPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_verify_workspace_bytes(int32_t B, int32_t K, int32_t V) {
+  if (B < 1 || K < 0 || V < 1) return 0;
+  return kVerifyWorkspaceBytes;
+}
+
+int spec_verify_workspace_init(void* d_workspace, size_t ws_bytes, samspec_stream_t stream) {
+  if (!d_workspace || ws_bytes < kVerifyWorkspaceBytes) return SAMSPEC_EINVAL;
+  return cudaMemsetAsync(d_workspace, 0, kVerifyWorkspaceBytes,
+                         reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? SAMSPEC_OK
+             : SAMSPEC_ECUDA;
+}
+
+int spec_verify(const void* d_target, int32_t target_dtype, const void* d_draft_logits,
+                int32_t draft_dtype, const int32_t* d_draft, const int32_t* d_draft_len,
+                int32_t B, int32_t K, int32_t V, float temperature, uint64_t seed, uint64_t step,
+                int32_t* d_accept_len, int32_t* d_out_token, int32_t* d_emit, int32_t* d_emit_len,
+                int32_t* d_status, const spec_verify_debug* dbg, void* d_workspace,
+                size_t ws_bytes, samspec_stream_t stream) {
+  VParams P;
+  int ddt = -1;
+  const int rc = verify_params(d_target, target_dtype, d_draft_logits, draft_dtype, d_draft,
+                               d_draft_len, B, K, V, temperature, seed, step, d_accept_len,
+                               d_out_token, d_emit, d_emit_len, d_status, dbg, &P, &ddt);
+  if (rc != SAMSPEC_OK) return rc;
+  if (!d_workspace) return SAMSPEC_EINVAL;
+  if (ws_bytes < spec_verify_workspace_bytes(B, K, V)) return SAMSPEC_ESIZE;
+  if (reinterpret_cast<uintptr_t>(d_workspace) % 256 != 0) return SAMSPEC_EALIGN;
+  P.ws = static_cast<uint32_t*>(d_workspace);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return greedy ? dispatch<true>(P, target_dtype, ddt, s)
-                : dispatch<false>(P, target_dtype, ddt, s);
+  return P.T == 0.f ? dispatch<true>(P, target_dtype, ddt, s) : dispatch<false>(P, target_dtype, ddt, s);
 }
 
 size_t spec_verify_sampling_workspace_bytes(int32_t B, int32_t K, int32_t V) {
@@ -2010,19 +2044,23 @@ int spec_verify_noalloc(const void* d_target, int32_t target_dtype, const void* 
                         uint64_t step, int32_t* d_accept_len, int32_t* d_out_token,
                         int32_t* d_emit, int32_t* d_emit_len, int32_t* d_status,
                         const spec_verify_debug* dbg, samspec_stream_t stream) {
-  const size_t need = spec_verify_workspace_bytes(B, K, V);
-  if (need > kNoAllocScratchBytes) return SAMSPEC_ESIZE;
-  void* ws = nullptr;
-  const int rc = noalloc_scratch_address(&ws);
+  static_assert(kVerifyWorkspaceBytes <= kNoAllocScratchBytes, "the counters fit the scratch");
+  // every argument and size is checked before anything is enqueued
+  VParams P;
+  int ddt = -1;
+  int rc = verify_params(d_target, target_dtype, d_draft_logits, draft_dtype, d_draft, d_draft_len,
+                         B, K, V, temperature, seed, step, d_accept_len, d_out_token, d_emit,
+                         d_emit_len, d_status, dbg, &P, &ddt);
   if (rc != SAMSPEC_OK) return rc;
+  void* ws = nullptr;
+  rc = noalloc_scratch_address(&ws);
+  if (rc != SAMSPEC_OK) return rc;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the counters must start at zero; the array keeps whatever the last call
   // on this device left there
-  if (need > 0 &&
-      cudaMemsetAsync(ws, 0, need, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return SAMSPEC_ECUDA;
-  return spec_verify(d_target, target_dtype, d_draft_logits, draft_dtype, d_draft, d_draft_len, B,
-                     K, V, temperature, seed, step, d_accept_len, d_out_token, d_emit, d_emit_len,
-                     d_status, dbg, ws, kNoAllocScratchBytes, stream);
+  if (cudaMemsetAsync(ws, 0, kVerifyWorkspaceBytes, s) != cudaSuccess) return SAMSPEC_ECUDA;
+  P.ws = static_cast<uint32_t*>(ws);
+  return P.T == 0.f ? dispatch<true>(P, target_dtype, ddt, s) : dispatch<false>(P, target_dtype, ddt, s);
 }
 
 }  // extern "C"

@@ -67,22 +67,31 @@ class Rollout:
         zero = torch.zeros(len(active), dtype=torch.int32, device=dev)
         # the first drafts: an empty extension that drafts k tokens
         draft, dlen, _, _ = self.batch.step_rows(rows, empty, zero, k)
+        # one workspace for the whole rollout, and one buffer for the per-step
+        # outputs the host reads (emit, emit_len, status, accept_len), so that
+        # a step costs one device-to-host copy
+        ws = verify_workspace(len(active), self.K, 1, dev)
+        hostbuf = torch.empty(len(active) * (self.K + 4), dtype=torch.int32, device=dev)
         step = 0
         while active:
             n = len(active)
             n_done = torch.tensor([len(out[b]) for b in active], dtype=torch.int64, device=dev)
             logits = self.model(rows, n_done, draft, dlen)
             k_next = speculation_k(n, self.threshold, self.K)
-            ws = verify_workspace(n, draft.shape[1], logits.shape[2], dev)
+            K1 = int(draft.shape[1]) + 1
+            o = {"emit": hostbuf[:n * K1].view(n, K1), "emit_len": hostbuf[n * K1:n * K1 + n],
+                 "status": hostbuf[n * K1 + n:n * K1 + 2 * n],
+                 "accept_len": hostbuf[n * K1 + 2 * n:n * K1 + 3 * n]}
             r = self.batch.spec_step(logits, draft, dlen, K_next=k_next, rows=rows,
                                      temperature=self.temperature, seed=self.seed, step=step,
-                                     workspace=ws)
+                                     workspace=ws, out=o)
             res.k_per_step.append(int(draft.shape[1]))
             res.active_per_step.append(n)
-            emit = r["emit"].cpu().tolist()
-            elen = r["emit_len"].cpu().tolist()
-            st = r["status"].cpu().tolist()
-            acc = r["accept_len"].cpu().tolist()
+            h = hostbuf[:n * K1 + 3 * n].cpu()
+            emit = h[:n * K1].view(n, K1).tolist()
+            elen = h[n * K1:n * K1 + n].tolist()
+            st = h[n * K1 + n:n * K1 + 2 * n].tolist()
+            acc = h[n * K1 + 2 * n:n * K1 + 3 * n].tolist()
             keep = []
             for i, b in enumerate(active):
                 if st[i] != 0:

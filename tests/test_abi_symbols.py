@@ -95,3 +95,21 @@ def test_sampling_entry_points_reject_bad_arguments_on_the_host():
     assert ver(K=33) == bd.ESIZE and ver(ws_bytes=256) == bd.ESIZE
     assert ver(V=48 * 24576 + 1) == bd.ESIZE and ver(dtype=bd.F32, V=48 * 12288 + 1) == bd.ESIZE
     assert ver(dtype=5) == bd.EDTYPE
+
+
+def test_strerror_names_every_code_the_header_defines():
+    """Every return code and status word in include/samspec.h has its own text."""
+    import sam_drafting_verification_gb300._binding as bd
+    lib = bd.lib()
+    src = open(os.path.join(ROOT, "include", "samspec.h")).read()
+    codes = {m[0]: int(m[1]) for m in
+             re.findall(r"#define\s+(SAMSPEC_(?:OK|E[A-Z]+|ST_[A-Z]+))\s+\(?(-?\d+)\)?", src)}
+    assert {"SAMSPEC_OK", "SAMSPEC_EINVAL", "SAMSPEC_ST_TIMEOUT", "SAMSPEC_ST_BADPARAM"} <= set(codes)
+    texts = {}
+    for name, v in codes.items():
+        t = lib.samspec_strerror(v)
+        assert t != b"unknown code", name
+        texts.setdefault(v, t)
+    # return codes and status words share only 0 (ok)
+    assert len(set(texts.values())) == len(texts)
+    assert lib.samspec_strerror(12345) == b"unknown code"

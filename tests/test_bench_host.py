@@ -1,7 +1,7 @@
 """Host logic of bench.py that needs no GPU: the DRAM-traffic tables that
-feed the roofline's `traffic` field are well formed, point at committed ncu
-summaries, and are used only while the kernel source still hashes to the
-one the counters were taken on."""
+feed the roofline's `traffic` field are well formed and used only while the
+kernel source still hashes to the one the counters were taken on; the
+oracle's thread-rate helper counts the work of every thread."""
 import hashlib
 import os
 import re
@@ -21,7 +21,7 @@ def test_traffic_tables_are_well_formed():
     seen = 0
     for _, source, workload, entry in _entries():
         assert entry["bytes"] > 0, workload
-        assert os.path.isfile(os.path.join(ROOT, entry["profile"])), entry["profile"]
+        assert set(entry) == {"bytes", source.replace(".", "_") + "_sha256"}, workload
         assert re.fullmatch(r"[0-9a-f]{64}", entry[source.replace(".", "_") + "_sha256"]), workload
         seen += 1
     assert seen >= 4
@@ -39,3 +39,22 @@ def test_traffic_only_for_the_captured_source():
         assert bench._traffic(other, workload, source) is None
         assert bench._traffic(table, "no_such_workload", source) is None
 
+
+
+def test_thread_rate_counts_every_thread():
+    calls = []
+
+    def work(t, i):
+        calls.append((t, i))
+        return 3
+
+    rate, units, wall = bench._threads_rate(work, 4, 0.2)
+    assert units == 3 * len(calls) and wall >= 0.2 and rate > 0
+    assert {t for t, _ in calls} == {0, 1, 2, 3}
+    assert bench._nproc() >= 1
+
+
+def test_default_workload_is_the_b1024_verify_point():
+    cfg = bench.head_config(1)
+    assert cfg["workload"] == bench.HEAD_WORKLOAD
+    assert (cfg["B_per_gpu"], cfg["K"], cfg["temperature"]) == (1024, 3, 1.0)

@@ -177,3 +177,28 @@ def sweep_device(seed: int, B: int, K: int, V: int, dtype, device):
     pick = torch.randint(0, 5, (B, K, 1), device=device, generator=g)
     drafts = torch.gather(top, -1, pick)[..., 0].to(torch.int32).contiguous()
     return logits.contiguous(), drafts
+
+
+def draft_model_device(seed: int, B: int, K: int, V: int, T: float, device, noise_sd: float = 1.0):
+    """The draft-model workload drawn on `device` from a seeded torch
+    generator (the same distributions as draft_model): target N(0, sd 2)
+    [B, K+1, V] fp32, draft logits = target[:, :K] + N(0, noise_sd), draft
+    tokens sampled from softmax(draft / T) by the Gumbel-max trick."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    target = torch.empty((B, K + 1, V), dtype=torch.float32, device=device).normal_(0.0, 2.0, generator=g)
+    noise = torch.empty((B, K, V), dtype=torch.float32, device=device).normal_(0.0, noise_sd, generator=g)
+    draftl = (target[:, :K] + noise).contiguous()
+    u = torch.rand((B, K, V), dtype=torch.float64, device=device, generator=g).clamp_min(1e-300)
+    drafts = torch.argmax(draftl.double() / T - torch.log(-torch.log(u)), dim=-1).to(torch.int32)
+    return target.contiguous(), draftl, drafts.contiguous()
+
+
+def sweep_host_bf16(seed: int, B: int, K: int, V: int = V_LARGE):
+    """Host sweep inputs rounded to bf16 (returned as the exact fp32 values),
+    drafts uniform among each rounded row's top-5."""
+    rng = np.random.default_rng(seed)
+    logits = to_bf16(gaussian_logits(rng, (B, K + 1, V), 2.0)).float().numpy()
+    drafts = topk_drafts(logits[:, :K], 5, rng)
+    return logits, drafts
