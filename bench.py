@@ -497,7 +497,7 @@ class OracleLoop:
         for p in range(npool):
             x = workloads.gaussian_logits(rng, (b1 - b0, K + 1, V), 2.0)
             workloads.boost_truth(x, cont[b0:b1, p * (K + 1):(p + 1) * (K + 1)], 4.0)
-            self.rows.append(workloads.to_bf16(x).float().numpy())
+            self.rows.append(workloads.round_bf16(x))
         self.sams = [oracle.Sam(V) for _ in range(b1 - b0)]
         for i in range(b1 - b0):
             self.sams[i].extend(hist[b0 + i])
@@ -515,9 +515,27 @@ class OracleLoop:
         self.emit[i] = list(d[0, :L]) + [int(r["out_token"][0])]
 
 
+def _step_worker(hist, cont, b0, b1, seconds, gate, q):
+    """One host core's share of the oracle's B=64 decode steps (spawned
+    process): builds its automata, waits at the gate, then steps its
+    sequences until `seconds` have passed."""
+    loop = OracleLoop(hist, cont, b0, b1)
+    gate.wait()
+    t_end = time.perf_counter() + seconds
+    n, i = 0, 0
+    while time.perf_counter() < t_end:
+        for b in range(b1 - b0):
+            loop.seq_step(b, i)
+        n += b1 - b0
+        i += 1
+    q.put(n)
+
+
 def oracle_step_rate(hist, cont, one_core_s, all_core_s):
     """Decode steps of the oracle on the B=64 workload: one thread over 16
-    sequences, then every host core, each thread with its own sequences."""
+    sequences, then one spawned process per host core, each with its own
+    sequences."""
+    import multiprocessing as mp
     nc = _nproc()
     one = OracleLoop(hist, cont, 0, 16)
 
@@ -528,18 +546,24 @@ def oracle_step_rate(hist, cont, one_core_s, all_core_s):
 
     r1, u1, el1 = _threads_rate(w1, 1, one_core_s)
     per = max(1, hist.shape[0] // nc)
-    loops = [OracleLoop(hist, cont, (t * per) % hist.shape[0], (t * per) % hist.shape[0] + per)
-             for t in range(nc)]
-
-    def wn(t, i):
-        for b in range(per):
-            loops[t].seq_step(b, i)
-        return per
-
-    rn, un, eln = _threads_rate(wn, nc, all_core_s)
+    ctx = mp.get_context("spawn")
+    gate = ctx.Barrier(nc + 1)
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_step_worker,
+                         args=(hist, cont, (t * per) % hist.shape[0], (t * per) % hist.shape[0] + per,
+                               all_core_s, gate, q)) for t in range(nc)]
+    for pr in procs:
+        pr.start()
+    gate.wait()
+    t0 = time.perf_counter()
+    un = sum(q.get(timeout=600) for _ in procs)
+    eln = time.perf_counter() - t0
+    for pr in procs:
+        pr.join(timeout=60)
+    rn = un / max(eln, all_core_s)
     return {"one_core": round(r1, 2), "all_cores": round(rn, 2), "nproc": nc,
             "ideal_all_cores": round(r1 * nc, 2),
-            "sample": f"one thread: 16 sequences, {u1} seq-steps in {el1:.2f} s; {nc} threads x "
+            "sample": f"one thread: 16 sequences, {u1} seq-steps in {el1:.2f} s; {nc} processes x "
                       f"{per} sequences, {un} seq-steps in {eln:.2f} s (extend + draft + fp64 verify)"}
 
 
@@ -679,62 +703,76 @@ def _rollout_inputs(rank):
     return w, pre, toks
 
 
-def oracle_rollout_rates(streams, lens, toks, n_new, K, one_core_seqs=16):
+def _rollout_worker(hists, toks, n_new, K, gate, q):
+    """One host core's share of the oracle's rollout (spawned process):
+    builds its automata over `hists` between two gates, then runs every step
+    of extend + draft between the next two."""
+    import oracle
+    V = workloads.V_LARGE
+    sams = [oracle.Sam(V) for _ in hists]
+    toks = np.ascontiguousarray(toks)
+    n_new = np.ascontiguousarray(n_new)
+    gate.wait()
+    t0 = time.perf_counter()
+    for i, h in enumerate(hists):
+        sams[i].extend(h)
+    t1 = time.perf_counter()
+    gate.wait()
+    t2 = time.perf_counter()
+    for s in range(toks.shape[0]):
+        oracle.step_batch(sams, toks[s], n_new[s], K)
+    t3 = time.perf_counter()
+    gate.wait()
+    q.put((t1 - t0, t3 - t2))
+
+
+def oracle_rollout_rates(streams, lens, toks, n_new, K, one_core_seqs=32):
     """The oracle's automata on samples of the rollout: the prefill build
     (tokens/s) and 512 steps of extend + draft (ns per sequence-step), on
-    one thread over `one_core_seqs` sequences, then on every host core with
-    the same number of sequences per thread."""
+    one thread over `one_core_seqs` sequences, then on every host core (one
+    spawned process each, with as many sequences)."""
+    import multiprocessing as mp
+
     import oracle
     V = workloads.V_LARGE
     nc = _nproc()
     steps = toks.shape[0]
-
-    def build_and_step(seqs):
-        sams = [oracle.Sam(V) for _ in seqs]
-        t0 = time.perf_counter()
-        for i, b in enumerate(seqs):
-            sams[i].extend(streams[b][:lens[b]])
-        t1 = time.perf_counter()
-        for s in range(steps):
-            oracle.step_batch(sams, toks[s, seqs], n_new[s, seqs], K)
-        t2 = time.perf_counter()
-        return t1 - t0, t2 - t1
-
-    seqs1 = list(range(one_core_seqs))
-    b1, s1 = build_and_step(seqs1)
-    tok1 = int(sum(int(lens[b]) for b in seqs1))
-    per = one_core_seqs
     B = len(lens)
+    per = one_core_seqs
+    seqs1 = list(range(per))
+    sams = [oracle.Sam(V) for _ in seqs1]
+    t0 = time.perf_counter()
+    for i, b in enumerate(seqs1):
+        sams[i].extend(streams[b][:lens[b]])
+    b1 = time.perf_counter() - t0
+    tk1 = np.ascontiguousarray(toks[:, seqs1])
+    nn1 = np.ascontiguousarray(n_new[:, seqs1])
+    t0 = time.perf_counter()
+    for s in range(steps):
+        oracle.step_batch(sams, tk1[s], nn1[s], K)
+    s1 = time.perf_counter() - t0
+    tok1 = int(sum(int(lens[b]) for b in seqs1))
+    del sams
     groups = [[(t * per + i) % B for i in range(per)] for t in range(nc)]
-    res = [None] * nc
-    gate = threading.Barrier(nc)
-    walls = {}
-
-    def run(t):
-        import oracle as o
-        sams = [o.Sam(V) for _ in groups[t]]
-        gate.wait()
-        if t == 0:
-            walls["b0"] = time.perf_counter()
-        for i, b in enumerate(groups[t]):
-            sams[i].extend(streams[b][:lens[b]])
-        gate.wait()
-        if t == 0:
-            walls["b1"] = time.perf_counter()
-        for s in range(steps):
-            o.step_batch(sams, toks[s, groups[t]], n_new[s, groups[t]], K)
-        gate.wait()
-        if t == 0:
-            walls["s1"] = time.perf_counter()
-        res[t] = True
-
-    ths = [threading.Thread(target=run, args=(t,)) for t in range(nc)]
-    for th in ths:
-        th.start()
-    for th in ths:
-        th.join()
+    ctx = mp.get_context("spawn")
+    gate = ctx.Barrier(nc + 1)
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rollout_worker,
+                         args=([streams[b][:lens[b]] for b in g], toks[:, g], n_new[:, g], K, gate, q))
+             for g in groups]
+    for pr in procs:
+        pr.start()
+    gate.wait()
+    w0 = time.perf_counter()
+    gate.wait()
+    w1 = time.perf_counter()
+    gate.wait()
+    w2 = time.perf_counter()
+    per_proc = [q.get(timeout=600) for _ in procs]
+    for pr in procs:
+        pr.join(timeout=60)
+    bn, sn = w1 - w0, w2 - w1
     tokn = int(sum(int(lens[b]) for g in groups for b in g))
-    bn, sn = walls["b1"] - walls["b0"], walls["s1"] - walls["b1"]
     return {"nproc": nc,
             "prefill_tokens_per_s": {"one_core": round(tok1 / b1, 1), "all_cores": round(tokn / bn, 1),
                                      "ideal_all_cores": round(tok1 / b1 * nc, 1)},
@@ -742,8 +780,9 @@ def oracle_rollout_rates(streams, lens, toks, n_new, K, one_core_seqs=16):
                                 "all_cores": round(sn / (steps * per * nc) * 1e9, 1),
                                 "ideal_all_cores": round(s1 / (steps * per) * 1e9 / nc, 1)},
             "sample": f"one thread: {per} sequences ({tok1} history tokens, build {b1:.2f} s, "
-                      f"{steps} steps {s1:.2f} s); {nc} threads x {per} sequences ({tokn} tokens, "
-                      f"build {bn:.2f} s, steps {sn:.2f} s)"}
+                      f"{steps} steps {s1:.3f} s); {nc} processes x {per} sequences ({tokn} tokens, "
+                      f"build {bn:.2f} s, steps {sn:.3f} s; slowest process build "
+                      f"{max(x[0] for x in per_proc):.2f} s, steps {max(x[1] for x in per_proc):.3f} s)"}
 
 
 def measure_rollout(dev, ws, rank, cpu=True, min_ms=400.0):

@@ -400,6 +400,21 @@ int sam_spec_step(sam_batch* batch, const int32_t* d_rows, int32_t n, const void
                   int32_t* d_match_len, int32_t* d_min_endpos, void* d_workspace,
                   size_t ws_bytes, samspec_stream_t stream);
 
+/* Test hook of the verification kernels' bounded waits.  Every on-chip wait of
+ * spec_verify, spec_verify_noalloc, spec_verify_tree, spec_verify_sampling and
+ * sam_spec_step's verification (a staging buffer to fill or to free, the
+ * records of a tile, an idle sequence slot) gives up after `ns` nanoseconds of
+ * global time instead of the default 2 s; ns = 0 restores the default.  A
+ * kernel whose wait runs out marks every sequence it has not finished with
+ * ST_TIMEOUT (accept_len and out_token -1, emit_len 0), waits for its own
+ * copies in flight to land (up to 2 s, a limit this hook does not shorten)
+ * and returns; sequences it finished keep their results, and the context and
+ * the workspace stay usable.  Process-wide; applies to launches made after
+ * the call (a launch captured in a CUDA graph keeps the value in force at its
+ * capture).  Returns the previous limit.  Meant for tests of the timeout
+ * path: production code never needs it. */
+uint64_t samspec_set_wait_limit_ns(uint64_t ns);
+
 /* Philox4x32-10 uniforms exactly as spec_verify draws them, for inspection:
  * d_u[2 * (b * (K+1) + j) + {0,1}] = (u_j, u'_j) of sequence b, for
  * 0 <= b < B and 0 <= j <= K ([B, K+1, 2] fp32, device).  Asynchronous. */

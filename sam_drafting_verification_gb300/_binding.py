@@ -26,7 +26,7 @@ EXPORTED = [
     "spec_verify_workspace_bytes", "spec_verify_workspace_init", "spec_verify", "spec_uniforms",
     "spec_verify_noalloc", "sam_step_rows", "sam_spec_step", "ssam_match", "sam_select_drafts",
     "spec_verify_tree", "spec_sampling_cut", "spec_verify_sampling_workspace_bytes",
-    "spec_verify_sampling",
+    "spec_verify_sampling", "samspec_set_wait_limit_ns",
 ]
 
 
@@ -64,6 +64,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "spec_verify": (ctypes.c_int, [P, I32, P, I32, P, P, I32, I32, I32, F, U64, U64,
                                        P, P, P, P, P, ctypes.POINTER(VerifyDebug), P, SZ, P]),
         "spec_uniforms": (ctypes.c_int, [I32, I32, U64, U64, P, P]),
+        "samspec_set_wait_limit_ns": (U64, [U64]),
         "spec_verify_noalloc": (ctypes.c_int, [P, I32, P, I32, P, P, I32, I32, I32, F, U64, U64,
                                                P, P, P, P, P, ctypes.POINTER(VerifyDebug), P]),
         "sam_step_rows": (ctypes.c_int, [P, P, I32, P, P, I32, I32, P, P, P, P, P]),

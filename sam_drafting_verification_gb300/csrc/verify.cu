@@ -43,6 +43,7 @@
 // deadline; a CTA that runs out of time marks its sequences
 // SAMSPEC_ST_TIMEOUT, lets its copies in flight land and exits.
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -67,7 +68,10 @@ constexpr int kMaxStages = 6;
 constexpr int kMinStages = 3;
 constexpr int kMaxChunks = 48;
 constexpr int kMaxChunksDraft = 32;  // with draft logits: both arrays' records must fit
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait (default)
+constexpr uint64_t kDrainNs = 2000000000ull;  // 2 s for copies in flight to land after an abort
+// the pipeline waits' limit for launches made from now on (test hook)
+std::atomic<uint64_t> g_wait_ns{kWaitNs};
 constexpr size_t kVerifyWorkspaceBytes = 256;  // work counters: claims, exits, error bits
 
 enum Kind : int32_t { kStats = 0, kResid = 1, kExit = 3 };
@@ -91,6 +95,7 @@ struct VParams {
   spec_verify_debug dbg;
   uint32_t* ws;  // [0] claim counter, [1] CTA exit counter, [2] error bits
   int32_t NC, NS;
+  uint64_t wait_ns;  // limit of every pipeline wait
   int32_t direct;  // 1: plain loads instead of bulk copies (unaligned rows)
   // draft trees (K = N - 1, row n scores the token after node n's path)
   const int32_t* ttok;  // [B, N] node tokens (node 0: the verified context)
@@ -155,7 +160,7 @@ struct Smem {
   int32_t pool_left;    // sequences not yet claimed, as of this CTA's last claim
   int32_t claim_lock;   // one control warp claims at a time
   int32_t pool_done;    // a claim found no sequence left: idle slots leave
-  int32_t tile_cnt[kSlots][kMaxChunks];  // consumer warps done with each tile of a job
+  uint64_t tile_bar[kSlots][kMaxChunks];  // one phase per job: the kCW records of a tile
   float4 pre[kSlots][kMaxChunks][2];     // control: mass before each tile {hi, lo, ref, 0}
 };
 
@@ -218,8 +223,13 @@ __device__ __forceinline__ DF df_sub(DF x, DF y) { return df_add(x, df_neg(y)); 
 __device__ __forceinline__ bool df_le(DF x, DF y) {
   return x.hi < y.hi || (x.hi == y.hi && x.lo <= y.lo);
 }
-// x * 2^k, exact while the parts stay normal
-__device__ __forceinline__ DF df_scale(DF x, int k) { return {ldexpf(x.hi, k), ldexpf(x.lo, k)}; }
+// x * 2^k: one multiply by the power of two when 2^k is a normal float,
+// ldexpf otherwise (exact while the result stays normal)
+__device__ __forceinline__ float scale2(float x, int k) {
+  if (k >= -126 && k <= 127) return x * __int_as_float((k + 127) << 23);
+  return ldexpf(x, k);
+}
+__device__ __forceinline__ DF df_scale(DF x, int k) { return {scale2(x.hi, k), scale2(x.lo, k)}; }
 // x * a with the product's rounding error carried (FMA two-product)
 __device__ __forceinline__ DF df_mul_f(DF x, float a) {
   const float p = x.hi * a;
@@ -907,8 +917,9 @@ struct Control {
     float4 r = make_float4(NEG_INF, NEG_INF, 0.f, 0.f);
     if (lane < kCW) r = f ? R(c, lane).b : R(c, lane).a;
     const bool nan = __any_sync(kFullMask, r.x != r.x || r.z != r.z);
-    const float mc = warp_max(r.x);
-    const float Rc = warp_max(r.y);
+    // (a NaN record makes the row bad whatever these maxima are)
+    const float mc = warp_max_nan(r.x);
+    const float Rc = warp_max_nan(r.y);
     DF v = {0.f, 0.f};
     if (Rc != NEG_INF && r.z != 0.f) v = df_scale(DF{r.z, r.w}, (int)(r.y - Rc));
     const DF t = df_warp_sum(v);  // the tile's mass over its 16 slices, units 2^Rc
@@ -922,13 +933,13 @@ struct Control {
     if (Rc != NEG_INF && Rc > R_.ref) {  // a larger reference: rescale what was summed so far
       if (R_.ref != NEG_INF) {
         const int sc = (int)(R_.ref - Rc);
-        R_.sum = DF{ldexpf(R_.sum.hi, sc), ldexpf(R_.sum.lo, sc)};
+        R_.sum = df_scale(R_.sum, sc);
       }
       R_.ref = Rc;
     }
     if (Rc != NEG_INF && (t.hi != 0.f || t.lo != 0.f)) {
       const int sc = (int)(Rc - R_.ref);
-      R_.sum = df_add(R_.sum, DF{ldexpf(t.hi, sc), ldexpf(t.lo, sc)});
+      R_.sum = df_add(R_.sum, df_scale(t, sc));
     }
   }
 
@@ -938,7 +949,7 @@ struct Control {
     if (GREEDY) {
       const float m = lane < kCW ? R(c, lane).a.x : -__int_as_float(0x7f800000);
       gnan_ |= __any_sync(kFullMask, lane < kCW && R(c, lane).a.z != 0.f);
-      const float M = warp_max(m);
+      const float M = warp_max_nan(m);
       if (M > gmax_) {  // tiles arrive in token order: keep the first maximum
         const unsigned h = __ballot_sync(kFullMask, lane < kCW && m == M);
         gmax_ = M;
@@ -1366,10 +1377,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
     sm.pool_left = P.B;
     sm.claim_lock = 0;
     sm.pool_done = 0;
-    for (int s = 0; s < kSlots; ++s)
-      for (int c = 0; c < kMaxChunks; ++c) sm.tile_cnt[s][c] = 0;
     mbar_fence_init();
   }
+  // tile barriers: each consumer warp arrives once per tile of a job
+  if (threadIdx.x < kSlots * kMaxChunks)
+    mbar_init(&sm.tile_bar[threadIdx.x / kMaxChunks][threadIdx.x % kMaxChunks], kCW);
   __syncthreads();
 
   if (warp < kCW) {
@@ -1381,7 +1393,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       if (!mbar_try_wait(&sm.full[cs], cph)) {
         const uint64_t t0 = gtimer();
         while (!mbar_try_wait(&sm.full[cs], cph)) {
-          if (vload(&sm.abort) || gtimer() - t0 > kWaitNs) {
+          if (vload(&sm.abort) || gtimer() - t0 > P.wait_ns) {
             ok = false;
             break;
           }
@@ -1395,15 +1407,26 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       if (tg.kind == kExit) break;
       Slot& S = sm.slot[tg.slot];
       const unsigned char* stage = stages + (size_t)cs * kStageBytes;
+      // a row's last tile is partial: slices past its end hold nothing (their
+      // records are empty), slices wholly inside it take the unmasked path
+      const int wbeg = warp * C::SL;
+      const bool none = wbeg >= tg.nel;
+      const bool full = wbeg + C::SL <= tg.nel;
       Slice<TT, DT> sl;
-      load_slice_tile<TT, DT>(sl, P, stage, tg, warp, lane);
+      if (!none) load_slice_tile<TT, DT>(sl, P, stage, tg, warp, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[cs]);
-      const bool full = tg.nel == C::E_TILE;
       Rec r;
       r.a = make_float4(0.f, 0.f, 0.f, 0.f);
       r.b = r.a;
-      if (tg.kind == kStats) {
+      if (none) {
+        // the records of an all -inf slice; a residual slice holds no mass
+        const float NEG_INF = -__int_as_float(0x7f800000);
+        if (tg.kind == kStats) {
+          r.a = make_float4(NEG_INF, GREEDY ? 0.f : NEG_INF, 0.f, 0.f);
+          r.b = make_float4(NEG_INF, NEG_INF, 0.f, 0.f);
+        }
+      } else if (tg.kind == kStats) {
         if (GREEDY) {
           r.a = full ? reduce_greedy<TT, DT, true>(sl, warp, lane, tg.nel)
                      : reduce_greedy<TT, DT, false>(sl, warp, lane, tg.nel);
@@ -1481,8 +1504,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         const size_t ri = ((size_t)tg.slot * P.NC + tg.chunk) * kCW + warp;
         rec[ri] = r.a;
         if (DT >= 0) rec[(size_t)kSlots * P.NC * kCW + ri] = r.b;
-        __threadfence_block();  // the record (and captured logits) before the count
-        atomicAdd(&sm.tile_cnt[tg.slot][tg.chunk], 1);
+        // release: the record (and the captured logits) before the arrival
+        mbar_arrive(&sm.tile_bar[tg.slot][tg.chunk]);
       }
       __syncwarp();
       if (++cs == NS) {
@@ -1511,7 +1534,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         if (si < 0) {
           vstore(&sm.prod_idle, 1);
           if (vload(&sm.ctrl_exited) == kSlots) break;
-          if (gtimer() - t_idle > kWaitNs) {
+          if (gtimer() - t_idle > P.wait_ns) {
             vstore(&sm.abort, 1);
             break;
           }
@@ -1531,7 +1554,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         for (int c = 0; c < P.NC && ok; ++c) {
           const uint64_t t0 = gtimer();
           while (!mbar_try_wait(&sm.empty[ps], pph ^ 1)) {
-            if (vload(&sm.abort) || gtimer() - t0 > kWaitNs) {
+            if (vload(&sm.abort) || gtimer() - t0 > P.wait_ns) {
               ok = false;
               break;
             }
@@ -1581,7 +1604,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         const uint64_t t0 = gtimer();
         bool ok = true;
         while (!mbar_try_wait(&sm.empty[ps], pph ^ 1)) {
-          if (gtimer() - t0 > kWaitNs) {
+          if (gtimer() - t0 > P.wait_ns) {
             ok = false;
             break;
           }
@@ -1596,12 +1619,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       }
       if (vload(&sm.abort)) {
         atomicOr(&P.ws[2], 1u);
-        // let every bulk copy this CTA issued land before the CTA exits
+        // let every bulk copy this CTA issued land before the CTA exits: a
+        // limit of its own, not shortened with the pipeline waits (a copy
+        // still in flight after it means the memory system has failed)
         for (int s = 0; s < NS; ++s) {
           if (sm.stage_parity[s] < 0) continue;
           const uint64_t t0 = gtimer();
           while (!mbar_try_wait(&sm.full[s], (uint32_t)sm.stage_parity[s]))
-            if (gtimer() - t0 > kWaitNs) break;
+            if (gtimer() - t0 > kDrainNs) break;
         }
       }
     }
@@ -1615,6 +1640,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
     Slot& S = sm.slot[si];
     Control<TT, DT, GREEDY, TREE, SAMP> ctl(P, sm, rec, lane, si);
     int last_jobs = -1;
+    uint32_t tpar = 0;  // phase parity of this slot's tile barriers for its current job
     uint64_t t_idle = gtimer();
     for (;;) {
       if (vload(&sm.abort)) break;
@@ -1663,7 +1689,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
           if (ji != last_jobs) {
             last_jobs = ji;
             t_idle = gtimer();
-          } else if (gtimer() - t_idle > kWaitNs) {
+          } else if (gtimer() - t_idle > P.wait_ns) {
             vstore(&sm.abort, 1);
             timeout = 1;
           }
@@ -1677,23 +1703,21 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       bool ok = true;
       uint64_t t0 = gtimer();
       for (int c = 0; c < P.NC;) {
-        const int cnt = __shfl_sync(kFullMask, vload(&sm.tile_cnt[si][c]), 0);
-        if (cnt == kCW) {
-          __threadfence_block();
+        // every lane waits (acquire: the tile's records are visible after it)
+        if (__all_sync(kFullMask, mbar_try_wait(&sm.tile_bar[si][c], tpar))) {
           ctl.merge_tile(c);
-          if (lane == 0) sm.tile_cnt[si][c] = 0;
           ++c;
           t0 = gtimer();
           continue;
         }
         int stop = 0;
-        if (lane == 0) stop = vload(&sm.abort) || gtimer() - t0 > kWaitNs;
+        if (lane == 0) stop = vload(&sm.abort) || gtimer() - t0 > P.wait_ns;
         if (__shfl_sync(kFullMask, stop, 0)) {
           ok = false;
           break;
         }
-        __nanosleep(64);
       }
+      tpar ^= 1u;  // the next job of this slot completes the next phase
       if (!ok) {
         if (lane == 0) vstore(&sm.abort, 1);
         break;
@@ -1703,8 +1727,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
     }
     if (lane == 0) {
       if (vload(&sm.abort)) {
-        // this slot's sequence, and (slot 0) any nobody will claim now
+        // this slot's sequence, and (slot 0) any nobody will claim now: the
+        // CTA's own first sequence if the abort came before its claim, and
+        // the pool past the first gridDim.x
         if (S.state != kEmpty) write_result(P, S.b, -1, -1, SAMSPEC_ST_TIMEOUT);
+        if (si == 0 && ctl.first_) write_result(P, (int)blockIdx.x, -1, -1, SAMSPEC_ST_TIMEOUT);
         if (si == 0 && gridDim.x < (uint32_t)P.B)
           for (uint32_t b = gridDim.x + atomicAdd(&P.ws[0], 1u); b < (uint32_t)P.B;
                b = gridDim.x + atomicAdd(&P.ws[0], 1u))
@@ -1768,6 +1795,7 @@ int launch(const VParams& P0, cudaStream_t stream) {
   if (ns > kMaxStages) ns = kMaxStages;
   if (ns < kMinStages) return SAMSPEC_ESIZE;
   P.NS = ns;
+  P.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   const size_t smem = head + (size_t)ns * kStageBytes;
   const int grid = P.B < sms[dev] ? P.B : sms[dev];
   verify_kernel<TT, DT, GREEDY, TREE, SAMP><<<grid, kThreads, smem, stream>>>(P);
@@ -2027,6 +2055,10 @@ int spec_verify_tree(const void* d_target, int32_t target_dtype, const int32_t* 
   if (greedy)
     return target_dtype == SAMSPEC_F32 ? launch<0, -1, true, true>(P, s) : launch<1, -1, true, true>(P, s);
   return target_dtype == SAMSPEC_F32 ? launch<0, -1, false, true>(P, s) : launch<1, -1, false, true>(P, s);
+}
+
+uint64_t samspec_set_wait_limit_ns(uint64_t ns) {
+  return g_wait_ns.exchange(ns == 0 ? kWaitNs : ns);
 }
 
 int spec_uniforms(int32_t B, int32_t K, uint64_t seed, uint64_t step, float* d_u,

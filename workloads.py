@@ -88,6 +88,15 @@ def boost_truth(logits: np.ndarray, truth: np.ndarray, amount: float) -> None:
                 logits[b, j, t] += np.float32(amount)
 
 
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """fp32 values rounded to the nearest bf16 (ties to even), returned as
+    fp32; NaN stays NaN.  The numpy twin of to_bf16(x).float()."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    r = ((b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) & np.uint32(0xFFFF0000))
+    r = np.where(np.isnan(x), b | np.uint32(0x00400000), r).astype(np.uint32)
+    return r.view(np.float32)
+
+
 def to_bf16(x: np.ndarray):
     """Round an fp32 array to a torch bfloat16 tensor (round-to-nearest-even)."""
     import torch
