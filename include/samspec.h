@@ -68,6 +68,10 @@ typedef struct CUstream_st* samspec_stream_t;
 #define SAMSPEC_ST_TIMEOUT 7   /* verify: a bounded on-chip wait ran out       */
 #define SAMSPEC_ST_BADPARAM 8  /* verify with sampling parameters: temperature  */
                                /* not > 0 and finite, or top_p not > 0         */
+#define SAMSPEC_ST_BOUNDS 9    /* automata, debug library only (built with     */
+                               /* SAMSPEC_CHECKS=1): an index into one of the  */
+                               /* sequence's arrays fell outside the array; the */
+                               /* access was skipped and the sequence frozen   */
 
 /* logits element types */
 #define SAMSPEC_F32 0

@@ -12,10 +12,13 @@ import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libsamspec.so")
+# the debug build: every automaton index checked against its array (ST_BOUNDS)
+CHECKS_LIB_PATH = os.path.join(_HERE, "_lib", "libsamspec_checks.so")
 
 # host-side return codes and per-sequence status words (include/samspec.h)
 OK, EINVAL, ESIZE, EDTYPE, ECUDA, EALIGN = 0, -1, -2, -3, -4, -5
-ST_OK, ST_CAPACITY, ST_HASHFULL, ST_TOKEN, ST_LOOPCAP, ST_BADROW, ST_BADDRAFT, ST_TIMEOUT, ST_BADPARAM = range(9)
+(ST_OK, ST_CAPACITY, ST_HASHFULL, ST_TOKEN, ST_LOOPCAP, ST_BADROW, ST_BADDRAFT, ST_TIMEOUT, ST_BADPARAM,
+ ST_BOUNDS) = range(10)
 F32, BF16 = 0, 1
 
 EXPORTED = [

@@ -22,6 +22,7 @@ const char* samspec_strerror(int code) {
     case SAMSPEC_ST_BADDRAFT: return "sequence: draft length, draft token or n_new out of range";
     case SAMSPEC_ST_TIMEOUT: return "sequence: a bounded on-chip wait ran out";
     case SAMSPEC_ST_BADPARAM: return "sequence: temperature not > 0 and finite, or top_p not > 0";
+    case SAMSPEC_ST_BOUNDS: return "sequence: an automaton index left its array (debug library)";
     default: return "unknown code";
   }
 }

@@ -50,6 +50,12 @@
 #include "common.cuh"
 #include "samspec.h"
 
+// SAMSPEC_CHECKS=1 builds the debug library: every index into a sequence's
+// arrays is checked (see the element access functions below).
+#ifndef SAMSPEC_CHECKS
+#define SAMSPEC_CHECKS 0
+#endif
+
 struct sam_batch {
   int32_t B, C, V, S, E;
   int64_t H;
@@ -63,7 +69,7 @@ namespace samspec {
 namespace {
 
 constexpr int kScal = 16;
-enum { SC_N = 0, SC_LAST, SC_NS, SC_NE, SC_STATUS, SC_LINKLAST, SC_LENLAST, SC_POOL, SC_CHAIN };
+enum { SC_N = 0, SC_LAST, SC_NS, SC_NE, SC_STATUS, SC_LINKLAST, SC_LENLAST, SC_POOL, SC_CHAIN, SC_CHECK };
 
 // The suffix chain of `last` (last, link(last), ..., root) is kept explicitly
 // while it has at most kChainMax states: 4 registers per lane inside a launch,
@@ -122,6 +128,73 @@ __device__ __forceinline__ SeqView seq_view(const BatchView& v, int b) {
   return s;
 }
 
+// ---- element access ----------------------------------------------------------
+// Every index into a sequence's arrays goes through these functions.  In the
+// debug build (SAMSPEC_CHECKS=1) an index outside its array is not used: a
+// read gives a neutral value, a write is dropped, and the sequence's check
+// word is set; its status becomes ST_BOUNDS when the launch ends.  In the
+// normal build they are plain loads and stores.
+__device__ __forceinline__ bool idx_ok(const SeqView& v, int64_t i, int64_t n) {
+#if SAMSPEC_CHECKS
+  if (i >= 0 && i < n) return true;
+  atomicOr(v.sc + SC_CHECK, 1);
+  return false;
+#else
+  (void)v;
+  (void)i;
+  (void)n;
+  return true;
+#endif
+}
+__device__ __forceinline__ int4 ST(const SeqView& v, int64_t x) {
+  return idx_ok(v, x, v.S) ? v.st[x] : make_int4(0, -1, -1, 0);
+}
+__device__ __forceinline__ void ST_W(const SeqView& v, int64_t x, int4 r) {
+  if (idx_ok(v, x, v.S)) v.st[x] = r;
+}
+__device__ __forceinline__ int32_t LK(const SeqView& v, int64_t x) {
+  return idx_ok(v, x, v.S) ? v.lk[x] : -1;
+}
+__device__ __forceinline__ void LK_W(const SeqView& v, int64_t x, int32_t y) {
+  if (idx_ok(v, x, v.S)) v.lk[x] = y;
+}
+__device__ __forceinline__ int32_t POOL(const SeqView& v, int64_t i) {
+  return idx_ok(v, i, v.P) ? v.pool[i] : 0;
+}
+__device__ __forceinline__ void POOL_W(const SeqView& v, int64_t i, int32_t t) {
+  if (idx_ok(v, i, v.P)) v.pool[i] = t;
+}
+__device__ __forceinline__ unsigned long long HS(const SeqView& v, int64_t i) {
+  return idx_ok(v, i, (int64_t)v.hmask + 1) ? v.hs[i] : 0ull;
+}
+__device__ __forceinline__ void HS_W(const SeqView& v, int64_t i, unsigned long long x) {
+  if (idx_ok(v, i, (int64_t)v.hmask + 1)) v.hs[i] = x;
+}
+__device__ __forceinline__ int32_t HIST(const SeqView& v, int64_t i) {
+  return idx_ok(v, i, v.C) ? v.hist[i] : -1;
+}
+__device__ __forceinline__ void HIST_W(const SeqView& v, int64_t i, int32_t t) {
+  if (idx_ok(v, i, v.C)) v.hist[i] = t;
+}
+__device__ __forceinline__ int32_t CHN(const SeqView& v, int64_t i) {
+  return idx_ok(v, i, kChainMax) ? v.chn[i] : -1;
+}
+__device__ __forceinline__ void CHN_W(const SeqView& v, int64_t i, int32_t x) {
+  if (idx_ok(v, i, kChainMax)) v.chn[i] = x;
+}
+// the aligned 4-slot group of the hash that holds slot p (one 32-byte sector)
+__device__ __forceinline__ void HS_GROUP(const SeqView& v, uint32_t p, ulonglong2& lo,
+                                         ulonglong2& hi) {
+  const uint32_t base = p & ~3u;
+  if (!idx_ok(v, (int64_t)base + 3, (int64_t)v.hmask + 1)) {
+    lo = hi = make_ulonglong2(0ull, 0ull);
+    return;
+  }
+  const ulonglong2* gp = reinterpret_cast<const ulonglong2*>(v.hs + base);
+  lo = gp[0];
+  hi = gp[1];
+}
+
 __device__ __forceinline__ uint32_t slot_hash(int32_t s, int32_t t) {
   uint64_t k = ((uint64_t)(uint32_t)s << 18) | (uint32_t)t;
   k ^= k >> 33;
@@ -147,8 +220,8 @@ __device__ __forceinline__ int lane_probe_from(const SeqView& v, uint64_t kb, ui
   const uint32_t ngroups = (v.hmask >> 2) + 2;
   for (uint32_t g = 0; g < ngroups; ++g) {
     const uint32_t base = p & ~3u;
-    const ulonglong2* gp = reinterpret_cast<const ulonglong2*>(v.hs + base);
-    const ulonglong2 lo = gp[0], hi = gp[1];
+    ulonglong2 lo, hi;
+    HS_GROUP(v, p, lo, hi);
     const unsigned long long x[4] = {lo.x, lo.y, hi.x, hi.y};
     const int k0 = (int)(p & 3u);
 #pragma unroll
@@ -185,11 +258,7 @@ __device__ __forceinline__ GroupLoad probe_issue(const SeqView& v, int32_t s, in
   g.p = slot_hash(s, t) & v.hmask;
   g.lo = make_ulonglong2(0ull, 0ull);
   g.hi = g.lo;
-  if (on) {
-    const ulonglong2* gp = reinterpret_cast<const ulonglong2*>(v.hs + (g.p & ~3u));
-    g.lo = gp[0];
-    g.hi = gp[1];
-  }
+  if (on) HS_GROUP(v, g.p, g.lo, g.hi);
   return g;
 }
 __device__ __forceinline__ int probe_finish(const SeqView& v, int32_t s, int32_t t,
@@ -226,12 +295,12 @@ __device__ __forceinline__ bool lane_place(const SeqView& v, uint32_t pos, unsig
     if (!__any_sync(kFullMask, want)) return true;
     const uint32_t q = p & v.hmask;
     bool empty = want;
-    if (want && !known_empty) empty = v.hs[q] == 0ull;
+    if (want && !known_empty) empty = HS(v, q) == 0ull;
     const uint32_t key = empty ? q : (0x80000000u | (uint32_t)lane);
     const unsigned grp = __match_any_sync(kFullMask, key);
     const bool win = empty && lane == __ffs(grp) - 1;
     __syncwarp();
-    if (win) v.hs[q] = val;
+    if (win) HS_W(v, q, val);
     __syncwarp();
     if (win) want = false;
     known_empty = false;
@@ -247,6 +316,9 @@ struct Scal {
 // Moves n tokens (n a multiple of 4; 16-byte aligned arrays) with int4 copies.
 __device__ __forceinline__ void pool_move(const SeqView& v, int32_t dst, int32_t src, int32_t n,
                                           int lane) {
+  if (n > 0 && !(idx_ok(v, src, v.P) && idx_ok(v, (int64_t)src + n - 1, v.P) && idx_ok(v, dst, v.P) &&
+                 idx_ok(v, (int64_t)dst + n - 1, v.P)))
+    return;  // (debug build: a range outside the pool; the warp leaves together)
   const int4* s4 = reinterpret_cast<const int4*>(v.pool + src);
   int4* d4 = reinterpret_cast<int4*>(v.pool + dst);
   const int32_t n4 = n >> 2;
@@ -303,8 +375,8 @@ __device__ __forceinline__ int append_out(const SeqView& v, Scal& sc, int32_t s,
     cap = ncap;
   }
   if (want) {
-    v.pool[off + n] = c;
-    v.st[s] = make_int4(r.x, r.y, off, (n + 1) | (log2_pow2(cap) << 24));
+    POOL_W(v, off + n, c);
+    ST_W(v, s, make_int4(r.x, r.y, off, (n + 1) | (log2_pow2(cap) << 24)));
   }
   sc.ne += __popc(wm);
   __syncwarp();
@@ -326,9 +398,9 @@ __device__ int extend_chase(const SeqView& v, Scal& sc, int32_t c, int lane) {
   const int32_t cur = sc.ns++;
   if (lane == 0) {
     // position i ends only suffixes of S c and exceeds every earlier end
-    v.st[cur] = make_int4(sc.len_last + 1, i, -1, 0);
-    v.lk[cur] = -1;
-    v.hist[i] = c;
+    ST_W(v, cur, make_int4(sc.len_last + 1, i, -1, 0));
+    LK_W(v, cur, -1);
+    HIST_W(v, i, c);
   }
   __syncwarp();
 
@@ -346,7 +418,7 @@ __device__ int extend_chase(const SeqView& v, Scal& sc, int32_t c, int lane) {
     int32_t mine = lane == 0 ? x : -1;
     int m = 1;
     while (m < W) {
-      const int32_t y = v.lk[x];
+      const int32_t y = LK(v, x);
       if (y == -1) break;
       x = y;
       if (lane == m) mine = x;
@@ -355,8 +427,8 @@ __device__ int extend_chase(const SeqView& v, Scal& sc, int32_t c, int lane) {
     guard -= m;
     if (guard < 0) return SAMSPEC_ST_LOOPCAP;
     const bool has = lane < m;
-    const int4 rec = has ? v.st[mine] : make_int4(0, 0, -1, 0);
-    const int32_t nx = v.lk[x];
+    const int4 rec = has ? ST(v, mine) : make_int4(0, 0, -1, 0);
+    const int32_t nx = LK(v, x);
     uint32_t pos = 0;
     int32_t val = -1;
     const int r = has ? lane_probe(v, mine, c, &pos, &val) : 0;
@@ -383,8 +455,8 @@ __device__ int extend_chase(const SeqView& v, Scal& sc, int32_t c, int lane) {
   }
 
   if (q >= 0) {
-    const int4 sq = v.st[q];
-    const int32_t lq = v.lk[q];
+    const int4 sq = ST(v, q);
+    const int32_t lq = LK(v, q);
     if (len_p + 1 == sq.x) {
       link_cur = q;
     } else {
@@ -399,25 +471,25 @@ __device__ int extend_chase(const SeqView& v, Scal& sc, int32_t c, int lane) {
       const int32_t coff = sc.pool;
       sc.pool += ccap;
       if (lane == 0) {
-        v.st[clone] = make_int4(len_p + 1, sq.y, coff, nq | (log2_pow2(ccap) << 24));
-        v.lk[clone] = lq;
+        ST_W(v, clone, make_int4(len_p + 1, sq.y, coff, nq | (log2_pow2(ccap) << 24)));
+        LK_W(v, clone, lq);
       }
       for (int32_t base = 0; base < nq; base += 32) {
         const bool own = base + lane < nq;
-        const int32_t t = own ? v.pool[sq.z + base + lane] : 0;
+        const int32_t t = own ? POOL(v, sq.z + base + lane) : 0;
         uint32_t qpos = 0, cpos = 0;
         int32_t to = -1, dummy = -1;
         const int r1 = own ? lane_probe(v, q, t, &qpos, &to) : 1;
         const int r2 = own ? lane_probe(v, clone, t, &cpos, &dummy) : 0;
         if (__any_sync(kFullMask, r1 != 1 || r2 != 0))
           return __any_sync(kFullMask, r1 < 0 || r2 < 0) ? SAMSPEC_ST_HASHFULL : SAMSPEC_ST_LOOPCAP;
-        if (own) v.pool[coff + base + lane] = t;
+        if (own) POOL_W(v, coff + base + lane, t);
         if (!lane_place(v, cpos, slot_value(clone, t, to), own, lane)) return SAMSPEC_ST_HASHFULL;
       }
       sc.ne += nq;
       // (p, c) -> clone, then the states after p on the chain while their
       // c-transition still leads to q (batched like the walk)
-      if (lane == 0) v.hs[p_pos] = slot_value(p, c, clone);
+      if (lane == 0) HS_W(v, p_pos, slot_value(p, c, clone));
       __syncwarp();
       int32_t y = after_p;
       W = 2;
@@ -425,7 +497,7 @@ __device__ int extend_chase(const SeqView& v, Scal& sc, int32_t c, int lane) {
         int32_t mine = lane == 0 ? y : -1;
         int m = 1;
         while (m < W) {
-          const int32_t z = v.lk[y];
+          const int32_t z = LK(v, y);
           if (z == -1) break;
           y = z;
           if (lane == m) mine = y;
@@ -434,24 +506,24 @@ __device__ int extend_chase(const SeqView& v, Scal& sc, int32_t c, int lane) {
         guard -= m;
         if (guard < 0) return SAMSPEC_ST_LOOPCAP;
         const bool has = lane < m;
-        const int32_t ny = v.lk[y];
+        const int32_t ny = LK(v, y);
         uint32_t pos = 0;
         int32_t val = -1;
         const int r = has ? lane_probe(v, mine, c, &pos, &val) : 1;
         if (__any_sync(kFullMask, has && r < 0)) return SAMSPEC_ST_HASHFULL;
         const unsigned stop = __ballot_sync(kFullMask, has && (r == 0 || val != q));
         const int ks = stop ? __ffs(stop) - 1 : m;
-        if (has && lane < ks) v.hs[pos] = slot_value(mine, c, clone);
+        if (has && lane < ks) HS_W(v, pos, slot_value(mine, c, clone));
         __syncwarp();
         if (stop) break;
         y = ny;
         W = W < 32 ? 2 * W : 32;
       }
-      if (lane == 0) v.lk[q] = clone;
+      if (lane == 0) LK_W(v, q, clone);
       link_cur = clone;
     }
   }
-  if (lane == 0) v.lk[cur] = link_cur;
+  if (lane == 0) LK_W(v, cur, link_cur);
   __syncwarp();
   sc.last = cur;
   sc.len_last += 1;
@@ -485,9 +557,9 @@ __device__ int extend_chain(const SeqView& v, Scal& sc, int32_t c, int lane,
   const int32_t cur = sc.ns++;
   if (lane == 0) {
     // position i ends only suffixes of S c and exceeds every earlier end
-    v.st[cur] = make_int4(sc.len_last + 1, i, -1, 0);
-    v.lk[cur] = -1;
-    v.hist[i] = c;
+    ST_W(v, cur, make_int4(sc.len_last + 1, i, -1, 0));
+    LK_W(v, cur, -1);
+    HIST_W(v, i, c);
   }
   bool has[kChR];
   int4 rec[kChR];
@@ -495,7 +567,7 @@ __device__ int extend_chain(const SeqView& v, Scal& sc, int32_t c, int lane,
 #pragma unroll
   for (int r = 0; r < kChR; ++r) {
     has[r] = 32 * r + lane < m;
-    rec[r] = has[r] ? v.st[chr[r]] : make_int4(0, 0, -1, 0);
+    rec[r] = has[r] ? ST(v, chr[r]) : make_int4(0, 0, -1, 0);
     gl[r] = probe_issue(v, chr[r], c, has[r]);
   }
   uint32_t pos[kChR];
@@ -537,8 +609,8 @@ __device__ int extend_chain(const SeqView& v, Scal& sc, int32_t c, int lane,
 #pragma unroll
     for (int r = 0; r < kChR; ++r) lens[r] = rec[r].x;
     const int32_t len_p = __shfl_sync(kFullMask, sel(lens, kr), kl);
-    const int4 sq = v.st[q];
-    const int32_t lq = v.lk[q];
+    const int4 sq = ST(v, q);
+    const int32_t lq = LK(v, q);
     int32_t clone = -1;
     if (len_p + 1 == sq.x) {
       link_cur = q;
@@ -554,19 +626,19 @@ __device__ int extend_chain(const SeqView& v, Scal& sc, int32_t c, int lane,
       const int32_t coff = sc.pool;
       sc.pool += ccap;
       if (lane == 0) {
-        v.st[clone] = make_int4(len_p + 1, sq.y, coff, nq | (log2_pow2(ccap) << 24));
-        v.lk[clone] = lq;
+        ST_W(v, clone, make_int4(len_p + 1, sq.y, coff, nq | (log2_pow2(ccap) << 24)));
+        LK_W(v, clone, lq);
       }
       for (int32_t base = 0; base < nq; base += 32) {
         const bool own = base + lane < nq;
-        const int32_t t = own ? v.pool[sq.z + base + lane] : 0;
+        const int32_t t = own ? POOL(v, sq.z + base + lane) : 0;
         uint32_t qpos = 0, cpos = 0;
         int32_t to = -1, dummy = -1;
         const int r1 = own ? lane_probe(v, q, t, &qpos, &to) : 1;
         const int r2 = own ? lane_probe(v, clone, t, &cpos, &dummy) : 0;
         if (__any_sync(kFullMask, r1 != 1 || r2 != 0))
           return __any_sync(kFullMask, r1 < 0 || r2 < 0) ? SAMSPEC_ST_HASHFULL : SAMSPEC_ST_LOOPCAP;
-        if (own) v.pool[coff + base + lane] = t;
+        if (own) POOL_W(v, coff + base + lane, t);
         if (!lane_place(v, cpos, slot_value(clone, t, to), own, lane)) return SAMSPEC_ST_HASHFULL;
       }
       sc.ne += nq;
@@ -576,12 +648,12 @@ __device__ int extend_chain(const SeqView& v, Scal& sc, int32_t c, int lane,
       for (int r = 0; r < kChR; ++r) {
         const int j = 32 * r + lane;
         if (has[r] && j >= k && pr[r] == 1 && val[r] == q)
-          v.hs[pos[r]] = slot_value(chr[r], c, clone);
+          HS_W(v, pos[r], slot_value(chr[r], c, clone));
       }
       (void)p;
       (void)p_pos;
       __syncwarp();
-      if (lane == 0) v.lk[q] = clone;
+      if (lane == 0) LK_W(v, q, clone);
       link_cur = clone;
     }
     // the new chain: cur, the distinct targets of x_k .. x_{m-1}, root
@@ -610,7 +682,7 @@ __device__ int extend_chain(const SeqView& v, Scal& sc, int32_t c, int lane,
   if (lane == 0) {
     sh[0] = cur;
     if (mn <= kChainMax + 1) sh[mn - 1] = 0;
-    v.lk[cur] = link_cur;
+    LK_W(v, cur, link_cur);
   }
   __syncwarp();
   if (mn <= kChainMax) {
@@ -634,7 +706,7 @@ __device__ void chain_rebuild(const SeqView& v, const Scal& sc, int lane, int32_
                               int& m) {
   m = 0;
   const int32_t ll = sc.link_last;
-  const int32_t bound = (ll < 0 ? 0 : v.st[ll].x) + 2;
+  const int32_t bound = (ll < 0 ? 0 : ST(v, ll).x) + 2;
   if (bound > kChainMax) return;
   int32_t x = sc.last;
   int n = 0;
@@ -645,7 +717,7 @@ __device__ void chain_rebuild(const SeqView& v, const Scal& sc, int lane, int32_
     for (int r = 0; r < kChR; ++r)
       if (n == 32 * r + lane) chr[r] = x;
     ++n;
-    x = v.lk[x];
+    x = LK(v, x);
   }
   if (x == -1) m = n;
 }
@@ -659,13 +731,13 @@ __device__ void draft_one(const SeqView& v, const Scal& sc, int32_t K, int32_t* 
     s = sc.link_last;
     int guard = sc.len_last + 1;
     while (s > 0) {
-      rec = v.st[s];
+      rec = ST(v, s);
       if (rec_nout(rec) > 0) break;
       if (--guard < 0) {
         s = 0;
         break;
       }
-      s = v.lk[s];
+      s = LK(v, s);
     }
     if (s < 0) s = 0;
   }
@@ -676,7 +748,7 @@ __device__ void draft_one(const SeqView& v, const Scal& sc, int32_t K, int32_t* 
     dl = min(K, sc.n - 1 - me);
     if (dl < 0) dl = 0;
   }
-  for (int t = lane; t < K; t += 32) draft_row[t] = t < dl ? v.hist[me + 1 + t] : -1;
+  for (int t = lane; t < K; t += 32) draft_row[t] = t < dl ? HIST(v, me + 1 + t) : -1;
   if (lane == 0) {
     if (dl_out) *dl_out = dl;
     if (ml_out) *ml_out = ml;
@@ -726,7 +798,7 @@ __global__ void __launch_bounds__(64) sam_step_kernel(BatchView bv, const int32_
     m = v.sc[SC_CHAIN];
     if (m < 0 || m > kChainMax) m = 0;
 #pragma unroll
-    for (int r = 0; r < kChR; ++r) chr[r] = 32 * r + lane < m ? v.chn[32 * r + lane] : -1;
+    for (int r = 0; r < kChR; ++r) chr[r] = 32 * r + lane < m ? CHN(v, 32 * r + lane) : -1;
     const int32_t nn = n_new[i];
     if (nn < 0 || nn > max_new) {
       sc.status = SAMSPEC_ST_BADDRAFT;
@@ -756,6 +828,14 @@ __global__ void __launch_bounds__(64) sam_step_kernel(BatchView bv, const int32_
     draft_one(v, sc, K, draft + (size_t)i * K, draft_len ? draft_len + i : nullptr,
               match_len ? match_len + i : nullptr, min_endpos ? min_endpos + i : nullptr, lane);
   }
+#if SAMSPEC_CHECKS
+  // an index that left its array in this launch freezes the sequence
+  __syncwarp();
+  if (v.sc[SC_CHECK] != 0) {
+    if (sc.status == SAMSPEC_ST_OK) sc.status = SAMSPEC_ST_BOUNDS;
+    if (!kExtend && lane == 0) v.sc[SC_STATUS] = SAMSPEC_ST_BOUNDS;
+  }
+#endif
   if (kExtend && lane == 0) {
     v.sc[SC_N] = sc.n;
     v.sc[SC_LAST] = sc.last;
@@ -770,7 +850,7 @@ __global__ void __launch_bounds__(64) sam_step_kernel(BatchView bv, const int32_
   if (kExtend && sc.status == SAMSPEC_ST_OK) {
 #pragma unroll
     for (int r = 0; r < kChR; ++r)
-      if (32 * r + lane < m) v.chn[32 * r + lane] = chr[r];
+      if (32 * r + lane < m) CHN_W(v, 32 * r + lane, chr[r]);
   }
 }
 
@@ -818,7 +898,7 @@ __global__ void __launch_bounds__(64) ssam_match_kernel(BatchView bv, int32_t cb
       int32_t mine = lane == 0 ? x : -1;
       int m = 1;
       while (m < W) {
-        const int32_t y = v.lk[x];
+        const int32_t y = LK(v, x);
         if (y == -1) break;
         x = y;
         if (lane == m) mine = x;
@@ -826,8 +906,8 @@ __global__ void __launch_bounds__(64) ssam_match_kernel(BatchView bv, int32_t cb
       }
       guard -= m;
       const bool has = lane < m;
-      const int32_t len_m = has ? v.st[mine].x : 0;
-      const int32_t nx = v.lk[x];
+      const int32_t len_m = has ? ST(v, mine).x : 0;
+      const int32_t nx = LK(v, x);
       uint32_t pos = 0;
       int32_t val = -1;
       const int r = has ? lane_probe(v, mine, c, &pos, &val) : 0;
@@ -856,16 +936,21 @@ __global__ void __launch_bounds__(64) ssam_match_kernel(BatchView bv, int32_t cb
     state[2 * i] = s;
     state[2 * i + 1] = l;
     if (match_len) match_len[i] = l;
-    if (min_endpos) min_endpos[i] = s != 0 ? v.st[s].y : -1;
+    if (min_endpos) min_endpos[i] = s != 0 ? ST(v, s).y : -1;
   }
   int32_t dl = 0, e = -1;
   if (s != 0 && l > 0) {
-    e = v.st[s].y;
+    e = ST(v, s).y;
     dl = min(K, ntext - 1 - e);
     if (dl < 0) dl = 0;
   }
-  for (int t = lane; t < K; t += 32) draft[(size_t)i * K + t] = t < dl ? v.hist[e + 1 + t] : -1;
+  for (int t = lane; t < K; t += 32) draft[(size_t)i * K + t] = t < dl ? HIST(v, e + 1 + t) : -1;
   if (lane == 0 && draft_len) draft_len[i] = dl;
+#if SAMSPEC_CHECKS
+  // an index that left the corpus's arrays marks the corpus automaton
+  __syncwarp();
+  if (lane == 0 && v.sc[SC_CHECK] != 0) v.sc[SC_STATUS] = SAMSPEC_ST_BOUNDS;
+#endif
 }
 
 // Adaptive draft selection ([P4] "Drafting with Suffix Automaton"): the
@@ -909,6 +994,7 @@ __global__ void sam_reset_kernel(BatchView bv, const int32_t* __restrict__ mask)
     sc[SC_LENLAST] = 0;
     sc[SC_POOL] = 0;
     sc[SC_CHAIN] = 1;
+    sc[SC_CHECK] = 0;
     bv.st[(size_t)b * bv.S] = make_int4(0, -1, -1, 0);
     bv.lk[(size_t)b * bv.S] = -1;
     bv.chn[(size_t)b * kChainMax] = 0;

@@ -95,6 +95,7 @@ struct VParams {
   spec_verify_debug dbg;
   uint32_t* ws;  // [0] claim counter, [1] CTA exit counter, [2] error bits
   int32_t NC, NS;
+  int32_t G;         // CTAs per thread-block cluster: a sequence's tiles are shared among them
   uint64_t wait_ns;  // limit of every pipeline wait
   int32_t direct;  // 1: plain loads instead of bulk copies (unaligned rows)
   // draft trees (K = N - 1, row n scores the token after node n's path)
@@ -163,6 +164,20 @@ struct Smem {
   uint64_t tile_bar[kSlots][kMaxChunks];  // one phase per job: the kCW records of a tile
   float4 pre[kSlots][kMaxChunks][2];     // control: mass before each tile {hi, lo, ref, 0}
 };
+
+// Sets this CTA's abort flag, and (clusters) every other CTA's of the cluster.
+__device__ __forceinline__ void set_abort(Smem& sm, int G) {
+  vstore(&sm.abort, 1);
+  if (G > 1) {
+    const uint32_t me = cluster_rank();
+    for (int r = 0; r < G; ++r)
+      if ((uint32_t)r != me) st_cluster_u32(cluster_map(&sm.abort, (uint32_t)r), 1u);
+  }
+}
+
+// Words of a slot that the other CTAs of a cluster need for a job (kind ..
+// depth; the state word is written after them).
+constexpr int kSlotSyncWords = 15;
 
 __device__ __forceinline__ uint64_t gtimer() {
   uint64_t t;
@@ -677,7 +692,7 @@ __device__ __forceinline__ float exp_ref(float x, float R, float cT, float cTl) 
   return ldexpf(exp2f((s - si) + (e1 + e2)), (int)fmaxf(si, -300.f));
 }
 
-template <int TT, int DT, bool GREEDY, bool TREE = false, bool SAMP = false>
+template <int TT, int DT, bool GREEDY, bool TREE = false, bool SAMP = false, bool CL = false>
 struct Control {
   using C = Cfg<TT, DT>;
   static constexpr int EPL = C::SL / 32;  // slice elements per lane (lane-major loads)
@@ -747,6 +762,22 @@ struct Control {
     __syncwarp();
   }
 
+  // Clusters: the job's words of the slot go to the same slot of every other
+  // CTA of the cluster (their producers stream the job's other tiles and
+  // their consumers read the residual pass's terms), then its ready state.
+  __device__ void publish() {
+    const int32_t* w = reinterpret_cast<const int32_t*>(&sm.slot[si]);
+    const int G = CL ? P.G : 1;
+    for (int k = lane; k < (G - 1) * kSlotSyncWords; k += 32) {
+      const int r = 1 + k / kSlotSyncWords, q = 1 + k % kSlotSyncWords;
+      st_cluster_u32(cluster_map(w + q, (uint32_t)r), (uint32_t)w[q]);
+    }
+    fence_cluster();
+    __syncwarp();
+    if (lane >= 1 && lane < G) st_cluster_u32(cluster_map(&sm.slot[si].state, (uint32_t)lane), (uint32_t)kReady);
+    __syncwarp();
+  }
+
   // Posts row j for the producer, then draws the row's coins while it streams.
   __device__ void post(int kind, int j) {
     Slot& S = sm.slot[si];
@@ -775,8 +806,10 @@ struct Control {
       S.dtok = (kind == kStats && j < S.nb) ? dt : -1;
       if (SAMP) S.tau = P.tau[(size_t)S.b * (P.K + 1) + j];
       __threadfence_block();
-      vstore(&S.state, kReady);
     }
+    __syncwarp();
+    if (CL) publish();
+    if (lane == 0) vstore(&S.state, kReady);
     __syncwarp();
     if (!GREEDY) verify_coins(P.seed, P.step, (uint32_t)S.b, (uint32_t)j, &ua, &ur);
   }
@@ -820,11 +853,13 @@ struct Control {
     while (more) {
       uint32_t b = 0;
       if (lane == 0) {
-        // CTA x's first sequence is x (grid <= B); later ones come from the
-        // shared counter, past the first gridDim.x (none when the grid
-        // covers the batch: the counter is then never touched)
-        b = first_ ? blockIdx.x
-                   : gridDim.x >= (uint32_t)P.B ? (uint32_t)P.B : gridDim.x + atomicAdd(&P.ws[0], 1u);
+        // cluster x's first sequence is x (clusters <= B); later ones come
+        // from the shared counter, past the first `ncl` (none when the
+        // clusters cover the batch: the counter is then never touched)
+        const uint32_t G = CL ? (uint32_t)P.G : 1u;
+        const uint32_t ncl = gridDim.x / G;
+        b = first_ ? blockIdx.x / G
+                   : ncl >= (uint32_t)P.B ? (uint32_t)P.B : ncl + atomicAdd(&P.ws[0], 1u);
         vstore(&sm.pool_left, b >= (uint32_t)P.B ? 0 : P.B - 1 - (int)b);
         if (b >= (uint32_t)P.B) vstore(&sm.pool_done, 1);
       }
@@ -1347,7 +1382,10 @@ struct Control {
   }
 };
 
-template <int TT, int DT, bool GREEDY, bool TREE = false, bool SAMP = false>
+// CL: launched in thread-block clusters of P.G CTAs that share each
+// sequence's tiles (small batches); without it, one CTA per sequence and no
+// cluster code at all in the instantiation.
+template <int TT, int DT, bool GREEDY, bool TREE = false, bool SAMP = false, bool CL = false>
 __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
   using C = Cfg<TT, DT>;
   extern __shared__ __align__(1024) unsigned char dsm[];
@@ -1359,6 +1397,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int NS = P.NS;
+  const int G = CL ? P.G : 1;                 // CTAs of this cluster (1: no cluster)
+  const uint32_t crank = CL ? cluster_rank() : 0u;  // 0: the leader, whose control warps decide
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -1380,9 +1420,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
     mbar_fence_init();
   }
   // tile barriers: each consumer warp arrives once per tile of a job
-  if (threadIdx.x < kSlots * kMaxChunks)
+  // (other CTAs of a cluster arrive on them: each init is fenced at cluster scope)
+  if (threadIdx.x < kSlots * kMaxChunks) {
     mbar_init(&sm.tile_bar[threadIdx.x / kMaxChunks][threadIdx.x % kMaxChunks], kCW);
+    mbar_fence_init();
+  }
   __syncthreads();
+  // clusters: no CTA writes into another's shared memory before it is set up
+  if (G > 1) cluster_sync_all();
 
   if (warp < kCW) {
     // ------------------------------ consumers ------------------------------
@@ -1400,7 +1445,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         }
       }
       if (!ok) {
-        if (lane == 0) vstore(&sm.abort, 1);
+        if (lane == 0) set_abort(sm, G);
         break;
       }
       const Tag tg = sm.tag[cs];
@@ -1478,7 +1523,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         r.a = full ? reduce_resid<TT, DT, true>(sl, warp, lane, tg.nel, S, P.cT)
                    : reduce_resid<TT, DT, false>(sl, warp, lane, tg.nel, S, P.cT);
       }
-      if (tg.dtok >= 0) {
+      if (tg.dtok >= 0 && !none) {
         // the lane holding the draft token keeps its logits for the decision
         const int o = tg.dtok - tg.elem0 - warp * C::SL;
         if (o >= 0 && o < C::SL && o + warp * C::SL < tg.nel) {
@@ -1494,18 +1539,30 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
                   x = sl.t[i].at(k);
                   if (DT >= 0 && tg.has_draft) g = sl.d[i].at(k);
                 }
-            S.xd = x;
-            S.gd = g;
+            if (G == 1) {
+              S.xd = x;
+              S.gd = g;
+            } else {  // the leader's slot takes the decision
+              st_cluster_u32(cluster_map(&S.xd, 0), __float_as_uint(x));
+              st_cluster_u32(cluster_map(&S.gd, 0), __float_as_uint(g));
+              fence_cluster();
+            }
           }
         }
       }
       __syncwarp();
       if (lane == 0) {
         const size_t ri = ((size_t)tg.slot * P.NC + tg.chunk) * kCW + warp;
-        rec[ri] = r.a;
-        if (DT >= 0) rec[(size_t)kSlots * P.NC * kCW + ri] = r.b;
         // release: the record (and the captured logits) before the arrival
-        mbar_arrive(&sm.tile_bar[tg.slot][tg.chunk]);
+        if (G == 1) {
+          rec[ri] = r.a;
+          if (DT >= 0) rec[(size_t)kSlots * P.NC * kCW + ri] = r.b;
+          mbar_arrive(&sm.tile_bar[tg.slot][tg.chunk]);
+        } else {  // into the cluster leader's records, on its tile barrier
+          st_cluster_f32x4(cluster_map(&rec[ri], 0), r.a);
+          if (DT >= 0) st_cluster_f32x4(cluster_map(&rec[(size_t)kSlots * P.NC * kCW + ri], 0), r.b);
+          mbar_arrive_cluster(cluster_map(&sm.tile_bar[tg.slot][tg.chunk], 0));
+        }
       }
       __syncwarp();
       if (++cs == NS) {
@@ -1535,13 +1592,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
           vstore(&sm.prod_idle, 1);
           if (vload(&sm.ctrl_exited) == kSlots) break;
           if (gtimer() - t_idle > P.wait_ns) {
-            vstore(&sm.abort, 1);
+            set_abort(sm, G);
             break;
           }
           __nanosleep(128);
           continue;
         }
         vstore(&sm.prod_idle, 0);
+        if (G > 1) fence_cluster();  // the job's words came from the cluster leader
         __threadfence_block();
         Slot& S = sm.slot[si];
         vstore(&S.state, kIssued);
@@ -1551,7 +1609,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         const bool with_draft =
             DT >= 0 && ((kind == kStats && j < S.nb) || (kind == kResid && S.smode == 1));
         bool ok = true;
-        for (int c = 0; c < P.NC && ok; ++c) {
+        // clusters: this CTA streams the job's tiles c = rank (mod G)
+        for (int c = (int)crank; c < P.NC && ok; c += G) {
           const uint64_t t0 = gtimer();
           while (!mbar_try_wait(&sm.empty[ps], pph ^ 1)) {
             if (vload(&sm.abort) || gtimer() - t0 > P.wait_ns) {
@@ -1593,7 +1652,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
           }
         }
         if (!ok) {
-          vstore(&sm.abort, 1);
+          set_abort(sm, G);
           break;
         }
         vstore(&sm.jobs_issued, vload(&sm.jobs_issued) + 1);
@@ -1614,7 +1673,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
           __threadfence_block();
           mbar_arrive(&sm.full[ps]);
         } else {
-          vstore(&sm.abort, 1);
+          set_abort(sm, G);
         }
       }
       if (vload(&sm.abort)) {
@@ -1630,7 +1689,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         }
       }
     }
-  } else if (warp >= kCtrlWarp && warp < kCtrlWarp + kSlots) {
+  } else if (warp >= kCtrlWarp && warp < kCtrlWarp + kSlots && crank == 0) {
     // ----------------------------- control warps ----------------------------
     // One warp per sequence slot.  Slot 0 claims at once; the others wait
     // until the producer has issued this CTA's first row (every CTA of the
@@ -1638,7 +1697,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
     // while large ones keep four sequences in flight per CTA.
     const int si = warp - kCtrlWarp;
     Slot& S = sm.slot[si];
-    Control<TT, DT, GREEDY, TREE, SAMP> ctl(P, sm, rec, lane, si);
+    Control<TT, DT, GREEDY, TREE, SAMP, CL> ctl(P, sm, rec, lane, si);
     int last_jobs = -1;
     uint32_t tpar = 0;  // phase parity of this slot's tile barriers for its current job
     uint64_t t_idle = gtimer();
@@ -1668,7 +1727,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
             const bool dry = vload(&sm.prod_idle) && ready == 0;
             // decisions after sampling take longer (resample): keep more in flight
             const int target = GREEDY ? 2 : 3;
-            want = dry || (busy < target && vload(&sm.pool_left) >= (int)gridDim.x);
+            want = dry || (busy < target && vload(&sm.pool_left) >= (int)(gridDim.x / G));
           }
           if (!want && vload(&sm.ctrl_exited) > 0) want = true;  // nothing else to wait for
           go = want && atomicCAS(&sm.claim_lock, 0, 1) == 0;
@@ -1690,7 +1749,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
             last_jobs = ji;
             t_idle = gtimer();
           } else if (gtimer() - t_idle > P.wait_ns) {
-            vstore(&sm.abort, 1);
+            set_abort(sm, G);
             timeout = 1;
           }
         }
@@ -1704,7 +1763,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       uint64_t t0 = gtimer();
       for (int c = 0; c < P.NC;) {
         // every lane waits (acquire: the tile's records are visible after it)
-        if (__all_sync(kFullMask, mbar_try_wait(&sm.tile_bar[si][c], tpar))) {
+        const bool done = G == 1 ? mbar_try_wait(&sm.tile_bar[si][c], tpar)
+                                 : mbar_try_wait_cluster(&sm.tile_bar[si][c], tpar);
+        if (__all_sync(kFullMask, done)) {
           ctl.merge_tile(c);
           ++c;
           t0 = gtimer();
@@ -1719,7 +1780,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       }
       tpar ^= 1u;  // the next job of this slot completes the next phase
       if (!ok) {
-        if (lane == 0) vstore(&sm.abort, 1);
+        if (lane == 0) set_abort(sm, G);
         break;
       }
       ctl.handle();
@@ -1731,18 +1792,25 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         // CTA's own first sequence if the abort came before its claim, and
         // the pool past the first gridDim.x
         if (S.state != kEmpty) write_result(P, S.b, -1, -1, SAMSPEC_ST_TIMEOUT);
-        if (si == 0 && ctl.first_) write_result(P, (int)blockIdx.x, -1, -1, SAMSPEC_ST_TIMEOUT);
-        if (si == 0 && gridDim.x < (uint32_t)P.B)
-          for (uint32_t b = gridDim.x + atomicAdd(&P.ws[0], 1u); b < (uint32_t)P.B;
-               b = gridDim.x + atomicAdd(&P.ws[0], 1u))
+        const uint32_t ncl = gridDim.x / (uint32_t)G;
+        if (si == 0 && ctl.first_) write_result(P, (int)(blockIdx.x / G), -1, -1, SAMSPEC_ST_TIMEOUT);
+        if (si == 0 && ncl < (uint32_t)P.B)
+          for (uint32_t b = ncl + atomicAdd(&P.ws[0], 1u); b < (uint32_t)P.B;
+               b = ncl + atomicAdd(&P.ws[0], 1u))
             write_result(P, (int)b, -1, -1, SAMSPEC_ST_TIMEOUT);
       }
       __threadfence_block();
       atomicAdd(&sm.ctrl_exited, 1);
+      // clusters: the other CTAs' producers stop once every control warp of
+      // the leader has
+      for (int r = 1; r < G; ++r) red_cluster_add_u32(cluster_map(&sm.ctrl_exited, (uint32_t)r), 1u);
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0 && gridDim.x < (uint32_t)P.B) {  // the claim counter was used
+  // clusters: every store into another CTA's shared memory has landed
+  // before any CTA of the cluster exits
+  if (G > 1) cluster_sync_all();
+  if (threadIdx.x == 0 && gridDim.x / G < (uint32_t)P.B) {  // the claim counter was used
     __threadfence();
     if (atomicAdd(&P.ws[1], 1u) == gridDim.x - 1) {
       // last CTA out: reset the counters for the next launch on this workspace
@@ -1789,6 +1857,12 @@ int launch(const VParams& P0, cudaStream_t stream) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem[dev]) !=
         cudaSuccess)
       return SAMSPEC_ECUDA;
+    if constexpr (!TREE && !SAMP) {
+      if (cudaFuncSetAttribute(verify_kernel<TT, DT, GREEDY, TREE, SAMP, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem[dev]) !=
+          cudaSuccess)
+        return SAMSPEC_ECUDA;
+    }
     attr_done[dev] = true;
   }
   int ns = (int)(((size_t)max_smem[dev] - head) / kStageBytes);
@@ -1797,9 +1871,50 @@ int launch(const VParams& P0, cudaStream_t stream) {
   P.NS = ns;
   P.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   const size_t smem = head + (size_t)ns * kStageBytes;
-  const int grid = P.B < sms[dev] ? P.B : sms[dev];
-  verify_kernel<TT, DT, GREEDY, TREE, SAMP><<<grid, kThreads, smem, stream>>>(P);
-  return cudaGetLastError() == cudaSuccess ? SAMSPEC_OK : SAMSPEC_ECUDA;
+  auto kernel = verify_kernel<TT, DT, GREEDY, TREE, SAMP>;
+  auto ckernel = verify_kernel<TT, DT, GREEDY, TREE, SAMP, !TREE && !SAMP>;
+  // A batch that leaves SMs idle shares each sequence's tiles among a cluster
+  // of G CTAs (linear chains with bulk copies): G = 8, 4 or 2, the largest
+  // with B * G CTAs on the SMs and at least two tiles per CTA of a row.
+  int G = 1;
+  if (!TREE && !SAMP && !P.direct)
+    for (int g = 8; g >= 2; g >>= 1)
+      if ((int64_t)P.B * g <= sms[dev] && P.NC >= 2 * g) {
+        G = g;
+        break;
+      }
+  int clusters = 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  if (G > 1) {
+    cfg.gridDim = dim3((unsigned)G, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)G;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // clusters of this size resident at once (looked up once per device)
+    static int max_clusters[kMaxDev][4] = {{0}};
+    int& mc = max_clusters[dev][G == 2 ? 1 : (G == 4 ? 2 : 3)];
+    if (mc == 0 && cudaOccupancyMaxActiveClusters(&mc, ckernel, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      mc = -1;
+    }
+    clusters = mc < P.B ? mc : P.B;
+    if (clusters < 1) G = 1;
+  }
+  P.G = G;
+  if (G == 1) {
+    const int grid = P.B < sms[dev] ? P.B : sms[dev];
+    kernel<<<grid, kThreads, smem, stream>>>(P);
+    return cudaGetLastError() == cudaSuccess ? SAMSPEC_OK : SAMSPEC_ECUDA;
+  }
+  cfg.gridDim = dim3((unsigned)(clusters * G), 1, 1);
+  return cudaLaunchKernelEx(&cfg, ckernel, P) == cudaSuccess ? SAMSPEC_OK : SAMSPEC_ECUDA;
 }
 
 template <bool GREEDY>

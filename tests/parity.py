@@ -79,3 +79,127 @@ def compare_verify(g, o, target_rows, draft, draft_len, T, draft_rows=None, chec
 
 def gpu_to_numpy(res):
     return {k: v.detach().cpu().numpy() for k, v in res.items()}
+
+
+# ---- per-request sampling parameters (top-k / top-p cuts) -------------------
+
+def _probs(row, T):
+    x = row.astype(np.float64)
+    p = np.exp(x / T - (x / T).max())
+    return p / p.sum()
+
+
+def cut_ok(row, T, k, top_p, tau_gpu, tau_oracle):
+    """(ok, excused): the GPU cut equals the oracle's, or lies within BAND of
+    the top-p boundary (its mass above and at the cut straddle top_p)."""
+    if tau_gpu == tau_oracle or (np.isnan(tau_gpu) and np.isnan(tau_oracle)):
+        return True, False
+    # a cut is the kept set {v : l_v >= tau}: two values that keep the same
+    # tokens are the same cut (with nothing cut the GPU reports -inf, the
+    # oracle the row's smallest logit)
+    x32 = np.asarray(row, np.float32)
+    if not np.isnan(tau_gpu) and not np.isnan(tau_oracle) and np.array_equal(x32 >= tau_gpu, x32 >= tau_oracle):
+        return True, False
+    if top_p >= 1.0:
+        return False, False
+    _, tau_k = oracle.truncate_row(row, T, k, 1.0)
+    x = row.astype(np.float64)
+    p = _probs(row, T)
+    kept_k = x >= tau_k
+    zk = p[kept_k].sum()
+    above = p[kept_k & (x > tau_gpu)].sum() / zk
+    incl = p[kept_k & (x >= tau_gpu)].sum() / zk
+    ok = tau_gpu >= tau_k and np.any(x == tau_gpu) and above < top_p + BAND and incl >= top_p - BAND
+    return bool(ok), True
+
+
+def compare_sampling(g, o, rows, draft, T, k, p, tau_g, budget=True):
+    """Verification under per-request (T, top_k, top_p): statuses equal; each
+    decision identical, or excused when a row's top-p cut lies on the other
+    side of its boundary (within BAND in mass) or the coin lies within BAND
+    of the oracle's threshold / CDF interval.  Returns (decisions, excused)."""
+    B, K1 = rows.shape[:2]
+    decisions = excused = 0
+    for b in range(B):
+        assert g["status"][b] == o["status"][b], b
+        if o["status"][b] != 0:
+            continue
+        Lg, Lo = int(g["accept_len"][b]), int(o["accept_len"][b])
+        # the emitted token is always inside the cut of its row
+        assert rows[b, Lg, g["out_token"][b]] >= tau_g[b, Lg], b
+        decisions += min(Lg, Lo) + 2
+        if Lg == Lo and g["out_token"][b] == o["out_token"][b]:
+            continue
+        other_side = False
+        for j in range(min(Lg, Lo) + 1):
+            ok, ex = cut_ok(rows[b, j], float(T[b]), int(k[b]), float(p[b]), float(tau_g[b, j]),
+                            float(o["tau"][b, j]))
+            assert ok, (b, j)
+            other_side |= ex
+        if other_side:  # a top-p cut on the other side of its boundary
+            excused += 1
+            continue
+        if Lg != Lo:
+            j = min(Lg, Lo)
+            assert abs(o["u_acc"][b, j] - o["p_d"][b, j]) < BAND, (b, j, o["u_acc"][b, j], o["p_d"][b, j])
+        else:
+            pp, _ = oracle.truncate_row(rows[b, Lo], float(T[b]), int(k[b]), float(p[b]))
+            r = pp.copy()
+            if Lo < draft.shape[1]:
+                r[draft[b, Lo]] = max(0.0, r[draft[b, Lo]] - 1.0)
+            mass = r.sum()
+            tok = int(g["out_token"][b])
+            lo = r[:tok].sum() / mass
+            hi = lo + r[tok] / mass
+            assert r[tok] > 0 and lo - BAND <= o["u_res"][b] < hi + BAND, (b, tok, lo, hi, o["u_res"][b])
+        excused += 1
+    if budget:
+        assert excused <= int(1e-4 * max(decisions, 1)), f"{excused} excused of {decisions}"
+    return decisions, excused
+
+
+# ---- draft trees -------------------------------------------------------------
+
+def tree_children(fc, ns, n):
+    out, c = [], fc[n]
+    while c != -1:
+        out.append(int(c))
+        c = ns[c]
+    return out
+
+
+def compare_trees(g, o, rows, tok, fc, ns, T, seed, step, budget=True, seq_index=None):
+    """Tree verification: statuses equal; accepted paths and emitted tokens
+    identical, or excused when the depth's coin lies within BAND of a child's
+    running-sum threshold or the final coin within BAND of the oracle's
+    interval of the GPU's token.  Returns (decisions, excused)."""
+    B = len(o["status"])
+    decisions = excused = 0
+    for b in range(B):
+        assert g["status"][b] == o["status"][b], b
+        if o["status"][b] != 0:
+            continue
+        Lg, Lo = int(g["accept_len"][b]), int(o["accept_len"][b])
+        pg, po = list(g["path"][b, :Lg]), list(o["path"][b, :Lo])
+        decisions += min(Lg, Lo) + 2
+        if pg == po and g["out_token"][b] == o["out_token"][b]:
+            # the emitted tokens: the path's tokens, then the out token
+            assert list(g["emit"][b, :Lg + 1]) == [int(tok[b, n]) for n in pg] + [int(o["out_token"][b])]
+            continue
+        assert T > 0, f"greedy tree differs at b={b}"
+        d = 0
+        while d < min(Lg, Lo) and pg[d] == po[d]:
+            d += 1
+        node = 0 if d == 0 else po[d - 1]
+        kids = tree_children(fc[b], ns[b], node)
+        acc, lo, hi, _ = oracle.tree_node_info(rows[b, node], T, [int(tok[b, c]) for c in kids],
+                                               int(g["out_token"][b]))
+        ua, ur = oracle.uniforms(seed, step, b if seq_index is None else int(seq_index[b]), d)
+        if d < Lg or d < Lo:  # the depth's coin against a running sum
+            assert any(abs(ua - a) < BAND for a in acc), (b, d, ua, acc)
+        else:  # same path, different final token
+            assert lo - BAND <= ur < hi + BAND, (b, ur, lo, hi)
+        excused += 1
+    if budget:
+        assert excused <= int(1e-4 * max(decisions, 1)), f"{excused} excused of {decisions}"
+    return decisions, excused

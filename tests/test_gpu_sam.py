@@ -114,11 +114,12 @@ def test_rs_bf16_b64_histories(ss, cuda_device):
     _check_states(batch, sams, [0, 17, 33, 63])
 
 
-def test_long_rollout_sampled(ss, cuda_device):
+def test_long_rollout_all_sequences(ss, cuda_device):
     """B=256 histories log-uniform in [16k, 32k] (copy prob 0.5, spans 16-256):
-    prefill, then 512 steps of U{1..4} tokens + K=3 drafts.  The oracle follows
-    a sample of 8 sequences step by step (drafts at every step, states at the
-    end); every sequence must stay healthy."""
+    prefill, then 512 steps of U{1..4} tokens + K=3 drafts.  The oracle
+    follows all 256 sequences: drafts, draft lengths, match lengths and first
+    ends after every step, and the full state arrays and transition triples
+    of 32 of them at the end; every sequence must stay healthy."""
     w = workloads.long_rollout()
     B, V, K, steps = w["B"], w["V"], w["K"], w["steps"]
     lens, n_new, streams = w["lens"], w["n_new"], w["streams"]
@@ -129,24 +130,27 @@ def test_long_rollout_sampled(ss, cuda_device):
     for b in range(B):
         pre[b, :lens[b]] = streams[b][:lens[b]]
     batch.extend(_i32(pre, cuda_device), _i32(lens, cuda_device))
-    sample = [0, 31, 64, 101, 128, 170, 222, 255]
-    sams = {b: oracle.Sam(V) for b in sample}
-    for b in sample:
+    sams = [oracle.Sam(V) for _ in range(B)]
+    for b in range(B):
         sams[b].extend(streams[b][:lens[b]])
     pos = lens.astype(np.int64).copy()
-    toks = np.zeros((B, 4), np.int32)
+    toks = np.zeros((steps, B, 4), np.int32)
     for s in range(steps):
         for b in range(B):
             k = n_new[s, b]
-            toks[b, :k] = streams[b][pos[b]:pos[b] + k]
-        out = batch.step(_i32(toks, cuda_device), _i32(n_new[s], cuda_device), K)
-        for b in sample:
-            sams[b].extend(toks[b, :n_new[s, b]])
+            toks[s, b, :k] = streams[b][pos[b]:pos[b] + k]
         pos += n_new[s]
-        if s % 64 == 0 or s == steps - 1:
-            _check_drafts(out, sams, K, sample)
+    toks_d = _i32(toks, cuda_device)
+    nn_d = _i32(n_new, cuda_device)
+    for s in range(steps):
+        d, dl, ml, me = (t.cpu().numpy() for t in batch.step(toks_d[s], nn_d[s], K))
+        od, info = oracle.step_batch(sams, toks[s], n_new[s], K)
+        np.testing.assert_array_equal(dl, info[:, 0], err_msg=f"draft_len, step {s}")
+        np.testing.assert_array_equal(ml, info[:, 1], err_msg=f"match_len, step {s}")
+        np.testing.assert_array_equal(me, info[:, 2], err_msg=f"min_endpos, step {s}")
+        np.testing.assert_array_equal(d, od, err_msg=f"drafts, step {s}")
     assert (batch.status() == 0).all()
-    _check_states(batch, sams, sample)
+    _check_states(batch, sams, list(range(0, B, 8)))
 
 
 def test_errors_freeze_one_sequence(ss, cuda_device):

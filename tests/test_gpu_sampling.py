@@ -10,40 +10,15 @@ from scipy import stats
 
 import oracle
 import workloads
+from parity import BAND, compare_sampling, cut_ok
 
 pytestmark = pytest.mark.gpu
-
-BAND = 1e-6
 
 
 @pytest.fixture(scope="module")
 def ss(cuda_device):
     import sam_drafting_verification_gb300 as ss
     return ss
-
-
-def _probs(row, T):
-    x = row.astype(np.float64)
-    p = np.exp(x / T - (x / T).max())
-    return p / p.sum()
-
-
-def _cut_ok(row, T, k, top_p, tau_gpu, tau_oracle):
-    """(ok, excused): the GPU cut equals the oracle's, or lies within BAND of
-    the top-p boundary."""
-    if tau_gpu == tau_oracle or (np.isnan(tau_gpu) and np.isnan(tau_oracle)):
-        return True, False
-    if top_p >= 1.0:
-        return False, False
-    _, tau_k = oracle.truncate_row(row, T, k, 1.0)
-    x = row.astype(np.float64)
-    p = _probs(row, T)
-    kept_k = x >= tau_k
-    zk = p[kept_k].sum()
-    above = p[kept_k & (x > tau_gpu)].sum() / zk
-    incl = p[kept_k & (x >= tau_gpu)].sum() / zk
-    ok = tau_gpu >= tau_k and np.any(x == tau_gpu) and above < top_p + BAND and incl >= top_p - BAND
-    return bool(ok), True
 
 
 def _params(rng, B, V):
@@ -74,10 +49,10 @@ def test_cut_matches_oracle(ss, cuda_device, dtype, V):
                 assert tau[b, r] == -np.inf
                 continue
             _, to = oracle.truncate_row(rows[b, r], float(T[b]), int(k[b]), float(p[b]))
-            ok, ex = _cut_ok(rows[b, r], float(T[b]), int(k[b]), float(p[b]), float(tau[b, r]), to)
+            ok, ex = cut_ok(rows[b, r], float(T[b]), int(k[b]), float(p[b]), float(tau[b, r]), to)
             assert ok, (b, r, T[b], k[b], p[b], tau[b, r], to)
             excused += ex
-    assert excused <= 2, excused
+    assert excused <= int(1e-4 * B * R), excused
 
 
 def test_cut_bad_parameters_and_rows(ss, cuda_device):
@@ -89,46 +64,6 @@ def test_cut_bad_parameters_and_rows(ss, cuda_device):
     tau = ss.sampling_cut(logits, T, 5, p).cpu().numpy()
     assert np.isnan(tau[:5]).all()
     assert np.isfinite(tau[5, 0]) and tau[5, 1] == -np.inf
-
-
-def _compare(g, o, rows, draft, T, k, p, tau_g):
-    B, K1 = rows.shape[:2]
-    decisions = excused = 0
-    for b in range(B):
-        assert g["status"][b] == o["status"][b], b
-        if o["status"][b] != 0:
-            continue
-        Lg, Lo = int(g["accept_len"][b]), int(o["accept_len"][b])
-        # the emitted token is always inside the cut of its row
-        assert rows[b, Lg, g["out_token"][b]] >= tau_g[b, Lg], b
-        decisions += min(Lg, Lo) + 2
-        if Lg == Lo and g["out_token"][b] == o["out_token"][b]:
-            continue
-        other_side = False
-        for j in range(min(Lg, Lo) + 1):
-            ok, ex = _cut_ok(rows[b, j], float(T[b]), int(k[b]), float(p[b]), float(tau_g[b, j]),
-                             float(o["tau"][b, j]))
-            assert ok, (b, j)
-            other_side |= ex
-        if other_side:  # a top-p cut on the other side of its boundary
-            excused += 1
-            continue
-        if Lg != Lo:
-            j = min(Lg, Lo)
-            assert abs(o["u_acc"][b, j] - o["p_d"][b, j]) < BAND, (b, j, o["u_acc"][b, j], o["p_d"][b, j])
-        else:
-            pp, _ = oracle.truncate_row(rows[b, Lo], float(T[b]), int(k[b]), float(p[b]))
-            r = pp.copy()
-            if Lo < draft.shape[1]:
-                r[draft[b, Lo]] = max(0.0, r[draft[b, Lo]] - 1.0)
-            mass = r.sum()
-            tok = int(g["out_token"][b])
-            lo = r[:tok].sum() / mass
-            hi = lo + r[tok] / mass
-            assert r[tok] > 0 and lo - BAND <= o["u_res"][b] < hi + BAND, (b, tok, lo, hi, o["u_res"][b])
-        excused += 1
-    assert excused <= max(2, int(1e-4 * decisions) + 2), (excused, decisions)
-    return decisions, excused
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
@@ -148,7 +83,7 @@ def test_verify_sampling_matches_oracle(ss, cuda_device, dtype):
     g = {key: v.cpu().numpy() for key, v in g.items()}
     tau_g = ss.sampling_cut(tl.to(dev), *args).cpu().numpy()
     o = oracle.verify_sampling(rows, draft, None, T, k, p, seed=17, step=5)
-    _compare(g, o, rows, draft, T, k, p, tau_g)
+    compare_sampling(g, o, rows, draft, T, k, p, tau_g)
     assert (g["accept_len"] > 0).any()
     # emitted tokens: the accepted drafts, then the final token
     for b in range(B):
@@ -230,7 +165,7 @@ def _check_cuts(ss, dev, rows_bf16, T, k, p):
             if res is None:  # a row the verifier refuses
                 assert tau[b, r] == -np.inf, (b, r)
                 continue
-            ok, ex = _cut_ok(rows[b, r], float(T[b]), int(k[b]), float(p[b]), float(tau[b, r]), res[1])
+            ok, ex = cut_ok(rows[b, r], float(T[b]), int(k[b]), float(p[b]), float(tau[b, r]), res[1])
             assert ok, (b, r, T[b], k[b], p[b], tau[b, r], res[1])
             excused += ex
     return excused
@@ -288,7 +223,7 @@ def test_cut_bf16_many_equal_logits(ss, cuda_device, value):
     T = np.array([1.0, 0.8, 1.0], np.float32)
     k = np.array([50, 0, 70000], np.int32)
     p = np.array([0.9, 0.95, 1.0], np.float32)
-    assert _check_cuts(ss, cuda_device, rows, T, k, p) <= 1
+    assert _check_cuts(ss, cuda_device, rows, T, k, p) == 0
     const = np.full((2, 1, V), value if np.isfinite(value) else 0.5, np.float32)
     assert _check_cuts(ss, cuda_device, const, np.ones(2, np.float32), np.array([10, 0], np.int32),
                        np.array([0.5, 0.3], np.float32)) == 0
@@ -316,10 +251,10 @@ def test_cut_full_vocab_sampled(ss, cuda_device):
             assert tau[b, r] == -np.inf
             continue
         _, to = oracle.truncate_row(rows[b, r], float(T[b]), int(k[b]), float(p[b]))
-        ok, ex = _cut_ok(rows[b, r], float(T[b]), int(k[b]), float(p[b]), float(tau[b, r]), to)
+        ok, ex = cut_ok(rows[b, r], float(T[b]), int(k[b]), float(p[b]), float(tau[b, r]), to)
         assert ok, (b, r, tau[b, r], to)
         excused += ex
-    assert excused <= 1
+    assert excused == 0
 
 
 @pytest.mark.parametrize("V", [1, 2, 7, 8, 9])
@@ -331,4 +266,4 @@ def test_cut_bf16_tiny_vocabularies(ss, cuda_device, V):
     T = np.array([1.0, 0.5, 2.0, 1.0, 0.7, 1.0], np.float32)
     k = np.array([1, 2, 0, 3, 1, 0], np.int32)
     p = np.array([1.0, 0.9, 0.5, 0.3, 0.99, 0.01], np.float32)
-    assert _check_cuts(ss, cuda_device, rows, T, k, p) <= 1
+    assert _check_cuts(ss, cuda_device, rows, T, k, p) == 0

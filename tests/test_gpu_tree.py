@@ -8,6 +8,7 @@ import torch
 
 import oracle
 import workloads
+from parity import compare_trees
 
 pytestmark = pytest.mark.gpu
 
@@ -46,46 +47,6 @@ def random_trees(rng, logits, N, width):
     return tok, fc, ns
 
 
-def _children(fc, ns, n):
-    out, c = [], fc[n]
-    while c != -1:
-        out.append(int(c))
-        c = ns[c]
-    return out
-
-
-def compare_trees(g, o, rows, tok, fc, ns, T):
-    B = len(o["status"])
-    decisions = excused = 0
-    for b in range(B):
-        assert g["status"][b] == o["status"][b], b
-        if o["status"][b] != 0:
-            continue
-        Lg, Lo = int(g["accept_len"][b]), int(o["accept_len"][b])
-        pg, po = list(g["path"][b, :Lg]), list(o["path"][b, :Lo])
-        decisions += min(Lg, Lo) + 2
-        if pg == po and g["out_token"][b] == o["out_token"][b]:
-            # the emitted tokens: the path's tokens, then the out token
-            assert list(g["emit"][b, :Lg + 1]) == [int(tok[b, n]) for n in pg] + [int(o["out_token"][b])]
-            continue
-        assert T > 0, f"greedy tree differs at b={b}"
-        d = 0
-        while d < min(Lg, Lo) and pg[d] == po[d]:
-            d += 1
-        node = 0 if d == 0 else po[d - 1]
-        kids = _children(fc[b], ns[b], node)
-        acc, lo, hi, _ = oracle.tree_node_info(rows[b, node], T, [int(tok[b, c]) for c in kids],
-                                               int(g["out_token"][b]))
-        ua, ur = oracle.uniforms(21, 3, b, d)
-        if d < Lg or d < Lo:  # the depths' coin against a running sum
-            assert any(abs(ua - a) < BAND for a in acc), (b, d, ua, acc)
-        else:  # same path, different final token
-            assert lo - BAND <= ur < hi + BAND, (b, ur, lo, hi)
-        excused += 1
-    assert excused <= max(1, int(1e-4 * decisions) + 1), (excused, decisions)
-    return decisions, excused
-
-
 @pytest.mark.parametrize("T", [0.0, 0.7, 1.0])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_random_trees(ss, cuda_device, T, dtype):
@@ -100,7 +61,7 @@ def test_random_trees(ss, cuda_device, T, dtype):
                             step=3, debug=True)
     g = {k: v.cpu().numpy() for k, v in g.items()}
     o = oracle.tree_verify(rows, tok, fc, ns, temperature=T, seed=21, step=3)
-    compare_trees(g, o, rows, tok, fc, ns, T)
+    compare_trees(g, o, rows, tok, fc, ns, T, seed=21, step=3)
     if T == 0.0:
         assert (g["accept_len"] > 0).any()
 

@@ -90,11 +90,17 @@ def boost_truth(logits: np.ndarray, truth: np.ndarray, amount: float) -> None:
 
 def round_bf16(x: np.ndarray) -> np.ndarray:
     """fp32 values rounded to the nearest bf16 (ties to even), returned as
-    fp32; NaN stays NaN.  The numpy twin of to_bf16(x).float()."""
-    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    r = ((b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) & np.uint32(0xFFFF0000))
-    r = np.where(np.isnan(x), b | np.uint32(0x00400000), r).astype(np.uint32)
-    return r.view(np.float32)
+    fp32; NaN becomes the canonical quiet NaN.  The numpy twin of
+    to_bf16(x).float()."""
+    b = np.array(x, dtype=np.float32, copy=True).view(np.uint32)
+    nan = (b & np.uint32(0x7FFFFFFF)) > np.uint32(0x7F800000)
+    lsb = b >> np.uint32(16)
+    lsb &= np.uint32(1)
+    b += np.uint32(0x7FFF)
+    b += lsb
+    b &= np.uint32(0xFFFF0000)
+    b[nan] = np.uint32(0x7FC00000)
+    return b.view(np.float32)
 
 
 def to_bf16(x: np.ndarray):
