@@ -247,11 +247,17 @@ class SamBatch:
 
 
 _ws_cache = {}
+# workspaces replaced in the cache by a larger one: kept allocated, since a
+# CUDA graph captured with the smaller one may still be replayed
+_ws_retired = []
 
 
 def verify_workspace(B: int, K: int, V: int, device=None, sampling: bool = False):
     """A zero-initialised verification workspace, cached per (device, stream);
-    sampling=True sizes it for spec_verify_sampling."""
+    sampling=True sizes it for spec_verify_sampling.  A cached workspace is
+    never freed (a larger need replaces it in the cache only), so graphs
+    captured with it stay valid; a workspace the caller allocates must stay
+    allocated while any graph that uses it can still be replayed."""
     lib = _b.lib()
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
     need = int(lib.spec_verify_sampling_workspace_bytes(B, K, V) if sampling
@@ -259,6 +265,8 @@ def verify_workspace(B: int, K: int, V: int, device=None, sampling: bool = False
     key = (dev.index, torch.cuda.current_stream(dev).cuda_stream)
     ws = _ws_cache.get(key)
     if ws is None or ws.numel() < need:
+        if ws is not None:
+            _ws_retired.append(ws)
         ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
         _b.check(lib.spec_verify_workspace_init(_ptr(ws), ws.numel(), _stream(dev)),
                  "spec_verify_workspace_init")

@@ -70,6 +70,7 @@ constexpr int kMaxChunks = 48;
 constexpr int kMaxChunksDraft = 32;  // with draft logits: both arrays' records must fit
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait (default)
 constexpr uint64_t kDrainNs = 2000000000ull;  // 2 s for copies in flight to land after an abort
+constexpr uint32_t kSuspendNs = 20000;  // longest suspension of one producer wait on a stage
 // the pipeline waits' limit for launches made from now on (test hook)
 std::atomic<uint64_t> g_wait_ns{kWaitNs};
 constexpr size_t kVerifyWorkspaceBytes = 256;  // work counters: claims, exits, error bits
@@ -109,10 +110,16 @@ struct VParams {
   const float* tau;
 };
 
-struct Tag {
-  int32_t slot, kind, chunk, nel, elem0, has_draft, b, j;
-  int32_t dtok;  // the row's draft token (statistics pass of a drafted row), else -1
-  int32_t pad[3];
+struct __align__(16) Tag {
+  // the consumers' words first: job kind; record index of (slot, tile, warp
+  // 0); warp slices wholly inside the tile, and with any element of it
+  int32_t kind, rbase, nfull, nany;
+  // the warp whose slice holds the row's draft token (statistics pass of a
+  // drafted row; -1: none in this tile) and the token's index in the tile
+  int32_t dwarp, dtile, slot, chunk;
+  int32_t nel, elem0, has_draft, b;
+  int32_t j, dtok;  // the row's draft token (statistics pass of a drafted row), else -1
+  int32_t pad[2];
 };
 
 struct Slot {
@@ -271,6 +278,20 @@ __device__ __forceinline__ DF split_warp_sum(float v) {
   const float sum = ah + small;
   const float bb = sum - ah;
   return {sum, (ah - (sum - bb)) + (small - bb)};
+}
+// Warp sum of lane values in [0, 32] whose total is at least 1/2, as a float
+// pair: each value is rounded to a multiple of 2^-26 (exact for values of at
+// least 1/8, at most 2^-27 off below that), and the integers are summed
+// exactly in two 16-bit halves, one warp reduction each.  The total is off by
+// at most 2^-22, a relative 2^-21.
+__device__ __forceinline__ DF fixed_warp_sum(float v) {
+  const uint32_t k = __float2uint_rn(v * 0x1p26f);
+  const uint32_t kh = __reduce_add_sync(kFullMask, k >> 16);     // < 2^20
+  const uint32_t kl = __reduce_add_sync(kFullMask, k & 0xFFFFu);  // < 2^21
+  const float hi = (float)kh * 0x1p-10f;  // both exact
+  const float lo = (float)kl * 0x1p-26f;
+  const float sum = hi + lo;  // hi > 1/4 > lo: the error of the add is exact
+  return {sum, lo - (sum - hi)};
 }
 // NaN-propagating warp maximum in one warp reduction instruction
 __device__ __forceinline__ float warp_max_nan(float v) {
@@ -528,7 +549,9 @@ __device__ __forceinline__ float packed_exp_sum(const Slice<TT, DT>& s, float cT
 // Records of one row combine by exact power-of-two scaling 2^(R - max R), so no
 // per-record exponential enters the row's masses.  The element with tile index
 // `excl` (the row's draft token, added back exactly by the control warp) is
-// left out.  An all -inf slice gives {-inf, -inf, 0, 0}; NaN gives NaNs.
+// left out; the caller passes it to the warp whose slice holds it only, and
+// -1 to the others.  An all -inf slice gives {-inf, -inf, 0, 0}; NaN gives
+// NaNs.
 template <int TT, int DT, bool FULL, bool DRAFT_ARRAY, bool MULTI = false, bool THR = false>
 __device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, int lane, int nel,
                                                  float cT, int excl, uint64_t xm = 0,
@@ -537,19 +560,24 @@ __device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, 
   const float NEG_INF = -__int_as_float(0x7f800000);
   const float QNAN = __int_as_float(0x7fc00000);
   const float m = warp_max_nan(lane_max<TT, DT, FULL, DRAFT_ARRAY>(s, w, lane, nel));
-  if (m != m) return make_float4(QNAN, QNAN, QNAN, QNAN);
-  if (m == NEG_INF) return make_float4(NEG_INF, NEG_INF, 0.f, 0.f);
+  if (!(m > NEG_INF))
+    return m != m ? make_float4(QNAN, QNAN, QNAN, QNAN) : make_float4(NEG_INF, NEG_INF, 0.f, 0.f);
   const float R = ceilf(m * cT);
   float z;
-  // `excl`: one element left out (slice-relative id, or -1).  MULTI: xm marks
-  // the lane's elements left out (bit i * VEC + k), e.g. a tree node's
-  // children; the warp takes the masked path if any lane has one
-  const bool single = excl >= w * C::SL && excl < (w + 1) * C::SL;
+  // `excl`: one element left out (tile index, or -1).  MULTI: xm marks the
+  // lane's elements left out (bit i * VEC + k), e.g. a tree node's children;
+  // the warp takes the masked path if any lane has one
+  const bool single = excl >= 0;
   const bool has_excl = single || (MULTI && __any_sync(kFullMask, xm != 0));
   // THR: logits below tau (a per-request cut) are left out too
   const bool cut = THR && tau > NEG_INF;
   if (FULL && !has_excl && !cut) {
+    // the slice's maximum is in the sum: its term is in (1/2, 1], so the
+    // total is at least 1/2 and each lane's at most its element count
+    static_assert(C::SL / 32 <= 32, "at most 32 elements per lane");
     z = packed_exp_sum<TT, DT, DRAFT_ARRAY, false>(s, cT, R, 0);
+    const DF zz = fixed_warp_sum(z);
+    return make_float4(m, R, zz.hi, zz.lo);
   } else if (THR && FULL && !has_excl) {
     z = packed_exp_sum<TT, DT, DRAFT_ARRAY, false, true>(s, cT, R, 0, tau);
   } else if (MULTI && FULL && !single) {
@@ -1454,9 +1482,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       const unsigned char* stage = stages + (size_t)cs * kStageBytes;
       // a row's last tile is partial: slices past its end hold nothing (their
       // records are empty), slices wholly inside it take the unmasked path
-      const int wbeg = warp * C::SL;
-      const bool none = wbeg >= tg.nel;
-      const bool full = wbeg + C::SL <= tg.nel;
+      const bool none = warp >= tg.nany;
+      const bool full = warp < tg.nfull;
       Slice<TT, DT> sl;
       if (!none) load_slice_tile<TT, DT>(sl, P, stage, tg, warp, lane);
       __syncwarp();
@@ -1478,7 +1505,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         } else {
           // one-hot drafts: the row's draft token is left out of the sums
           // (tile index, or -1), so the residual of a rejection is exact
-          const int ex = (DT < 0 && tg.dtok >= 0) ? tg.dtok - tg.elem0 : -1;
+          const int ex = (DT < 0 && warp == tg.dwarp) ? tg.dtile : -1;
           if (TREE) {
             // a tree node's children are left out of the sums: the lane
             // holding one keeps its logit and marks it in its mask
@@ -1523,36 +1550,34 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         r.a = full ? reduce_resid<TT, DT, true>(sl, warp, lane, tg.nel, S, P.cT)
                    : reduce_resid<TT, DT, false>(sl, warp, lane, tg.nel, S, P.cT);
       }
-      if (tg.dtok >= 0 && !none) {
+      if (warp == tg.dwarp) {
         // the lane holding the draft token keeps its logits for the decision
-        const int o = tg.dtok - tg.elem0 - warp * C::SL;
-        if (o >= 0 && o < C::SL && o + warp * C::SL < tg.nel) {
-          const int v = o / C::VEC, kk = o % C::VEC;
-          if ((v & 31) == lane) {
-            const int ii = v >> 5;
-            float x = 0.f, g = 0.f;
+        const int o = tg.dtile - warp * C::SL;
+        const int v = o / C::VEC, kk = o % C::VEC;
+        if ((v & 31) == lane) {
+          const int ii = v >> 5;
+          float x = 0.f, g = 0.f;
 #pragma unroll
-            for (int i = 0; i < C::VPL; ++i)
+          for (int i = 0; i < C::VPL; ++i)
 #pragma unroll
-              for (int k = 0; k < C::VEC; ++k)
-                if (i == ii && k == kk) {
-                  x = sl.t[i].at(k);
-                  if (DT >= 0 && tg.has_draft) g = sl.d[i].at(k);
-                }
-            if (G == 1) {
-              S.xd = x;
-              S.gd = g;
-            } else {  // the leader's slot takes the decision
-              st_cluster_u32(cluster_map(&S.xd, 0), __float_as_uint(x));
-              st_cluster_u32(cluster_map(&S.gd, 0), __float_as_uint(g));
-              fence_cluster();
-            }
+            for (int k = 0; k < C::VEC; ++k)
+              if (i == ii && k == kk) {
+                x = sl.t[i].at(k);
+                if (DT >= 0 && tg.has_draft) g = sl.d[i].at(k);
+              }
+          if (G == 1) {
+            S.xd = x;
+            S.gd = g;
+          } else {  // the leader's slot takes the decision
+            st_cluster_u32(cluster_map(&S.xd, 0), __float_as_uint(x));
+            st_cluster_u32(cluster_map(&S.gd, 0), __float_as_uint(g));
+            fence_cluster();
           }
         }
       }
       __syncwarp();
       if (lane == 0) {
-        const size_t ri = ((size_t)tg.slot * P.NC + tg.chunk) * kCW + warp;
+        const int ri = tg.rbase + warp;
         // release: the record (and the captured logits) before the arrival
         if (G == 1) {
           rec[ri] = r.a;
@@ -1612,7 +1637,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         // clusters: this CTA streams the job's tiles c = rank (mod G)
         for (int c = (int)crank; c < P.NC && ok; c += G) {
           const uint64_t t0 = gtimer();
-          while (!mbar_try_wait(&sm.empty[ps], pph ^ 1)) {
+          // (suspended on the barrier, not spinning: the consumers need the issue slots)
+          while (!mbar_try_wait_hint(&sm.empty[ps], pph ^ 1, kSuspendNs)) {
             if (vload(&sm.abort) || gtimer() - t0 > P.wait_ns) {
               ok = false;
               break;
@@ -1631,6 +1657,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
           tg.b = b;
           tg.j = j;
           tg.dtok = kind == kStats ? S.dtok : -1;
+          tg.rbase = (si * P.NC + c) * kCW;
+          tg.nfull = nel / C::SL;
+          tg.nany = (nel + C::SL - 1) / C::SL;
+          tg.dtile = tg.dtok >= 0 ? tg.dtok - elem0 : -1;
+          tg.dwarp = (tg.dtile >= 0 && tg.dtile < nel) ? tg.dtile / C::SL : -1;
           unsigned char* dst = stages + (size_t)ps * kStageBytes;
           if (P.direct) {
             mbar_arrive(&sm.full[ps]);
