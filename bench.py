@@ -66,8 +66,12 @@ HEAD_MIN_TIMED_MS = 500.0
 # verify kernel from one ncu capture of each workload, with the SHA-256 of
 # verify.cu it was taken on: a changed kernel reports null until captured again.
 VERIFY_TRAFFIC = {
-    "rs_bf16_b64": {"bytes": 19537920.0,
-                    "verify_cu_sha256": "bbb652d498d8e15843e7c24655bb1eb7a46a9b7e25e1c39905f50390e090f3fe"},
+    "verify_b1024_k3_bf16_t1": {"bytes": 317728512.0,
+                                "verify_cu_sha256": "78bb5cb14fda415bf29fadeab76b1a4d0858e5cf19ce413dd742ee60b86a061d"},
+    "draft_model_b32": {"bytes": 85977856.0,
+                        "verify_cu_sha256": "78bb5cb14fda415bf29fadeab76b1a4d0858e5cf19ce413dd742ee60b86a061d"},
+    "rs_bf16_b64": {"bytes": 19553536.0,
+                    "verify_cu_sha256": "78bb5cb14fda415bf29fadeab76b1a4d0858e5cf19ce413dd742ee60b86a061d"},
     "long_rollout_b256": {"bytes": 78981542.0,
                           "verify_cu_sha256": "501dfc92dfa938d5aaadc35a389107c2249f8a4a90a8c3e282f45d804219eb47"},
     "tree_b256": {"bytes": 161624064.0,
