@@ -75,7 +75,9 @@ constexpr uint32_t kSuspendNs = 20000;  // longest suspension of one producer wa
 std::atomic<uint64_t> g_wait_ns{kWaitNs};
 constexpr size_t kVerifyWorkspaceBytes = 256;  // work counters: claims, exits, error bits
 
-enum Kind : int32_t { kStats = 0, kResid = 1, kExit = 3 };
+// kSkip: a tile requested ahead for a job that did not come (its stage is
+// released unread)
+enum Kind : int32_t { kStats = 0, kResid = 1, kSkip = 2, kExit = 3 };
 enum State : int32_t { kEmpty = 0, kReady = 1, kIssued = 2 };
 
 struct VParams {
@@ -1478,6 +1480,15 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       }
       const Tag tg = sm.tag[cs];
       if (tg.kind == kExit) break;
+      if (tg.kind == kSkip) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[cs]);
+        if (++cs == NS) {
+          cs = 0;
+          cph ^= 1;
+        }
+        continue;
+      }
       Slot& S = sm.slot[tg.slot];
       const unsigned char* stage = stages + (size_t)cs * kStageBytes;
       // a row's last tile is partial: slices past its end hold nothing (their
@@ -1600,6 +1611,28 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
     if (lane == 0) {
       int ps = 0;
       uint32_t pph = 0;
+      // Row 0 of the CTA's first sequence is read whatever its drafts are (it
+      // scores draft 0, or it is the bonus row), so its first tiles are
+      // requested at once, before the control warp has claimed the sequence
+      // and loaded its drafts.  Their stages are published (tag, then the
+      // producer's arrival) when the job is posted; if another job comes
+      // first (the sequence's drafts were bad), they are released unread.
+      int npre = 0;
+      const int b0 = (int)(blockIdx.x / G);
+      if (DT < 0 && !TREE && !SAMP && !P.direct && b0 < P.B) {
+        const int mine = (P.NC - (int)crank + G - 1) / G;
+        npre = mine < NS ? mine : NS;
+        for (int i = 0; i < npre; ++i) {
+          const int elem0 = ((int)crank + i * G) * C::E_TILE;
+          const uint32_t bt = (uint32_t)min(C::E_TILE, P.V - elem0) * C::ST;
+          const size_t rt = (size_t)b0 * (P.K + 1) * (size_t)P.V + elem0;
+          mbar_expect_tx(&sm.full[i], bt);
+          bulk_g2s(stages + (size_t)i * kStageBytes, P.target + rt * C::ST, bt, &sm.full[i]);
+          sm.stage_parity[i] = 0;
+        }
+        ps = npre == NS ? 0 : npre;
+        pph = npre == NS ? 1u : 0u;
+      }
       uint64_t t_idle = gtimer();
       for (;;) {
         if (vload(&sm.abort)) break;
@@ -1633,21 +1666,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         // statistics, and the residual pass
         const bool with_draft =
             DT >= 0 && ((kind == kStats && j < S.nb) || (kind == kResid && S.smode == 1));
-        bool ok = true;
-        // clusters: this CTA streams the job's tiles c = rank (mod G)
-        for (int c = (int)crank; c < P.NC && ok; c += G) {
-          const uint64_t t0 = gtimer();
-          // (suspended on the barrier, not spinning: the consumers need the issue slots)
-          while (!mbar_try_wait_hint(&sm.empty[ps], pph ^ 1, kSuspendNs)) {
-            if (vload(&sm.abort) || gtimer() - t0 > P.wait_ns) {
-              ok = false;
-              break;
-            }
-          }
-          if (!ok) break;
+        auto set_tag = [&](Tag& tg, int c) {
           const int elem0 = c * C::E_TILE;
           const int nel = min(C::E_TILE, P.V - elem0);
-          Tag& tg = sm.tag[ps];
           tg.slot = si;
           tg.kind = kind;
           tg.chunk = c;
@@ -1662,6 +1683,34 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
           tg.nany = (nel + C::SL - 1) / C::SL;
           tg.dtile = tg.dtok >= 0 ? tg.dtok - elem0 : -1;
           tg.dwarp = (tg.dtile >= 0 && tg.dtile < nel) ? tg.dtile / C::SL : -1;
+        };
+        bool ok = true;
+        int c_from = (int)crank;
+        if (npre > 0) {
+          // the tiles requested ahead: this job's if it is that row, else none
+          const bool match = si == 0 && kind == kStats && b == b0 && j == 0;
+          for (int i = 0; i < npre; ++i) {
+            if (match) set_tag(sm.tag[i], (int)crank + i * G);
+            else sm.tag[i].kind = kSkip;
+            mbar_arrive(&sm.full[i]);  // release: the tag before the arrival
+          }
+          if (match) c_from = (int)crank + npre * G;
+          npre = 0;
+        }
+        // clusters: this CTA streams the job's tiles c = rank (mod G)
+        for (int c = c_from; c < P.NC && ok; c += G) {
+          const uint64_t t0 = gtimer();
+          // (suspended on the barrier, not spinning: the consumers need the issue slots)
+          while (!mbar_try_wait_hint(&sm.empty[ps], pph ^ 1, kSuspendNs)) {
+            if (vload(&sm.abort) || gtimer() - t0 > P.wait_ns) {
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          const int elem0 = c * C::E_TILE;
+          const int nel = min(C::E_TILE, P.V - elem0);
+          set_tag(sm.tag[ps], c);
           unsigned char* dst = stages + (size_t)ps * kStageBytes;
           if (P.direct) {
             mbar_arrive(&sm.full[ps]);
@@ -1688,6 +1737,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         }
         vstore(&sm.jobs_issued, vload(&sm.jobs_issued) + 1);
         t_idle = gtimer();
+      }
+      // tiles requested ahead for a job that never came: released unread (and,
+      // after an abort, their copies complete the stages' phases for the drain)
+      for (int i = 0; i < npre; ++i) {
+        sm.tag[i].kind = kSkip;
+        mbar_arrive(&sm.full[i]);
       }
       if (!vload(&sm.abort)) {
         // tell the consumers to stop
