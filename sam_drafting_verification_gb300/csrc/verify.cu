@@ -1458,6 +1458,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
   __syncthreads();
   // clusters: no CTA writes into another's shared memory before it is set up
   if (G > 1) cluster_sync_all();
+  // programmatic dependent launch: the next kernel on the stream may start
+  // its own set-up now; this one touches global memory only once the
+  // kernel before it has completed and its writes are visible
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp < kCW) {
     // ------------------------------ consumers ------------------------------
@@ -1994,11 +1999,26 @@ int launch(const VParams& P0, cudaStream_t stream) {
     if (clusters < 1) G = 1;
   }
   P.G = G;
+  // launched with programmatic stream serialisation: the kernel's set-up
+  // (shared memory, barriers) overlaps the previous kernel's tail, and
+  // griddepcontrol.wait orders every global access after it
+  cudaLaunchAttribute pattr[2];
+  pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pattr[0].val.programmaticStreamSerializationAllowed = 1;
   if (G == 1) {
     const int grid = P.B < sms[dev] ? P.B : sms[dev];
-    kernel<<<grid, kThreads, smem, stream>>>(P);
-    return cudaGetLastError() == cudaSuccess ? SAMSPEC_OK : SAMSPEC_ECUDA;
+    cudaLaunchConfig_t c1 = {};
+    c1.gridDim = dim3((unsigned)grid, 1, 1);
+    c1.blockDim = dim3(kThreads, 1, 1);
+    c1.dynamicSmemBytes = smem;
+    c1.stream = stream;
+    c1.attrs = pattr;
+    c1.numAttrs = 1;
+    return cudaLaunchKernelEx(&c1, kernel, P) == cudaSuccess ? SAMSPEC_OK : SAMSPEC_ECUDA;
   }
+  pattr[1] = attr[0];
+  cfg.attrs = pattr;
+  cfg.numAttrs = 2;
   cfg.gridDim = dim3((unsigned)(clusters * G), 1, 1);
   return cudaLaunchKernelEx(&cfg, ckernel, P) == cudaSuccess ? SAMSPEC_OK : SAMSPEC_ECUDA;
 }
