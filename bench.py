@@ -66,16 +66,16 @@ HEAD_MIN_TIMED_MS = 500.0
 # verify kernel from one ncu capture of each workload, with the SHA-256 of
 # verify.cu it was taken on: a changed kernel reports null until captured again.
 VERIFY_TRAFFIC = {
-    "verify_b1024_k3_bf16_t1": {"bytes": 317728512.0,
-                                "verify_cu_sha256": "78bb5cb14fda415bf29fadeab76b1a4d0858e5cf19ce413dd742ee60b86a061d"},
-    "draft_model_b32": {"bytes": 85977856.0,
-                        "verify_cu_sha256": "78bb5cb14fda415bf29fadeab76b1a4d0858e5cf19ce413dd742ee60b86a061d"},
-    "rs_bf16_b64": {"bytes": 19553536.0,
-                    "verify_cu_sha256": "78bb5cb14fda415bf29fadeab76b1a4d0858e5cf19ce413dd742ee60b86a061d"},
-    "long_rollout_b256": {"bytes": 78981542.0,
-                          "verify_cu_sha256": "501dfc92dfa938d5aaadc35a389107c2249f8a4a90a8c3e282f45d804219eb47"},
-    "tree_b256": {"bytes": 161624064.0,
-                  "verify_cu_sha256": "501dfc92dfa938d5aaadc35a389107c2249f8a4a90a8c3e282f45d804219eb47"},
+    "verify_b1024_k3_bf16_t1": {"bytes": 317673472.0,
+                                "verify_cu_sha256": "12b899faba6a4af792b10afb9438adb117549545eadc593131aa3b4ed7fe117f"},
+    "draft_model_b32": {"bytes": 86244096.0,
+                        "verify_cu_sha256": "12b899faba6a4af792b10afb9438adb117549545eadc593131aa3b4ed7fe117f"},
+    "rs_bf16_b64": {"bytes": 19560960.0,
+                    "verify_cu_sha256": "12b899faba6a4af792b10afb9438adb117549545eadc593131aa3b4ed7fe117f"},
+    "long_rollout_b256": {"bytes": 78972940.8,
+                          "verify_cu_sha256": "12b899faba6a4af792b10afb9438adb117549545eadc593131aa3b4ed7fe117f"},
+    "tree_b256": {"bytes": 161305088.0,
+                  "verify_cu_sha256": "12b899faba6a4af792b10afb9438adb117549545eadc593131aa3b4ed7fe117f"},
 }
 # the same for the sampling cut kernel (sampling.cu)
 CUT_TRAFFIC = {"sampling_b256": {"bytes": 277559040.0,
