@@ -891,7 +891,9 @@ struct Control {
         b = first_ ? blockIdx.x / G
                    : ncl >= (uint32_t)P.B ? (uint32_t)P.B : ncl + atomicAdd(&P.ws[0], 1u);
         vstore(&sm.pool_left, b >= (uint32_t)P.B ? 0 : P.B - 1 - (int)b);
-        if (b >= (uint32_t)P.B) vstore(&sm.pool_done, 1);
+        // no sequence left: none beyond this one either when the clusters
+        // cover the batch, so the slots leave without another claim
+        if (b >= (uint32_t)P.B || ncl >= (uint32_t)P.B) vstore(&sm.pool_done, 1);
       }
       first_ = false;
       b = __shfl_sync(kFullMask, b, 0);
@@ -1658,7 +1660,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
             set_abort(sm, G);
             break;
           }
-          __nanosleep(128);
+          __nanosleep(32);
           continue;
         }
         vstore(&sm.prod_idle, 0);
