@@ -1470,9 +1470,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
     // ------------------------------ consumers ------------------------------
     int cs = 0;
     uint32_t cph = 0;
+    bool nxt_ready = false;  // the next stage was seen full before this slice's record
     for (;;) {
       bool ok = true;
-      if (!mbar_try_wait(&sm.full[cs], cph)) {
+      if (!nxt_ready && !mbar_try_wait(&sm.full[cs], cph)) {
         const uint64_t t0 = gtimer();
         while (!mbar_try_wait(&sm.full[cs], cph)) {
           if (vload(&sm.abort) || gtimer() - t0 > P.wait_ns) {
@@ -1488,6 +1489,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       const Tag tg = sm.tag[cs];
       if (tg.kind == kExit) break;
       if (tg.kind == kSkip) {
+        nxt_ready = false;
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[cs]);
         if (++cs == NS) {
@@ -1592,6 +1594,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
             fence_cluster();
           }
         }
+      }
+      if (!CL) {
+        // streaming batches: test the next stage now, so that the loop's
+        // next wait costs nothing when its tile has landed (small batches,
+        // whose next tile is rarely there yet, skip the extra test)
+        const int ncs = cs + 1 == NS ? 0 : cs + 1;
+        nxt_ready = mbar_test_wait(&sm.full[ncs], cs + 1 == NS ? cph ^ 1u : cph);
       }
       __syncwarp();
       if (lane == 0) {
