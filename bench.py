@@ -66,16 +66,16 @@ HEAD_MIN_TIMED_MS = 500.0
 # verify kernel from one ncu capture of each workload, with the SHA-256 of
 # verify.cu it was taken on: a changed kernel reports null until captured again.
 VERIFY_TRAFFIC = {
-    "verify_b1024_k3_bf16_t1": {"bytes": 317673472.0,
-                                "verify_cu_sha256": "12b899faba6a4af792b10afb9438adb117549545eadc593131aa3b4ed7fe117f"},
-    "draft_model_b32": {"bytes": 86244096.0,
-                        "verify_cu_sha256": "12b899faba6a4af792b10afb9438adb117549545eadc593131aa3b4ed7fe117f"},
-    "rs_bf16_b64": {"bytes": 19560960.0,
-                    "verify_cu_sha256": "12b899faba6a4af792b10afb9438adb117549545eadc593131aa3b4ed7fe117f"},
-    "long_rollout_b256": {"bytes": 78972940.8,
-                          "verify_cu_sha256": "12b899faba6a4af792b10afb9438adb117549545eadc593131aa3b4ed7fe117f"},
-    "tree_b256": {"bytes": 161305088.0,
-                  "verify_cu_sha256": "12b899faba6a4af792b10afb9438adb117549545eadc593131aa3b4ed7fe117f"},
+    "verify_b1024_k3_bf16_t1": {"bytes": 317836288.0,
+                                "verify_cu_sha256": "e72e93e289bbda6ee3198e2aaff0215d3b173d7df9db56d7f7aac01ffb0f797c"},
+    "draft_model_b32": {"bytes": 85797888.0,
+                        "verify_cu_sha256": "e72e93e289bbda6ee3198e2aaff0215d3b173d7df9db56d7f7aac01ffb0f797c"},
+    "rs_bf16_b64": {"bytes": 19565312.0,
+                    "verify_cu_sha256": "e72e93e289bbda6ee3198e2aaff0215d3b173d7df9db56d7f7aac01ffb0f797c"},
+    "long_rollout_b256": {"bytes": 78968601.60000001,
+                          "verify_cu_sha256": "e72e93e289bbda6ee3198e2aaff0215d3b173d7df9db56d7f7aac01ffb0f797c"},
+    "tree_b256": {"bytes": 161445632.0,
+                  "verify_cu_sha256": "e72e93e289bbda6ee3198e2aaff0215d3b173d7df9db56d7f7aac01ffb0f797c"},
 }
 # the same for the sampling cut kernel (sampling.cu)
 CUT_TRAFFIC = {"sampling_b256": {"bytes": 277559040.0,
