@@ -116,6 +116,24 @@ __device__ __forceinline__ void st_cluster_f32x4(uint32_t addr, float4 v) {
                "f"(v.y), "f"(v.z), "f"(v.w)
                : "memory");
 }
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+// fetch-and-add at cluster scope, acquire and release: the adders' earlier
+// stores are visible to whoever adds after them
+__device__ __forceinline__ uint32_t atom_add_acq_rel_cluster_u32(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cluster.shared::cluster.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(addr), "r"(v)
+               : "memory");
+  return old;
+}
 __device__ __forceinline__ void red_cluster_add_u32(uint32_t addr, uint32_t v) {
   asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v)
                : "memory");

@@ -172,6 +172,10 @@ struct Smem {
   int32_t pool_done;    // a claim found no sequence left: idle slots leave
   uint64_t tile_bar[kSlots][kMaxChunks];  // one phase per job: the kCW records of a tile
   float4 pre[kSlots][kMaxChunks][2];     // control: mass before each tile {hi, lo, ref, 0}
+                                         // (clusters: first the tile's summary)
+  // clusters: the tile's warps that have stored their records (the last one
+  // merges them; its summary goes to the leader's `pre` entry of the tile)
+  uint32_t tcnt[kSlots][kMaxChunks];
 };
 
 // Sets this CTA's abort flag, and (clusters) every other CTA's of the cluster.
@@ -705,6 +709,46 @@ __device__ __forceinline__ float warp_incl_scan_f(float v, int lane) {
 }
 
 // ---- control warp ------------------------------------------------------------
+// Clusters: which side merges a tile's kCW records.  With fp32 targets, or a
+// draft array to merge as well, tiles complete faster than one control warp
+// merges them, so the tile's last consumer warp does it (records stay in the
+// streaming CTA).  bf16 one-hot rows keep the control warp's merge (records
+// go to the leader): there the extra work in the consumers costs more.
+template <int TT, int DT, bool CL>
+__host__ __device__ constexpr bool consumers_merge() {
+  return CL && (TT == 0 || DT >= 0);
+}
+
+// ---- tile summaries: the warp-wide part of merging a tile's kCW records ----
+// Lane w < kCW holds record w of the tile, the other lanes a neutral record.
+// Softmax array: {max logit, max reference Rc, the tile's mass in units 2^Rc
+// as a float pair}, the max logit NaN when a record holds a NaN (it makes the
+// row bad whatever the maxima are).
+__device__ __forceinline__ float4 softmax_tile_summary(float4 r) {
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const bool nan = __any_sync(kFullMask, r.x != r.x || r.z != r.z);
+  const float mc = nan ? __int_as_float(0x7fc00000) : warp_max_nan(r.x);
+  const float Rc = warp_max_nan(r.y);
+  DF v = {0.f, 0.f};
+  if (Rc != NEG_INF && r.z != 0.f) v = df_scale(DF{r.z, r.w}, (int)(r.y - Rc));
+  const DF t = df_warp_sum(v);
+  return make_float4(mc, Rc, t.hi, t.lo);
+}
+// Greedy: {tile max M, first slice holding M, 1 if a record saw a NaN, 0}.
+__device__ __forceinline__ float4 greedy_tile_summary(float4 r, int lane) {
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const float m = lane < kCW ? r.x : NEG_INF;
+  const bool nan = __any_sync(kFullMask, lane < kCW && r.z != 0.f);
+  const float M = warp_max_nan(m);
+  const unsigned h = __ballot_sync(kFullMask, lane < kCW && m == M);
+  return make_float4(M, (float)(h ? __ffs(h) - 1 : 0), nan ? 1.f : 0.f, 0.f);
+}
+// Residual pass: the tile's residual mass as a float pair {hi, lo, 0, 0}.
+__device__ __forceinline__ float4 resid_tile_summary(float4 r, int lane) {
+  const DF t = df_warp_sum(lane < kCW ? DF{r.x, r.y} : DF{0.f, 0.f});
+  return make_float4(t.hi, t.lo, 0.f, 0.f);
+}
+
 // Records of a slot are indexed r = c * kCW + w (tile c, warp slice w); a
 // merge of tile c gives lane w < kCW the record (c, w).
 
@@ -754,11 +798,20 @@ struct Control {
   }
   __device__ float tau_() const { return SAMP ? sm.slot[si].tau : -__int_as_float(0x7f800000); }
 
+  // Record (tile c, slice w) of the slot.  When the consumers merge, it
+  // lives in the shared memory of the CTA that streamed tile c (rank c mod G).
   __device__ Rec R(int c, int w) const {
     const size_t i = ((size_t)si * P.NC + c) * kCW + w;
+    const size_t ib = (size_t)kSlots * P.NC * kCW + i;
     Rec r;
-    r.a = rec[i];
-    r.b = DT >= 0 ? rec[(size_t)kSlots * P.NC * kCW + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const uint32_t owner = consumers_merge<TT, DT, CL>() ? (uint32_t)(c % P.G) : 0u;
+    if (owner != 0) {
+      r.a = ld_cluster_f32x4(cluster_map(&rec[i], owner));
+      r.b = DT >= 0 ? ld_cluster_f32x4(cluster_map(&rec[ib], owner)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      r.a = rec[i];
+      r.b = DT >= 0 ? rec[ib] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     return r;
   }
 
@@ -979,17 +1032,29 @@ struct Control {
   }
 
   // Adds tile c's slices of array f (records in lanes 0..15) to run[f].
+  // The summary of array f of tile c: computed here from the records, or,
+  // in clusters, the one the tile's last warp wrote into pre[si][c][f] (read
+  // by every lane before lane 0 overwrites that entry).
+  __device__ float4 summary(int c, int f) {
+    if (consumers_merge<TT, DT, CL>()) {
+      const float4 v = sm.pre[si][c][f];
+      __syncwarp();
+      return v;
+    }
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    const Rec r = R(c, lane < kCW ? lane : 0);
+    const float4 x = lane < kCW ? (f ? r.b : r.a) : make_float4(NEG_INF, NEG_INF, 0.f, 0.f);
+    if (GREEDY) return greedy_tile_summary(x, lane);
+    if (sm.slot[si].kind != kStats) return resid_tile_summary(x, lane);
+    return softmax_tile_summary(x);
+  }
+
   __device__ void merge_softmax(int c, int f) {
     const float NEG_INF = -__int_as_float(0x7f800000);
-    float4 r = make_float4(NEG_INF, NEG_INF, 0.f, 0.f);
-    if (lane < kCW) r = f ? R(c, lane).b : R(c, lane).a;
-    const bool nan = __any_sync(kFullMask, r.x != r.x || r.z != r.z);
-    // (a NaN record makes the row bad whatever these maxima are)
-    const float mc = warp_max_nan(r.x);
-    const float Rc = warp_max_nan(r.y);
-    DF v = {0.f, 0.f};
-    if (Rc != NEG_INF && r.z != 0.f) v = df_scale(DF{r.z, r.w}, (int)(r.y - Rc));
-    const DF t = df_warp_sum(v);  // the tile's mass over its 16 slices, units 2^Rc
+    const float4 sv = summary(c, f);
+    const bool nan = sv.x != sv.x;
+    const float mc = sv.x, Rc = sv.y;
+    const DF t = {sv.z, sv.w};  // the tile's mass over its slices, units 2^Rc
     Run& R_ = run[f];
     if (lane == 0) sm.pre[si][c][f] = make_float4(R_.sum.hi, R_.sum.lo, R_.ref, 0.f);
     R_.nan |= nan;
@@ -1014,19 +1079,18 @@ struct Control {
     Slot& S = sm.slot[si];
     if (c == 0) reset_row();
     if (GREEDY) {
-      const float m = lane < kCW ? R(c, lane).a.x : -__int_as_float(0x7f800000);
-      gnan_ |= __any_sync(kFullMask, lane < kCW && R(c, lane).a.z != 0.f);
-      const float M = warp_max_nan(m);
-      if (M > gmax_) {  // tiles arrive in token order: keep the first maximum
-        const unsigned h = __ballot_sync(kFullMask, lane < kCW && m == M);
-        gmax_ = M;
-        gfirst_ = c * kCW + __ffs(h) - 1;
+      const float4 sv = summary(c, 0);
+      gnan_ |= sv.z != 0.f;
+      if (sv.x > gmax_) {  // tiles arrive in token order: keep the first maximum
+        gmax_ = sv.x;
+        gfirst_ = c * kCW + (int)sv.y;
       }
     } else if (S.kind == kStats) {
       merge_softmax(c, 0);
       if (DT >= 0 && S.j < S.nb) merge_softmax(c, 1);
     } else {  // residual pass: plain running sum in units of p
-      const DF t = df_warp_sum(lane < kCW ? DF{R(c, lane).a.x, R(c, lane).a.y} : DF{0.f, 0.f});
+      const float4 sv = summary(c, 0);
+      const DF t = {sv.x, sv.y};
       if (lane == 0) sm.pre[si][c][0] = make_float4(run[0].sum.hi, run[0].sum.lo, 0.f, 0.f);
       run[0].sum = df_add(run[0].sum, t);
       run[0].ref = 0.f;
@@ -1454,7 +1518,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
   // tile barriers: each consumer warp arrives once per tile of a job
   // (other CTAs of a cluster arrive on them: each init is fenced at cluster scope)
   if (threadIdx.x < kSlots * kMaxChunks) {
-    mbar_init(&sm.tile_bar[threadIdx.x / kMaxChunks][threadIdx.x % kMaxChunks], kCW);
+    // one arrival when the tile's last consumer warp merges its records
+    mbar_init(&sm.tile_bar[threadIdx.x / kMaxChunks][threadIdx.x % kMaxChunks],
+              consumers_merge<TT, DT, CL>() ? 1 : kCW);
+    sm.tcnt[threadIdx.x / kMaxChunks][threadIdx.x % kMaxChunks] = 0;
     mbar_fence_init();
   }
   __syncthreads();
@@ -1603,6 +1670,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         nxt_ready = mbar_test_wait(&sm.full[ncs], cs + 1 == NS ? cph ^ 1u : cph);
       }
       __syncwarp();
+      int last = 0;
       if (lane == 0) {
         const int ri = tg.rbase + warp;
         // release: the record (and the captured logits) before the arrival
@@ -1610,9 +1678,47 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
           rec[ri] = r.a;
           if (DT >= 0) rec[(size_t)kSlots * P.NC * kCW + ri] = r.b;
           mbar_arrive(&sm.tile_bar[tg.slot][tg.chunk]);
+        } else if (consumers_merge<TT, DT, CL>()) {
+          // the tile's last warp (all of them are this CTA's) merges
+          rec[ri] = r.a;
+          if (DT >= 0) rec[(size_t)kSlots * P.NC * kCW + ri] = r.b;
+          __threadfence_block();
+          last = atomicAdd(&sm.tcnt[tg.slot][tg.chunk], 1u) == (uint32_t)kCW - 1u;
         } else {  // into the cluster leader's records, on its tile barrier
           st_cluster_f32x4(cluster_map(&rec[ri], 0), r.a);
           if (DT >= 0) st_cluster_f32x4(cluster_map(&rec[(size_t)kSlots * P.NC * kCW + ri], 0), r.b);
+          mbar_arrive_cluster(cluster_map(&sm.tile_bar[tg.slot][tg.chunk], 0));
+        }
+      }
+      if (consumers_merge<TT, DT, CL>() && __shfl_sync(kFullMask, last, 0)) {
+        // Clusters: the last of the tile's warps reduces its kCW records (all
+        // in this CTA's shared memory) to the tile's summary, for the leader's
+        // control warp, which then only folds it into the row's running state.
+        __threadfence_block();
+        __syncwarp();
+        const float NEG_INF = -__int_as_float(0x7f800000);
+        const size_t base = ((size_t)tg.slot * P.NC + tg.chunk) * kCW;
+        const bool two = DT >= 0 && tg.kind == kStats && tg.has_draft;
+        float4 ra = make_float4(NEG_INF, NEG_INF, 0.f, 0.f), rb = ra;
+        if (lane < kCW) {
+          ra = rec[base + lane];
+          if (two) rb = rec[(size_t)kSlots * P.NC * kCW + base + lane];
+        }
+        float4 s0, s1 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (GREEDY) {
+          s0 = greedy_tile_summary(ra, lane);
+        } else if (tg.kind == kStats) {
+          s0 = softmax_tile_summary(ra);
+          if (two) s1 = softmax_tile_summary(rb);
+        } else {
+          s0 = resid_tile_summary(ra, lane);
+        }
+        if (lane == 0) {
+          st_cluster_f32x4(cluster_map(&sm.pre[tg.slot][tg.chunk][0], 0), s0);
+          if (two) st_cluster_f32x4(cluster_map(&sm.pre[tg.slot][tg.chunk][1], 0), s1);
+          // the counter for the slot's next job (posted only after the control
+          // warp has seen this arrival)
+          sm.tcnt[tg.slot][tg.chunk] = 0;
           mbar_arrive_cluster(cluster_map(&sm.tile_bar[tg.slot][tg.chunk], 0));
         }
       }
