@@ -66,16 +66,16 @@ HEAD_MIN_TIMED_MS = 500.0
 # verify kernel from one ncu capture of each workload, with the SHA-256 of
 # verify.cu it was taken on: a changed kernel reports null until captured again.
 VERIFY_TRAFFIC = {
-    "verify_b1024_k3_bf16_t1": {"bytes": 317836288.0,
-                                "verify_cu_sha256": "e72e93e289bbda6ee3198e2aaff0215d3b173d7df9db56d7f7aac01ffb0f797c"},
-    "draft_model_b32": {"bytes": 85797888.0,
-                        "verify_cu_sha256": "e72e93e289bbda6ee3198e2aaff0215d3b173d7df9db56d7f7aac01ffb0f797c"},
-    "rs_bf16_b64": {"bytes": 19565312.0,
-                    "verify_cu_sha256": "e72e93e289bbda6ee3198e2aaff0215d3b173d7df9db56d7f7aac01ffb0f797c"},
-    "long_rollout_b256": {"bytes": 78968601.60000001,
-                          "verify_cu_sha256": "e72e93e289bbda6ee3198e2aaff0215d3b173d7df9db56d7f7aac01ffb0f797c"},
-    "tree_b256": {"bytes": 161445632.0,
-                  "verify_cu_sha256": "e72e93e289bbda6ee3198e2aaff0215d3b173d7df9db56d7f7aac01ffb0f797c"},
+    "verify_b1024_k3_bf16_t1": {"bytes": 317619456.0,
+                                "verify_cu_sha256": "1ef59479f5cfcf825fb8b09d9d6f9263bcbf523f50142a509ea2c39574df224e"},
+    "draft_model_b32": {"bytes": 86087168.0,
+                        "verify_cu_sha256": "1ef59479f5cfcf825fb8b09d9d6f9263bcbf523f50142a509ea2c39574df224e"},
+    "rs_bf16_b64": {"bytes": 19560448.0,
+                    "verify_cu_sha256": "1ef59479f5cfcf825fb8b09d9d6f9263bcbf523f50142a509ea2c39574df224e"},
+    "long_rollout_b256": {"bytes": 78961574.4,
+                          "verify_cu_sha256": "1ef59479f5cfcf825fb8b09d9d6f9263bcbf523f50142a509ea2c39574df224e"},
+    "tree_b256": {"bytes": 161767936.0,
+                  "verify_cu_sha256": "1ef59479f5cfcf825fb8b09d9d6f9263bcbf523f50142a509ea2c39574df224e"},
 }
 # the same for the sampling cut kernel (sampling.cu)
 CUT_TRAFFIC = {"sampling_b256": {"bytes": 277559040.0,
