@@ -170,6 +170,7 @@ struct Smem {
   int32_t pool_left;    // sequences not yet claimed, as of this CTA's last claim
   int32_t claim_lock;   // one control warp claims at a time
   int32_t pool_done;    // a claim found no sequence left: idle slots leave
+  int32_t claims_ended; // this CTA has counted itself out of the claim counter
   uint64_t tile_bar[kSlots][kMaxChunks];  // one phase per job: the kCW records of a tile
   float4 pre[kSlots][kMaxChunks][2];     // control: mass before each tile {hi, lo, ref, 0}
                                          // (clusters: first the tile's summary)
@@ -185,6 +186,22 @@ __device__ __forceinline__ void set_abort(Smem& sm, int G) {
     const uint32_t me = cluster_rank();
     for (int r = 0; r < G; ++r)
       if ((uint32_t)r != me) st_cluster_u32(cluster_map(&sm.abort, (uint32_t)r), 1u);
+  }
+}
+
+// Called once a CTA will claim no more sequences from the shared counter
+// (once per CTA): counts the CTA out, and the last CTA out resets the
+// counters for the next launch on this workspace.  Done as soon as the
+// CTA's claiming ends, not at its exit, so the global atomics are off the
+// end of the launch.
+__device__ __forceinline__ void end_claims(const VParams& P, Smem& sm, int G) {
+  if (gridDim.x / (uint32_t)G >= (uint32_t)P.B) return;  // the counter is not used
+  if (atomicExch(&sm.claims_ended, 1) != 0) return;
+  __threadfence();
+  if (atomicAdd(&P.ws[1], 1u) == gridDim.x - 1) {
+    P.ws[0] = 0;
+    P.ws[1] = 0;
+    __threadfence();
   }
 }
 
@@ -941,12 +958,16 @@ struct Control {
         // clusters cover the batch: the counter is then never touched)
         const uint32_t G = CL ? (uint32_t)P.G : 1u;
         const uint32_t ncl = gridDim.x / G;
+        // (claims are made under the CTA's claim lock: once one found the
+        // pool empty, none is made again)
         b = first_ ? blockIdx.x / G
-                   : ncl >= (uint32_t)P.B ? (uint32_t)P.B : ncl + atomicAdd(&P.ws[0], 1u);
+                   : (ncl >= (uint32_t)P.B || vload(&sm.pool_done)) ? (uint32_t)P.B
+                                                                     : ncl + atomicAdd(&P.ws[0], 1u);
         vstore(&sm.pool_left, b >= (uint32_t)P.B ? 0 : P.B - 1 - (int)b);
         // no sequence left: none beyond this one either when the clusters
         // cover the batch, so the slots leave without another claim
         if (b >= (uint32_t)P.B || ncl >= (uint32_t)P.B) vstore(&sm.pool_done, 1);
+        if (b >= (uint32_t)P.B) end_claims(P, sm, (int)G);
       }
       first_ = false;
       b = __shfl_sync(kFullMask, b, 0);
@@ -1513,6 +1534,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
     sm.pool_left = P.B;
     sm.claim_lock = 0;
     sm.pool_done = 0;
+    sm.claims_ended = 0;
     mbar_fence_init();
   }
   // tile barriers: each consumer warp arrives once per tile of a job
@@ -2002,10 +2024,22 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         if (S.state != kEmpty) write_result(P, S.b, -1, -1, SAMSPEC_ST_TIMEOUT);
         const uint32_t ncl = gridDim.x / (uint32_t)G;
         if (si == 0 && ctl.first_) write_result(P, (int)(blockIdx.x / G), -1, -1, SAMSPEC_ST_TIMEOUT);
-        if (si == 0 && ncl < (uint32_t)P.B)
-          for (uint32_t b = ncl + atomicAdd(&P.ws[0], 1u); b < (uint32_t)P.B;
-               b = ncl + atomicAdd(&P.ws[0], 1u))
-            write_result(P, (int)b, -1, -1, SAMSPEC_ST_TIMEOUT);
+        if (si == 0 && ncl < (uint32_t)P.B) {
+          // under the claim lock (a slot may be claiming): unless a claim
+          // already found the pool empty, claim the rest to mark them
+          const uint64_t t0 = gtimer();
+          bool locked = false;
+          while (!(locked = atomicCAS(&sm.claim_lock, 0, 1) == 0) && gtimer() - t0 < kDrainNs) {
+          }
+          if (!vload(&sm.pool_done)) {
+            for (uint32_t b = ncl + atomicAdd(&P.ws[0], 1u); b < (uint32_t)P.B;
+                 b = ncl + atomicAdd(&P.ws[0], 1u))
+              write_result(P, (int)b, -1, -1, SAMSPEC_ST_TIMEOUT);
+            vstore(&sm.pool_done, 1);
+          }
+          end_claims(P, sm, G);
+          if (locked) atomicExch(&sm.claim_lock, 0);
+        }
       }
       __threadfence_block();
       atomicAdd(&sm.ctrl_exited, 1);
@@ -2018,15 +2052,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
   // clusters: every store into another CTA's shared memory has landed
   // before any CTA of the cluster exits
   if (G > 1) cluster_sync_all();
-  if (threadIdx.x == 0 && gridDim.x / G < (uint32_t)P.B) {  // the claim counter was used
-    __threadfence();
-    if (atomicAdd(&P.ws[1], 1u) == gridDim.x - 1) {
-      // last CTA out: reset the counters for the next launch on this workspace
-      P.ws[0] = 0;
-      P.ws[1] = 0;
-      __threadfence();
-    }
-  }
+  // (every CTA normally counted itself out when its claiming ended)
+  if (threadIdx.x == 0) end_claims(P, sm, G);
 }
 
 __global__ void uniforms_kernel(int32_t B, int32_t K, uint64_t seed, uint64_t step, float* u) {
