@@ -66,16 +66,16 @@ HEAD_MIN_TIMED_MS = 500.0
 # verify kernel from one ncu capture of each workload, with the SHA-256 of
 # verify.cu it was taken on: a changed kernel reports null until captured again.
 VERIFY_TRAFFIC = {
-    "verify_b1024_k3_bf16_t1": {"bytes": 317619456.0,
-                                "verify_cu_sha256": "1ef59479f5cfcf825fb8b09d9d6f9263bcbf523f50142a509ea2c39574df224e"},
-    "draft_model_b32": {"bytes": 86087168.0,
-                        "verify_cu_sha256": "1ef59479f5cfcf825fb8b09d9d6f9263bcbf523f50142a509ea2c39574df224e"},
-    "rs_bf16_b64": {"bytes": 19560448.0,
-                    "verify_cu_sha256": "1ef59479f5cfcf825fb8b09d9d6f9263bcbf523f50142a509ea2c39574df224e"},
-    "long_rollout_b256": {"bytes": 78961574.4,
-                          "verify_cu_sha256": "1ef59479f5cfcf825fb8b09d9d6f9263bcbf523f50142a509ea2c39574df224e"},
-    "tree_b256": {"bytes": 161767936.0,
-                  "verify_cu_sha256": "1ef59479f5cfcf825fb8b09d9d6f9263bcbf523f50142a509ea2c39574df224e"},
+    "verify_b1024_k3_bf16_t1": {"bytes": 317786112.0,
+                                "verify_cu_sha256": "fe3e9420ca228fe069236e67964c3205386800d4744d35c327d5ed3bdd3a1d2c"},
+    "draft_model_b32": {"bytes": 85661440.0,
+                        "verify_cu_sha256": "fe3e9420ca228fe069236e67964c3205386800d4744d35c327d5ed3bdd3a1d2c"},
+    "rs_bf16_b64": {"bytes": 19561216.0,
+                    "verify_cu_sha256": "fe3e9420ca228fe069236e67964c3205386800d4744d35c327d5ed3bdd3a1d2c"},
+    "long_rollout_b256": {"bytes": 78965760.0,
+                          "verify_cu_sha256": "fe3e9420ca228fe069236e67964c3205386800d4744d35c327d5ed3bdd3a1d2c"},
+    "tree_b256": {"bytes": 161200128.0,
+                  "verify_cu_sha256": "fe3e9420ca228fe069236e67964c3205386800d4744d35c327d5ed3bdd3a1d2c"},
 }
 # the same for the sampling cut kernel (sampling.cu)
 CUT_TRAFFIC = {"sampling_b256": {"bytes": 277559040.0,
