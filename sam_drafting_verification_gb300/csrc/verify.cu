@@ -121,7 +121,8 @@ struct __align__(16) Tag {
   int32_t dwarp, dtile, slot, chunk;
   int32_t nel, elem0, has_draft, b;
   int32_t j, dtok;  // the row's draft token (statistics pass of a drafted row), else -1
-  int32_t pad[2];
+  uint32_t cwarps;  // trees: the warps whose slices hold one of the node's children
+  int32_t pad;
 };
 
 struct Slot {
@@ -578,7 +579,7 @@ __device__ __forceinline__ float packed_exp_sum(const Slice<TT, DT>& s, float cT
 template <int TT, int DT, bool FULL, bool DRAFT_ARRAY, bool MULTI = false, bool THR = false>
 __device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, int lane, int nel,
                                                  float cT, int excl, uint64_t xm = 0,
-                                                 float tau = 0.f) {
+                                                 float tau = 0.f, bool any_xm = true) {
   using C = Cfg<TT, DT>;
   const float NEG_INF = -__int_as_float(0x7f800000);
   const float QNAN = __int_as_float(0x7fc00000);
@@ -589,9 +590,10 @@ __device__ __forceinline__ float4 reduce_softmax(const Slice<TT, DT>& s, int w, 
   float z;
   // `excl`: one element left out (tile index, or -1).  MULTI: xm marks the
   // lane's elements left out (bit i * VEC + k), e.g. a tree node's children;
-  // the warp takes the masked path if any lane has one
+  // the warp takes the masked path if any lane has one (any_xm false: the
+  // caller knows that none has)
   const bool single = excl >= 0;
-  const bool has_excl = single || (MULTI && __any_sync(kFullMask, xm != 0));
+  const bool has_excl = single || (MULTI && any_xm && __any_sync(kFullMask, xm != 0));
   // THR: logits below tau (a per-request cut) are left out too
   const bool cut = THR && tau > NEG_INF;
   if (FULL && !has_excl && !cut) {
@@ -1619,7 +1621,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
             // a tree node's children are left out of the sums: the lane
             // holding one keeps its logit and marks it in its mask
             static_assert(C::VPL * C::VEC <= 64, "one mask bit per element of a lane");
-            const int nex = S.nex;
+            // (only the warps whose slices hold a child look them up)
+            const bool holds = (tg.cwarps >> warp) & 1u;
+            const int nex = holds ? S.nex : 0;
             uint64_t xm = 0;
             for (int k = 0; k < nex; ++k) {
               const int o = S.ex[k] - tg.elem0 - warp * C::SL;
@@ -1638,8 +1642,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
                 }
               }
             }
-            r.a = full ? reduce_softmax<TT, DT, true, false, true>(sl, warp, lane, tg.nel, P.cT, -1, xm)
-                       : reduce_softmax<TT, DT, false, false, true>(sl, warp, lane, tg.nel, P.cT, -1, xm);
+            r.a = full ? reduce_softmax<TT, DT, true, false, true>(sl, warp, lane, tg.nel, P.cT, -1, xm, 0.f, holds)
+                       : reduce_softmax<TT, DT, false, false, true>(sl, warp, lane, tg.nel, P.cT, -1, xm, 0.f, holds);
           } else {
           if (SAMP) {  // the sequence's temperature; logits below the row's cut left out
             const float cTs = S.cT, th = S.tau;
@@ -1827,6 +1831,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
           tg.nany = (nel + C::SL - 1) / C::SL;
           tg.dtile = tg.dtok >= 0 ? tg.dtok - elem0 : -1;
           tg.dwarp = (tg.dtile >= 0 && tg.dtile < nel) ? tg.dtile / C::SL : -1;
+          uint32_t cw = 0;
+          if (TREE && kind == kStats)
+            for (int k = 0; k < S.nex; ++k) {
+              const int o = S.ex[k] - elem0;
+              if (o >= 0 && o < nel) cw |= 1u << (o / C::SL);
+            }
+          tg.cwarps = cw;
         };
         bool ok = true;
         int c_from = (int)crank;
