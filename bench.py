@@ -66,16 +66,16 @@ HEAD_MIN_TIMED_MS = 500.0
 # verify kernel from one ncu capture of each workload, with the SHA-256 of
 # verify.cu it was taken on: a changed kernel reports null until captured again.
 VERIFY_TRAFFIC = {
-    "verify_b1024_k3_bf16_t1": {"bytes": 317786112.0,
-                                "verify_cu_sha256": "fe3e9420ca228fe069236e67964c3205386800d4744d35c327d5ed3bdd3a1d2c"},
-    "draft_model_b32": {"bytes": 85661440.0,
-                        "verify_cu_sha256": "fe3e9420ca228fe069236e67964c3205386800d4744d35c327d5ed3bdd3a1d2c"},
-    "rs_bf16_b64": {"bytes": 19561216.0,
-                    "verify_cu_sha256": "fe3e9420ca228fe069236e67964c3205386800d4744d35c327d5ed3bdd3a1d2c"},
-    "long_rollout_b256": {"bytes": 78965760.0,
-                          "verify_cu_sha256": "fe3e9420ca228fe069236e67964c3205386800d4744d35c327d5ed3bdd3a1d2c"},
-    "tree_b256": {"bytes": 161200128.0,
-                  "verify_cu_sha256": "fe3e9420ca228fe069236e67964c3205386800d4744d35c327d5ed3bdd3a1d2c"},
+    "verify_b1024_k3_bf16_t1": {"bytes": 317982464.0,
+                                "verify_cu_sha256": "b509911ec6570936ee792d3386bd89b7b24f6735de4c8add1e17cf798338cc0f"},
+    "draft_model_b32": {"bytes": 85948928.0,
+                        "verify_cu_sha256": "b509911ec6570936ee792d3386bd89b7b24f6735de4c8add1e17cf798338cc0f"},
+    "rs_bf16_b64": {"bytes": 19563008.0,
+                    "verify_cu_sha256": "b509911ec6570936ee792d3386bd89b7b24f6735de4c8add1e17cf798338cc0f"},
+    "long_rollout_b256": {"bytes": 78974668.8,
+                          "verify_cu_sha256": "b509911ec6570936ee792d3386bd89b7b24f6735de4c8add1e17cf798338cc0f"},
+    "tree_b256": {"bytes": 161336064.0,
+                  "verify_cu_sha256": "b509911ec6570936ee792d3386bd89b7b24f6735de4c8add1e17cf798338cc0f"},
 }
 # the same for the sampling cut kernel (sampling.cu)
 CUT_TRAFFIC = {"sampling_b256": {"bytes": 277559040.0,
