@@ -27,11 +27,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
-__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t cnt) {
-  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(cnt)
-               : "memory");
-}
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
                    smem_u32(bar)),
@@ -124,16 +119,6 @@ __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
                : "memory");
   return v;
 }
-// fetch-and-add at cluster scope, acquire and release: the adders' earlier
-// stores are visible to whoever adds after them
-__device__ __forceinline__ uint32_t atom_add_acq_rel_cluster_u32(uint32_t addr, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.cluster.shared::cluster.add.u32 %0, [%1], %2;"
-               : "=r"(old)
-               : "r"(addr), "r"(v)
-               : "memory");
-  return old;
-}
 __device__ __forceinline__ void red_cluster_add_u32(uint32_t addr, uint32_t v) {
   asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v)
                : "memory");
@@ -174,17 +159,7 @@ __device__ __forceinline__ void vstore(int32_t* p, int32_t v) {
 }
 
 // ---- warp reductions / scans -----------------------------------------------
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
-  return v;
-}
 __device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFullMask, v, o);
-  return v;
-}
-__device__ __forceinline__ double warp_sum_d(double v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFullMask, v, o);
   return v;
