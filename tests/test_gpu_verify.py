@@ -187,6 +187,38 @@ def test_malformed_rows_and_drafts(ss, cuda_device):
         assert g["status"][2] == (5 if T > 0 else 0)
 
 
+@pytest.mark.parametrize("with_draft", [False, True])
+def test_malformed_rows_in_clusters(ss, cuda_device, with_draft):
+    """The same malformed rows at the full vocabulary and B=8, where a
+    sequence's fp32 tiles are shared by a cluster of CTAs and the tile's last
+    warp merges its records: the NaN, the +inf and the only finite logit sit
+    in tiles that the cluster's other CTAs stream (tile 1: logits 12288 up
+    with fp32 rows, 6144 up with draft logits as well)."""
+    B, K, V = 8, 2, workloads.V_LARGE
+    logits, draft = workloads.sweep_host(510, B, K, V)
+    rng = np.random.default_rng(511)
+    tile1 = 6144 if with_draft else 12288
+    draft[:] = np.argmax(logits[:, :K], axis=-1).astype(np.int32)
+    logits[0, 0, tile1 + 17] = np.nan
+    logits[1, 0, :] = -np.inf
+    logits[2, 0, tile1 + 3] = np.inf     # +inf: bad only when T > 0
+    logits[3, 0, :100] = -np.inf         # masked vocabulary: fine
+    logits[4, 0, :] = -np.inf            # only the draft token finite
+    draft[4, 0] = tile1 + 40
+    logits[4, 0, tile1 + 40] = 1.5
+    dl = None
+    if with_draft:
+        dl = (logits[:, :K] + workloads.gaussian_logits(rng, (B, K, V), 1.0)).astype(np.float32)
+        dl[np.isnan(dl) | np.isinf(dl)] = 0.0
+    for T in ((0.0, 1.0) if not with_draft else (1.0,)):
+        g, o, te, de = _run_both(ss, cuda_device, logits, draft, None, T=T, seed=3,
+                                 draft_logits=dl)
+        _check(g, o, te, de, draft, None, T)
+        assert g["status"][0] == 5 and g["status"][1] == 5
+        assert g["status"][3] == 0 and g["status"][4] == 0 and g["accept_len"][4] >= 1
+        assert g["status"][2] == (5 if T > 0 else 0)
+
+
 def test_determinism_and_single_sequence(ss, cuda_device):
     B, K, V = 1, 3, 151936
     logits, draft = workloads.sweep_host(600, B, K, V)
