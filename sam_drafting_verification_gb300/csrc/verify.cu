@@ -1766,6 +1766,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       // producer's arrival) when the job is posted; if another job comes
       // first (the sequence's drafts were bad), they are released unread.
       int npre = 0;
+      bool early = false;  // the requested-ahead tiles are published already
       const int b0 = (int)(blockIdx.x / G);
       if (DT < 0 && !TREE && !SAMP && !P.direct && b0 < P.B) {
         const int mine = (P.NC - (int)crank + G - 1) / G;
@@ -1780,6 +1781,44 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         }
         ps = npre == NS ? 0 : npre;
         pph = npre == NS ? 1u : 0u;
+        // Of the sequence's drafts these tiles need only the first (left out
+        // of the sums) and their validity.  Checked here as the control warp
+        // checks them when it claims the sequence (it posts exactly this job
+        // then), valid rows are published at once instead of after the claim.
+        const int nb = P.draft_len ? P.draft_len[b0] : P.K;
+        bool valid = nb >= 0 && nb <= P.K;
+        int d0 = -1;
+        if (valid)
+          for (int k = 0; k < nb; ++k) {
+            const int32_t t = P.draft[(size_t)b0 * P.K + k];
+            valid = valid && t >= 0 && t < P.V;
+            if (k == 0) d0 = t;
+          }
+        if (valid) {
+          for (int i = 0; i < npre; ++i) {
+            const int c = (int)crank + i * G;
+            const int elem0 = c * C::E_TILE;
+            const int nel = min(C::E_TILE, P.V - elem0);
+            Tag& tg = sm.tag[i];
+            tg.slot = 0;
+            tg.kind = kStats;
+            tg.chunk = c;
+            tg.nel = nel;
+            tg.elem0 = elem0;
+            tg.has_draft = 0;
+            tg.b = b0;
+            tg.j = 0;
+            tg.dtok = d0;
+            tg.rbase = c * kCW;
+            tg.nfull = nel / C::SL;
+            tg.nany = (nel + C::SL - 1) / C::SL;
+            tg.dtile = d0 >= 0 ? d0 - elem0 : -1;
+            tg.dwarp = (tg.dtile >= 0 && tg.dtile < nel) ? tg.dtile / C::SL : -1;
+            tg.cwarps = 0;
+            mbar_arrive(&sm.full[i]);  // release: the tag before the arrival
+          }
+          early = true;
+        }
       }
       uint64_t t_idle = gtimer();
       for (;;) {
@@ -1843,8 +1882,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         int c_from = (int)crank;
         if (npre > 0) {
           // the tiles requested ahead: this job's if it is that row, else none
-          const bool match = si == 0 && kind == kStats && b == b0 && j == 0;
-          for (int i = 0; i < npre; ++i) {
+          // (published already: the job is that row, its drafts were valid)
+          const bool match = early || (si == 0 && kind == kStats && b == b0 && j == 0);
+          for (int i = 0; i < npre && !early; ++i) {
             if (match) set_tag(sm.tag[i], (int)crank + i * G);
             else sm.tag[i].kind = kSkip;
             mbar_arrive(&sm.full[i]);  // release: the tag before the arrival
@@ -1895,7 +1935,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
       }
       // tiles requested ahead for a job that never came: released unread (and,
       // after an abort, their copies complete the stages' phases for the drain)
-      for (int i = 0; i < npre; ++i) {
+      for (int i = 0; i < npre && !early; ++i) {
         sm.tag[i].kind = kSkip;
         mbar_arrive(&sm.full[i]);
       }
