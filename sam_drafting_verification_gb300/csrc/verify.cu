@@ -1784,9 +1784,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VParams P) {
         // Of the sequence's drafts these tiles need only the first (left out
         // of the sums) and their validity.  Checked here as the control warp
         // checks them when it claims the sequence (it posts exactly this job
-        // then), valid rows are published at once instead of after the claim.
-        const int nb = P.draft_len ? P.draft_len[b0] : P.K;
-        bool valid = nb >= 0 && nb <= P.K;
+        // then), valid rows are published at once instead of after the claim
+        // -- when the CTAs (clusters) cover the batch, each verifying one
+        // sequence: larger batches keep their consumers busy meanwhile.
+        const bool covers = gridDim.x / (uint32_t)G >= (uint32_t)P.B;
+        const int nb = !covers ? -1 : (P.draft_len ? P.draft_len[b0] : P.K);
+        bool valid = covers && nb >= 0 && nb <= P.K;
         int d0 = -1;
         if (valid)
           for (int k = 0; k < nb; ++k) {
