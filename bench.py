@@ -66,16 +66,16 @@ HEAD_MIN_TIMED_MS = 500.0
 # verify kernel from one ncu capture of each workload, with the SHA-256 of
 # verify.cu it was taken on: a changed kernel reports null until captured again.
 VERIFY_TRAFFIC = {
-    "verify_b1024_k3_bf16_t1": {"bytes": 317982464.0,
-                                "verify_cu_sha256": "b509911ec6570936ee792d3386bd89b7b24f6735de4c8add1e17cf798338cc0f"},
-    "draft_model_b32": {"bytes": 85948928.0,
-                        "verify_cu_sha256": "b509911ec6570936ee792d3386bd89b7b24f6735de4c8add1e17cf798338cc0f"},
-    "rs_bf16_b64": {"bytes": 19563008.0,
-                    "verify_cu_sha256": "b509911ec6570936ee792d3386bd89b7b24f6735de4c8add1e17cf798338cc0f"},
-    "long_rollout_b256": {"bytes": 78974668.8,
-                          "verify_cu_sha256": "b509911ec6570936ee792d3386bd89b7b24f6735de4c8add1e17cf798338cc0f"},
-    "tree_b256": {"bytes": 161336064.0,
-                  "verify_cu_sha256": "b509911ec6570936ee792d3386bd89b7b24f6735de4c8add1e17cf798338cc0f"},
+    "verify_b1024_k3_bf16_t1": {"bytes": 317743872.0,
+                                "verify_cu_sha256": "19a514fea2a968c7d6dc7c6763fd5217966b19cda3478e90d98983535f0c71a7"},
+    "draft_model_b32": {"bytes": 86080512.0,
+                        "verify_cu_sha256": "19a514fea2a968c7d6dc7c6763fd5217966b19cda3478e90d98983535f0c71a7"},
+    "rs_bf16_b64": {"bytes": 19564800.0,
+                    "verify_cu_sha256": "19a514fea2a968c7d6dc7c6763fd5217966b19cda3478e90d98983535f0c71a7"},
+    "long_rollout_b256": {"bytes": 78983744.0,
+                          "verify_cu_sha256": "19a514fea2a968c7d6dc7c6763fd5217966b19cda3478e90d98983535f0c71a7"},
+    "tree_b256": {"bytes": 161326336.0,
+                  "verify_cu_sha256": "19a514fea2a968c7d6dc7c6763fd5217966b19cda3478e90d98983535f0c71a7"},
 }
 # the same for the sampling cut kernel (sampling.cu)
 CUT_TRAFFIC = {"sampling_b256": {"bytes": 277559040.0,
