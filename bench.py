@@ -63,34 +63,51 @@ HEAD_WORKLOAD = "verify_b1024_k3_bf16_t1"
 HEAD_MIN_TIMED_MS = 500.0
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
-# verify kernel from one ncu capture of each workload, with the SHA-256 of
-# verify.cu it was taken on: a changed kernel reports null until captured again.
+# verify kernel from one ncu capture of each workload, with the SHA-256 of the
+# code of verify.cu it was taken on (comments and blank lines left out, see
+# _code_sha256): a changed kernel reports null until captured again.
 VERIFY_TRAFFIC = {
     "verify_b1024_k3_bf16_t1": {"bytes": 317743872.0,
-                                "verify_cu_sha256": "19a514fea2a968c7d6dc7c6763fd5217966b19cda3478e90d98983535f0c71a7"},
+                                "verify_cu_code_sha256": "412da9b7976facf2f3c2017bfd38a3ed29ed9ede0a25db6f033f807a5d99adf9"},
     "draft_model_b32": {"bytes": 86080512.0,
-                        "verify_cu_sha256": "19a514fea2a968c7d6dc7c6763fd5217966b19cda3478e90d98983535f0c71a7"},
+                        "verify_cu_code_sha256": "412da9b7976facf2f3c2017bfd38a3ed29ed9ede0a25db6f033f807a5d99adf9"},
     "rs_bf16_b64": {"bytes": 19564800.0,
-                    "verify_cu_sha256": "19a514fea2a968c7d6dc7c6763fd5217966b19cda3478e90d98983535f0c71a7"},
+                    "verify_cu_code_sha256": "412da9b7976facf2f3c2017bfd38a3ed29ed9ede0a25db6f033f807a5d99adf9"},
     "long_rollout_b256": {"bytes": 78983744.0,
-                          "verify_cu_sha256": "19a514fea2a968c7d6dc7c6763fd5217966b19cda3478e90d98983535f0c71a7"},
+                          "verify_cu_code_sha256": "412da9b7976facf2f3c2017bfd38a3ed29ed9ede0a25db6f033f807a5d99adf9"},
     "tree_b256": {"bytes": 161326336.0,
-                  "verify_cu_sha256": "19a514fea2a968c7d6dc7c6763fd5217966b19cda3478e90d98983535f0c71a7"},
+                  "verify_cu_code_sha256": "412da9b7976facf2f3c2017bfd38a3ed29ed9ede0a25db6f033f807a5d99adf9"},
 }
 # the same for the sampling cut kernel (sampling.cu)
 CUT_TRAFFIC = {"sampling_b256": {"bytes": 277559040.0,
-                                 "sampling_cu_sha256": "78f29c9034b75bbbe1bded1e886e3e513b3184c3ee3411e7902190e5669d7d55"}}
+                                 "sampling_cu_code_sha256": "59249b3d5dcfb17bf2ce046d51e0251d5996f96244f02d50b98cd55992ebfca3"}}
+
+
+def _code_sha256(path):
+    """SHA-256 of a CUDA source's code: every line with its // comment and
+    trailing blanks cut, empty lines left out (the sources hold no block
+    comments and no // inside a string), so that a comment edit keeps a
+    capture valid and any code edit does not."""
+    import hashlib
+    lines = []
+    with open(path, encoding="utf-8") as f:
+        for ln in f.read().split("\n"):
+            i = ln.find("//")
+            if i >= 0:
+                ln = ln[:i]
+            ln = ln.rstrip()
+            if ln:
+                lines.append(ln)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
 
 
 def _traffic(table, workload, source):
-    import hashlib
     t = table.get(workload)
     if t is None:
         return None
     src = os.path.join(ROOT, "sam_drafting_verification_gb300", "csrc", source)
-    with open(src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != t[source.replace(".", "_") + "_sha256"]:
-            return None
+    if _code_sha256(src) != t[source.replace(".", "_") + "_code_sha256"]:
+        return None
     return t["bytes"]
 
 

@@ -39,9 +39,16 @@
 // work of producer, consumers and control is amortised over more logits.
 // 24 consumer warps measured faster than 8, 12 or 16: a warp's per-tile chain
 // (load, max, exponentials, warp reductions, record) is latency-bound, and
-// more warps overlap more chains.  Every wait is bounded by a global-timer
-// deadline; a CTA that runs out of time marks its sequences
-// SAMSPEC_ST_TIMEOUT, lets its copies in flight land and exits.
+// more warps overlap more chains.  The producer writes per-tile fields the
+// consumers would otherwise recompute per slice (record index, full and
+// non-empty slices, the warp holding the draft token or a tree's children),
+// and the first tiles of a CTA's first sequence are requested at launch.
+// Small batches run as thread-block clusters whose CTAs stream a sequence's
+// tiles round robin; with fp32 targets or draft logits the tile's last
+// consumer warp merges the records there, so one control warp does not set
+// the pace.  Launches use programmatic dependent launch.  Every wait is
+// bounded by a global-timer deadline; a CTA that runs out of time marks its
+// sequences SAMSPEC_ST_TIMEOUT, lets its copies in flight land and exits.
 
 #include <atomic>
 #include <cstdint>

@@ -21,8 +21,8 @@ def test_traffic_tables_are_well_formed():
     seen = 0
     for _, source, workload, entry in _entries():
         assert entry["bytes"] > 0, workload
-        assert set(entry) == {"bytes", source.replace(".", "_") + "_sha256"}, workload
-        assert re.fullmatch(r"[0-9a-f]{64}", entry[source.replace(".", "_") + "_sha256"]), workload
+        assert set(entry) == {"bytes", source.replace(".", "_") + "_code_sha256"}, workload
+        assert re.fullmatch(r"[0-9a-f]{64}", entry[source.replace(".", "_") + "_code_sha256"]), workload
         seen += 1
     assert seen >= 4
 
@@ -30,15 +30,25 @@ def test_traffic_tables_are_well_formed():
 def test_traffic_only_for_the_captured_source():
     for table, source, workload, entry in _entries():
         path = os.path.join(ROOT, "sam_drafting_verification_gb300", "csrc", source)
-        with open(path, "rb") as f:
-            current = hashlib.sha256(f.read()).hexdigest()
-        key = source.replace(".", "_") + "_sha256"
+        current = bench._code_sha256(path)
+        key = source.replace(".", "_") + "_code_sha256"
         same = {workload: dict(entry, **{key: current})}
         other = {workload: dict(entry, **{key: "0" * 64})}
         assert bench._traffic(same, workload, source) == entry["bytes"]
         assert bench._traffic(other, workload, source) is None
         assert bench._traffic(table, "no_such_workload", source) is None
 
+
+def test_code_hash_ignores_comments_only(tmp_path):
+    a = tmp_path / "a.cu"
+    a.write_text("int f() {  // one\n  return 1;\n}\n")
+    b = tmp_path / "b.cu"
+    b.write_text("// a new header\nint f() {  // two\n\n  return 1;   \n}\n")
+    c = tmp_path / "c.cu"
+    c.write_text("int f() {  // one\n  return 2;\n}\n")
+    assert bench._code_sha256(a) == bench._code_sha256(b)
+    assert bench._code_sha256(a) != bench._code_sha256(c)
+    assert bench._code_sha256(a) != hashlib.sha256(a.read_bytes()).hexdigest()
 
 
 def test_thread_rate_counts_every_thread():
