@@ -4,7 +4,8 @@ The pages draw their coins with torch.rand; the reproducible coins here come
 from Philox4x32-10 (Salmon et al., SC'11).  The oracle's implementation is
 checked bit for bit against an independent third-party implementation, the
 one in Triton's language library, run by Triton's CPU interpreter in a child
-process; the uniform map is checked at its end points and for uniformity.
+process, both for raw counters and for the counter layout of the coins;
+the uniform map is checked at its end points and for uniformity.
 """
 import json
 import os
@@ -44,8 +45,18 @@ print(json.dumps(res))
 """
 
 
-def test_philox_matches_triton_library():
+def _triton_philox(req):
+    """Philox4x32-10 words from Triton's library for [(seed, [counter, ...])]."""
     pytest.importorskip("triton")
+    p = subprocess.run([sys.executable, "-c", _TRITON_SCRIPT], input=json.dumps(req),
+                       capture_output=True, text=True, timeout=600,
+                       env={**os.environ, "TRITON_INTERPRET": "1"})
+    if p.returncode != 0:
+        pytest.skip("triton interpreter unavailable: " + p.stderr.strip().splitlines()[-1][:200])
+    return json.loads(p.stdout.strip().splitlines()[-1])
+
+
+def test_philox_matches_triton_library():
     rng = np.random.default_rng(41)
     req = []
     seeds = [0, 1, 0xFFFFFFFF, 0x123456789ABCDEF, 2**64 - 1]
@@ -54,16 +65,26 @@ def test_philox_matches_triton_library():
         ctrs[0] = 0
         ctrs[1] = 2**32 - 1
         req.append([seed, ctrs.tolist()])
-    p = subprocess.run([sys.executable, "-c", _TRITON_SCRIPT], input=json.dumps(req),
-                       capture_output=True, text=True, timeout=600,
-                       env={**os.environ, "TRITON_INTERPRET": "1"})
-    if p.returncode != 0:
-        pytest.skip("triton interpreter unavailable: " + p.stderr.strip().splitlines()[-1][:200])
-    got = json.loads(p.stdout.strip().splitlines()[-1])
+    got = _triton_philox(req)
     for (seed, ctrs), tri in zip(req, got):
         key = [seed & 0xFFFFFFFF, seed >> 32]
         for c, t in zip(ctrs, tri):
             assert list(oracle.philox4x32_10(c, key)) == t, (seed, c)
+
+
+def test_coin_counter_layout_matches_triton_library():
+    # The coins of sequence b at draft position j in decoding step `step`:
+    # key = (seed lo, seed hi), counter = (j, b, step lo, step hi); word 0
+    # gives the accept coin u_j and word 1 the resample coin u'_j, each through
+    # U(x) = ((x >> 9) + 1/2) * 2^-23.  Positions, sequences and steps are
+    # chosen with distinct values so that a transposed counter word shows.
+    cases = [(7, 3, 5, 2), (2**40 + 9, 2**33 + 17, 1000, 7), (0, 0, 0, 0), (12345, 1, 2**31 + 5, 31)]
+    req = [[seed, [[j, b, step & 0xFFFFFFFF, step >> 32]]] for seed, step, b, j in cases]
+    got = _triton_philox(req)
+    for (seed, step, b, j), tri in zip(cases, got):
+        w = tri[0]
+        want = [((w[i] >> 9) + 0.5) * 2.0**-23 for i in (0, 1)]
+        assert list(oracle.uniforms(seed, step, b, j)) == want, (seed, step, b, j)
 
 
 def test_uniform_map_end_points_and_exactness():
