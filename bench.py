@@ -38,6 +38,7 @@ import argparse
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -64,49 +65,91 @@ HEAD_MIN_TIMED_MS = 500.0
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
 # verify kernel from one ncu capture of each workload, with the SHA-256 of the
-# code of verify.cu it was taken on (comments and blank lines left out, see
-# _code_sha256): a changed kernel reports null until captured again.
+# code of the translation unit it was taken on (verify.cu and every header it
+# includes; comments and blank lines left out, see _code_sha256): a changed
+# kernel reports null until captured again.
+_VERIFY_TU = "10209560a99b9cc8583f03087bc0f389234495d313e9f20d9306041be47c2231"
 VERIFY_TRAFFIC = {
-    "verify_b1024_k3_bf16_t1": {"bytes": 317743872.0,
-                                "verify_cu_code_sha256": "412da9b7976facf2f3c2017bfd38a3ed29ed9ede0a25db6f033f807a5d99adf9"},
-    "draft_model_b32": {"bytes": 86080512.0,
-                        "verify_cu_code_sha256": "412da9b7976facf2f3c2017bfd38a3ed29ed9ede0a25db6f033f807a5d99adf9"},
-    "rs_bf16_b64": {"bytes": 19564800.0,
-                    "verify_cu_code_sha256": "412da9b7976facf2f3c2017bfd38a3ed29ed9ede0a25db6f033f807a5d99adf9"},
-    "long_rollout_b256": {"bytes": 78983744.0,
-                          "verify_cu_code_sha256": "412da9b7976facf2f3c2017bfd38a3ed29ed9ede0a25db6f033f807a5d99adf9"},
-    "tree_b256": {"bytes": 161326336.0,
-                  "verify_cu_code_sha256": "412da9b7976facf2f3c2017bfd38a3ed29ed9ede0a25db6f033f807a5d99adf9"},
+    "verify_b1024_k3_bf16_t1": {"bytes": 317743872.0, "code_sha256": _VERIFY_TU},
+    "draft_model_b32": {"bytes": 86080512.0, "code_sha256": _VERIFY_TU},
+    "rs_bf16_b64": {"bytes": 19564800.0, "code_sha256": _VERIFY_TU},
+    "long_rollout_b256": {"bytes": 78983744.0, "code_sha256": _VERIFY_TU},
+    "tree_b256": {"bytes": 161326336.0, "code_sha256": _VERIFY_TU},
 }
-# the same for the sampling cut kernel (sampling.cu)
-CUT_TRAFFIC = {"sampling_b256": {"bytes": 277559040.0,
-                                 "sampling_cu_code_sha256": "59249b3d5dcfb17bf2ce046d51e0251d5996f96244f02d50b98cd55992ebfca3"}}
+# the same for the sampling cut kernel (sampling.cu and its headers)
+CUT_TRAFFIC = {"sampling_b256": {"bytes": 277508096.0,
+                                 "code_sha256": "80868dc4d90963fa9ff9dc55167b6e2d48b049d28b8d7ebe5bffb0d539c8f2da"}}
+
+CSRC = os.path.join(ROOT, "sam_drafting_verification_gb300", "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+_INCLUDE_RE = re.compile(r'^[ \t]*#[ \t]*include[ \t]+"([^"]+)"', re.M)
 
 
-def _code_sha256(path):
-    """SHA-256 of a CUDA source's code: every line with its // comment and
-    trailing blanks cut, empty lines left out (the sources hold no block
-    comments and no // inside a string), so that a comment edit keeps a
-    capture valid and any code edit does not."""
+def _strip_comments(text):
+    """C/C++/CUDA source without its // and /* */ comments; string and
+    character literals are kept as they are."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c and text[j] != "\n":
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
+def _tu_sources(source):
+    """A CUDA source of the library and every header it includes with quotes,
+    recursively (looked up in csrc/, then include/), each once."""
+    order, todo = [], [os.path.join(CSRC, source)]
+    while todo:
+        path = todo.pop(0)
+        if path in order:
+            continue
+        order.append(path)
+        with open(path, encoding="utf-8") as f:
+            names = _INCLUDE_RE.findall(_strip_comments(f.read()))
+        for name in names:
+            found = [os.path.join(d, name) for d in (CSRC, INCLUDE) if os.path.exists(os.path.join(d, name))]
+            if not found:
+                raise FileNotFoundError(f"{name}, included by {path}")
+            todo.append(found[0])
+    return order
+
+
+def _code_sha256(*paths):
+    """SHA-256 of the code of the given sources: comments cut, trailing blanks
+    cut, empty lines left out, each file's code preceded by its name, so that
+    a comment edit keeps a capture valid and any code edit does not."""
     import hashlib
-    lines = []
-    with open(path, encoding="utf-8") as f:
-        for ln in f.read().split("\n"):
-            i = ln.find("//")
-            if i >= 0:
-                ln = ln[:i]
-            ln = ln.rstrip()
-            if ln:
-                lines.append(ln)
-    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, encoding="utf-8") as f:
+            lines = [ln.rstrip() for ln in _strip_comments(f.read()).split("\n")]
+        h.update(os.path.basename(str(path)).encode() + b"\0")
+        h.update("\n".join(ln for ln in lines if ln).encode() + b"\0")
+    return h.hexdigest()
+
+
+def _tu_code_sha256(source):
+    return _code_sha256(*_tu_sources(source))
 
 
 def _traffic(table, workload, source):
     t = table.get(workload)
-    if t is None:
-        return None
-    src = os.path.join(ROOT, "sam_drafting_verification_gb300", "csrc", source)
-    if _code_sha256(src) != t[source.replace(".", "_") + "_code_sha256"]:
+    if t is None or _tu_code_sha256(source) != t["code_sha256"]:
         return None
     return t["bytes"]
 
