@@ -8,6 +8,7 @@ must make at least one pin fail; the unchanged copy, built the same way,
 must pass them all.  The mistakes stay inside the copy: the oracle's own
 source and library are never touched.
 """
+import importlib.util
 import os
 import subprocess
 import sys
@@ -132,9 +133,13 @@ def test_every_planted_mistake_fails_a_pin(tmp_path):
     for name, old, new, _ in MUTANTS:
         assert src.count(old) == 1, f"mutation site not unique or missing: {name}"
 
+    # the Philox pins compare with Triton's implementation: without Triton
+    # they skip, and the Philox mutants are left out
+    have_triton = importlib.util.find_spec("triton") is not None
     jobs = [("unchanged", src, "sam")]
     for name, old, new, first in MUTANTS:
-        jobs.append((name, src.replace(old, new), first))
+        if first != "philox" or have_triton:
+            jobs.append((name, src.replace(old, new), first))
 
     def run(i_job):
         i, (name, text, first) = i_job
