@@ -275,7 +275,7 @@ int spec_verify(const void* d_target, int32_t target_dtype, const void* d_draft_
  * where cudaMalloc is off limits (a host framework that owns every device
  * allocation through its own pool, a plugin loaded into such a runtime, or a
  * caller in a context where allocating would synchronise the device).  The
- * paper has no counterpart; it is a convenience of this library.
+ * method's pages have no counterpart; it is a convenience of this library.
  *
  * Same arguments, outputs and limits as spec_verify, without the workspace:
  * its scratch (the kernel's work counters) is a fixed 256-byte array inside
