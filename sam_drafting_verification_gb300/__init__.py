@@ -45,8 +45,14 @@ def _stream(device=None):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
-def _req(t, dtype, name, shape=None):
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+def _is_cuda(t):
+    return t.is_cuda
+
+
+def _req(t, dtype, name, shape=None, device=None):
+    """t, checked: a contiguous CUDA tensor of `dtype` (and `shape`, on
+    `device`, where given) -- the kernels take its pointer as it is."""
+    if not isinstance(t, torch.Tensor) or not _is_cuda(t):
         raise TypeError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
@@ -54,7 +60,33 @@ def _req(t, dtype, name, shape=None):
         raise ValueError(f"{name} must be contiguous")
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
     return t
+
+
+def _need(res, key, shape, dev, dtype=torch.int32, fill=None):
+    """res[key]: the caller's output buffer, checked, or a new one."""
+    if key in res:
+        _req(res[key], dtype, f"out[{key}]", shape, dev)
+    else:
+        res[key] = (torch.empty(shape, dtype=dtype, device=dev) if fill is None
+                    else torch.full(shape, fill, dtype=dtype, device=dev))
+
+
+def _cuda_device(device=None):
+    """torch.device of a CUDA device, with its index."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if dev.type == "cuda" and dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    return dev
+
+
+def _workspace(workspace, B, K, V, dev, sampling=False):
+    """The caller's verification workspace, checked, or the cached one."""
+    if workspace is None:
+        return verify_workspace(B, K, V, dev, sampling=sampling)
+    return _req(workspace, torch.uint8, "workspace", None, dev)
 
 
 class SamBatch:
@@ -63,7 +95,7 @@ class SamBatch:
     def __init__(self, B: int, capacity_tokens: int, vocab: int, device=None):
         self.lib = _b.lib()
         self.B, self.C, self.V = int(B), int(capacity_tokens), int(vocab)
-        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.device = _cuda_device(device)
         nbytes = self.lib.sam_batch_workspace_bytes(self.B, self.C)
         if nbytes == 0:
             raise SamspecError(f"sizes outside the limits: B={B}, capacity={capacity_tokens}")
@@ -84,14 +116,14 @@ class SamBatch:
 
     def reset(self, mask=None):
         if mask is not None:
-            _req(mask, torch.int32, "mask", (self.B,))
+            _req(mask, torch.int32, "mask", (self.B,), self.device)
         _b.check(self.lib.sam_reset(self._h, _ptr(mask), _stream(self.device)), "sam_reset")
 
     def extend(self, tokens, n_new):
-        _req(tokens, torch.int32, "tokens")
+        _req(tokens, torch.int32, "tokens", device=self.device)
         if tokens.dim() != 2 or tokens.shape[0] != self.B:
             raise ValueError("tokens must be [B, max_new]")
-        _req(n_new, torch.int32, "n_new", (self.B,))
+        _req(n_new, torch.int32, "n_new", (self.B,), self.device)
         _b.check(self.lib.sam_extend(self._h, _ptr(tokens), _ptr(n_new), int(tokens.shape[1]),
                                      _stream(self.device)), "sam_extend")
 
@@ -100,10 +132,22 @@ class SamBatch:
             z = lambda *s: torch.empty(s, dtype=torch.int32, device=self.device)  # noqa: E731
             out = (z(self.B, K), z(self.B), z(self.B), z(self.B))
         d, dl, ml, me = out
-        _req(d, torch.int32, "draft", (self.B, K))
+        _req(d, torch.int32, "draft", (self.B, K), self.device)
         for t, n in ((dl, "draft_len"), (ml, "match_len"), (me, "min_endpos")):
             if t is not None:
-                _req(t, torch.int32, n, (self.B,))
+                _req(t, torch.int32, n, (self.B,), self.device)
+        return out
+
+    def _outs_n(self, n, K, out):
+        """Output buffers of n sequences: the caller's, checked, or new ones."""
+        if out is None:
+            z = lambda *s: torch.empty(s, dtype=torch.int32, device=self.device)  # noqa: E731
+            return z(n, K), z(n), z(n), z(n)
+        d, dl, ml, me = out
+        _req(d, torch.int32, "draft", (n, K), self.device)
+        for t, nm in ((dl, "draft_len"), (ml, "match_len"), (me, "min_endpos")):
+            if t is not None:
+                _req(t, torch.int32, nm, (n,), self.device)
         return out
 
     def draft(self, K: int, out=None):
@@ -113,10 +157,10 @@ class SamBatch:
         return d, dl, ml, me
 
     def step(self, tokens, n_new, K: int, out=None):
-        _req(tokens, torch.int32, "tokens")
+        _req(tokens, torch.int32, "tokens", device=self.device)
         if tokens.dim() != 2 or tokens.shape[0] != self.B:
             raise ValueError("tokens must be [B, max_new]")
-        _req(n_new, torch.int32, "n_new", (self.B,))
+        _req(n_new, torch.int32, "n_new", (self.B,), self.device)
         d, dl, ml, me = self._outs(K, out)
         _b.check(self.lib.sam_step(self._h, _ptr(tokens), _ptr(n_new), int(tokens.shape[1]), int(K),
                                    _ptr(d), _ptr(dl), _ptr(ml), _ptr(me), _stream(self.device)),
@@ -125,17 +169,14 @@ class SamBatch:
 
     def step_rows(self, rows, tokens, n_new, K: int, out=None):
         """sam_step on the automata `rows` (int32 [n], or None for 0..n-1)."""
-        _req(tokens, torch.int32, "tokens")
+        _req(tokens, torch.int32, "tokens", device=self.device)
         if tokens.dim() != 2:
             raise ValueError("tokens must be [n, max_new]")
         n = int(tokens.shape[0])
         if rows is not None:
-            _req(rows, torch.int32, "rows", (n,))
-        _req(n_new, torch.int32, "n_new", (n,))
-        if out is None:
-            z = lambda *s: torch.empty(s, dtype=torch.int32, device=self.device)  # noqa: E731
-            out = (z(n, K), z(n), z(n), z(n))
-        d, dl, ml, me = out
+            _req(rows, torch.int32, "rows", (n,), self.device)
+        _req(n_new, torch.int32, "n_new", (n,), self.device)
+        d, dl, ml, me = self._outs_n(n, K, out)
         _b.check(self.lib.sam_step_rows(self._h, _ptr(rows), n, _ptr(tokens), _ptr(n_new),
                                         int(tokens.shape[1]), int(K), _ptr(d) if K > 0 else None,
                                         _ptr(dl), _ptr(ml), _ptr(me), _stream(self.device)),
@@ -157,24 +198,20 @@ class SamBatch:
         dt = {torch.float32: F32, torch.bfloat16: BF16}.get(target.dtype)
         if dt is None:
             raise TypeError("target must be float32 or bfloat16")
-        _req(target, target.dtype, "target")
-        _req(draft, torch.int32, "draft", (n, K))
+        dev = self.device
+        _req(target, target.dtype, "target", device=dev)
+        _req(draft, torch.int32, "draft", (n, K), dev)
         if draft_len is not None:
-            _req(draft_len, torch.int32, "draft_len", (n,))
+            _req(draft_len, torch.int32, "draft_len", (n,), dev)
         if rows is not None:
-            _req(rows, torch.int32, "rows", (n,))
+            _req(rows, torch.int32, "rows", (n,), dev)
         res = out if out is not None else {}
-
-        def need(key, shape):
-            if key not in res:
-                res[key] = torch.empty(shape, dtype=torch.int32, device=self.device)
-
         for k in ("accept_len", "out_token", "emit_len", "status", "next_draft_len", "match_len",
                   "min_endpos"):
-            need(k, (n,))
-        need("emit", (n, K1))
-        need("next_draft", (n, int(K_next)))
-        ws = workspace if workspace is not None else verify_workspace(n, K, V, self.device)
+            _need(res, k, (n,), dev)
+        _need(res, "emit", (n, K1), dev)
+        _need(res, "next_draft", (n, int(K_next)), dev)
+        ws = _workspace(workspace, n, K, V, dev)
         _b.check(self.lib.sam_spec_step(
             self._h, _ptr(rows), n, _ptr(target), dt, _ptr(draft) if K > 0 else None,
             _ptr(draft_len), K, V, float(temperature), int(seed) & (2**64 - 1),
@@ -190,18 +227,15 @@ class SamBatch:
         `state` (int32 [n, 2], in place) by tokens [n, max_new] / n_new [n] and
         drafts K corpus tokens.  Returns (draft, draft_len, match_len,
         min_endpos)."""
-        _req(state, torch.int32, "state")
+        _req(state, torch.int32, "state", device=self.device)
         if state.dim() != 2 or state.shape[1] != 2:
             raise ValueError("state must be [n, 2]")
         n = int(state.shape[0])
-        _req(tokens, torch.int32, "tokens")
+        _req(tokens, torch.int32, "tokens", device=self.device)
         if tokens.dim() != 2 or tokens.shape[0] != n:
             raise ValueError("tokens must be [n, max_new]")
-        _req(n_new, torch.int32, "n_new", (n,))
-        if out is None:
-            z = lambda *s: torch.empty(s, dtype=torch.int32, device=self.device)  # noqa: E731
-            out = (z(n, K), z(n), z(n), z(n))
-        d, dl, ml, me = out
+        _req(n_new, torch.int32, "n_new", (n,), self.device)
+        d, dl, ml, me = self._outs_n(n, K, out)
         _b.check(self.lib.ssam_match(self._h, int(row), n, _ptr(state), _ptr(tokens), _ptr(n_new),
                                      int(tokens.shape[1]), int(K), _ptr(d) if K > 0 else None,
                                      _ptr(dl), _ptr(ml), _ptr(me), _stream(self.device)),
@@ -222,7 +256,7 @@ class SamBatch:
         return blob
 
     def import_(self, blob):
-        _req(blob, torch.uint8, "blob")
+        _req(blob, torch.uint8, "blob", device=self.device)
         _b.check(self.lib.sam_import(self._h, _ptr(blob), blob.numel(), _stream(self.device)),
                  "sam_import")
 
@@ -259,7 +293,7 @@ def verify_workspace(B: int, K: int, V: int, device=None, sampling: bool = False
     captured with it stay valid; a workspace the caller allocates must stay
     allocated while any graph that uses it can still be replayed."""
     lib = _b.lib()
-    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    dev = _cuda_device(device)
     need = int(lib.spec_verify_sampling_workspace_bytes(B, K, V) if sampling
                else lib.spec_verify_workspace_bytes(B, K, V))
     key = (dev.index, torch.cuda.current_stream(dev).cuda_stream)
@@ -290,38 +324,33 @@ def spec_verify(target, draft, draft_len=None, temperature: float = 0.0, seed: i
     if dt is None:
         raise TypeError("target must be float32 or bfloat16")
     _req(target, target.dtype, "target")
-    _req(draft, torch.int32, "draft", (B, K))
+    dev = target.device
+    _req(draft, torch.int32, "draft", (B, K), dev)
     if draft_len is not None:
-        _req(draft_len, torch.int32, "draft_len", (B,))
+        _req(draft_len, torch.int32, "draft_len", (B,), dev)
     ddt = F32
     if draft_logits is not None:
         ddt = {torch.float32: F32, torch.bfloat16: BF16}.get(draft_logits.dtype)
         if ddt is None:
             raise TypeError("draft_logits must be float32 or bfloat16")
-        _req(draft_logits, draft_logits.dtype, "draft_logits", (B, K, V))
-    dev = target.device
+        _req(draft_logits, draft_logits.dtype, "draft_logits", (B, K, V), dev)
     res = out if out is not None else {}
-
-    def need(key, shape, dtype=torch.int32, fill=None):
-        if key not in res:  # allocate only what the caller did not pass
-            res[key] = (torch.empty(shape, dtype=dtype, device=dev) if fill is None
-                        else torch.full(shape, fill, dtype=dtype, device=dev))
-
-    need("accept_len", (B,))
-    need("out_token", (B,))
-    if emit:
-        need("emit", (B, K1))
-        need("emit_len", (B,))
-    if status:
-        need("status", (B,))
+    # the caller's buffers are checked and reused; the others are allocated
+    _need(res, "accept_len", (B,), dev)
+    _need(res, "out_token", (B,), dev)
+    for key, shape in (("emit", (B, K1)), ("emit_len", (B,))):
+        if emit or key in res:
+            _need(res, key, shape, dev)
+    if status or "status" in res:
+        _need(res, "status", (B,), dev)
     dbg = None
     if debug:
         for k in ("row_m", "row_z", "p_d", "q_d"):
-            need(k, (B, K1), torch.float32, float("nan"))
-        need("row_arg", (B, K1), torch.int32, -1)
-        need("res_mass", (B,), torch.float32, float("nan"))
+            _need(res, k, (B, K1), dev, torch.float32, float("nan"))
+        _need(res, "row_arg", (B, K1), dev, torch.int32, -1)
+        _need(res, "res_mass", (B,), dev, torch.float32, float("nan"))
         dbg = _b.VerifyDebug(*[res[k].data_ptr() for k in ("row_m", "row_z", "p_d", "q_d", "row_arg", "res_mass")])
-    ws = workspace if workspace is not None else verify_workspace(B, K, V, dev)
+    ws = _workspace(workspace, B, K, V, dev)
     rc = lib.spec_verify(_ptr(target), dt, _ptr(draft_logits), ddt, _ptr(draft) if K > 0 else None,
                          _ptr(draft_len),
                          B, K, V, float(temperature), int(seed) & (2**64 - 1), int(step) & (2**64 - 1),
@@ -340,12 +369,15 @@ def select_drafts(dynamic, static, l_bias: int):
     draft_len, source) with source 1 where the static draft was taken."""
     dd, dl, dm = dynamic
     sd, sl, sm = static
+    _req(dd, torch.int32, "dynamic draft")
+    if dd.dim() != 2:
+        raise ValueError("dynamic draft must be [n, K]")
     n, K = (int(x) for x in dd.shape)
-    for t, nm in ((dd, "dynamic draft"), (sd, "static draft")):
-        _req(t, torch.int32, nm, (n, K))
+    dev = dd.device
+    _req(sd, torch.int32, "static draft", (n, K), dev)
     for t, nm in ((dl, "dynamic draft_len"), (dm, "dynamic match_len"), (sl, "static draft_len"),
                   (sm, "static match_len")):
-        _req(t, torch.int32, nm, (n,))
+        _req(t, torch.int32, nm, (n,), dev)
     od = torch.empty_like(dd)
     ol = torch.empty_like(dl)
     src = torch.empty_like(dl)
@@ -370,18 +402,13 @@ def spec_verify_tree(target, tok, first_child, next_sibling, temperature: float 
     if dt is None:
         raise TypeError("target must be float32 or bfloat16")
     _req(target, target.dtype, "target")
-    for t, nm in ((tok, "tok"), (first_child, "first_child"), (next_sibling, "next_sibling")):
-        _req(t, torch.int32, nm, (B, N))
     dev = target.device
-    z = lambda *s: torch.empty(s, dtype=torch.int32, device=dev)  # noqa: E731
-    if out is not None:
-        res = out
-        for k, shp in (("accept_len", (B,)), ("out_token", (B,)), ("path", (B, N)), ("emit", (B, N)),
-                       ("emit_len", (B,)), ("status", (B,))):
-            _req(res[k], torch.int32, "out[" + k + "]", shp)
-    else:
-        res = {"accept_len": z(B), "out_token": z(B), "path": z(B, N), "emit": z(B, N),
-               "emit_len": z(B), "status": z(B)}
+    for t, nm in ((tok, "tok"), (first_child, "first_child"), (next_sibling, "next_sibling")):
+        _req(t, torch.int32, nm, (B, N), dev)
+    res = out if out is not None else {}
+    for k, shp in (("accept_len", (B,)), ("out_token", (B,)), ("path", (B, N)), ("emit", (B, N)),
+                   ("emit_len", (B,)), ("status", (B,))):
+        _need(res, k, shp, dev)
     dbg = None
     if debug:
         for k in ("row_m", "row_z"):
@@ -390,7 +417,7 @@ def spec_verify_tree(target, tok, first_child, next_sibling, temperature: float 
         res["res_mass"] = torch.full((B,), float("nan"), dtype=torch.float32, device=dev)
         dbg = _b.VerifyDebug(res["row_m"].data_ptr(), res["row_z"].data_ptr(), 0, 0,
                              res["row_arg"].data_ptr(), res["res_mass"].data_ptr())
-    ws = workspace if workspace is not None else verify_workspace(B, N - 1, V, dev)
+    ws = _workspace(workspace, B, N - 1, V, dev)
     _b.check(lib.spec_verify_tree(_ptr(target), dt, _ptr(tok), _ptr(first_child), _ptr(next_sibling),
                                   B, N, V, float(temperature), int(seed) & (2**64 - 1),
                                   int(step) & (2**64 - 1), _ptr(res["accept_len"]), _ptr(res["out_token"]),
@@ -403,7 +430,7 @@ def spec_verify_tree(target, tok, first_child, next_sibling, temperature: float 
 def _per_seq(x, B, dtype, dev, name):
     """A [B] device tensor of `dtype` from a scalar or a [B] tensor."""
     if isinstance(x, torch.Tensor):
-        return _req(x, dtype, name, (B,))
+        return _req(x, dtype, name, (B,), dev)
     return torch.full((B,), x, dtype=dtype, device=dev)
 
 
@@ -445,35 +472,28 @@ def spec_verify_sampling(target, draft, draft_len=None, temperature=1.0, top_k=0
     if dt is None:
         raise TypeError("target must be float32 or bfloat16")
     _req(target, target.dtype, "target")
-    _req(draft, torch.int32, "draft", (B, K))
-    if draft_len is not None:
-        _req(draft_len, torch.int32, "draft_len", (B,))
     dev = target.device
+    _req(draft, torch.int32, "draft", (B, K), dev)
+    if draft_len is not None:
+        _req(draft_len, torch.int32, "draft_len", (B,), dev)
     T = _per_seq(temperature, B, torch.float32, dev, "temperature")
     k = _per_seq(top_k, B, torch.int32, dev, "top_k")
     p = _per_seq(top_p, B, torch.float32, dev, "top_p")
     res = out if out is not None else {}
-
-    def need(key, shape, dtype=torch.int32, fill=None):
-        if key not in res:
-            res[key] = (torch.empty(shape, dtype=dtype, device=dev) if fill is None
-                        else torch.full(shape, fill, dtype=dtype, device=dev))
-
-    need("accept_len", (B,))
-    need("out_token", (B,))
-    need("status", (B,))
-    if emit:
-        need("emit", (B, K1))
-        need("emit_len", (B,))
+    for key in ("accept_len", "out_token", "status"):
+        _need(res, key, (B,), dev)
+    for key, shape in (("emit", (B, K1)), ("emit_len", (B,))):
+        if emit or key in res:
+            _need(res, key, shape, dev)
     dbg = None
     if debug:
         for key in ("row_m", "row_z", "p_d"):
-            need(key, (B, K1), torch.float32, float("nan"))
-        need("row_arg", (B, K1), torch.int32, -1)
-        need("res_mass", (B,), torch.float32, float("nan"))
+            _need(res, key, (B, K1), dev, torch.float32, float("nan"))
+        _need(res, "row_arg", (B, K1), dev, torch.int32, -1)
+        _need(res, "res_mass", (B,), dev, torch.float32, float("nan"))
         dbg = _b.VerifyDebug(res["row_m"].data_ptr(), res["row_z"].data_ptr(), res["p_d"].data_ptr(), 0,
                              res["row_arg"].data_ptr(), res["res_mass"].data_ptr())
-    ws = workspace if workspace is not None else verify_workspace(B, K, V, dev, sampling=True)
+    ws = _workspace(workspace, B, K, V, dev, sampling=True)
     rc = lib.spec_verify_sampling(_ptr(target), dt, _ptr(draft) if K > 0 else None, _ptr(draft_len),
                                   B, K, V, _ptr(T), _ptr(k), _ptr(p), int(seed) & (2**64 - 1),
                                   int(step) & (2**64 - 1), _ptr(res["accept_len"]),
@@ -487,7 +507,7 @@ def spec_verify_sampling(target, draft, draft_len=None, temperature=1.0, top_k=0
 
 def spec_uniforms(B: int, K: int, seed: int, step: int, device=None):
     """[B, K+1, 2] float32: (u_j, u'_j) exactly as spec_verify draws them."""
-    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    dev = _cuda_device(device)
     u = torch.empty((B, K + 1, 2), dtype=torch.float32, device=dev)
     _b.check(_b.lib().spec_uniforms(int(B), int(K), int(seed) & (2**64 - 1), int(step) & (2**64 - 1),
                                     _ptr(u), _stream(dev)), "spec_uniforms")

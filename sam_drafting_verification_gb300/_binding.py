@@ -1,9 +1,10 @@
 """ctypes binding of libsamspec.so: argument marshalling only.
 
 Every computation runs in the library's CUDA kernels; torch supplies device
-memory and the current stream.  Importing this module loads the in-tree
-library and raises if it is missing (build it with
-``python -m sam_drafting_verification_gb300.build``): there is no fallback.
+memory and the current stream.  The in-tree library is loaded at the first
+call that needs it; if it is missing, that call raises SamspecError (build it
+with ``python -m sam_drafting_verification_gb300.build``): there is no
+fallback.
 """
 from __future__ import annotations
 
