@@ -52,7 +52,14 @@ class Rollout:
 
     def run(self, max_new_tokens) -> RolloutResult:
         """Generates up to max_new_tokens[b] tokens per sequence (or until eos)
-        from the automata's current texts (prompts already extended)."""
+        from the automata's current texts (prompts already extended).
+
+        The step that finishes a sequence extends its automaton by every token
+        that step emitted, so the automaton may hold up to K tokens beyond the
+        ones returned for it (those after its eos or past its limit).  A
+        finished sequence's automaton is not used again by this rollout; a
+        caller that goes on with it should reset and rebuild it from the
+        returned text."""
         dev = self.batch.device
         B = self.batch.B
         limit = [int(x) for x in max_new_tokens]
