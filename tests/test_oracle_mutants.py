@@ -78,6 +78,11 @@ MUTANTS = [
      "if (std::isnan(x)) return false;", "verify"),
     ("draft logits softmaxed at temperature 1", "softmax_row(drow0 + (int64_t)j * V, V, T, q, &mq, &zq)",
      "softmax_row(drow0 + (int64_t)j * V, V, 1.0, q, &mq, &zq)", "verify"),
+    ("CDF interval of the previous token", "for (int32_t v = 0; v <= token && v < V; ++v) {",
+     "for (int32_t v = 0; v < token && v < V; ++v) {", "verify"),
+    ("CDF interval with draft logits at temperature 1",
+     "if (drow && rejected_token >= 0) softmax_row(drow, V, T, q, &m, &z);",
+     "if (drow && rejected_token >= 0) softmax_row(drow, V, 1.0, q, &m, &z);", "verify"),
     # tree verification
     ("siblings tested without the running sum", "acc += p[tk[c]];", "acc = p[tk[c]];", "tree"),
     ("rejected siblings stay in the final distribution", "r[tk[c]] = 0.0;  // tried", "(void)0;  // tried", "tree"),
@@ -85,6 +90,11 @@ MUTANTS = [
     ("tree node linked twice accepted", "for (int32_t n = 1; !bad && n < N; ++n) bad = refs[n] != 1;", "",
      "tree"),
     ("siblings with equal tokens accepted", "bad = tk[a] == tk[c];", "bad = false;", "tree"),
+    ("tree interval starts after the token", "for (int32_t v = 0; v < token; ++v) before += r[v];",
+     "for (int32_t v = 0; v <= token; ++v) before += r[v];", "tree"),
+    ("tree interval keeps the tried children", "    r[children[i]] = 0.0;\n", "\n", "tree"),
+    ("tree interval without the token's own mass", "lo_hi_mass[1] = (before + r[token]) / mass;",
+     "lo_hi_mass[1] = before / mass;", "tree"),
     # per-request truncation
     ("top-k drops the ties at the k-th value", "keep[v] = row[v] >= tk;", "keep[v] = row[v] > tk;", "sampling"),
     ("top-k kth value off by one", "const float tk = sorted[top_k - 1];", "const float tk = sorted[top_k];", "sampling"),

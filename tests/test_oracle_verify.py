@@ -142,9 +142,11 @@ def test_bonus_row_samples_target():
     assert stats.chisquare(hist, p0 * B).pvalue > 1e-3
 
 
-def test_resample_lies_in_its_cdf_interval():
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_resample_lies_in_its_cdf_interval(T):
+    # at T != 1 too: the draft distribution is softmax(draft logits / T)
     rng = np.random.default_rng(26)
-    B, K, V, T = 16, 3, 300, 1.0
+    B, K, V = 16, 3, 300
     target = workloads.gaussian_logits(rng, (B, K + 1, V), 2.0)
     draftl = (target[:, :K] + workloads.gaussian_logits(rng, (B, K, V), 1.0)).astype(np.float32)
     draft = rng.integers(0, V, size=(B, K)).astype(np.int32)
