@@ -69,6 +69,8 @@ MUTANTS = [
     ("one-hot residual keeps the rejected token", "(v == rejected_token ? 1.0 : 0.0)", "0.0", "verify"),
     ("resample drawn with the accept coin", "out_token[b] = sample_cdf(r, ur * mass);\n    if (u_res) u_res[b] = ur;\n    if (res_mass) res_mass[b] = mass;\n  }\n  return 0;\n}\n\n// Tree",
      "out_token[b] = sample_cdf(r, ua * mass);\n    if (u_res) u_res[b] = ur;\n    if (res_mass) res_mass[b] = mass;\n  }\n  return 0;\n}\n\n// Tree", "verify"),
+    ("caller's sequence index ignored", "const int64_t sb = seq_index ? seq_index[b] : b;",
+     "const int64_t sb = b;", "verify"),
     ("greedy emits the draft, not the argmax", "      accept_len[b] = L;\n      out_token[b] = a;",
      "      accept_len[b] = L;\n      out_token[b] = L < nb ? d[L] : a;", "verify"),
     ("NaN logit not refused by greedy", "    if (std::isnan(x)) return false;\n    if (x > bv)",
@@ -87,6 +89,8 @@ MUTANTS = [
     ("siblings tested without the running sum", "acc += p[tk[c]];", "acc = p[tk[c]];", "tree"),
     ("rejected siblings stay in the final distribution", "r[tk[c]] = 0.0;  // tried", "(void)0;  // tried", "tree"),
     ("greedy tree takes the first child", "if (tk[c] == a) next = c;", "if (next == -1) next = c;", "tree"),
+    ("tree coin of the next depth", "uniforms(seed, step, b, depth, &ua, &ur);",
+     "uniforms(seed, step, b, depth + 1, &ua, &ur);", "tree"),
     ("tree node linked twice accepted", "for (int32_t n = 1; !bad && n < N; ++n) bad = refs[n] != 1;", "",
      "tree"),
     ("siblings with equal tokens accepted", "bad = tk[a] == tk[c];", "bad = false;", "tree"),
@@ -105,6 +109,20 @@ MUTANTS = [
     ("sampling residual keeps the rejected draft", "residual(p, nullptr, rejected ? d[L] : -1, r);",
      "residual(p, nullptr, -1, r);", "sampling"),
     ("top_p of zero accepted", "|| !(tp > 0.0)) {", ") {", "sampling"),
+    ("top-k of 1 ignored", "if (top_k > 0 && top_k < V) {", "if (top_k > 1 && top_k < V) {", "sampling"),
+    ("top-p groups split at equal logits",
+     "while (g < idx.size() && row[idx[g]] == row[idx[i]]) gm += p[idx[g++]];", "gm = p[idx[g++]];",
+     "sampling"),
+    ("cut reported at the largest kept logit", "if (keep[v] && row[v] < tau) tau = row[v];",
+     "if (keep[v] && (tau == std::numeric_limits<float>::infinity() || row[v] > tau)) tau = row[v];",
+     "sampling"),
+    ("top-p walks the logits upwards",
+     "std::sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) { return row[a] > row[b]; });",
+     "std::sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) { return row[a] < row[b]; });", "sampling"),
+    ("sampling coin of the next position",
+     "uniforms(seed, step, b, j, &ua, &ur);\n      if (p_d) p_d[o] = p[d[j]];\n      if (u_acc) u_acc[o] = ua;\n      if (!(ua <= p[d[j]]))",
+     "uniforms(seed, step, b, j + 1, &ua, &ur);\n      if (p_d) p_d[o] = p[d[j]];\n      if (u_acc) u_acc[o] = ua;\n      if (!(ua <= p[d[j]]))",
+     "sampling"),
     ("infinite temperature accepted", "if (!(T > 0.0) || T == std::numeric_limits<double>::infinity()",
      "if (!(T > 0.0)", "sampling"),
 ]

@@ -142,6 +142,26 @@ def test_bonus_row_samples_target():
     assert stats.chisquare(hist, p0 * B).pvalue > 1e-3
 
 
+def test_a_subset_with_its_sequence_indices_equals_the_full_batch():
+    # a sequence's coins are keyed by its index (counter word 1), so a subset
+    # verified with the caller's indices gives the full batch's results for
+    # those sequences, and its resample coins are U(word 1) of those indices
+    rng = np.random.default_rng(27)
+    B, K, V, T = 12, 3, 200, 1.0
+    target = workloads.gaussian_logits(rng, (B, K + 1, V), 2.0)
+    top = np.argsort(-target[:, :K], axis=2)[:, :, :5]
+    draft = np.take_along_axis(top, rng.integers(0, 5, (B, K, 1)), axis=2)[:, :, 0].astype(np.int32)
+    full = oracle.verify(target, draft, temperature=T, seed=4, step=6)
+    idx = np.array([7, 2, 11, 5])
+    sub = oracle.verify(target[idx], draft[idx], temperature=T, seed=4, step=6, seq_index=idx)
+    for key in ("accept_len", "out_token", "status", "u_res"):
+        assert np.array_equal(sub[key], full[key][idx]), key
+    for i, b in enumerate(idx):
+        assert sub["u_res"][i] == oracle.uniforms(4, 6, int(b), int(sub["accept_len"][i]))[1]
+    plain = oracle.verify(target[idx], draft[idx], temperature=T, seed=4, step=6)
+    assert not np.array_equal(plain["u_res"], sub["u_res"])
+
+
 @pytest.mark.parametrize("T", [1.0, 0.7])
 def test_resample_lies_in_its_cdf_interval(T):
     # at T != 1 too: the draft distribution is softmax(draft logits / T)
