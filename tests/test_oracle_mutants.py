@@ -28,7 +28,10 @@ PINS = {
     "sampling": "tests/test_oracle_sampling.py",
 }
 
-# (name, text in oracle.cpp, replacement, pin file that should catch it first)
+# (name, text in oracle.cpp, replacement, pin file that should catch it first).
+# Each mistake keeps the copy's memory accesses in bounds and its loops
+# finite (no suffix-link cycle, no index past an array), so that a pin, not
+# a crash or a hang, has to catch it.
 MUTANTS = [
     # suffix automaton construction (Blumer's online step)
     ("new-state length off by one", "new_state(len[last] + 1, -1, i)", "new_state(len[last], -1, i)", "sam"),
@@ -41,6 +44,12 @@ MUTANTS = [
     ("no-transition case links to the last state", "link[cur] = 0;", "link[cur] = last;", "sam"),
     ("new state's end position one early", "new_state(len[last] + 1, -1, i)",
      "new_state(len[last] + 1, -1, i - 1)", "sam"),
+    ("a clone on every existing transition", "if (len[p] + 1 == len[q]) {", "if (len[p] + 1 == len[q] && false) {",
+     "sam"),
+    ("out-of-vocabulary token accepted", "if (tok[i] < 0 || tok[i] >= sam->vocab) return 3;",
+     "if (tok[i] < 0) return 3;", "sam"),
+    ("dumped edge fields swapped", "edges[3 * e + 1] = kv.first;\n      edges[3 * e + 2] = kv.second;",
+     "edges[3 * e + 1] = kv.second;\n      edges[3 * e + 2] = kv.first;", "sam"),
     # draft from the dynamic automaton
     ("draft copies the matched token", "for (int32_t t = 0; t < dl; ++t) out[t] = text[e + 1 + t];\n    }\n    for (int32_t t = dl; t < K; ++t) out[t] = -1;\n    *draft_len = dl;\n  }\n\n  // Static",
      "for (int32_t t = 0; t < dl; ++t) out[t] = text[e + t];\n    }\n    for (int32_t t = dl; t < K; ++t) out[t] = -1;\n    *draft_len = dl;\n  }\n\n  // Static", "sam"),
@@ -149,8 +158,11 @@ def _run_pins(src_text, workdir, first):
     files = [PINS[first]] + [p for k, p in PINS.items() if k != first]
     args = files + ["-x", "-q", "-m", "not gpu", "-p", "no:cacheprovider"]
     code = _CHILD.format(root=ROOT, lib=lib, args=args)
-    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
-                       timeout=600)
+    try:
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                           timeout=180)
+    except subprocess.TimeoutExpired:
+        return None, "timed out"
     return r.returncode, (r.stdout + r.stderr)[-1500:]
 
 
